@@ -1,0 +1,155 @@
+"""CPU fp64 oracle for MLA speculative-decoding verify attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's
+CPU-baseline leg are the only callers.  The product path never imports this
+package; it shares no code with the GPU path (only the seeded input generator
+is common to both).
+
+The arithmetic lives in verify_oracle.c (plain C, fp64, pthreads over query
+rows); this module compiles it with gcc when the shared object is missing or
+older than the source, and wraps it for numpy arrays.  See the C file's
+header for the definition it evaluates and the passages it follows.
+
+Parity status of each function (what pins it is listed in the tests):
+  verify / verify_rows  pinned: library SDPA, closed forms, invariants
+  verify_split          pinned: equals the unsplit result (merge identity)
+  merge                 pinned: closed forms, equals the unsplit result
+  tree_masks            pinned: graph-library ancestor sets
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "verify_oracle.c")
+LIB = os.path.join(_HERE, "liboracle.so")
+D_QK = 576
+D_V = 512
+
+_lib = None
+
+
+def build(src: str = SRC, out: str = LIB, force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math: IEEE fp64 throughout)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = f"{out}.{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+                               "-o", tmp, src, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str):
+    L = ctypes.CDLL(path)
+    vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    prob = [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, dbl]
+    L.oracle_verify.argtypes = prob + [vp, vp, i32]
+    L.oracle_verify_rows.argtypes = prob + [vp, i64, vp, vp, i32]
+    L.oracle_verify_split.argtypes = prob + [i32, vp, vp, i32]
+    L.oracle_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp]
+    L.oracle_tree_masks.argtypes = [vp, vp, i32, vp]
+    L.oracle_num_cpus.argtypes = []
+    for f in (L.oracle_verify, L.oracle_verify_rows, L.oracle_verify_split, L.oracle_merge,
+              L.oracle_tree_masks, L.oracle_num_cpus):
+        f.restype = ctypes.c_int
+    return L
+
+
+def lib(path: Optional[str] = None):
+    """The loaded oracle library (built on first use); `path` loads another build."""
+    global _lib
+    if path is not None:
+        return _bind(path)
+    if _lib is None:
+        _lib = _bind(build())
+    return _lib
+
+
+def num_cpus() -> int:
+    return int(lib().oracle_num_cpus())
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _prob(case, draft_mask: Optional[np.ndarray], use_parent: bool = True):
+    q = np.ascontiguousarray(case.q, dtype=np.uint16)
+    kv = np.ascontiguousarray(case.kv_pool, dtype=np.uint16)
+    kvp = np.ascontiguousarray(case.kv_indptr, dtype=np.int32)
+    kvi = np.ascontiguousarray(case.kv_indices, dtype=np.int32)
+    qop = np.ascontiguousarray(case.qo_indptr, dtype=np.int32)
+    dm = None if draft_mask is None else np.ascontiguousarray(draft_mask, dtype=np.uint64)
+    par = None
+    if use_parent and case.parent is not None and dm is None:
+        par = np.ascontiguousarray(case.parent, dtype=np.int32)
+    keep = (q, kv, kvp, kvi, qop, dm, par)
+    args = [q.ctypes.data, kv.ctypes.data, kv.shape[0], kvp.ctypes.data, kvi.ctypes.data, qop.ctypes.data,
+            _ptr(dm), _ptr(par), len(kvp) - 1, q.shape[1], float(case.sm_scale)]
+    return keep, args
+
+
+def verify(case, draft_mask: Optional[np.ndarray] = None, threads: int = 0, lib_=None):
+    """Every row: (out [T_q, H, 512] f64, lse [T_q, H] f64)."""
+    L = lib_ or lib()
+    keep, args = _prob(case, draft_mask)
+    T, H = case.q.shape[0], case.q.shape[1]
+    out = np.zeros((T, H, D_V), dtype=np.float64)
+    lse = np.zeros((T, H), dtype=np.float64)
+    rc = L.oracle_verify(*args, out.ctypes.data, lse.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle_verify rejected its inputs")
+    return out, lse
+
+
+def verify_rows(case, rows: np.ndarray, draft_mask: Optional[np.ndarray] = None, threads: int = 0, lib_=None):
+    """Selected rows (global id t*H + h): (out [n, 512], lse [n])."""
+    L = lib_ or lib()
+    keep, args = _prob(case, draft_mask)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), D_V), dtype=np.float64)
+    lse = np.zeros(len(rows), dtype=np.float64)
+    rc = L.oracle_verify_rows(*args, rows.ctypes.data, len(rows), out.ctypes.data, lse.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle_verify_rows rejected its inputs")
+    return out, lse
+
+
+def verify_split(case, splits: int, draft_mask: Optional[np.ndarray] = None, threads: int = 0, lib_=None):
+    L = lib_ or lib()
+    keep, args = _prob(case, draft_mask)
+    T, H = case.q.shape[0], case.q.shape[1]
+    out = np.zeros((T, H, D_V), dtype=np.float64)
+    lse = np.zeros((T, H), dtype=np.float64)
+    rc = L.oracle_verify_split(*args, int(splits), out.ctypes.data, lse.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle_verify_split rejected its inputs")
+    return out, lse
+
+
+def merge(o_parts: np.ndarray, lse_parts: np.ndarray, lib_=None):
+    """o_parts [S, R, D], lse_parts [S, R] -> (o [R, D], lse [R])."""
+    L = lib_ or lib()
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    S, R, D = o_parts.shape
+    o = np.zeros((R, D), dtype=np.float64)
+    lse = np.zeros(R, dtype=np.float64)
+    L.oracle_merge(o_parts.ctypes.data, lse_parts.ctypes.data, S, R, D, o.ctypes.data, lse.ctypes.data)
+    return o, lse
+
+
+def tree_masks(parent: np.ndarray, qo_indptr: np.ndarray, lib_=None) -> np.ndarray:
+    L = lib_ or lib()
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    out = np.zeros(int(qo_indptr[-1]), dtype=np.uint64)
+    rc = L.oracle_tree_masks(parent.ctypes.data, qo_indptr.ctypes.data, len(qo_indptr) - 1, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_tree_masks: parents must precede their children")
+    return out
