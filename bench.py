@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of the MLA speculative-decoding verify attention on GB300.
+
+One step = one verify call (mask expansion when a tree is given, the verify
+kernel, the split merge) over one batch of seeded synthetic inputs resident in
+HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: long_185k (1 sequence, 185,000-token prefix + 16 causal draft
+positions, 64 heads, 576-dim bf16 latent rows at page_size = 1 with permuted
+slots in a 200,000-slot pool), the shape the >= 60 % roofline target is stated
+on.  Its KV rows (213 MB) exceed the 129 MB L2, so no L2 flush is needed
+between steps; smaller workloads get a 512 MB L2 flush before each step
+(outside the kernel events, inside the step).
+
+Metric: KV tokens per second (sum over sequences of N_b, per step), plus
+algorithmic TFLOP/s and HBM GB/s.  Algorithmic work per launch:
+  bytes = sum_b [N_b * (1152 + 4) + Q_b * H * (1152 + 1024 + 4)]
+  flops = 2 * H * (576 + 512) * V,   V = sum_b (Q_b * P_b + sum_i |mask_i|)
+Roofline: the verify kernel's achieved TFLOP/s (algorithmic flops / its mean
+event-timed duration) against the measured dense bf16 peak.
+
+--impl reference times the CPU fp64 oracle on the host cores on a bounded
+sample of the same workload (a subset of query rows), scaled to the metric.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path shards by sequence with no exchange), value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algorithmic_work(case):
+    """(bytes, flops, kv_tokens) of one call, from the shapes and visibility counts."""
+    H = case.num_heads
+    nkv = np.diff(case.kv_indptr).astype(np.int64)
+    nq = np.diff(case.qo_indptr).astype(np.int64)
+    prefix = nkv - nq
+    vis_draft = 0
+    for b in range(case.batch):
+        n = int(nq[b])
+        if case.parent is None:
+            vis_draft += n * (n + 1) // 2
+        else:
+            par = case.parent[case.qo_indptr[b]:case.qo_indptr[b + 1]]
+            depth = np.zeros(n, np.int64)
+            for i in range(n):
+                depth[i] = 0 if par[i] < 0 else depth[par[i]] + 1
+            vis_draft += int((depth + 1).sum())
+    V = int((nq * prefix).sum()) + vis_draft
+    bytes_ = int((nkv * (1152 + 4)).sum() + (nq * H * (1152 + 1024 + 4)).sum())
+    flops = 2 * H * (576 + 512) * V
+    return bytes_, flops, int(nkv.sum())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": float(max(maxes)), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("VMLA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def reduce_max_sum(value_max: float, value_sum: float, world: int, device=None):
+    """(max over ranks of value_max, sum over ranks of value_sum); identity when world == 1."""
+    if world <= 1:
+        return value_max, value_sum
+    import torch
+    import torch.distributed as dist
+    t1 = torch.tensor([value_max], dtype=torch.float64, device=device)
+    t2 = torch.tensor([value_sum], dtype=torch.float64, device=device)
+    dist.all_reduce(t1, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t2, op=dist.ReduceOp.SUM)
+    return float(t1.item()), float(t2.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_sample(case, budget_s: float = 15.0, max_rows: int = 4096):
+    """Times the oracle on a growing sample of rows; returns (kv tokens/s, cores, sample text)."""
+    import oracle
+    H = case.num_heads
+    T = case.q.shape[0]
+    total_rows = T * H
+    cores = oracle.num_cpus()
+    # KV keys each row reads (its sequence's N_b)
+    nkv = np.diff(case.kv_indptr).astype(np.int64)
+    seq_of_t = np.repeat(np.arange(case.batch), np.diff(case.qo_indptr))
+    keys_per_row = np.repeat(nkv[seq_of_t], H)
+    rng_rows = synth_rows(total_rows)
+    n = min(total_rows, max(cores, 16))
+    spent = 0.0
+    done_rows = 0
+    done_keys = 0
+    while True:
+        rows = rng_rows[done_rows:done_rows + n]
+        if len(rows) == 0:
+            break
+        t0 = time.perf_counter()
+        oracle.verify_rows(case, rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_rows += len(rows)
+        done_keys += int(keys_per_row[rows].sum())
+        if spent >= budget_s or done_rows >= min(total_rows, max_rows):
+            break
+        n = int(min(total_rows - done_rows, max(len(rows), len(rows) * max(1.0, (budget_s - spent) / max(dt, 1e-3)))))
+    # whole-job time estimate: (all rows' keys) / (keys per second achieved on the sample)
+    keys_per_s = done_keys / spent
+    all_keys = int(keys_per_row.sum())
+    job_s = all_keys / keys_per_s
+    tokens = int(nkv.sum())
+    sample = f"{done_rows} of {total_rows} query rows (seeded), {spent:.1f} s of CPU wall time, scaled by row keys"
+    return tokens / job_s, cores, sample, spent
+
+
+def synth_rows(total_rows: int) -> np.ndarray:
+    from speculative_decoding_mla_gb300 import synth
+    w = synth.words(17, synth.TAG_AUX, total_rows)
+    return np.argsort(w, kind="stable").astype(np.int64)
+
+
+def run_reference(args, rank, world):
+    from speculative_decoding_mla_gb300 import synth
+    if rank != 0:
+        barrier(world)
+        return
+    case = synth.workload(args.workload)
+    per_step = max(1.0, args.ref_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(case, budget_s=0.5, max_rows=16)
+    vals = []
+    total_s = 0.0
+    for _ in range(args.steps):
+        v, cores, sample, spent = cpu_oracle_sample(case, budget_s=per_step)
+        vals.append(v)
+        total_s += spent
+    value = float(np.median(vals))
+    nbytes, flops, tokens = algorithmic_work(case)
+    ms = tokens / value * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64/Box-Muller, bf16 inputs)",
+        "config": {"workload": args.workload, "heads": case.num_heads, "batch": case.batch,
+                   "kv_tokens": tokens, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": "KV tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def run_ours(args, rank, local, world):
+    import torch
+    from speculative_decoding_mla_gb300 import build as vbuild
+    if not os.path.exists(os.path.join(ROOT, "speculative_decoding_mla_gb300", "libvmla.so")):
+        vbuild.build()
+    from speculative_decoding_mla_gb300 import binding, device, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = synth.workload(args.workload)
+    dc = device.to_device(case, device=dev)
+    out, lse = device.alloc_outputs(dc)
+    ws = device.alloc_workspace(dc, args.splits)
+    nbytes, flops, tokens = algorithmic_work(case)
+    input_bytes = int(case.kv_indices.max() + 1) * 1152 if case.batch else 0
+    flush = input_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+    kernel = "simt" if args.kernel == "simt" else "tc"
+
+    def step():
+        if flush_buf is not None:
+            flush_buf.fill_(1)
+        device.run(dc, kernel=kernel, splits=args.splits, out=out, lse=lse, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = binding.verify_attn_mla_check(ws)
+    if st != 0:
+        raise RuntimeError(f"kernel status {binding.status_string(st)}")
+
+    # kernel events on the launching stream, recorded inside the library
+    binding.verify_attn_mla_timing_enable(args.steps)
+    sampler = ClockSampler(local) if rank == 0 or True else None
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms_total = ev0.elapsed_time(ev1)
+    verify_ms, merge_ms = binding.verify_attn_mla_timing_read(args.steps)
+    binding.verify_attn_mla_timing_enable(0)
+
+    kernel_ms = float(verify_ms.mean() + merge_ms.mean())  # verify + merge per step, excluding the L2 flush
+    if flush_buf is None:
+        step_ms = step_ms_total / args.steps
+    else:
+        step_ms = kernel_ms  # the flush is not part of the work
+    max_ms, sum_tokens = reduce_max_sum(step_ms, float(tokens), world, dev if world > 1 else None)
+    value = sum_tokens / (max_ms / 1e3)
+
+    # end to end through the host-buffer entry point: H2D of the step's inputs,
+    # the call, D2H of out and lse, synchronised, wall clock
+    T, H = case.q.shape[0], case.num_heads
+    q_h = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    kvi_h = torch.from_numpy(case.kv_indices).pin_memory()
+    out_h = torch.empty((T, H, 512), dtype=torch.int16).pin_memory()
+    lse_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    par_h = torch.from_numpy(case.parent).pin_memory() if case.parent is not None else None
+    nbuf = binding.verify_attn_mla_host_buffer_size(case.qo_indptr, case.kv_indptr, H, args.splits,
+                                                    has_parent=par_h is not None)
+    dbuf = torch.empty(nbuf, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        binding.verify_attn_mla_host(q_h, dc.kv_pool, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, dbuf,
+                                     case.sm_scale, parent_host=par_h, splits=args.splits, stream=stream)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1)
+            torch.cuda.synchronize()
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_max, e2e_tokens = reduce_max_sum(e2e_s, float(tokens), world, dev if world > 1 else None)
+    h2d = q_h.numel() * 2 + kvi_h.numel() * 4 + 2 * (case.batch + 1) * 4 + (par_h.numel() * 4 if par_h is not None
+                                                                               else 0)
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    peaks = load_peaks()
+    v_ms = float(verify_ms.mean())
+    achieved_tflops = flops / (v_ms / 1e3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, spent = cpu_oracle_sample(case, budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "KV tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    launches_per_step = 1 + (1 if float(merge_ms.max()) > 0 else 0) + (1 if case.parent is not None else 0)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, bf16 inputs)",
+            "config": {"workload": args.workload, "batch": case.batch, "heads": H, "kv_tokens": tokens,
+                       "draft_tokens": T, "kernel": kernel, "splits": args.splits or "auto",
+                       "l2": "flushed (512 MB write) before every step" if flush_buf is not None
+                       else "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "tflops": flops / (max_ms / 1e3) / 1e12,
+            "hbm_gbs": nbytes / (max_ms / 1e3) / 1e9,
+            "roofline": {"bound": "tensor", "achieved": achieved_tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"], "traffic": None,
+                         "kernel": "verify", "peak_source": f"{peaks['source']} dense bf16 burst",
+                         "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                         "verify_ms": v_ms, "merge_ms": float(merge_ms.mean()),
+                         "roofline_ms": max(flops / (peaks["bf16_tflops"] * 1e12),
+                                            nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e3},
+            "roofline_frac_step": max(flops / (peaks["bf16_tflops"] * 1e12),
+                                      nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e3 / max_ms,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_tokens / e2e_max, "unit": "KV tokens/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h),
+                    "note": "q, indptr/indices (and parents) copied in, out and lse copied back every step; "
+                            "the KV cache stays resident in HBM"},
+            "gpu_launches": int(launches_per_step * args.steps),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_185k")
+    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    rank, local, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * verify_attn_mla.h -- C ABI of the MLA speculative-decoding verify attention
+ * for GB300 (sm_103a).
+ *
+ * The operation (the "verify attention" of "The Build That Unlocked 3-6x
+ * Decode Speedup", section "The Context: A Custom Kernel for an Unsupported
+ * Architecture"): every draft query of a sequence, per head, is scored against
+ * that sequence's latent KV rows, masked, soft-maxed and used to weight the
+ * latent rows.  The layout and the mask follow "The Build That Bridged Design
+ * and Deployment", section "What This Build Achieves: The paged+bf16 Kernel":
+ * bf16 rows read through a slot indirection at page_size = 1, several
+ * requests per call, and a mask made of a prefix length plus a small q x q
+ * visibility matrix over the draft tail.  Splitting the key range across
+ * SMs and merging the partial softmaxes is the NSPLIT split-KV of "The Build
+ * Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel".
+ *
+ * Definition, for sequence b (N_b keys, Q_b drafts, prefix P_b = N_b - Q_b),
+ * draft query i (token t = qo_indptr[b] + i) and head h:
+ *   row_j  = kv_pool[kv_indices[kv_indptr[b] + j]]          576 bf16: [0,512) latent, [512,576) rope
+ *   J      = { j < P_b } U { P_b + k : bit k of mask_i }
+ *   mask_i = draft_mask[t] | ancestors-and-self from parent[] | causal bits 0..i
+ *   s_j    = sm_scale * <q[t,h,0:576], row_j[0:576]>
+ *   out[t,h,:] = sum_{j in J} softmax(s)_j * row_j[0:512]   (bf16, round-to-nearest-even)
+ *   lse[t,h]   = ln sum_{j in J} exp(s_j)                    (fp32, natural log)
+ * A query with no visible key gets out = 0 and lse = -inf.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers unless the name ends in _host.  bf16 data is passed as
+ *     raw 16-bit patterns (`const void*`).  `stream` is a cudaStream_t (NULL =
+ *     legacy default stream).  All device work is asynchronous on `stream`
+ *     unless stated otherwise.
+ *   - The caller owns every buffer.  The library keeps no pointer after a call
+ *     returns and allocates no device memory in these entry points.
+ *   - Errors are returned as a vmla_status (int); nothing throws.  Argument
+ *     errors are detected on the host before any launch.  Faults seen by a
+ *     kernel (a slot index outside the pool, malformed parents, a bounded wait
+ *     that ran out) are recorded in the workspace's status word and reported by
+ *     verify_attn_mla_check().
+ */
+#ifndef VERIFY_ATTN_MLA_H
+#define VERIFY_ATTN_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VMLA_D_QK 576     /* latent (512) + rope (64) per token and per query head */
+#define VMLA_D_V 512      /* latent width; also the output width */
+#define VMLA_MAX_DRAFT 64 /* draft positions per sequence (one 64-bit visibility word each) */
+#define VMLA_MAX_BATCH 512
+#define VMLA_MAX_HEADS 128
+#define VMLA_WORKSPACE_ALIGN 256
+
+typedef enum vmla_status {
+  VMLA_OK = 0,
+  VMLA_ERR_NULL = -1,      /* a required pointer is NULL */
+  VMLA_ERR_SHAPE = -2,     /* sizes out of range or indptr arrays inconsistent */
+  VMLA_ERR_ALIGN = -3,     /* a pointer misses its alignment (16 B for bf16 arrays, 256 B workspace) */
+  VMLA_ERR_WORKSPACE = -4, /* workspace smaller than verify_attn_mla_workspace_size() */
+  VMLA_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed */
+  VMLA_ERR_TIMEOUT = -6,   /* a kernel's bounded wait expired (kernel returned early) */
+  VMLA_ERR_INDEX = -7,     /* a kv slot index was outside [0, pool_slots) (key skipped) */
+  VMLA_ERR_DEVICE = -8,    /* no usable sm_103 device for this library */
+  VMLA_ERR_PARENT = -9     /* a parent index was not in [-1, i) (mask left empty) */
+} vmla_status;
+
+/* Description of the split plan a call would use (host only, no GPU needed). */
+typedef struct vmla_plan_info {
+  int32_t num_units;        /* work units (one CTA each, or one CTA pair for the tensor-core kernel) */
+  int32_t max_splits;       /* largest split count of any sequence */
+  int64_t partial_rows;     /* fp32 partial (row, split) results kept in the workspace */
+  int64_t merge_rows;       /* query rows whose splits the merge kernel combines */
+  size_t workspace_bytes;   /* bytes verify_attn_mla needs in `workspace` */
+} vmla_plan_info;
+
+/* Kernel families a plan can be made for. */
+#define VMLA_KERNEL_TC 0   /* tcgen05 / TMEM tensor-core kernel (what verify_attn_mla runs) */
+#define VMLA_KERNEL_SIMT 1 /* plain CUDA-core kernel (verify_attn_mla_simt) */
+
+/* Split planner.  Splits each sequence's key range into contiguous pieces so
+ * that the work units fill `num_sms` SMs (the NSPLIT occupancy fix of "The
+ * Build That Unlocked 3-6x Decode Speedup", section "Broader Significance").
+ *   qo_indptr_host, kv_indptr_host: host arrays [batch+1], starting at 0.
+ *   splits: 0 = choose per sequence; k > 0 = k pieces for every sequence
+ *           (capped so that no piece is empty).
+ *   splits_out: optional host array [batch] receiving each sequence's count.
+ * Returns VMLA_OK or VMLA_ERR_NULL / VMLA_ERR_SHAPE.  Pure host code. */
+int verify_attn_mla_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_host,
+                         const int32_t* kv_indptr_host, int splits, int num_sms, vmla_plan_info* info,
+                         int32_t* splits_out);
+
+/* Workspace bytes verify_attn_mla needs for these lengths on the current
+ * device (its SM count enters the plan).  Writes *bytes; returns a status. */
+int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                   const int32_t* kv_indptr_host, int splits, size_t* bytes);
+
+/* The verify attention (tensor-core kernel, plus the merge kernel when a
+ * sequence is split, plus the mask-expansion kernel when `parent` is given).
+ *   q           [T_q, H, 576] bf16, T_q = qo_indptr_host[batch]; 16 B aligned
+ *   kv_pool     [pool_slots, 576] bf16 row-major (row stride 1152 B); 16 B aligned
+ *   kv_indptr   [batch+1] int32; sequence b owns kv_indices[kv_indptr[b] .. kv_indptr[b+1])
+ *   kv_indices  [kv_indptr[batch]] int32 slots; the LAST Q_b entries of each
+ *               sequence are its draft tokens' rows, in draft order
+ *   qo_indptr   [batch+1] int32; Q_b = qo_indptr[b+1] - qo_indptr[b] in [0, 64]
+ *   draft_mask  [T_q] uint64 or NULL: bit k = query sees draft k of its sequence
+ *   parent      [T_q] int32 or NULL: local parent of each draft (-1 = root;
+ *               parent[i] < i).  Used only when draft_mask is NULL.  Both NULL
+ *               means causal among the drafts.
+ *   kv_indptr_host, qo_indptr_host: host copies of the two indptr arrays; read
+ *               during the call to build the plan, not retained.
+ *   sm_scale    score scale (1/sqrt(192) for the target model)
+ *   splits      0 = planner's choice; k > 0 forces k pieces per sequence
+ *   out         [T_q, H, 512] bf16 (16 B aligned);  lse [T_q, H] fp32
+ *   workspace   >= verify_attn_mla_workspace_size() bytes, 256 B aligned.
+ *               Holds the status word, ancestor masks and split partials.
+ *               Calls that share a workspace must be ordered on one stream.
+ * No host synchronisation and no allocation happen inside the call. */
+int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                    const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                    const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
+                    int batch, int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Same operation and arguments on the plain CUDA-core kernel (one warp per
+ * four query rows, scores by FMA and warp shuffles).  A second, independent
+ * GPU implementation used to cross-check the tensor-core kernel; its plan
+ * and workspace come from verify_attn_mla_plan(VMLA_KERNEL_SIMT, ...). */
+int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                         const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
+                         int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The split merge on its own: o_parts [num_splits, rows, 512] fp32 (each part
+ * already normalised by its own softmax sum), lse_parts [num_splits, rows]
+ * fp32 (-inf = empty part).  Writes out [rows, 512] bf16 and lse [rows]:
+ *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.
+ * 16 B aligned o_parts/out. */
+int verify_attn_mla_merge(const float* o_parts, const float* lse_parts, int num_splits, int64_t rows, void* out,
+                          float* lse, void* stream);
+
+/* Expands draft-tree parents into per-query visibility words (bit k set for
+ * k = i and every ancestor of i), the tree form of the q x q visibility
+ * matrix.  parent [T_q] int32 local indices, qo_indptr [batch+1] device,
+ * mask_out [T_q] uint64.  A malformed parent (not in [-1, i)) leaves that
+ * query's word 0 and, if status_word (device uint32) is not NULL, records
+ * VMLA_ERR_PARENT there. */
+int verify_attn_mla_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q,
+                              uint64_t* mask_out, uint32_t* status_word, void* stream);
+
+/* Synchronises `stream`, reads the device status word of `workspace` left by
+ * the last call that used it, and returns it (VMLA_OK when no kernel recorded
+ * a fault).  Test and debugging aid; it blocks the host. */
+int verify_attn_mla_check(const void* workspace, void* stream);
+
+/* Host-buffer form for callers whose per-step inputs live in host memory.
+ * Copies q, the indptr/indices arrays and the optional mask/parent array from
+ * host memory into `device_buffer`, runs verify_attn_mla against the
+ * device-resident kv_pool, copies out and lse back into host memory, and
+ * synchronises `stream` before returning (so the returned status includes the
+ * device status word).  Host buffers should be pinned for asynchronous copies.
+ * device_buffer must hold verify_attn_mla_host_buffer_size() bytes (256 B
+ * aligned). */
+int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                     const int32_t* kv_indptr_host, int splits, int has_mask, int has_parent,
+                                     size_t* bytes);
+int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr_host,
+                         const int32_t* kv_indices_host, const int32_t* qo_indptr_host,
+                         const uint64_t* draft_mask_host, const int32_t* parent_host, int batch, int num_heads,
+                         float sm_scale, int splits, void* out_host, float* lse_host, void* device_buffer,
+                         size_t device_buffer_bytes, void* stream);
+
+/* Measurement aid.  verify_attn_mla_timing_enable(n) creates host-side CUDA
+ * events for the next n run calls (0 turns it off and frees them); while it is
+ * on, every verify_attn_mla / verify_attn_mla_simt call records events on its
+ * stream around the verify kernel and around the merge kernel.
+ * verify_attn_mla_timing_read() waits for those events and writes, per call in
+ * launch order, the verify kernel's and the merge kernel's device time in ms
+ * (merge_ms = 0 when no merge ran) into arrays of `capacity` entries, sets
+ * *count, and starts a new recording.  Not for concurrent use from several
+ * host threads. */
+int verify_attn_mla_timing_enable(int capacity);
+int verify_attn_mla_timing_read(float* verify_ms, float* merge_ms, int capacity, int* count);
+
+/* Human-readable name of a status code (static string). */
+const char* verify_attn_mla_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int verify_attn_mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_MLA_H */

@@ -1,0 +1,228 @@
+"""Thin Python binding of the C ABI in include/verify_attn_mla.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  The functions keep the C names and take torch tensors for device
+(and pinned host) buffers; `stream` defaults to torch's current stream.  A
+status other than VMLA_OK raises VmlaError.  If libvmla.so is missing the
+import of this module fails: there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libvmla.so")
+
+VMLA_OK = 0
+VMLA_ERR_NULL = -1
+VMLA_ERR_SHAPE = -2
+VMLA_ERR_ALIGN = -3
+VMLA_ERR_WORKSPACE = -4
+VMLA_ERR_CUDA = -5
+VMLA_ERR_TIMEOUT = -6
+VMLA_ERR_INDEX = -7
+VMLA_ERR_DEVICE = -8
+VMLA_ERR_PARENT = -9
+VMLA_KERNEL_TC = 0
+VMLA_KERNEL_SIMT = 1
+D_QK = 576
+D_V = 512
+
+EXPORTS = (
+    "verify_attn_mla_plan", "verify_attn_mla_workspace_size", "verify_attn_mla", "verify_attn_mla_simt",
+    "verify_attn_mla_merge", "verify_attn_mla_tree_mask", "verify_attn_mla_check",
+    "verify_attn_mla_host_buffer_size", "verify_attn_mla_host", "verify_attn_mla_status_string",
+    "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
+)
+
+
+class VmlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_units", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("partial_rows", ctypes.c_int64),
+                ("merge_rows", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
+
+
+def _load(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with speculative_decoding_mla_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    run = [vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp, sz, vp]
+    sig = {
+        "verify_attn_mla_plan": [i32, i32, i32, vp, vp, i32, i32, ctypes.POINTER(PlanInfo), vp],
+        "verify_attn_mla_workspace_size": [i32, i32, vp, vp, i32, ctypes.POINTER(sz)],
+        "verify_attn_mla": run,
+        "verify_attn_mla_simt": run,
+        "verify_attn_mla_merge": [vp, vp, i32, i64, vp, vp, vp],
+        "verify_attn_mla_tree_mask": [vp, vp, i32, i32, vp, vp, vp],
+        "verify_attn_mla_check": [vp, vp],
+        "verify_attn_mla_host_buffer_size": [i32, i32, vp, vp, i32, i32, i32, ctypes.POINTER(sz)],
+        "verify_attn_mla_host": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp, sz, vp],
+        "verify_attn_mla_status_string": [i32],
+        "verify_attn_mla_version": [],
+        "verify_attn_mla_timing_enable": [i32],
+        "verify_attn_mla_timing_read": [vp, vp, i32, ctypes.POINTER(i32)],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_char_p if name == "verify_attn_mla_status_string" else ctypes.c_int
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.verify_attn_mla_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != VMLA_OK:
+        raise VmlaError(rc, where)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _host_i32(a) -> np.ndarray:
+    if hasattr(a, "cpu"):
+        a = a.cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def verify_attn_mla_plan(kernel: int, qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0,
+                         num_sms: int = 152):
+    """Host-only split plan: (PlanInfo, splits per sequence)."""
+    qo = _host_i32(qo_indptr_host)
+    kv = _host_i32(kv_indptr_host)
+    B = len(qo) - 1
+    info = PlanInfo()
+    per = np.zeros(max(B, 1), dtype=np.int32)
+    _check(_lib.verify_attn_mla_plan(kernel, B, num_heads, qo.ctypes.data, kv.ctypes.data, splits, num_sms,
+                                     ctypes.byref(info), per.ctypes.data), "verify_attn_mla_plan")
+    return info, per[:B]
+
+
+def verify_attn_mla_workspace_size(qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0) -> int:
+    qo = _host_i32(qo_indptr_host)
+    kv = _host_i32(kv_indptr_host)
+    n = ctypes.c_size_t(0)
+    _check(_lib.verify_attn_mla_workspace_size(len(qo) - 1, num_heads, qo.ctypes.data, kv.ctypes.data, splits,
+                                               ctypes.byref(n)), "verify_attn_mla_workspace_size")
+    return int(n.value)
+
+
+def _run(fn, name, q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+         workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None, num_heads=None, pool_slots=None):
+    kvh = _host_i32(kv_indptr_host)
+    qoh = _host_i32(qo_indptr_host)
+    H = int(num_heads if num_heads is not None else q.shape[1])
+    S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
+    rc = fn(_ptr(q), _ptr(kv_pool), S, _ptr(kv_indptr), _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask),
+            _ptr(parent), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, H, float(sm_scale), int(splits), _ptr(out),
+            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, name)
+
+
+def verify_attn_mla(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+                    workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    """Tensor-core verify attention into `out` [T,H,512] bf16 and `lse` [T,H] fp32."""
+    _run(_lib.verify_attn_mla, "verify_attn_mla", q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host,
+         qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+
+
+def verify_attn_mla_simt(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+                         workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    """Same operation on the CUDA-core kernel."""
+    _run(_lib.verify_attn_mla_simt, "verify_attn_mla_simt", q, kv_pool, kv_indptr, kv_indices, qo_indptr,
+         kv_indptr_host, qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+
+
+def verify_attn_mla_merge(o_parts, lse_parts, out, lse, stream=None):
+    S, R = int(o_parts.shape[0]), int(o_parts.shape[1])
+    _check(_lib.verify_attn_mla_merge(_ptr(o_parts), _ptr(lse_parts), S, R, _ptr(out), _ptr(lse), _stream(stream)),
+           "verify_attn_mla_merge")
+
+
+def verify_attn_mla_tree_mask(parent, qo_indptr, mask_out, status_word=None, stream=None):
+    B = int(qo_indptr.shape[0]) - 1
+    T = int(parent.shape[0])
+    _check(_lib.verify_attn_mla_tree_mask(_ptr(parent), _ptr(qo_indptr), B, T, _ptr(mask_out), _ptr(status_word),
+                                          _stream(stream)), "verify_attn_mla_tree_mask")
+
+
+def verify_attn_mla_check(workspace, stream=None) -> int:
+    """Device status of the last call on `workspace` (synchronises the stream)."""
+    return int(_lib.verify_attn_mla_check(_ptr(workspace), _stream(stream)))
+
+
+def verify_attn_mla_host_buffer_size(qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0,
+                                     has_mask: bool = False, has_parent: bool = False) -> int:
+    qo = _host_i32(qo_indptr_host)
+    kv = _host_i32(kv_indptr_host)
+    n = ctypes.c_size_t(0)
+    _check(_lib.verify_attn_mla_host_buffer_size(len(qo) - 1, num_heads, qo.ctypes.data, kv.ctypes.data, splits,
+                                                 int(has_mask), int(has_parent), ctypes.byref(n)),
+           "verify_attn_mla_host_buffer_size")
+    return int(n.value)
+
+
+def verify_attn_mla_host(q_host, kv_pool, kv_indptr_host, kv_indices_host, qo_indptr_host, out_host, lse_host,
+                         device_buffer, sm_scale, draft_mask_host=None, parent_host=None, splits=0, stream=None,
+                         num_heads=None):
+    """Host-memory inputs/outputs, device-resident kv_pool; returns after the stream has finished."""
+    kvh = _host_i32(kv_indptr_host)
+    qoh = _host_i32(qo_indptr_host)
+    H = int(num_heads if num_heads is not None else q_host.shape[1])
+    rc = _lib.verify_attn_mla_host(_ptr(q_host), _ptr(kv_pool), int(kv_pool.shape[0]), kvh.ctypes.data,
+                                   _ptr(kv_indices_host), qoh.ctypes.data, _ptr(draft_mask_host), _ptr(parent_host),
+                                   len(kvh) - 1, H, float(sm_scale), int(splits), _ptr(out_host), _ptr(lse_host),
+                                   _ptr(device_buffer), device_buffer.numel() * device_buffer.element_size(),
+                                   _stream(stream))
+    _check(rc, "verify_attn_mla_host")
+
+
+def verify_attn_mla_version() -> int:
+    return int(_lib.verify_attn_mla_version())
+
+
+def verify_attn_mla_timing_enable(capacity: int):
+    _check(_lib.verify_attn_mla_timing_enable(int(capacity)), "verify_attn_mla_timing_enable")
+
+
+def verify_attn_mla_timing_read(capacity: int):
+    """(verify_ms, merge_ms) arrays of the recorded calls, in launch order."""
+    v = np.zeros(max(capacity, 1), np.float32)
+    m = np.zeros(max(capacity, 1), np.float32)
+    n = ctypes.c_int(0)
+    _check(_lib.verify_attn_mla_timing_read(v.ctypes.data, m.ctypes.data, int(capacity), ctypes.byref(n)),
+           "verify_attn_mla_timing_read")
+    return v[: n.value].copy(), m[: n.value].copy()

@@ -1,0 +1,360 @@
+// C ABI of the verify attention: argument checks, planning, workspace carving
+// and the launches, in stream order.  Exports are declared in
+// include/verify_attn_mla.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "vmla_internal.h"
+
+using namespace vmla;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by every run entry point; host arrays only.
+int check_common(const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
+                 int64_t pool_slots, int splits) {
+  if (!kv_indptr_host || !qo_indptr_host) return VMLA_ERR_NULL;
+  if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
+  if (splits < 0 || splits > 64 || pool_slots < 0 || pool_slots > INT32_MAX) return VMLA_ERR_SHAPE;
+  if (kv_indptr_host[0] != 0 || qo_indptr_host[0] != 0) return VMLA_ERR_SHAPE;
+  for (int b = 0; b < batch; ++b) {
+    int64_t nq = (int64_t)qo_indptr_host[b + 1] - qo_indptr_host[b];
+    int64_t nk = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+    if (nq < 0 || nq > VMLA_MAX_DRAFT || nk < nq) return VMLA_ERR_SHAPE;
+  }
+  return VMLA_OK;
+}
+
+// Optional per-call kernel timing (see verify_attn_mla_timing_enable).
+struct Timing {
+  std::mutex mu;
+  int cap = 0;
+  int n = 0;
+  std::vector<cudaEvent_t> ev;  // 4 per call: verify begin/end, merge begin/end
+  std::vector<char> merged;
+};
+Timing g_timing;
+
+cudaEvent_t timing_event(int call, int k) { return g_timing.ev[(size_t)call * 4 + k]; }
+
+int current_sm_count(int* sms, bool require_sm103) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VMLA_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return VMLA_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return VMLA_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return VMLA_ERR_DEVICE;
+  if (require_sm103 && !(major == 10 && minor == 3)) return VMLA_ERR_DEVICE;
+  return VMLA_OK;
+}
+
+int run(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+        const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask, const int32_t* parent,
+        const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
+        int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
+  if (rc != VMLA_OK) return rc;
+  const int64_t total_q = qo_indptr_host[batch];
+  const int64_t total_kv = kv_indptr_host[batch];
+  if (!workspace) return VMLA_ERR_NULL;
+  if (total_q > 0 && (!q || !kv_pool || !kv_indptr || !kv_indices || !qo_indptr || !out || !lse))
+    return VMLA_ERR_NULL;
+  if (total_kv > 0 && pool_slots == 0) return VMLA_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, VMLA_WORKSPACE_ALIGN) || !aligned(draft_mask, 8) || !aligned(parent, 4))
+    return VMLA_ERR_ALIGN;
+  int sms = 0;
+  rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  static thread_local PlanParams plan;  // large (20 KB); kept off the stack
+  vmla_plan_info info;
+  rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &plan, &info);
+  if (rc != VMLA_OK) return rc;
+  if (workspace_bytes < info.workspace_bytes) return VMLA_ERR_WORKSPACE;
+  const WorkspaceLayout L = workspace_layout(total_q, info.partial_rows);
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(status, 0, 8, st) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (total_q == 0) return VMLA_OK;
+
+  const uint64_t* masks = draft_mask;
+  if (!masks && parent) {
+    uint64_t* m = reinterpret_cast<uint64_t*>(ws + L.masks_off);
+    rc = launch_tree_mask(parent, qo_indptr, batch, (int)total_q, m, status, stream);
+    if (rc != VMLA_OK) return rc;
+    masks = m;
+  }
+  RunArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint16_t*>(kv_pool);
+  a.pool_slots = pool_slots;
+  a.kv_indices = kv_indices;
+  a.masks = masks;
+  a.sm_scale = sm_scale;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
+  a.status = status;
+  int slot = -1;
+  {
+    std::lock_guard<std::mutex> g(g_timing.mu);
+    if (g_timing.n < g_timing.cap) slot = g_timing.n++;
+  }
+  if (slot >= 0) cudaEventRecord(timing_event(slot, 0), st);
+  rc = kernel == VMLA_KERNEL_SIMT ? launch_simt(plan, a, stream) : launch_tc(plan, a, stream);
+  if (rc != VMLA_OK) return rc;
+  if (slot >= 0) {
+    cudaEventRecord(timing_event(slot, 1), st);
+    g_timing.merged[slot] = plan.merge_rows > 0;
+    if (plan.merge_rows > 0) cudaEventRecord(timing_event(slot, 2), st);
+  }
+  rc = launch_merge(plan, a.part_o, a.part_lse, 1, a.out, a.lse, stream);
+  if (slot >= 0 && plan.merge_rows > 0) cudaEventRecord(timing_event(slot, 3), st);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int verify_attn_mla_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_host,
+                         const int32_t* kv_indptr_host, int splits, int num_sms, vmla_plan_info* info,
+                         int32_t* splits_out) {
+  if (!info) return VMLA_ERR_NULL;
+  static thread_local PlanParams plan;
+  int rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, num_sms, &plan, info);
+  if (rc == VMLA_OK && splits_out)
+    for (int b = 0; b < batch; ++b) splits_out[b] = plan.seq[b].n_split;
+  return rc;
+}
+
+int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                   const int32_t* kv_indptr_host, int splits, size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int sms = 0;
+  int rc = current_sm_count(&sms, false);
+  if (rc != VMLA_OK) return rc;
+  vmla_plan_info info;
+  rc = verify_attn_mla_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &info,
+                            nullptr);
+  if (rc != VMLA_OK) return rc;
+  vmla_plan_info info2;
+  rc = verify_attn_mla_plan(VMLA_KERNEL_SIMT, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &info2,
+                            nullptr);
+  if (rc != VMLA_OK) return rc;
+  // one size serves both kernels
+  *bytes = info.workspace_bytes > info2.workspace_bytes ? info.workspace_bytes : info2.workspace_bytes;
+  return VMLA_OK;
+}
+
+int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                    const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                    const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch,
+                    int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return run(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
+             kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
+             workspace_bytes, stream);
+}
+
+int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                         const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
+                         int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return run(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
+             kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
+             workspace_bytes, stream);
+}
+
+int verify_attn_mla_merge(const float* o_parts, const float* lse_parts, int num_splits, int64_t rows, void* out,
+                          float* lse, void* stream) {
+  if (num_splits < 1 || num_splits > 64 || rows < 0 || rows > (INT32_MAX / 64)) return VMLA_ERR_SHAPE;
+  if (rows == 0) return VMLA_OK;
+  if (!o_parts || !lse_parts || !out || !lse) return VMLA_ERR_NULL;
+  if (!aligned(o_parts, 16) || !aligned(out, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
+    return VMLA_ERR_ALIGN;
+  int sms = 0;
+  int rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  // one "sequence" whose rows are the given rows, split num_splits ways
+  static thread_local PlanParams plan;
+  std::memset(&plan, 0, sizeof plan);
+  plan.batch = 1;
+  plan.num_heads = 1;
+  plan.merge_rows = (int32_t)rows;
+  plan.seq[0].n_q = (int32_t)rows;
+  plan.seq[0].n_split = num_splits;
+  plan.seq[0].part_off = 0;
+  plan.seq[0].merge_off = 0;
+  plan.seq[0].q_off = 0;
+  return launch_merge(plan, o_parts, lse_parts, 0, static_cast<uint16_t*>(out), lse, stream);
+}
+
+int verify_attn_mla_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q,
+                              uint64_t* mask_out, uint32_t* status_word, void* stream) {
+  if (batch < 0 || batch > VMLA_MAX_BATCH || total_q < 0) return VMLA_ERR_SHAPE;
+  if (total_q == 0) return VMLA_OK;
+  if (!parent || !qo_indptr || !mask_out) return VMLA_ERR_NULL;
+  if (!aligned(mask_out, 8)) return VMLA_ERR_ALIGN;
+  int sms = 0;
+  int rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  return launch_tree_mask(parent, qo_indptr, batch, total_q, mask_out, status_word, stream);
+}
+
+int verify_attn_mla_check(const void* workspace, void* stream) {
+  if (!workspace) return VMLA_ERR_NULL;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return VMLA_ERR_CUDA;
+  uint32_t word[2] = {0, 0};
+  if (cudaMemcpy(word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return VMLA_ERR_CUDA;
+  return (int)(int32_t)word[0];
+}
+
+int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                     const int32_t* kv_indptr_host, int splits, int has_mask, int has_parent,
+                                     size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, 0, splits);
+  if (rc != VMLA_OK) return rc;
+  size_t ws = 0;
+  rc = verify_attn_mla_workspace_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits, &ws);
+  if (rc != VMLA_OK) return rc;
+  auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
+  const size_t T = (size_t)qo_indptr_host[batch], N = (size_t)kv_indptr_host[batch], B = (size_t)batch;
+  size_t total = up(ws);
+  total += up(T * num_heads * VMLA_D_QK * 2);  // q
+  total += 2 * up((B + 1) * 4);                // indptr arrays
+  total += up(N * 4);                          // kv_indices
+  if (has_mask) total += up(T * 8);
+  if (has_parent) total += up(T * 4);
+  total += up(T * num_heads * VMLA_D_V * 2);   // out
+  total += up(T * num_heads * 4);              // lse
+  *bytes = total;
+  return VMLA_OK;
+}
+
+int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr_host,
+                         const int32_t* kv_indices_host, const int32_t* qo_indptr_host,
+                         const uint64_t* draft_mask_host, const int32_t* parent_host, int batch, int num_heads,
+                         float sm_scale, int splits, void* out_host, float* lse_host, void* device_buffer,
+                         size_t device_buffer_bytes, void* stream) {
+  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
+  if (rc != VMLA_OK) return rc;
+  if (!device_buffer) return VMLA_ERR_NULL;
+  if (!aligned(device_buffer, VMLA_WORKSPACE_ALIGN)) return VMLA_ERR_ALIGN;
+  const size_t T = (size_t)qo_indptr_host[batch], N = (size_t)kv_indptr_host[batch], B = (size_t)batch;
+  if (T > 0 && (!q_host || !kv_indices_host || !out_host || !lse_host || !kv_pool)) return VMLA_ERR_NULL;
+  size_t need = 0;
+  rc = verify_attn_mla_host_buffer_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits,
+                                        draft_mask_host != nullptr, parent_host != nullptr, &need);
+  if (rc != VMLA_OK) return rc;
+  if (device_buffer_bytes < need) return VMLA_ERR_WORKSPACE;
+  size_t ws = 0;
+  rc = verify_attn_mla_workspace_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits, &ws);
+  if (rc != VMLA_OK) return rc;
+  auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
+  char* p = static_cast<char*>(device_buffer);
+  char* d_ws = p;            p += up(ws);
+  char* d_q = p;             p += up(T * num_heads * VMLA_D_QK * 2);
+  char* d_kvp = p;           p += up((B + 1) * 4);
+  char* d_qop = p;           p += up((B + 1) * 4);
+  char* d_kvi = p;           p += up(N * 4);
+  char* d_mask = nullptr;
+  if (draft_mask_host) { d_mask = p; p += up(T * 8); }
+  char* d_par = nullptr;
+  if (parent_host) { d_par = p; p += up(T * 4); }
+  char* d_out = p;           p += up(T * num_heads * VMLA_D_V * 2);
+  char* d_lse = p;           p += up(T * num_heads * 4);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  bool ok = true;
+  ok = ok && cudaMemcpyAsync(d_kvp, kv_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(d_qop, qo_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
+  if (T > 0) {
+    ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, st) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(d_kvi, kv_indices_host, N * 4, h2d, st) == cudaSuccess;
+    if (d_mask) ok = ok && cudaMemcpyAsync(d_mask, draft_mask_host, T * 8, h2d, st) == cudaSuccess;
+    if (d_par) ok = ok && cudaMemcpyAsync(d_par, parent_host, T * 4, h2d, st) == cudaSuccess;
+  }
+  if (!ok) return VMLA_ERR_CUDA;
+  rc = verify_attn_mla(d_q, kv_pool, pool_slots, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
+                       (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
+                       qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream);
+  if (rc != VMLA_OK) return rc;
+  if (T > 0) {
+    ok = ok && cudaMemcpyAsync(out_host, d_out, T * num_heads * VMLA_D_V * 2, d2h, st) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(lse_host, d_lse, T * num_heads * 4, d2h, st) == cudaSuccess;
+  }
+  if (!ok) return VMLA_ERR_CUDA;
+  return verify_attn_mla_check(d_ws, stream);
+}
+
+int verify_attn_mla_timing_enable(int capacity) {
+  std::lock_guard<std::mutex> g(g_timing.mu);
+  for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);
+  g_timing.ev.clear();
+  g_timing.merged.clear();
+  g_timing.cap = 0;
+  g_timing.n = 0;
+  if (capacity <= 0) return VMLA_OK;
+  if (capacity > (1 << 20)) return VMLA_ERR_SHAPE;
+  g_timing.ev.resize((size_t)capacity * 4);
+  g_timing.merged.assign((size_t)capacity, 0);
+  for (auto& e : g_timing.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      return VMLA_ERR_CUDA;
+    }
+  g_timing.cap = capacity;
+  return VMLA_OK;
+}
+
+int verify_attn_mla_timing_read(float* verify_ms, float* merge_ms, int capacity, int* count) {
+  if (!verify_ms || !merge_ms || !count) return VMLA_ERR_NULL;
+  std::lock_guard<std::mutex> g(g_timing.mu);
+  int n = g_timing.n < capacity ? g_timing.n : capacity;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(timing_event(i, 1)) != cudaSuccess) return VMLA_ERR_CUDA;
+    if (cudaEventElapsedTime(&verify_ms[i], timing_event(i, 0), timing_event(i, 1)) != cudaSuccess)
+      return VMLA_ERR_CUDA;
+    merge_ms[i] = 0.f;
+    if (g_timing.merged[i]) {
+      if (cudaEventSynchronize(timing_event(i, 3)) != cudaSuccess) return VMLA_ERR_CUDA;
+      if (cudaEventElapsedTime(&merge_ms[i], timing_event(i, 2), timing_event(i, 3)) != cudaSuccess)
+        return VMLA_ERR_CUDA;
+    }
+  }
+  *count = n;
+  g_timing.n = 0;
+  return VMLA_OK;
+}
+
+const char* verify_attn_mla_status_string(int status) {
+  switch (status) {
+    case VMLA_OK: return "ok";
+    case VMLA_ERR_NULL: return "a required pointer is NULL";
+    case VMLA_ERR_SHAPE: return "sizes out of range or inconsistent indptr arrays";
+    case VMLA_ERR_ALIGN: return "a pointer misses its required alignment";
+    case VMLA_ERR_WORKSPACE: return "workspace too small";
+    case VMLA_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case VMLA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+    case VMLA_ERR_INDEX: return "a kv slot index was outside the pool";
+    case VMLA_ERR_DEVICE: return "no usable sm_103 device";
+    case VMLA_ERR_PARENT: return "a draft parent index was malformed";
+    default: return "unknown status";
+  }
+}
+
+int verify_attn_mla_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vmla_internal.h"
+
+namespace vmla {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// float -> bf16 bits, round to nearest even (finite inputs; NaN stays NaN)
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
+}
+
+// First fault wins: records code and info in the workspace status word.
+__device__ __forceinline__ void record_status(uint32_t* status, int code, uint32_t info) {
+  if (!status) return;
+  if (atomicCAS(status, 0u, (uint32_t)code) == 0u) status[1] = info;
+}
+
+// Visibility word of draft query i when no explicit word is given: bits 0..i.
+__device__ __forceinline__ uint64_t causal_bits(int i) { return ~0ull >> (63 - i); }
+
+// Sequence owning work unit `unit` (largest b with seq[b].unit_start <= unit and rows to do).
+__device__ __forceinline__ int seq_of_unit(const PlanParams& p, int unit) {
+  int lo = 0, hi = p.batch;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (p.seq[mid].unit_start <= unit) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace vmla

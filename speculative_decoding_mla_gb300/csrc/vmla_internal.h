@@ -1,0 +1,89 @@
+// Internal declarations shared by the library's translation units (host and device).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "verify_attn_mla.h"
+
+namespace vmla {
+
+constexpr int kDqk = VMLA_D_QK;
+constexpr int kDv = VMLA_D_V;
+constexpr int kRowBytes = kDqk * 2;  // 1152 bytes per latent KV row / per query head
+
+// Per-sequence entry of a split plan (passed to the kernels by value).
+struct SeqPlan {
+  int32_t kv_off;      // kv_indptr[b]
+  int32_t n_kv;        // N_b keys (prefix + drafts)
+  int32_t q_off;       // qo_indptr[b]
+  int32_t n_q;         // Q_b drafts
+  int32_t unit_start;  // first work unit of this sequence
+  int32_t n_rb;        // row blocks (rows r = i*H + h, in blocks of rows_per_unit)
+  int32_t n_split;     // key-range pieces
+  int32_t chunk;       // keys per piece (piece s covers [s*chunk, min(N_b, (s+1)*chunk)))
+  int32_t part_off;    // first partial row of this sequence (partial row = part_off + s*R_b + r)
+  int32_t merge_off;   // first merge row (monotone over b; only split sequences own merge rows)
+};
+
+struct PlanParams {
+  int32_t batch;
+  int32_t num_heads;
+  int32_t total_units;
+  int32_t merge_rows;
+  int32_t rows_per_unit;
+  int32_t max_splits;
+  int32_t partial_rows;
+  int32_t pad;
+  SeqPlan seq[VMLA_MAX_BATCH];
+};
+
+// Planner knobs of one kernel family.
+struct PlanShape {
+  int rows_per_unit;   // query rows one unit covers
+  int units_per_sm;    // concurrent units per SM (fractional pairs expressed by the caller)
+  int key_align;       // piece boundaries are multiples of this many keys
+  int min_chunk;       // smallest piece the planner chooses on its own
+  int max_splits;
+};
+
+PlanShape plan_shape(int kernel);
+
+// Host planner: fills `pp` and `info`.  Returns a vmla_status.
+int build_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_host,
+               const int32_t* kv_indptr_host, int splits, int num_sms, PlanParams* pp, vmla_plan_info* info);
+
+// Workspace layout (offsets in bytes from the workspace base, each 256 B aligned).
+struct WorkspaceLayout {
+  size_t status_off;  // uint32 status, uint32 info
+  size_t masks_off;   // uint64 [T_q] ancestor masks
+  size_t part_o_off;  // float [partial_rows, 512]
+  size_t part_lse_off;// float [partial_rows]   (log2 domain)
+  size_t total;
+};
+WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows);
+
+// Device-side entry points implemented in the .cu files (launch only; no sync).
+struct RunArgs {
+  const uint16_t* q;
+  const uint16_t* kv;
+  int64_t pool_slots;
+  const int32_t* kv_indices;
+  const uint64_t* masks;  // visibility words per query, or NULL for causal
+  float scale_log2;       // sm_scale * log2(e)
+  float sm_scale;
+  uint16_t* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;  // log2 domain
+  uint32_t* status;
+};
+
+int launch_simt(const PlanParams& plan, const RunArgs& args, void* stream);
+int launch_tc(const PlanParams& plan, const RunArgs& args, void* stream);
+int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
+                 uint16_t* out, float* lse, void* stream);
+int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q, uint64_t* mask_out,
+                     uint32_t* status, void* stream);
+
+}  // namespace vmla

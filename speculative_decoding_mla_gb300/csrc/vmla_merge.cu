@@ -1,0 +1,129 @@
+// Split merge and draft-tree mask expansion.
+//
+// Merge: each split piece s of a query row left a normalised partial output
+// o_s and its log-sum-exp; the row's result is
+//   lse = log sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s,
+// the combination of partial softmaxes that the NSPLIT split-KV of "The Build
+// Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel",
+// implies.  One warp per row; pieces with lse = -inf carry no weight.
+//
+// Tree masks: the q x q visibility matrix of "The Build That Bridged Design
+// and Deployment", section "What This Build Achieves: The paged+bf16 Kernel",
+// for a draft tree is each node's ancestor set plus itself; one thread per
+// draft query walks its parent chain.
+#include <cuda_runtime.h>
+
+#include "vmla_device.cuh"
+
+namespace vmla {
+namespace {
+
+constexpr int kMergeWarps = 8;
+
+__global__ void __launch_bounds__(kMergeWarps * 32)
+merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ part_o,
+             const float* __restrict__ part_lse, int lse_is_log2, uint16_t* __restrict__ out,
+             float* __restrict__ lse) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mrow = blockIdx.x * kMergeWarps + warp;
+  if (mrow >= plan.merge_rows) return;
+  // sequence owning merge row mrow: last b with merge_off <= mrow
+  int lo = 0, hi = plan.batch;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (plan.seq[mid].merge_off <= mrow) lo = mid; else hi = mid;
+  }
+  const SeqPlan& sp = plan.seq[lo];
+  const int H = plan.num_heads;
+  const int R = sp.n_q * H;
+  const int r = mrow - sp.merge_off;
+  const int S = sp.n_split;
+  const float to2 = lse_is_log2 ? 1.f : 1.4426950408889634f;
+  // lse of pieces lane and lane + 32 (S <= 64)
+  float l0 = -INFINITY, l1 = -INFINITY;
+  if (lane < S) l0 = part_lse[(int64_t)sp.part_off + (int64_t)lane * R + r] * to2;
+  if (lane + 32 < S) l1 = part_lse[(int64_t)sp.part_off + (int64_t)(lane + 32) * R + r] * to2;
+  const float M = warp_max(fmaxf(l0, l1));
+  const int64_t orow = (int64_t)sp.q_off * H + r;
+  uint2* dst = reinterpret_cast<uint2*>(out + orow * kDv);
+  if (M == -INFINITY) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dst[c * 32 + lane] = make_uint2(0u, 0u);
+    if (lane == 0) lse[orow] = -INFINITY;
+    return;
+  }
+  const float w0 = exp2f(l0 - M), w1 = exp2f(l1 - M);
+  const float W = warp_sum(w0 + w1);
+  const float invW = 1.f / W;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+    if (ws == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + (int64_t)s * R + r) * kDv);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 v = __ldg(src + c * 32 + lane);
+      acc[4 * c + 0] = fmaf(ws, v.x, acc[4 * c + 0]);
+      acc[4 * c + 1] = fmaf(ws, v.y, acc[4 * c + 1]);
+      acc[4 * c + 2] = fmaf(ws, v.z, acc[4 * c + 2]);
+      acc[4 * c + 3] = fmaf(ws, v.w, acc[4 * c + 3]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    dst[c * 32 + lane] = make_uint2(pack_bf16x2(acc[4 * c] * invW, acc[4 * c + 1] * invW),
+                                    pack_bf16x2(acc[4 * c + 2] * invW, acc[4 * c + 3] * invW));
+  if (lane == 0) lse[orow] = (M + log2f(W)) * 0.6931471805599453f;
+}
+
+__global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ qo_indptr,
+                                 int batch, int total_q, uint64_t* __restrict__ mask_out, uint32_t* status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total_q) return;
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (qo_indptr[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int q0 = qo_indptr[lo];
+  const int n = qo_indptr[lo + 1] - q0;
+  const int i = t - q0;
+  uint64_t bits = 0;
+  int k = i;
+  bool bad = n > VMLA_MAX_DRAFT;
+  for (int steps = 0; k >= 0 && !bad; ++steps) {
+    if (k >= n || steps > VMLA_MAX_DRAFT) { bad = true; break; }
+    bits |= 1ull << k;
+    const int p = parent[q0 + k];
+    if (p >= k || p < -1) { bad = true; break; }
+    k = p;
+  }
+  if (bad) {
+    bits = 0;
+    record_status(status, VMLA_ERR_PARENT, (uint32_t)t);
+  }
+  mask_out[t] = bits;
+}
+
+}  // namespace
+
+int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
+                 uint16_t* out, float* lse, void* stream) {
+  if (plan.merge_rows == 0) return VMLA_OK;
+  const int blocks = (plan.merge_rows + kMergeWarps - 1) / kMergeWarps;
+  merge_kernel<<<blocks, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, lse_is_log2, out,
+                                                                       lse);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q, uint64_t* mask_out,
+                     uint32_t* status, void* stream) {
+  if (total_q == 0) return VMLA_OK;
+  tree_mask_kernel<<<(total_q + 127) / 128, 128, 0, (cudaStream_t)stream>>>(parent, qo_indptr, batch, total_q,
+                                                                             mask_out, status);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+}  // namespace vmla

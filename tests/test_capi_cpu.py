@@ -1,0 +1,125 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared
+symbol, validates arguments before touching a device, and plans splits."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from speculative_decoding_mla_gb300 import build as vbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    vbuild.build()
+    from speculative_decoding_mla_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "verify_attn_mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(verify_attn_mla\w*)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(B):
+    names = declared_functions()
+    assert len(names) >= 10
+    L = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(B.EXPORTS)
+
+
+def test_status_strings(B):
+    assert B.status_string(0) == "ok"
+    for code in range(-9, 0):
+        assert B.status_string(code) != "unknown status"
+    assert B.verify_attn_mla_version() >= 100
+
+
+def _run_raw(B, **kw):
+    args = dict(q=None, kv=None, S=16, kvp=None, kvi=None, qop=None, dm=None, par=None,
+                kvh=np.array([0, 8], np.int32), qoh=np.array([0, 2], np.int32), batch=1, H=4, scale=0.1,
+                splits=0, out=None, lse=None, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    kvh, qoh = args["kvh"], args["qoh"]
+    return B.lib().verify_attn_mla(args["q"], args["kv"], args["S"], args["kvp"], args["kvi"], args["qop"],
+                                   args["dm"], args["par"], kvh.ctypes.data if kvh is not None else None,
+                                   qoh.ctypes.data if qoh is not None else None, args["batch"], args["H"],
+                                   args["scale"], args["splits"], args["out"], args["lse"], args["ws"], args["wsb"],
+                                   args["stream"])
+
+
+def test_argument_errors_before_any_launch(B):
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    good = dict(q=fake, kv=fake, kvp=fake, kvi=fake, qop=fake, out=fake, lse=fake, ws=fake * 2, wsb=1 << 20)
+    assert _run_raw(B, **{**good, "kvh": None}) == B.VMLA_ERR_NULL
+    assert _run_raw(B, **{**good, "ws": None}) == B.VMLA_ERR_NULL
+    assert _run_raw(B, **{**good, "q": None}) == B.VMLA_ERR_NULL
+    assert _run_raw(B, **{**good, "H": 0}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "batch": -1}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "qoh": np.array([0, 65], np.int32), "kvh": np.array([0, 80], np.int32)}) == \
+        B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "qoh": np.array([0, 9], np.int32)}) == B.VMLA_ERR_SHAPE  # drafts > keys
+    assert _run_raw(B, **{**good, "kvh": np.array([1, 8], np.int32)}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "splits": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "q": fake + 2}) == B.VMLA_ERR_ALIGN
+    assert _run_raw(B, **{**good, "ws": fake + 16}) == B.VMLA_ERR_ALIGN
+    # valid arguments on a machine without an sm_103 device
+    import torch
+    if not torch.cuda.is_available():
+        assert _run_raw(B, **good) == B.VMLA_ERR_DEVICE
+
+
+def _plan(B, kernel, prefixes, drafts, H=64, splits=0, sms=152):
+    qo = np.zeros(len(prefixes) + 1, np.int32)
+    qo[1:] = np.cumsum(drafts)
+    kv = np.zeros(len(prefixes) + 1, np.int32)
+    kv[1:] = np.cumsum(np.array(prefixes) + np.array(drafts))
+    info, per = B.verify_attn_mla_plan(kernel, qo, kv, H, splits, sms)
+    return info, per, qo, kv
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_plan_covers_work(B, kernel):
+    rpu = 128 if kernel == 0 else 32
+    for prefixes, drafts in [([185000], [16]), ([4096, 8192, 16384, 32768], [16] * 4), ([1024], [16]),
+                             ([32768] * 8, [64] * 8), ([3, 0, 70000], [1, 0, 4])]:
+        info, per, qo, kv = _plan(B, kernel, prefixes, drafts)
+        units = 0
+        part = 0
+        merge = 0
+        for b in range(len(prefixes)):
+            nq, nk = drafts[b], prefixes[b] + drafts[b]
+            if nq == 0:
+                continue
+            rows = nq * 64
+            s = int(per[b])
+            assert 1 <= s <= 64
+            assert s <= max(1, nk)
+            units += -(-rows // rpu) * s
+            if s > 1:
+                part += rows * s
+                merge += rows
+        assert info.num_units == units
+        assert info.partial_rows == part and info.merge_rows == merge
+        assert info.workspace_bytes >= part * 512 * 4
+
+
+def test_plan_fills_the_gpu_for_one_long_sequence(B):
+    info, per, _, _ = _plan(B, 0, [185000], [16])
+    # 8 row blocks of 128 rows on 76 SM pairs: several key pieces each
+    assert per[0] >= 8 and info.num_units >= 64
+    info, per, _, _ = _plan(B, 0, [185000], [16], splits=3)
+    assert per[0] == 3 and info.num_units == 24
+
+
+def test_plan_rejects_bad_shapes(B):
+    with pytest.raises(B.VmlaError):
+        _plan(B, 0, [10], [65])
+    with pytest.raises(B.VmlaError):
+        B.verify_attn_mla_plan(0, np.array([0, 4], np.int32), np.array([0, 2], np.int32), 64)

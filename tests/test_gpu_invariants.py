@@ -1,0 +1,151 @@
+"""GPU checks of properties, of the merge and mask kernels on their own, of the
+host-buffer entry point, and of the faults kernels report (bad slot index,
+malformed parents) through the workspace status word."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_mla_gb300 import synth
+from tests.test_gpu_parity import compare, run_full, small
+
+pytestmark = pytest.mark.gpu
+
+
+def _mods():
+    import torch
+    from speculative_decoding_mla_gb300 import build as vbuild
+    vbuild.build()
+    from speculative_decoding_mla_gb300 import binding, device
+    return torch, binding, device
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_permuted_pool_bitwise(kernel):
+    case = small("ragged", seed=300)
+    o1, l1, _ = run_full(case, kernel)
+    pi = synth.permutation(7, synth.TAG_AUX, case.pool_slots)
+    pool2 = np.empty_like(case.kv_pool)
+    pool2[pi] = case.kv_pool
+    case2 = synth.Case(name="perm", q=case.q, kv_pool=pool2, kv_indptr=case.kv_indptr,
+                       kv_indices=pi[case.kv_indices].astype(np.int32), qo_indptr=case.qo_indptr,
+                       sm_scale=case.sm_scale)
+    o2, l2, _ = run_full(case2, kernel)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_parent_chain_equals_causal_bitwise(kernel):
+    case = small("ragged", seed=301)
+    o1, l1, _ = run_full(case, kernel)
+    chain = []
+    for b in range(case.batch):
+        n = int(case.qo_indptr[b + 1] - case.qo_indptr[b])
+        chain += list(range(-1, n - 1))
+    case.parent = np.array(chain, np.int32)
+    o2, l2, _ = run_full(case, kernel)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_zero_queries_give_mean():
+    case = small("one_seq", seed=302)
+    case.q[:] = 0
+    ref_o, ref_l = oracle.verify(case)
+    o, l, st = run_full(case, "tc")
+    compare(o, l, ref_o, ref_l, "q = 0")
+
+
+def test_merge_kernel_alone():
+    torch, binding, device = _mods()
+    rng = np.random.default_rng(3)
+    S, R = 7, 300
+    o_parts = rng.normal(size=(S, R, 512)).astype(np.float32)
+    lse_parts = rng.normal(scale=3.0, size=(S, R)).astype(np.float32)
+    lse_parts[2, :50] = -np.inf
+    lse_parts[:, 7] = -np.inf  # a row with every part empty
+    ref_o, ref_l = oracle.merge(o_parts.astype(np.float64), lse_parts.astype(np.float64))
+    out = torch.empty((R, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(R, dtype=torch.float32, device="cuda")
+    binding.verify_attn_mla_merge(torch.from_numpy(o_parts).cuda(), torch.from_numpy(lse_parts).cuda(), out, lse)
+    torch.cuda.synchronize()
+    compare(device.bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_o, ref_l, "merge")
+
+
+def test_tree_mask_kernel_alone():
+    torch, binding, device = _mods()
+    parents = np.concatenate([synth.tree_parents(9, n, 8, s) for s, n in enumerate([64, 1, 17, 40])])
+    qo = np.array([0, 64, 65, 82, 122], np.int32)
+    ref = oracle.tree_masks(parents, qo)
+    out = torch.empty(len(parents), dtype=torch.int64, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    binding.verify_attn_mla_tree_mask(torch.from_numpy(parents).cuda(), torch.from_numpy(qo).cuda(), out, st)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint64), ref)
+    assert int(st[0]) == 0
+
+
+def test_bad_parent_is_reported():
+    torch, binding, device = _mods()
+    case = small("tree", seed=303)
+    case.parent = case.parent.copy()
+    case.parent[5] = 9  # a parent after its child
+    o, l, st = run_full(case, "tc")
+    assert st == binding.VMLA_ERR_PARENT
+
+
+@pytest.mark.parametrize("kernel", ["tc", "simt"])
+def test_bad_slot_index_is_reported(kernel):
+    torch, binding, device = _mods()
+    case = small("one_seq", seed=304)
+    case.kv_indices = case.kv_indices.copy()
+    case.kv_indices[17] = case.pool_slots + 5
+    o, l, st = run_full(case, kernel)
+    assert st == binding.VMLA_ERR_INDEX
+    assert np.all(np.isfinite(l))
+
+
+def test_host_entry_point_matches_device_path():
+    torch, binding, device = _mods()
+    case = small("tree", seed=305)
+    o1, l1, _ = run_full(case, "tc")
+    kv = device.to_device(case).kv_pool
+    T, H = case.q.shape[0], case.num_heads
+    q_h = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    out_h = torch.empty((T, H, 512), dtype=torch.int16).pin_memory()
+    lse_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    kvi_h = torch.from_numpy(case.kv_indices).pin_memory()
+    par_h = torch.from_numpy(case.parent).pin_memory()
+    n = binding.verify_attn_mla_host_buffer_size(case.qo_indptr, case.kv_indptr, H, has_parent=True)
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    binding.verify_attn_mla_host(q_h, kv, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, buf, case.sm_scale,
+                                 parent_host=par_h)
+    o2 = synth.bf16_bits_to_f64(out_h.numpy().view(np.uint16))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, lse_h.numpy().astype(np.float64))
+
+
+def test_empty_batch_and_empty_sequences():
+    torch, binding, device = _mods()
+    case = synth.make_case("empties", [0, 40, 0], [0, 3, 0], num_heads=8, pool_slots=60, seed=306)
+    ref_o, ref_l = oracle.verify(case)
+    o, l, st = run_full(case, "tc")
+    assert st == 0
+    compare(o, l, ref_o, ref_l, "empties")
+    case0 = synth.make_case("none", [], [], num_heads=8, pool_slots=1, seed=307)
+    dc = device.to_device(case0)
+    out, lse = device.alloc_outputs(dc)
+    ws = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    binding.verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
+                            dc.qo_indptr_host, out, lse, ws, dc.sm_scale)
+    assert binding.verify_attn_mla_check(ws) == 0
+
+
+def test_small_workspace_is_rejected():
+    torch, binding, device = _mods()
+    case = small("ragged", seed=308)
+    dc = device.to_device(case)
+    out, lse = device.alloc_outputs(dc)
+    n = binding.verify_attn_mla_workspace_size(dc.qo_indptr_host, dc.kv_indptr_host, dc.num_heads, 7)
+    ws = torch.empty(n // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.VmlaError) as e:
+        binding.verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
+                                dc.qo_indptr_host, out, lse, ws, dc.sm_scale, splits=7)
+    assert e.value.status == binding.VMLA_ERR_WORKSPACE
