@@ -38,6 +38,20 @@ struct PlanParams {
   SeqPlan seq[VMLA_MAX_BATCH];
 };
 
+// Work order of the tensor-core kernel: cluster c processes the units
+// order[start[c] .. start[c+1]) in that order (longest-first greedy balance).
+constexpr int kMaxTcUnits = 3072;
+constexpr int kMaxClusters = 128;
+struct TcSched {
+  int32_t num_clusters;
+  int32_t total_units;
+  uint16_t start[kMaxClusters + 1];
+  uint16_t order[kMaxTcUnits];
+};
+
+// Builds the per-cluster unit lists for a plan (host).  Returns a vmla_status.
+int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched);
+
 // Planner knobs of one kernel family.
 struct PlanShape {
   int rows_per_unit;   // query rows one unit covers
@@ -55,7 +69,7 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_ho
 
 // Workspace layout (offsets in bytes from the workspace base, each 256 B aligned).
 struct WorkspaceLayout {
-  size_t status_off;  // uint32 status, uint32 info
+  size_t status_off;  // uint32 status, uint32 info, 2 spare words
   size_t masks_off;   // uint64 [T_q] ancestor masks
   size_t part_o_off;  // float [partial_rows, 512]
   size_t part_lse_off;// float [partial_rows]   (log2 domain)

@@ -7,6 +7,7 @@
 // and the SM count instead of one global constant.
 #include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "vmla_internal.h"
 
@@ -21,9 +22,10 @@ PlanShape plan_shape(int kernel) {
     s.min_chunk = 256;
     s.max_splits = 64;
   } else {
-    // tensor-core kernel: one unit = 128 query rows on a pair of SMs
+    // tensor-core kernel: one unit = 128 query rows on a pair of SMs (a cluster);
+    // about two units per cluster leave the greedy schedule room to balance
     s.rows_per_unit = 128;
-    s.units_per_sm = 1;  // per pair of SMs; the caller halves the SM count
+    s.units_per_sm = 2;  // per pair of SMs; the caller halves the SM count
     s.key_align = 64;
     s.min_chunk = 1024;
     s.max_splits = 64;
@@ -63,7 +65,7 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   pp->rows_per_unit = sh.rows_per_unit;
 
   // slots: units that run at once
-  int64_t slots = kernel == VMLA_KERNEL_TC ? std::max(1, num_sms / 2) * sh.units_per_sm
+  int64_t slots = kernel == VMLA_KERNEL_TC ? (int64_t)std::max(1, num_sms / 2) * sh.units_per_sm
                                            : (int64_t)num_sms * sh.units_per_sm;
   int64_t total_work = 0;  // (row block) x (keys)
   for (int b = 0; b < batch; ++b) {
@@ -112,6 +114,7 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
     max_s = std::max<int>(max_s, (int)pieces);
   }
   if (unit > INT32_MAX || part > INT32_MAX / kDv) return VMLA_ERR_SHAPE;
+  if (kernel == VMLA_KERNEL_TC && unit > kMaxTcUnits) return VMLA_ERR_SHAPE;
   pp->total_units = (int32_t)unit;
   pp->merge_rows = (int32_t)merge;
   pp->max_splits = max_s;
@@ -123,6 +126,47 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
     info->merge_rows = merge;
     info->workspace_bytes = workspace_layout(qo[batch], part).total;
   }
+  return VMLA_OK;
+}
+
+int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched) {
+  if (!sched || num_clusters < 1) return VMLA_ERR_SHAPE;
+  if (num_clusters > kMaxClusters) num_clusters = kMaxClusters;
+  const int U = plan.total_units;
+  if (U > kMaxTcUnits) return VMLA_ERR_SHAPE;
+  sched->num_clusters = num_clusters;
+  sched->total_units = U;
+  // cost of a unit: its keys plus a fixed charge for filling and draining the pipeline
+  struct Item { int64_t cost; int unit; };
+  std::vector<Item> items;
+  items.reserve(U);
+  for (int b = 0; b < plan.batch; ++b) {
+    const SeqPlan& s = plan.seq[b];
+    for (int piece = 0; piece < s.n_split; ++piece) {
+      const int64_t lo = (int64_t)piece * s.chunk;
+      const int64_t hi = std::min<int64_t>(s.n_kv, lo + s.chunk);
+      for (int rb = 0; rb < s.n_rb; ++rb) items.push_back({(hi - lo) + 256, s.unit_start + piece * s.n_rb + rb});
+    }
+  }
+  // longest first, ties by unit id (deterministic)
+  std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) { return x.cost > y.cost; });
+  std::vector<int64_t> load(num_clusters, 0);
+  std::vector<std::vector<int>> lists(num_clusters);
+  for (const Item& it : items) {
+    int best = 0;
+    for (int c = 1; c < num_clusters; ++c)
+      if (load[c] < load[best]) best = c;
+    load[best] += it.cost;
+    lists[best].push_back(it.unit);
+  }
+  int pos = 0;
+  for (int c = 0; c < num_clusters; ++c) {
+    sched->start[c] = (uint16_t)pos;
+    // within a cluster, units of the same piece next to each other keep KV reuse in L2
+    std::sort(lists[c].begin(), lists[c].end());
+    for (int u : lists[c]) sched->order[pos++] = (uint16_t)u;
+  }
+  sched->start[num_clusters] = (uint16_t)pos;
   return VMLA_OK;
 }
 
