@@ -237,6 +237,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     const int r = ui.rb * kRowsTC + row;
     const bool valid = r < ui.R;
     // Q rows of this unit into TMEM columns 0..287 (two bf16 per column)
+    __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
@@ -268,6 +269,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       // a failed wait leaves garbage in this tile; the group still meets at every
       // barrier below and stops together at the end of the tile
       wait_bar(sm, &sm.sfull[s], ph, a.status, 300);
+      __syncwarp();
       tc_fence_after();
       uint32_t v[64];
       tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -462,11 +464,13 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     named_bar_sync(2, 128);
     const uint32_t cmd = sm.wg_cmd;
     if ((cmd & 0xFF) == kCmdExit) return;
+    __syncwarp();
     tc_fence_after();
+    // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform
     if ((cmd & 0xFF) == kCmdRescale) {
       const int s = (cmd >> 8) & 1;
       const float alpha = sm.msg[s].alpha[row];
-      if (alpha != 1.f) {
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < kDv / 32; ++c) {
           uint32_t v[32];
@@ -485,17 +489,18 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const int f = uu & 1;
       const float m = sm.fin[f].m[row], lsum = sm.fin[f].l[row];
       const int r = ui.rb * kRowsTC + row;
-      if (r < ui.R) {
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
-        if (sp.n_split == 1) {
-          const int64_t orow = (int64_t)sp.q_off * H + r;
-          uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kDv);
+      const bool valid = r < ui.R;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
+      if (sp.n_split == 1) {
+        const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kDv);
 #pragma unroll 1
-          for (int c = 0; c < kDv / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
-            tmem_wait_ld();
+        for (int c = 0; c < kDv / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_wait_ld();
+          if (valid) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               dst[c * 4 + k] = make_uint4(
@@ -504,22 +509,26 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
                   pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
           }
-          a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
-        } else {
-          const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + r;
-          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDv);
+          __syncwarp();
+        }
+        if (valid) a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
+      } else {
+        const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + (valid ? r : 0);
+        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDv);
 #pragma unroll 1
-          for (int c = 0; c < kDv / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
-            tmem_wait_ld();
+        for (int c = 0; c < kDv / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_wait_ld();
+          if (valid) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               dst[c * 8 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
                                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
           }
-          a.part_lse[prow] = lse2;
+          __syncwarp();
         }
+        if (valid) a.part_lse[prow] = lse2;
       }
       ++uu;
       ++ui_idx;
@@ -567,6 +576,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     fence_mbar_init();
     prefetch_tensormap(&kv_map);
   }
+  __syncwarp();
   if (warp == 0) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
@@ -578,6 +588,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     for (int s = 0; s < 2 && s < total; ++s) mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
     for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&sm.finfull[s], sizeof(Finals));
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -598,11 +609,14 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   } else if (lane == 0 && rank == 1) {
     mixer_release_role(sm, plan, sched, a, u_begin, u_end);
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
   // neither CTA leaves while the other may still address its shared memory
   cluster_arrive();
   cluster_wait();
+  __syncwarp();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
