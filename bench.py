@@ -293,10 +293,10 @@ def run_ours(args, rank, local, world):
     barrier(world)
     clocks = sampler.stop()
     step_ms_total = ev0.elapsed_time(ev1)
-    verify_ms, merge_ms = binding.verify_attn_mla_timing_read(args.steps)
+    gather_ms, verify_ms, merge_ms = binding.verify_attn_mla_timing_read(args.steps)
     binding.verify_attn_mla_timing_enable(0)
 
-    kernel_ms = float(verify_ms.mean() + merge_ms.mean())  # verify + merge per step, excluding the L2 flush
+    kernel_ms = float(gather_ms.mean() + verify_ms.mean() + merge_ms.mean())  # per step, excluding the L2 flush
     if flush_buf is None:
         step_ms = step_ms_total / args.steps
     else:
@@ -342,7 +342,8 @@ def run_ours(args, rank, local, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample, spent = cpu_oracle_sample(case, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "KV tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
-    launches_per_step = 1 + (1 if float(merge_ms.max()) > 0 else 0) + (1 if case.parent is not None else 0)
+    launches_per_step = (1 + (1 if float(merge_ms.max()) > 0 else 0) + (1 if float(gather_ms.max()) > 0 else 0)
+                         + (1 if case.parent is not None else 0))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world, "steps": args.steps,
@@ -359,7 +360,7 @@ def run_ours(args, rank, local, world):
                          "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"], "traffic": None,
                          "kernel": "verify", "peak_source": f"{peaks['source']} dense bf16 burst",
                          "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-                         "verify_ms": v_ms, "merge_ms": float(merge_ms.mean()),
+                         "verify_ms": v_ms, "merge_ms": float(merge_ms.mean()), "gather_ms": float(gather_ms.mean()),
                          "roofline_ms": max(flops / (peaks["bf16_tflops"] * 1e12),
                                             nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e3},
             "roofline_frac_step": max(flops / (peaks["bf16_tflops"] * 1e12),

@@ -97,8 +97,12 @@ int verify_attn_mla_plan(int kernel, int batch, int num_heads, const int32_t* qo
 int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
                                    const int32_t* kv_indptr_host, int splits, size_t* bytes);
 
-/* The verify attention (tensor-core kernel, plus the merge kernel when a
- * sequence is split, plus the mask-expansion kernel when `parent` is given).
+/* The verify attention.  In stream order: the mask-expansion kernel when
+ * `parent` is given; a gather kernel that copies every sequence's KV rows
+ * (through kv_indices) into a contiguous area of the workspace, the
+ * defragmentation step of "The Build That Unlocked 3-6x Decode Speedup",
+ * section "The Context: A Custom Kernel for an Unsupported Architecture";
+ * the tensor-core kernel; the merge kernel when a sequence is split.
  *   q           [T_q, H, 576] bf16, T_q = qo_indptr_host[batch]; 16 B aligned
  *   kv_pool     [pool_slots, 576] bf16 row-major (row stride 1152 B); 16 B aligned
  *   kv_indptr   [batch+1] int32; sequence b owns kv_indices[kv_indptr[b] .. kv_indptr[b+1])
@@ -115,7 +119,8 @@ int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_i
  *   splits      0 = planner's choice; k > 0 forces k pieces per sequence
  *   out         [T_q, H, 512] bf16 (16 B aligned);  lse [T_q, H] fp32
  *   workspace   >= verify_attn_mla_workspace_size() bytes, 256 B aligned.
- *               Holds the status word, ancestor masks and split partials.
+ *               Holds the status word, ancestor masks, split partials and a
+ *               contiguous copy of the gathered KV rows (1152 B per key).
  *               Calls that share a workspace must be ordered on one stream.
  * No host synchronisation and no allocation happen inside the call. */
 int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
@@ -176,14 +181,14 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
 /* Measurement aid.  verify_attn_mla_timing_enable(n) creates host-side CUDA
  * events for the next n run calls (0 turns it off and frees them); while it is
  * on, every verify_attn_mla / verify_attn_mla_simt call records events on its
- * stream around the verify kernel and around the merge kernel.
- * verify_attn_mla_timing_read() waits for those events and writes, per call in
- * launch order, the verify kernel's and the merge kernel's device time in ms
- * (merge_ms = 0 when no merge ran) into arrays of `capacity` entries, sets
+ * stream around each kernel it launches.  verify_attn_mla_timing_read() waits
+ * for those events and writes, per call in launch order, the device time in ms
+ * of the KV gather kernel, the verify kernel and the merge kernel (0 for a
+ * kernel the call did not launch) into arrays of `capacity` entries, sets
  * *count, and starts a new recording.  Not for concurrent use from several
  * host threads. */
 int verify_attn_mla_timing_enable(int capacity);
-int verify_attn_mla_timing_read(float* verify_ms, float* merge_ms, int capacity, int* count);
+int verify_attn_mla_timing_read(float* gather_ms, float* verify_ms, float* merge_ms, int capacity, int* count);
 
 /* Human-readable name of a status code (static string). */
 const char* verify_attn_mla_status_string(int status);

@@ -70,7 +70,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_status_string": [i32],
         "verify_attn_mla_version": [],
         "verify_attn_mla_timing_enable": [i32],
-        "verify_attn_mla_timing_read": [vp, vp, i32, ctypes.POINTER(i32)],
+        "verify_attn_mla_timing_read": [vp, vp, vp, i32, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -219,10 +219,11 @@ def verify_attn_mla_timing_enable(capacity: int):
 
 
 def verify_attn_mla_timing_read(capacity: int):
-    """(verify_ms, merge_ms) arrays of the recorded calls, in launch order."""
+    """(gather_ms, verify_ms, merge_ms) arrays of the recorded calls, in launch order."""
+    g = np.zeros(max(capacity, 1), np.float32)
     v = np.zeros(max(capacity, 1), np.float32)
     m = np.zeros(max(capacity, 1), np.float32)
     n = ctypes.c_int(0)
-    _check(_lib.verify_attn_mla_timing_read(v.ctypes.data, m.ctypes.data, int(capacity), ctypes.byref(n)),
-           "verify_attn_mla_timing_read")
-    return v[: n.value].copy(), m[: n.value].copy()
+    _check(_lib.verify_attn_mla_timing_read(g.ctypes.data, v.ctypes.data, m.ctypes.data, int(capacity),
+                                            ctypes.byref(n)), "verify_attn_mla_timing_read")
+    return g[: n.value].copy(), v[: n.value].copy(), m[: n.value].copy()

@@ -36,12 +36,12 @@ struct Timing {
   std::mutex mu;
   int cap = 0;
   int n = 0;
-  std::vector<cudaEvent_t> ev;  // 4 per call: verify begin/end, merge begin/end
+  std::vector<cudaEvent_t> ev;  // 6 per call: verify begin/end, merge begin/end, gather begin/end
   std::vector<char> merged;
 };
 Timing g_timing;
 
-cudaEvent_t timing_event(int call, int k) { return g_timing.ev[(size_t)call * 4 + k]; }
+cudaEvent_t timing_event(int call, int k) { return g_timing.ev[(size_t)call * 6 + k]; }
 
 int current_sm_count(int* sms, bool require_sm103) {
   int dev = 0;
@@ -77,7 +77,7 @@ int run(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, cons
   rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &plan, &info);
   if (rc != VMLA_OK) return rc;
   if (workspace_bytes < info.workspace_bytes) return VMLA_ERR_WORKSPACE;
-  const WorkspaceLayout L = workspace_layout(total_q, info.partial_rows);
+  const WorkspaceLayout L = workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC ? total_kv : 0);
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
   cudaStream_t st = (cudaStream_t)stream;
@@ -103,18 +103,28 @@ int run(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, cons
   a.lse = lse;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
+  a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
+  a.total_kv = total_kv;
   a.status = status;
   int slot = -1;
   {
     std::lock_guard<std::mutex> g(g_timing.mu);
     if (g_timing.n < g_timing.cap) slot = g_timing.n++;
   }
+  if (kernel == VMLA_KERNEL_TC) {
+    // KV rows of every sequence gathered once into a contiguous staging area, so
+    // that the verify kernel streams them with tiled TMA loads
+    if (slot >= 0) cudaEventRecord(timing_event(slot, 4), st);
+    rc = launch_gather(a, stream);
+    if (rc != VMLA_OK) return rc;
+    if (slot >= 0) cudaEventRecord(timing_event(slot, 5), st);
+  }
   if (slot >= 0) cudaEventRecord(timing_event(slot, 0), st);
   rc = kernel == VMLA_KERNEL_SIMT ? launch_simt(plan, a, stream) : launch_tc(plan, a, stream);
   if (rc != VMLA_OK) return rc;
   if (slot >= 0) {
     cudaEventRecord(timing_event(slot, 1), st);
-    g_timing.merged[slot] = plan.merge_rows > 0;
+    g_timing.merged[slot] = (char)((plan.merge_rows > 0 ? 1 : 0) | (kernel == VMLA_KERNEL_TC ? 2 : 0));
     if (plan.merge_rows > 0) cudaEventRecord(timing_event(slot, 2), st);
   }
   rc = launch_merge(plan, a.part_o, a.part_lse, 1, a.out, a.lse, stream);
@@ -308,7 +318,7 @@ int verify_attn_mla_timing_enable(int capacity) {
   g_timing.n = 0;
   if (capacity <= 0) return VMLA_OK;
   if (capacity > (1 << 20)) return VMLA_ERR_SHAPE;
-  g_timing.ev.resize((size_t)capacity * 4);
+  g_timing.ev.resize((size_t)capacity * 6);
   g_timing.merged.assign((size_t)capacity, 0);
   for (auto& e : g_timing.ev)
     if (cudaEventCreate(&e) != cudaSuccess) {
@@ -319,20 +329,20 @@ int verify_attn_mla_timing_enable(int capacity) {
   return VMLA_OK;
 }
 
-int verify_attn_mla_timing_read(float* verify_ms, float* merge_ms, int capacity, int* count) {
-  if (!verify_ms || !merge_ms || !count) return VMLA_ERR_NULL;
+int verify_attn_mla_timing_read(float* gather_ms, float* verify_ms, float* merge_ms, int capacity, int* count) {
+  if (!gather_ms || !verify_ms || !merge_ms || !count) return VMLA_ERR_NULL;
   std::lock_guard<std::mutex> g(g_timing.mu);
   int n = g_timing.n < capacity ? g_timing.n : capacity;
+  auto elapsed = [](float* out, int call, int k0, int k1) {
+    if (cudaEventSynchronize(timing_event(call, k1)) != cudaSuccess) return false;
+    return cudaEventElapsedTime(out, timing_event(call, k0), timing_event(call, k1)) == cudaSuccess;
+  };
   for (int i = 0; i < n; ++i) {
-    if (cudaEventSynchronize(timing_event(i, 1)) != cudaSuccess) return VMLA_ERR_CUDA;
-    if (cudaEventElapsedTime(&verify_ms[i], timing_event(i, 0), timing_event(i, 1)) != cudaSuccess)
-      return VMLA_ERR_CUDA;
+    if (!elapsed(&verify_ms[i], i, 0, 1)) return VMLA_ERR_CUDA;
     merge_ms[i] = 0.f;
-    if (g_timing.merged[i]) {
-      if (cudaEventSynchronize(timing_event(i, 3)) != cudaSuccess) return VMLA_ERR_CUDA;
-      if (cudaEventElapsedTime(&merge_ms[i], timing_event(i, 2), timing_event(i, 3)) != cudaSuccess)
-        return VMLA_ERR_CUDA;
-    }
+    gather_ms[i] = 0.f;
+    if ((g_timing.merged[i] & 1) && !elapsed(&merge_ms[i], i, 2, 3)) return VMLA_ERR_CUDA;
+    if ((g_timing.merged[i] & 2) && !elapsed(&gather_ms[i], i, 4, 5)) return VMLA_ERR_CUDA;
   }
   *count = n;
   g_timing.n = 0;

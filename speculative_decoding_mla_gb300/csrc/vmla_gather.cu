@@ -1,0 +1,70 @@
+// KV gather ("defragmentation"): copies every sequence's KV rows, read through
+// kv_indices at page_size = 1, into one contiguous [total_kv, 576] bf16 area of
+// the workspace, in sequence order.  Scattered 1152-byte rows are fetched once
+// here, so the tensor-core kernel streams contiguous 64-row tiles with tiled
+// TMA loads instead of row-by-row gathers.  This is the compaction of scattered
+// page_size = 1 slots into contiguous runs that "The Build That Unlocked 3-6x
+// Decode Speedup" names as the plan's next phase (section "The Context: A
+// Custom Kernel for an Unsupported Architecture"), done per call.
+//
+// One warp per row: lane l moves 16-byte granules l, l+32 and l+64 (< 72), so
+// every warp instruction reads and writes 512 contiguous bytes.  A slot outside
+// [0, pool_slots) records VMLA_ERR_INDEX and stages a zero row.
+#include <cuda_runtime.h>
+
+#include "vmla_device.cuh"
+
+namespace vmla {
+namespace {
+
+constexpr int kGatherWarps = 8;
+constexpr int kRowU4 = kRowBytes / 16;  // 72
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int32_t* __restrict__ kv_indices,
+                   int64_t total_kv, uint4* __restrict__ staged, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kGatherWarps;
+  for (int64_t j = warp0; j < total_kv; j += nwarps) {
+    const int32_t slot = kv_indices[j];
+    const bool ok = slot >= 0 && (int64_t)slot < pool_slots;
+    if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)j);
+    const uint4* src = pool + (int64_t)(ok ? slot : 0) * kRowU4;
+    uint4* dst = staged + j * kRowU4;
+    uint4 v0 = ok ? ld_stream(src + lane) : make_uint4(0, 0, 0, 0);
+    uint4 v1 = ok ? ld_stream(src + lane + 32) : make_uint4(0, 0, 0, 0);
+    uint4 v2 = make_uint4(0, 0, 0, 0);
+    if (lane < kRowU4 - 64 && ok) v2 = ld_stream(src + lane + 64);
+    dst[lane] = v0;
+    dst[lane + 32] = v1;
+    if (lane < kRowU4 - 64) dst[lane + 64] = v2;
+  }
+}
+
+}  // namespace
+
+int launch_gather(const RunArgs& a, void* stream) {
+  if (a.total_kv == 0) return VMLA_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return VMLA_ERR_CUDA;
+  const int64_t need = (a.total_kv + kGatherWarps - 1) / kGatherWarps;
+  const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM keep enough rows in flight
+  const int blocks = (int)(need < cap ? need : cap);
+  gather_rows_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_indices, a.total_kv, reinterpret_cast<uint4*>(a.staged),
+      a.status);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+}  // namespace vmla

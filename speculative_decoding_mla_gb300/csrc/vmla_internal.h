@@ -73,9 +73,10 @@ struct WorkspaceLayout {
   size_t masks_off;   // uint64 [T_q] ancestor masks
   size_t part_o_off;  // float [partial_rows, 512]
   size_t part_lse_off;// float [partial_rows]   (log2 domain)
+  size_t staged_off;  // bf16 [staged_rows, 576]: every sequence's KV rows, contiguous (tensor-core kernel)
   size_t total;
 };
-WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows);
+WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows);
 
 // Device-side entry points implemented in the .cu files (launch only; no sync).
 struct RunArgs {
@@ -90,11 +91,14 @@ struct RunArgs {
   float* lse;
   float* part_o;
   float* part_lse;  // log2 domain
+  uint16_t* staged; // contiguous copy of the gathered KV rows, [total_kv, 576] (tensor-core kernel)
+  int64_t total_kv;
   uint32_t* status;
 };
 
 int launch_simt(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_tc(const PlanParams& plan, const RunArgs& args, void* stream);
+int launch_gather(const RunArgs& args, void* stream);
 int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
                  uint16_t* out, float* lse, void* stream);
 int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q, uint64_t* mask_out,

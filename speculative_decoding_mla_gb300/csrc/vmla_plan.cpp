@@ -35,14 +35,15 @@ PlanShape plan_shape(int kernel) {
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows) {
+WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   WorkspaceLayout w;
   w.status_off = 0;
   w.masks_off = up(16);
   w.part_o_off = w.masks_off + up((size_t)total_q * 8);
   w.part_lse_off = w.part_o_off + up((size_t)partial_rows * kDv * 4);
-  w.total = w.part_lse_off + up((size_t)partial_rows * 4);
+  w.staged_off = w.part_lse_off + up((size_t)partial_rows * 4);
+  w.total = w.staged_off + up((size_t)staged_rows * kRowBytes);
   return w;
 }
 
@@ -124,7 +125,7 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
     info->max_splits = max_s;
     info->partial_rows = part;
     info->merge_rows = merge;
-    info->workspace_bytes = workspace_layout(qo[batch], part).total;
+    info->workspace_bytes = workspace_layout(qo[batch], part, kernel == VMLA_KERNEL_TC ? kv[batch] : 0).total;
   }
   return VMLA_OK;
 }

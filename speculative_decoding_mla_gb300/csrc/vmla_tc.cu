@@ -130,16 +130,14 @@ __device__ __forceinline__ int clamp_slot(int32_t slot, int64_t pool_slots, uint
   return slot;
 }
 
-// ------------------------------------------------------------------ producer (warp 0, both CTAs)
-// Gathers each 64-key tile of the unit's key range through kv_indices with
-// tile::gather4 (4 rows x 64 columns per copy, 9 or 8 column chunks).  Lane 0
-// takes every wait and every stop decision and the warp follows it, so the
-// warp never diverges around its shuffles.
+// ------------------------------------------------------------------ producer (warp 0, lane 0, both CTAs)
+// Loads each 64-key tile of the unit's key range from the contiguous staged
+// copy of the KV rows: one 64-row x 64-column box (8 KB, 128-byte swizzle) per
+// column chunk, 9 chunks for the scorer (K), 8 for the mixer (V).  Rows past
+// the piece's end belong to other keys and are masked by the softmax.
 __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
                               const RunArgs& a, int u_begin, int u_end, int nch) {
-  const int lane = threadIdx.x & 31;
   int it = 0;
-  const int g = lane & 15;
   bool ok = true;
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
@@ -147,38 +145,24 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
     for (int t = 0; t < ui.n_tiles; ++t) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      int go = 1;
-      if (lane == 0) go = wait_bar(sm, &sm.kfree[s], ph ^ 1, a.status, 100) ? 1 : 0;
-      go = __shfl_sync(0xffffffffu, go, 0);
-      if (!go) {
+      if (!wait_bar(sm, &sm.kfree[s], ph ^ 1, a.status, 100)) {
         ok = false;
         break;
       }
-      const int key0 = ui.k_lo + t * kTileKeys;
-      const int ka = key0 + 2 * lane, kb = ka + 1;
-      int sa = (int)a.pool_slots, sb = (int)a.pool_slots;
-      if (ka < ui.k_hi) sa = clamp_slot(a.kv_indices[sp.kv_off + ka], a.pool_slots, a.status, sp.kv_off + ka);
-      if (kb < ui.k_hi) sb = clamp_slot(a.kv_indices[sp.kv_off + kb], a.pool_slots, a.status, sp.kv_off + kb);
-      if (lane == 0) mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
-      __syncwarp();
-      const int y0 = __shfl_sync(0xffffffffu, sa, 2 * g), y1 = __shfl_sync(0xffffffffu, sb, 2 * g);
-      const int y2 = __shfl_sync(0xffffffffu, sa, 2 * g + 1), y3 = __shfl_sync(0xffffffffu, sb, 2 * g + 1);
+      const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
+      mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
       const uint32_t bar = smem_u32(&sm.kfull[s]);
-      for (int c = lane >> 4; c < nch; c += 2)
-        tma_gather4(smem_u32(&sm.kv[s][c][0]) + g * 512, map, 64 * c, y0, y1, y2, y3, bar);
+      for (int c = 0; c < nch; ++c) tma_load_2d(smem_u32(&sm.kv[s][c][0]), map, 64 * c, y, bar);
       ++it;
     }
   }
   // drain: the loads of the last two stages have landed before the CTA may exit
-  if (lane == 0) {
-    for (int k = 1; k <= 2 && it - k >= 0; ++k) {
-      const int j = it - k;
-      long long t0 = clock64();
-      while (!mbar_try_wait(&sm.kfull[j & 1], (j >> 1) & 1) && clock64() - t0 < kWaitCycles) {
-      }
+  for (int k = 1; k <= 2 && it - k >= 0; ++k) {
+    const int j = it - k;
+    long long t0 = clock64();
+    while (!mbar_try_wait(&sm.kfull[j & 1], (j >> 1) & 1) && clock64() - t0 < kWaitCycles) {
     }
   }
-  __syncwarp();
 }
 
 // ------------------------------------------------------------------ CTA 0: QK^T issuer (warp 1, lane 0)
@@ -597,7 +581,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const uint32_t tbase = sm.tmem_base;
 
   if (warp == 0) {
-    producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks);
+    if (lane == 0) producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
@@ -691,13 +675,13 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   static thread_local TcSched sched;
   rc = build_tc_schedule(plan, clusters, &sched);
   if (rc != VMLA_OK) return rc;
-  // 2-D map over the pool [pool_slots rows x 576 bf16], boxes of 64 columns x 1 row, 128-byte swizzle
+  // 2-D map over the staged rows [total_kv x 576 bf16], boxes of 64 columns x 64 rows, 128-byte swizzle
   CUtensorMap map;
-  cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(a.pool_slots > 0 ? a.pool_slots : 1)};
+  cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(a.total_kv > 0 ? a.total_kv : 1)};
   cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  cuuint32_t box[2] = {64, 1};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
   cuuint32_t estride[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.kv), gdim, gstride, box, estride,
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, box, estride,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return VMLA_ERR_CUDA;
