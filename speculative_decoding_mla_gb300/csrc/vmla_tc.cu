@@ -49,6 +49,7 @@ constexpr int kThreadsTC = 224;
 constexpr uint32_t kSCol = 384;      // S buffers at TMEM columns 384 and 448 (Q uses 0..287)
 constexpr float kTau = 8.0f;         // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr int kPrefetchTiles = 6;  // tiles the scorer's producer prefetches into L2 ahead of its loads
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
@@ -122,26 +123,27 @@ __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ int clamp_slot(int32_t slot, int64_t pool_slots, uint32_t* status, int where) {
-  if (slot < 0 || (int64_t)slot >= pool_slots) {
-    record_status(status, VMLA_ERR_INDEX, (uint32_t)where);
-    return (int)pool_slots;  // past the end: the TMA fills the row with zeros
-  }
-  return slot;
-}
-
 // ------------------------------------------------------------------ producer (warp 0, lane 0, both CTAs)
 // Loads each 64-key tile of the unit's key range from the contiguous staged
 // copy of the KV rows: one 64-row x 64-column box (8 KB, 128-byte swizzle) per
 // column chunk, 9 chunks for the scorer (K), 8 for the mixer (V).  Rows past
 // the piece's end belong to other keys and are masked by the softmax.
 __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
-                              const RunArgs& a, int u_begin, int u_end, int nch) {
+                              const RunArgs& a, int u_begin, int u_end, int nch, bool prefetch) {
   int it = 0;
   bool ok = true;
+  // L2 prefetch of the staged rows of tile t (contiguous: 64 rows x 1152 bytes), clamped to the staged area
+  auto prefetch_tile = [&](const SeqPlan& sp, const UnitInfo& ui, int t) {
+    if (!prefetch || t >= ui.n_tiles) return;
+    const int64_t row0 = (int64_t)sp.kv_off + ui.k_lo + (int64_t)t * kTileKeys;
+    int64_t rows = a.total_kv - row0;
+    if (rows > kTileKeys) rows = kTileKeys;
+    if (rows > 0) prefetch_l2_bulk(a.staged + row0 * kDqk, (uint32_t)(rows * kRowBytes));
+  };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
+    for (int t = 0; t < kPrefetchTiles && t < ui.n_tiles; ++t) prefetch_tile(sp, ui, t);
     for (int t = 0; t < ui.n_tiles; ++t) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -153,6 +155,7 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
       mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
       const uint32_t bar = smem_u32(&sm.kfull[s]);
       for (int c = 0; c < nch; ++c) tma_load_2d(smem_u32(&sm.kv[s][c][0]), map, 64 * c, y, bar);
+      prefetch_tile(sp, ui, t + kPrefetchTiles);
       ++it;
     }
   }
@@ -581,7 +584,8 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const uint32_t tbase = sm.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks);
+    if (lane == 0)
+      producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks, rank == 0);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
