@@ -53,6 +53,24 @@ constexpr int kPrefetchTiles = 6;  // tiles the scorer's producer prefetches int
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
+// Optional pipeline trace (compile with -DVMLA_TRACE): global-timer stamps of
+// each hand-off for the first kTraceTiles tiles of cluster 0.
+#ifdef VMLA_TRACE
+constexpr int kTraceTiles = 256;
+constexpr int kTraceEvents = 12;
+__device__ uint64_t g_vmla_trace[kTraceEvents * kTraceTiles];
+__device__ __forceinline__ void vtrace(int ev, int tile) {
+  if (cluster_id_x() == 0 && tile < kTraceTiles) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_vmla_trace[ev * kTraceTiles + tile] = t;
+  }
+}
+#define VTRACE(ev, tile) vtrace(ev, tile)
+#else
+#define VTRACE(ev, tile) ((void)0)
+#endif
+
 struct __align__(1024) PMsg {
   uint8_t p[kRowsTC * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
   float alpha[kRowsTC];      // factor for O rows before this tile's product (1 = unchanged)
@@ -151,6 +169,7 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
         ok = false;
         break;
       }
+      VTRACE(prefetch ? 0 : 6, it);
       const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
       mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
       const uint32_t bar = smem_u32(&sm.kfull[s]);
@@ -181,10 +200,16 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 201) || !wait_bar(sm, &sm.sfree[s], ph ^ 1, a.status, 202)) {
+      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 201)) {
         ok = false;
         break;
       }
+      VTRACE(1, it);
+      if (!wait_bar(sm, &sm.sfree[s], ph ^ 1, a.status, 202)) {
+        ok = false;
+        break;
+      }
+      VTRACE(2, it);
       tc_fence_after();
       const uint32_t d = tbase + kSCol + (uint32_t)s * kTileKeys;
 #pragma unroll
@@ -256,6 +281,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       // a failed wait leaves garbage in this tile; the group still meets at every
       // barrier below and stops together at the end of the tile
       wait_bar(sm, &sm.sfull[s], ph, a.status, 300);
+      if (tid == 0) VTRACE(3, it);
       __syncwarp();
       tc_fence_after();
       uint32_t v[64];
@@ -307,6 +333,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
 
       const int ms = it & 1;  // message slot (one message per tile)
       const bool last = t == ui.n_tiles - 1;
+      if (tid == 0) VTRACE(4, it);
       if (tid == 0 && it >= 2) bulk_wait_group_read<1>();
       named_bar_sync(1, 128);
       // P row -> staging, 128-byte swizzle (16-byte granule k of row `row` at k ^ (row & 7))
@@ -332,6 +359,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
           go = wait_bar(sm, &sm.pfree[ms], ((it >> 1) & 1) ^ 1, a.status, 301, true);
         }
         if (go) {
+          VTRACE(5, it);
           bulk_s2s_cluster(peer_msg[ms], smem_u32(&sm.msg[ms]), kMsgBytes, peer_pfull[ms]);
           if (last)
             bulk_s2s_cluster(mapa(smem_u32(&sm.fin[uu & 1]), 1), smem_u32(&sm.fin_stage[uu & 1]), sizeof(Finals),
@@ -375,10 +403,16 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 400) || !wait_bar(sm, &sm.pfull[s], ph, a.status, 401, true)) {
+      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 400)) {
         ok = false;
         break;
       }
+      VTRACE(7, it);
+      if (!wait_bar(sm, &sm.pfull[s], ph, a.status, 401, true)) {
+        ok = false;
+        break;
+      }
+      VTRACE(8, it);
       if (t > 0 && (sm.msg[s].flags & 1u)) {
         if (!quiesce() || !command(kCmdRescale | ((uint32_t)s << 8))) {
           ok = false;
@@ -398,6 +432,7 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
       }
       mma_commit(&sm.kfree[s]);
       mma_commit(&sm.pdone[s]);
+      VTRACE(9, it);
     }
     if (!ok) break;
     if (!quiesce() || !command(kCmdEpilogue)) ok = false;
@@ -416,6 +451,7 @@ __device__ void mixer_release_role(TcSmem& sm, const PlanParams& plan, const TcS
   for (int n = 0; n < total; ++n) {
     const int s = n & 1;
     if (!wait_bar(sm, &sm.pdone[s], (n >> 1) & 1, a.status, 500)) return;
+    VTRACE(10, n);
     if (n + 2 < total) {
       mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
       mbar_arrive_remote(peer_pfree[s]);
@@ -706,3 +742,15 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
 }
 
 }  // namespace vmla
+
+#ifdef VMLA_TRACE
+extern "C" int vmla_trace_read(uint64_t* host, int n) {
+  const int total = vmla::kTraceEvents * vmla::kTraceTiles;
+  if (n > total) n = total;
+  return cudaMemcpyFromSymbol(host, vmla::g_vmla_trace, sizeof(uint64_t) * n) == cudaSuccess ? n : -1;
+}
+extern "C" int vmla_trace_clear(void) {
+  static uint64_t zeros[vmla::kTraceEvents * vmla::kTraceTiles] = {};
+  return cudaMemcpyToSymbol(vmla::g_vmla_trace, zeros, sizeof zeros) == cudaSuccess ? 0 : -1;
+}
+#endif
