@@ -22,8 +22,9 @@
 // The split of the work follows from tensor-memory capacity: O for 128 rows
 // fills one SM's 512 TMEM columns, so Q and S live on the partner SM.
 //
-// Warp roles (224 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5
-// softmax (CTA 0) or rescale/epilogue (CTA 1), warp 6 P-slot release (CTA 1).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer; CTA 0:
+// warps 2-9 softmax, two threads per row (each 32 of the tile's 64 keys);
+// CTA 1: warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
 // status word, tells the partner CTA to stop, drains its own copies and MMAs,
 // frees tensor memory and returns.
@@ -45,7 +46,7 @@ constexpr int kVChunks = kDv / 64;   // 8 of them are the latent / value part
 constexpr int kChunkBytes = kTileKeys * 128;
 constexpr int kStages = 2;
 constexpr int kRowsTC = 128;
-constexpr int kThreadsTC = 224;
+constexpr int kThreadsTC = 320;      // 10 warps
 constexpr uint32_t kSCol = 384;      // S buffers at TMEM columns 384 and 448 (Q uses 0..287)
 constexpr float kTau = 8.0f;         // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
@@ -98,7 +99,9 @@ struct TcSmem {
   uint32_t cmd;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
-  uint32_t warp_flags[4];
+  uint32_t warp_flags[8];
+  float pmax[2][kRowsTC];     // CTA 0: per-half partial row maxima of the current tile
+  float lpart[kRowsTC];       // CTA 0: second half's row sums at a unit's last tile
   volatile uint32_t wg_stop;  // CTA 0 softmax group: stop after this tile
   volatile uint32_t wg_cmd;   // CTA 1 epilogue group: command broadcast
 };
@@ -231,15 +234,22 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   }
 }
 
-// ------------------------------------------------------------------ CTA 0: softmax (warps 2-5)
+// ------------------------------------------------------------------ CTA 0: softmax (warps 2-9)
+// Thread (half, row): row = TMEM lane, keys [32*half, 32*half + 32) of each tile.
+// The two halves of a row agree on the tile max through shared memory, so
+// both keep the same running reference max m_ref (raised only when a tile
+// exceeds it by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
 __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp & 3;             // TMEM lane quarter this warp may access
-  const int row = wq * 32 + lane;      // query row within the unit = TMEM lane
-  const int tid = threadIdx.x - 64;    // 0..127 within the softmax group
+  const int wq = warp & 3;                 // TMEM lane quarter this warp may access
+  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a tile
+  const int row = wq * 32 + lane;          // query row within the unit = TMEM lane
+  const int tid = threadIdx.x - 64;        // 0..255 within the softmax group
+  const int wslot = warp - 2;              // 0..7
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
+  const float scale = a.scale_log2;
   const uint32_t peer_pfull[2] = {mapa(smem_u32(&sm.pfull[0]), 1), mapa(smem_u32(&sm.pfull[1]), 1)};
   const uint32_t peer_msg[2] = {mapa(smem_u32(&sm.msg[0]), 1), mapa(smem_u32(&sm.msg[1]), 1)};
   int it = 0, uu = 0;
@@ -248,12 +258,13 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsTC + row;
     const bool valid = r < ui.R;
-    // Q rows of this unit into TMEM columns 0..287 (two bf16 per column)
+    // Q rows of this unit into TMEM columns 0..287 (two bf16 per column); each
+    // half of the group writes its own column chunks
     __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = half; c < kChunks; c += 2) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -267,7 +278,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       }
       tmem_wait_st();
       tc_fence_before();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (tid == 0) mbar_arrive(&sm.qfull);
     }
     const int i = valid ? r / H : 0;
@@ -284,77 +295,89 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       if (tid == 0) VTRACE(3, it);
       __syncwarp();
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      uint32_t v[32];
+      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys + (uint32_t)half * 32, v);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.sfree[s]);
 
-      const int key0 = ui.k_lo + t * kTileKeys;
-      float x[64];
+      const int key0 = ui.k_lo + t * kTileKeys + half * 32;
+      float x[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(v[j]) * a.scale_log2;
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * scale;
       if (!valid) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = -INFINITY;
-      } else if (key0 + kTileKeys > mask_from) {
+        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
+      } else if (key0 + 32 > mask_from) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 32; ++j) {
           const int key = key0 + j;
           bool vis_j = key < ui.k_hi;
           if (vis_j && key >= ui.prefix) vis_j = ((vis >> (key - ui.prefix)) & 1ull) != 0;
           if (!vis_j) x[j] = -INFINITY;
         }
       }
-      float mt = x[0];
+      float mh = x[0];
 #pragma unroll
-      for (int j = 1; j < 64; ++j) mt = fmaxf(mt, x[j]);
+      for (int j = 1; j < 32; ++j) mh = fmaxf(mh, x[j]);
+      sm.pmax[half][row] = mh;
+      const int ms = it & 1;  // message slot (one message per tile)
+      const bool last = t == ui.n_tiles - 1;
+      if (tid == 0) VTRACE(4, it);
+      if (tid == 0 && it >= 2) bulk_wait_group_read<1>();
+      named_bar_sync(1, 256);  // partial maxima visible; staging slot ms free
+      const float mt = fmaxf(mh, sm.pmax[half ^ 1][row]);
       float alpha = 1.f;
       if (mt > m_ref + kTau) {
-        alpha = exp2f(m_ref - mt);  // 0 when m_ref = -inf
+        alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
         l *= alpha;
         m_ref = mt;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
       float lsum = 0.f;
       if (m_ref == -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = 0u;
+        for (int k = 0; k < 16; ++k) pk[k] = 0u;
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = exp2f(x[2 * k] - m_ref), p1 = exp2f(x[2 * k + 1] - m_ref);
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2_approx(x[2 * k] - m_ref), p1 = ex2_approx(x[2 * k + 1] - m_ref);
           lsum += p0 + p1;
           pk[k] = pack_bf16x2(p0, p1);
         }
       }
       l += lsum;
-
-      const int ms = it & 1;  // message slot (one message per tile)
-      const bool last = t == ui.n_tiles - 1;
-      if (tid == 0) VTRACE(4, it);
-      if (tid == 0 && it >= 2) bulk_wait_group_read<1>();
-      named_bar_sync(1, 128);
-      // P row -> staging, 128-byte swizzle (16-byte granule k of row `row` at k ^ (row & 7))
+      // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
+      // this half owns granules 4*half .. 4*half + 3
       uint8_t* prow = sm.msg[ms].p + row * 128;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(prow + ((k ^ (row & 7)) << 4)) =
+      for (int k = 0; k < 4; ++k) {
+        const int g = 4 * half + k;
+        *reinterpret_cast<uint4*>(prow + ((g ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-      sm.msg[ms].alpha[row] = alpha;
-      const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
-      if (lane == 0) sm.warp_flags[wq] = any ? 1u : 0u;
-      if (last) {
-        sm.fin_stage[uu & 1].m[row] = m_ref;
-        sm.fin_stage[uu & 1].l[row] = l;
       }
+      if (half == 0) sm.msg[ms].alpha[row] = alpha;
+      const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
+      if (lane == 0) sm.warp_flags[wslot] = any ? 1u : 0u;
+      if (last && half == 1) sm.lpart[row] = l;
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
+      if (last) {
+        // unit finals: running max and the row sum of both halves
+        if (half == 0) {
+          sm.fin_stage[uu & 1].m[row] = m_ref;
+          sm.fin_stage[uu & 1].l[row] = l + sm.lpart[row];
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+      }
       if (tid == 0) {
         bool go = !sm.abort_flag;
         if (go) {
-          sm.msg[ms].flags = sm.warp_flags[0] | sm.warp_flags[1] | sm.warp_flags[2] | sm.warp_flags[3];
+          uint32_t f = 0;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) f |= sm.warp_flags[w];
+          sm.msg[ms].flags = f;
           fence_proxy_async_smem();
           go = wait_bar(sm, &sm.pfree[ms], ((it >> 1) & 1) ^ 1, a.status, 301, true);
         }
@@ -368,7 +391,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
         }
         sm.wg_stop = go ? 0 : 1;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (sm.wg_stop) {
         stop = true;
         break;
@@ -585,7 +608,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.sfull[s], 1);
-      mbar_init(&sm.sfree[s], 128);
+      mbar_init(&sm.sfree[s], 256);
       mbar_init(&sm.pfull[s], 1);
       mbar_init(&sm.pfree[s], 1);
       mbar_init(&sm.pdone[s], 1);
@@ -604,7 +627,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
-  if (rank == 1 && threadIdx.x == 64) {
+  if (rank == 1 && threadIdx.x == 64) {  // thread 0 of the epilogue group
     // receive slots and finals buffers armed before the partner can send
     int n_units = u_end - u_begin, total = 0;
     for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.order[k]).n_tiles;
@@ -627,10 +650,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
       else mixer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
     }
+  } else if (rank == 0) {
+    scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end);
   } else if (warp < 6) {
-    if (rank == 0) scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end);
-    else mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end);
-  } else if (lane == 0 && rank == 1) {
+    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end);
+  } else if (warp == 6 && lane == 0) {
     mixer_release_role(sm, plan, sched, a, u_begin, u_end);
   }
   __syncwarp();
