@@ -1,5 +1,5 @@
 // Tensor-core verify attention for sm_103a: tcgen05 MMAs with TMEM
-// accumulators, KV rows gathered by TMA (tile::gather4) at page_size = 1.
+// accumulators over KV rows streamed by tiled TMA loads.
 //
 // The method is the KV-split flash-decode of "The Build That Unlocked 3-6x
 // Decode Speedup", section "The Context: A Custom Kernel for an Unsupported
@@ -7,23 +7,26 @@
 // one read of each KV tile shared by many query rows.  The pages share a tile
 // across a head tile of 8 heads (section "Context: The Long Road to a Custom
 // sm_120 Kernel" of "The Build Script Edit"); here a tile serves 128 query
-// rows (heads x draft positions of one sequence) in a single MMA.
+// rows (heads x draft positions of one sequence) in a single MMA.  The KV rows
+// are read from the contiguous copy the gather kernel made of each sequence's
+// page_size = 1 slots.
 //
 // A work unit is 128 query rows (r = i*H + h) of one sequence over one
 // contiguous piece of its key range, and runs on a cluster of two CTAs:
-//   CTA 0 ("scorer")  keeps Q [128 x 576] in tensor memory (A operand),
-//                     computes S = Q K^T for 64-key tiles into double-buffered
-//                     TMEM columns, runs the online softmax (one thread per
-//                     row), and ships P (bf16, 128 x 64) plus per-row rescale
-//                     factors to CTA 1 by a shared-memory bulk copy.
+//   CTA 0 ("scorer")  keeps Q's 512 latent dims in tensor memory (A operand)
+//                     and its 64 rope dims in shared memory, computes S = Q K^T
+//                     for 128-key tiles (N = 128 MMAs) into double-buffered TMEM
+//                     columns, runs the online softmax (two threads per row),
+//                     and ships P (bf16) as two 64-key messages with per-row
+//                     rescale factors to CTA 1 by shared-memory bulk copies.
 //   CTA 1 ("mixer")   keeps O [128 x 512] fp32 in tensor memory and computes
-//                     O = alpha * O + P V with V the latent part of the same
-//                     gathered rows, then normalises and writes the result.
+//                     O = alpha * O + P V over 64-key tiles of the latent part
+//                     of the same rows, then normalises and writes the result.
 // The split of the work follows from tensor-memory capacity: O for 128 rows
 // fills one SM's 512 TMEM columns, so Q and S live on the partner SM.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer; CTA 0:
-// warps 2-9 softmax, two threads per row (each 32 of the tile's 64 keys);
+// warps 2-9 softmax, two threads per row (each 64 of the tile's 128 keys);
 // CTA 1: warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
 // status word, tells the partner CTA to stop, drains its own copies and MMAs,
@@ -40,22 +43,25 @@ namespace vmla {
 using namespace sm100;
 namespace {
 
-constexpr int kTileKeys = 64;
-constexpr int kChunks = kDqk / 64;   // 9 column chunks of 64 bf16 (128 bytes) per row
-constexpr int kVChunks = kDv / 64;   // 8 of them are the latent / value part
-constexpr int kChunkBytes = kTileKeys * 128;
-constexpr int kStages = 2;
 constexpr int kRowsTC = 128;
-constexpr int kThreadsTC = 320;      // 10 warps
-constexpr uint32_t kSCol = 384;      // S buffers at TMEM columns 384 and 448 (Q uses 0..287)
-constexpr float kTau = 8.0f;         // the running max is raised only when a tile exceeds it by 2^8
+constexpr int kThreadsTC = 320;       // 10 warps
+constexpr int kChunks = kDqk / 64;    // 9 column chunks of 64 bf16 (128 bytes) per row
+constexpr int kVChunks = kDv / 64;    // 8 of them are the latent / value part
+constexpr int kKTile = 128;           // keys per score tile (scorer)
+constexpr int kVTile = 64;            // keys per value tile (mixer) = keys per P message
+constexpr int kRing = 10;             // scorer K ring: column chunks of one 128-key tile (16 KB each)
+constexpr int kKChunkBytes = kKTile * 128;
+constexpr int kVChunkBytes = kVTile * 128;
+constexpr int kSlots = 4;             // mixer P receive slots
+constexpr uint32_t kSCol = 256;       // S buffers at TMEM columns 256 and 384 (Q latent uses 0..255)
+constexpr float kTau = 8.0f;          // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-constexpr int kPrefetchTiles = 6;  // tiles the scorer's producer prefetches into L2 ahead of its loads
+constexpr int kPrefetchTiles = 3;     // 128-key tiles the scorer prefetches into L2 ahead of its loads
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
 // Optional pipeline trace (compile with -DVMLA_TRACE): global-timer stamps of
-// each hand-off for the first kTraceTiles tiles of cluster 0.
+// each hand-off for the first kTraceTiles steps of cluster 0.
 #ifdef VMLA_TRACE
 constexpr int kTraceTiles = 256;
 constexpr int kTraceEvents = 12;
@@ -74,7 +80,7 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 
 struct __align__(1024) PMsg {
   uint8_t p[kRowsTC * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
-  float alpha[kRowsTC];      // factor for O rows before this tile's product (1 = unchanged)
+  float alpha[kRowsTC];      // factor for O rows before this message's product (1 = unchanged)
   uint32_t flags;            // bit 0: some alpha differs from 1
   uint32_t pad[3];
 };
@@ -85,29 +91,57 @@ struct __align__(16) Finals {
   float l[kRowsTC];  // softmax denominator relative to m
 };
 
-struct TcSmem {
-  uint8_t kv[kStages][kChunks][kChunkBytes];  // gathered rows, 128-byte swizzled chunks
-  PMsg msg[2];                                // CTA 0: staging; CTA 1: receive slots
-  Finals fin_stage[2];                        // CTA 0 staging of per-unit finals
-  Finals fin[2];                              // CTA 1 receive
-  uint64_t kfull[kStages], kfree[kStages];
-  uint64_t sfull[2], sfree[2];
-  uint64_t qfull;
-  uint64_t pfull[2], pfree[2], pdone[2];
-  uint64_t finfull[2];
+// Shared-memory map (byte offsets from the 1024-aligned base).  The two CTAs
+// use different regions; the barriers and small state sit at the same offset
+// in both, so either CTA can address the other's copy through mapa.
+constexpr uint32_t kQRopeOff = 0;                                   // CTA 0: Q rope chunk, 16 KB
+constexpr uint32_t kKRingOff = kQRopeOff + kRowsTC * 128;           // CTA 0: 10 x 16 KB
+constexpr uint32_t kStageOff = kKRingOff + kRing * kKChunkBytes;    // CTA 0: 2 outgoing messages
+constexpr uint32_t kFinStageOff = kStageOff + 2 * sizeof(PMsg);     // CTA 0: 2 x Finals
+constexpr uint32_t kScorerEnd = kFinStageOff + 2 * sizeof(Finals);
+constexpr uint32_t kVOff = 0;                                       // CTA 1: 2 stages x 8 x 8 KB
+constexpr uint32_t kRecvOff = kVOff + 2 * kVChunks * kVChunkBytes;  // CTA 1: 4 incoming messages
+constexpr uint32_t kFinOff = kRecvOff + kSlots * sizeof(PMsg);      // CTA 1: 2 x Finals
+constexpr uint32_t kMixerEnd = kFinOff + 2 * sizeof(Finals);
+constexpr uint32_t kCommonOff = (kScorerEnd > kMixerEnd ? kScorerEnd : kMixerEnd);
+
+struct Common {
+  uint64_t cfull[kRing], cfree[kRing];  // CTA 0: K chunk ring
+  uint64_t vfull[2], vfree[2];          // CTA 1: V stages
+  uint64_t sfull[2], sfree[2];          // CTA 0: S buffers
+  uint64_t qfull;                       // CTA 0: Q of the unit in place
+  uint64_t pfull[kSlots];               // CTA 1: message received
+  uint64_t pdone[kSlots];               // CTA 1: message consumed by the MMAs
+  uint64_t pfree[kSlots];               // CTA 0: receive slot free again (arrived by CTA 1)
+  uint64_t finfull[2];                  // CTA 1: unit finals received
   uint64_t cmd_full, cmd_done, obar;
   uint32_t cmd;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
+  volatile uint32_t wg_stop;            // CTA 0 softmax group: stop after this tile
+  volatile uint32_t wg_cmd;             // CTA 1 epilogue group: command broadcast
   uint32_t warp_flags[8];
-  float pmax[2][kRowsTC];     // CTA 0: per-half partial row maxima of the current tile
-  float lpart[kRowsTC];       // CTA 0: second half's row sums at a unit's last tile
-  volatile uint32_t wg_stop;  // CTA 0 softmax group: stop after this tile
-  volatile uint32_t wg_cmd;   // CTA 1 epilogue group: command broadcast
+  float pmax[2][kRowsTC];               // CTA 0: per-half partial row maxima of the current tile
+  float lpart[kRowsTC];                 // CTA 0: second half's row sums at a unit's last tile
+};
+
+constexpr size_t kSmemBytes = kCommonOff + sizeof(Common) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Smem {
+  uint8_t* base;
+  Common* c;
+  __device__ uint8_t* qrope() const { return base + kQRopeOff; }
+  __device__ uint8_t* kslot(int s) const { return base + kKRingOff + s * kKChunkBytes; }
+  __device__ PMsg* stage(int m) const { return reinterpret_cast<PMsg*>(base + kStageOff) + m; }
+  __device__ Finals* fin_stage(int f) const { return reinterpret_cast<Finals*>(base + kFinStageOff) + f; }
+  __device__ uint8_t* vchunk(int s, int c) const { return base + kVOff + (s * kVChunks + c) * kVChunkBytes; }
+  __device__ PMsg* recv(int s) const { return reinterpret_cast<PMsg*>(base + kRecvOff) + s; }
+  __device__ Finals* fin(int f) const { return reinterpret_cast<Finals*>(base + kFinOff) + f; }
 };
 
 struct UnitInfo {
-  int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;
+  int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;  // n_tiles: 128-key tiles
 };
 
 __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
@@ -121,165 +155,202 @@ __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
   ui.prefix = s.n_kv - s.n_q;
   ui.k_lo = ui.piece * s.chunk;
   ui.k_hi = min(s.n_kv, ui.k_lo + s.chunk);
-  ui.n_tiles = (ui.k_hi - ui.k_lo + kTileKeys - 1) / kTileKeys;
+  ui.n_tiles = (ui.k_hi - ui.k_lo + kKTile - 1) / kKTile;
   return ui;
 }
 
 // Bounded wait; false on expiry or when the CTA is aborting.
-__device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where,
+__device__ __noinline__ bool wait_bar(Common& c, uint64_t* bar, uint32_t parity, uint32_t* status, int where,
                                       bool cluster_scope = false) {
   long long t0 = clock64();
   for (;;) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (sm.abort_flag) return false;
+    if (c.abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
-      sm.abort_flag = 1;
+      c.abort_flag = 1;
       // tell the partner CTA to stop too
       const uint32_t peer = cluster_ctarank() ^ 1u;
-      const uint32_t remote = mapa(smem_u32((const void*)const_cast<int32_t*>(&sm.abort_flag)), peer);
+      const uint32_t remote = mapa(smem_u32((const void*)const_cast<int32_t*>(&c.abort_flag)), peer);
       asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
       return false;
     }
   }
 }
 
-// ------------------------------------------------------------------ producer (warp 0, lane 0, both CTAs)
-// Loads each 64-key tile of the unit's key range from the contiguous staged
-// copy of the KV rows: one 64-row x 64-column box (8 KB, 128-byte swizzle) per
-// column chunk, 9 chunks for the scorer (K), 8 for the mixer (V).  Rows past
-// the piece's end belong to other keys and are masked by the softmax.
-__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
-                              const RunArgs& a, int u_begin, int u_end, int nch, bool prefetch) {
-  int it = 0;
+// Waits (bounded) for the phase of `bar` with parity `parity`, ignoring the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitCycles) {
+  }
+}
+
+// ------------------------------------------------------------------ CTA 0: K producer (warp 0, lane 0)
+// Each 128-key tile is 9 column chunks (16 KB each: 128 rows x 64 columns,
+// 128-byte swizzle) of the staged rows, streamed through a 10-slot ring so a
+// chunk of the next tile loads as soon as the MMAs free a slot.
+__device__ void scorer_producer_role(const Smem& sm, const CUtensorMap* map, const PlanParams& plan,
+                                     const TcSched& sched, const RunArgs& a, int u_begin, int u_end) {
+  Common& c = *sm.c;
+  int g = 0;
   bool ok = true;
-  // L2 prefetch of the staged rows of tile t (contiguous: 64 rows x 1152 bytes), clamped to the staged area
   auto prefetch_tile = [&](const SeqPlan& sp, const UnitInfo& ui, int t) {
-    if (!prefetch || t >= ui.n_tiles) return;
-    const int64_t row0 = (int64_t)sp.kv_off + ui.k_lo + (int64_t)t * kTileKeys;
+    if (t >= ui.n_tiles) return;
+    const int64_t row0 = (int64_t)sp.kv_off + ui.k_lo + (int64_t)t * kKTile;
     int64_t rows = a.total_kv - row0;
-    if (rows > kTileKeys) rows = kTileKeys;
+    if (rows > kKTile) rows = kKTile;
     if (rows > 0) prefetch_l2_bulk(a.staged + row0 * kDqk, (uint32_t)(rows * kRowBytes));
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
-    for (int t = 0; t < kPrefetchTiles && t < ui.n_tiles; ++t) prefetch_tile(sp, ui, t);
-    for (int t = 0; t < ui.n_tiles; ++t) {
+    for (int t = 0; t < kPrefetchTiles; ++t) prefetch_tile(sp, ui, t);
+    for (int t = 0; t < ui.n_tiles && ok; ++t) {
+      VTRACE(0, g / kChunks);
+      const int y = sp.kv_off + ui.k_lo + t * kKTile;
+      for (int ch = 0; ch < kChunks; ++ch, ++g) {
+        const int slot = g % kRing;
+        if (!wait_bar(c, &c.cfree[slot], ((g / kRing) & 1) ^ 1, a.status, 100)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&c.cfull[slot], (uint32_t)kKChunkBytes);
+        tma_load_2d(smem_u32(sm.kslot(slot)), map, 64 * ch, y, smem_u32(&c.cfull[slot]));
+      }
+      prefetch_tile(sp, ui, t + kPrefetchTiles);
+    }
+  }
+  // drain: every issued load has landed before the CTA may exit
+  for (int k = 1; k <= kRing && g - k >= 0; ++k) drain_wait(&c.cfull[(g - k) % kRing], ((g - k) / kRing) & 1);
+}
+
+// ------------------------------------------------------------------ CTA 1: V producer (warp 0, lane 0)
+__device__ void mixer_producer_role(const Smem& sm, const CUtensorMap* map, const PlanParams& plan,
+                                    const TcSched& sched, const RunArgs& a, int u_begin, int u_end) {
+  Common& c = *sm.c;
+  int it = 0;
+  bool ok = true;
+  for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
+    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const SeqPlan& sp = plan.seq[ui.b];
+    for (int t = 0; t < 2 * ui.n_tiles; ++t, ++it) {
       const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfree[s], ph ^ 1, a.status, 100)) {
+      if (!wait_bar(c, &c.vfree[s], ((it >> 1) & 1) ^ 1, a.status, 110)) {
         ok = false;
         break;
       }
-      VTRACE(prefetch ? 0 : 6, it);
-      const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
-      mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
-      const uint32_t bar = smem_u32(&sm.kfull[s]);
-      for (int c = 0; c < nch; ++c) tma_load_2d(smem_u32(&sm.kv[s][c][0]), map, 64 * c, y, bar);
-      prefetch_tile(sp, ui, t + kPrefetchTiles);
-      ++it;
+      VTRACE(6, it);
+      const int y = sp.kv_off + ui.k_lo + t * kVTile;
+      mbar_arrive_expect_tx(&c.vfull[s], (uint32_t)(kVChunks * kVChunkBytes));
+      for (int ch = 0; ch < kVChunks; ++ch) tma_load_2d(smem_u32(sm.vchunk(s, ch)), map, 64 * ch, y, smem_u32(&c.vfull[s]));
     }
   }
-  // drain: the loads of the last two stages have landed before the CTA may exit
-  for (int k = 1; k <= 2 && it - k >= 0; ++k) {
-    const int j = it - k;
-    long long t0 = clock64();
-    while (!mbar_try_wait(&sm.kfull[j & 1], (j >> 1) & 1) && clock64() - t0 < kWaitCycles) {
-    }
-  }
+  for (int k = 1; k <= 2 && it - k >= 0; ++k) drain_wait(&c.vfull[(it - k) & 1], ((it - k) >> 1) & 1);
 }
 
 // ------------------------------------------------------------------ CTA 0: QK^T issuer (warp 1, lane 0)
-__device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+__device__ void scorer_mma_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                 uint32_t tbase, int u_begin, int u_end) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kTileKeys, 0, 0);
-  int it = 0, uu = 0;
-  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
+  Common& c = *sm.c;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, kKTile, 0, 0);
+  const uint32_t rope = smem_u32(sm.qrope());
+  int g = 0, it = 0, uu = 0;
+  bool ok = true;
+  for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    if (!wait_bar(sm, &sm.qfull, uu & 1, a.status, 200)) break;
+    if (!wait_bar(c, &c.qfull, uu & 1, a.status, 200)) break;
     tc_fence_after();
-    bool ok = true;
-    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 201)) {
-        ok = false;
-        break;
-      }
-      VTRACE(1, it);
-      if (!wait_bar(sm, &sm.sfree[s], ph ^ 1, a.status, 202)) {
+    for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
+      const int sb = it & 1;
+      if (!wait_bar(c, &c.sfree[sb], ((it >> 1) & 1) ^ 1, a.status, 202)) {
         ok = false;
         break;
       }
       VTRACE(2, it);
-      tc_fence_after();
-      const uint32_t d = tbase + kSCol + (uint32_t)s * kTileKeys;
+      const uint32_t d = tbase + kSCol + (uint32_t)sb * kKTile;
+      for (int ch = 0; ch < kChunks; ++ch, ++g) {
+        const int slot = g % kRing;
+        if (!wait_bar(c, &c.cfull[slot], (g / kRing) & 1, a.status, 201)) {
+          ok = false;
+          break;
+        }
+        if (ch == 0) VTRACE(1, it);
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sm.kslot(slot));
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint32_t kbase = smem_u32(&sm.kv[s][c][0]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(d, tbase + (uint32_t)(c * 32 + k * 8), smem_desc(kbase + k * 32, 16, 1024), idesc, (c | k) != 0);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t bdesc = smem_desc(kb + k * 32, 16, 1024);
+          if (ch < kVChunks)
+            mma_ts(d, tbase + (uint32_t)(ch * 32 + k * 8), bdesc, idesc, (ch | k) != 0);
+          else
+            mma_ss(d, smem_desc(rope + k * 32, 16, 1024), bdesc, idesc, 1u);
+        }
+        mma_commit(&c.cfree[slot]);
       }
-      mma_commit(&sm.sfull[s]);
-      mma_commit(&sm.kfree[s]);
+      if (!ok) break;
+      mma_commit(&c.sfull[sb]);
     }
-    if (!ok) break;
   }
   // all issued MMAs complete before the CTA may exit
-  mma_commit(&sm.obar);
-  long long t0 = clock64();
-  while (!mbar_try_wait(&sm.obar, 0) && clock64() - t0 < kWaitCycles) {
-  }
+  mma_commit(&c.obar);
+  drain_wait(&c.obar, 0);
 }
 
 // ------------------------------------------------------------------ CTA 0: softmax (warps 2-9)
-// Thread (half, row): row = TMEM lane, keys [32*half, 32*half + 32) of each tile.
-// The two halves of a row agree on the tile max through shared memory, so
-// both keep the same running reference max m_ref (raised only when a tile
-// exceeds it by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
-__device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+// Thread (half, row): row = TMEM lane, keys [64*half, 64*half + 64) of each
+// 128-key tile; it builds message `half` of the tile (P for those 64 keys).
+// The two halves of a row agree on the tile max through shared memory, so both
+// keep the same running reference max m_ref (raised only when a tile exceeds it
+// by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
+__device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end) {
+  Common& c = *sm.c;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;                 // TMEM lane quarter this warp may access
-  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a tile
+  const int half = (warp - 2) >> 2;        // 0: keys 0..63, 1: keys 64..127 of a tile
   const int row = wq * 32 + lane;          // query row within the unit = TMEM lane
   const int tid = threadIdx.x - 64;        // 0..255 within the softmax group
   const int wslot = warp - 2;              // 0..7
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
   const float scale = a.scale_log2;
-  const uint32_t peer_pfull[2] = {mapa(smem_u32(&sm.pfull[0]), 1), mapa(smem_u32(&sm.pfull[1]), 1)};
-  const uint32_t peer_msg[2] = {mapa(smem_u32(&sm.msg[0]), 1), mapa(smem_u32(&sm.msg[1]), 1)};
   int it = 0, uu = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsTC + row;
     const bool valid = r < ui.R;
-    // Q rows of this unit into TMEM columns 0..287 (two bf16 per column); each
-    // half of the group writes its own column chunks
+    // Q rows of this unit: latent chunks 0..7 into TMEM columns 0..255 (two
+    // bf16 per column, half 0 the even chunks, half 1 the odd ones); the rope
+    // chunk into shared memory (K-major, 128-byte swizzle) by half 1
     __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
-      for (int c = half; c < kChunks; c += 2) {
+      for (int ch = half; ch < kVChunks; ch += 2) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          uint4 x = valid ? __ldg(qrow + c * 8 + k) : make_uint4(0, 0, 0, 0);
+          const uint4 x = valid ? __ldg(qrow + ch * 8 + k) : make_uint4(0, 0, 0, 0);
           v[4 * k] = x.x;
           v[4 * k + 1] = x.y;
           v[4 * k + 2] = x.z;
           v[4 * k + 3] = x.w;
         }
-        tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
+        tmem_st32(tbase + lane_base + (uint32_t)(ch * 32), v);
+      }
+      if (half == 1) {
+        uint8_t* dst = sm.qrope() + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(dst + ((k ^ (row & 7)) << 4)) =
+              valid ? __ldg(qrow + kVChunks * 8 + k) : make_uint4(0, 0, 0, 0);
       }
       tmem_wait_st();
+      fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 256);
-      if (tid == 0) mbar_arrive(&sm.qfull);
+      if (tid == 0) mbar_arrive(&c.qfull);
     }
     const int i = valid ? r / H : 0;
     const uint64_t vis = a.masks ? a.masks[sp.q_off + i] : causal_bits(i);
@@ -287,30 +358,31 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     float m_ref = -INFINITY, l = 0.f;
     bool stop = false;
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
+      const int sb = it & 1;
       // a failed wait leaves garbage in this tile; the group still meets at every
       // barrier below and stops together at the end of the tile
-      wait_bar(sm, &sm.sfull[s], ph, a.status, 300);
+      wait_bar(c, &c.sfull[sb], (it >> 1) & 1, a.status, 300);
       if (tid == 0) VTRACE(3, it);
       __syncwarp();
       tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys + (uint32_t)half * 32, v);
+      uint32_t v[64];
+      const uint32_t scol = tbase + lane_base + kSCol + (uint32_t)sb * kKTile + (uint32_t)half * 64;
+      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&sm.sfree[s]);
+      mbar_arrive(&c.sfree[sb]);
 
-      const int key0 = ui.k_lo + t * kTileKeys + half * 32;
-      float x[32];
+      const int key0 = ui.k_lo + t * kKTile + half * 64;
+      float x[64];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * scale;
+      for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(v[j]) * scale;
       if (!valid) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
-      } else if (key0 + 32 > mask_from) {
+        for (int j = 0; j < 64; ++j) x[j] = -INFINITY;
+      } else if (key0 + 64 > mask_from) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 64; ++j) {
           const int key = key0 + j;
           bool vis_j = key < ui.k_hi;
           if (vis_j && key >= ui.prefix) vis_j = ((vis >> (key - ui.prefix)) & 1ull) != 0;
@@ -319,80 +391,84 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       }
       float mh = x[0];
 #pragma unroll
-      for (int j = 1; j < 32; ++j) mh = fmaxf(mh, x[j]);
-      sm.pmax[half][row] = mh;
-      const int ms = it & 1;  // message slot (one message per tile)
+      for (int j = 1; j < 64; ++j) mh = fmaxf(mh, x[j]);
+      c.pmax[half][row] = mh;
       const bool last = t == ui.n_tiles - 1;
       if (tid == 0) VTRACE(4, it);
-      if (tid == 0 && it >= 2) bulk_wait_group_read<1>();
-      named_bar_sync(1, 256);  // partial maxima visible; staging slot ms free
-      const float mt = fmaxf(mh, sm.pmax[half ^ 1][row]);
+      if (tid == 0) bulk_wait_group_read<0>();  // the previous tile's messages have left the staging slots
+      named_bar_sync(1, 256);
+      const float mt = fmaxf(mh, c.pmax[half ^ 1][row]);
       float alpha = 1.f;
       if (mt > m_ref + kTau) {
         alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
         l *= alpha;
         m_ref = mt;
       }
-      uint32_t pk[16];
+      uint32_t pk[32];
       float lsum = 0.f;
       if (m_ref == -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = 0u;
+        for (int k = 0; k < 32; ++k) pk[k] = 0u;
       } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 32; ++k) {
           const float p0 = ex2_approx(x[2 * k] - m_ref), p1 = ex2_approx(x[2 * k + 1] - m_ref);
           lsum += p0 + p1;
           pk[k] = pack_bf16x2(p0, p1);
         }
       }
       l += lsum;
-      // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
-      // this half owns granules 4*half .. 4*half + 3
-      uint8_t* prow = sm.msg[ms].p + row * 128;
+      // P row -> message `half`, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7))
+      PMsg* msg = sm.stage(half);
+      uint8_t* prow = msg->p + row * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int g = 4 * half + k;
+      for (int g = 0; g < 8; ++g)
         *reinterpret_cast<uint4*>(prow + ((g ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-      }
-      if (half == 0) sm.msg[ms].alpha[row] = alpha;
-      const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
-      if (lane == 0) sm.warp_flags[wslot] = any ? 1u : 0u;
-      if (last && half == 1) sm.lpart[row] = l;
+            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      // the rescale goes with the tile's first message; the second leaves O as it is
+      msg->alpha[row] = half == 0 ? alpha : 1.f;
+      const unsigned any = __ballot_sync(0xffffffffu, half == 0 && alpha != 1.f);
+      if (lane == 0) c.warp_flags[wslot] = any ? 1u : 0u;
+      if (last && half == 1) c.lpart[row] = l;
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
       if (last) {
         // unit finals: running max and the row sum of both halves
         if (half == 0) {
-          sm.fin_stage[uu & 1].m[row] = m_ref;
-          sm.fin_stage[uu & 1].l[row] = l + sm.lpart[row];
+          sm.fin_stage(uu & 1)->m[row] = m_ref;
+          sm.fin_stage(uu & 1)->l[row] = l + c.lpart[row];
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 256);
       }
       if (tid == 0) {
-        bool go = !sm.abort_flag;
+        bool go = !c.abort_flag;
         if (go) {
           uint32_t f = 0;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) f |= sm.warp_flags[w];
-          sm.msg[ms].flags = f;
+          for (int w = 0; w < 8; ++w) f |= c.warp_flags[w];
+          sm.stage(0)->flags = f;
+          sm.stage(1)->flags = 0;
           fence_proxy_async_smem();
-          go = wait_bar(sm, &sm.pfree[ms], ((it >> 1) & 1) ^ 1, a.status, 301, true);
         }
-        if (go) {
-          VTRACE(5, it);
-          bulk_s2s_cluster(peer_msg[ms], smem_u32(&sm.msg[ms]), kMsgBytes, peer_pfull[ms]);
-          if (last)
-            bulk_s2s_cluster(mapa(smem_u32(&sm.fin[uu & 1]), 1), smem_u32(&sm.fin_stage[uu & 1]), sizeof(Finals),
-                             mapa(smem_u32(&sm.finfull[uu & 1]), 1));
-          bulk_commit_group();
+        for (int m = 0; m < 2 && go; ++m) {
+          const int n = 2 * it + m;  // message index
+          const int slot = n % kSlots;
+          go = wait_bar(c, &c.pfree[slot], ((n / kSlots) & 1) ^ 1, a.status, 301, true);
+          if (go) {
+            if (m == 0) VTRACE(5, it);
+            bulk_s2s_cluster(mapa(smem_u32(sm.recv(slot)), 1), smem_u32(sm.stage(m)), kMsgBytes,
+                             mapa(smem_u32(&c.pfull[slot]), 1));
+          }
         }
-        sm.wg_stop = go ? 0 : 1;
+        if (go && last)
+          bulk_s2s_cluster(mapa(smem_u32(sm.fin(uu & 1)), 1), smem_u32(sm.fin_stage(uu & 1)), sizeof(Finals),
+                           mapa(smem_u32(&c.finfull[uu & 1]), 1));
+        bulk_commit_group();
+        c.wg_stop = go ? 0 : 1;
       }
       named_bar_sync(1, 256);
-      if (sm.wg_stop) {
+      if (c.wg_stop) {
         stop = true;
         break;
       }
@@ -403,88 +479,89 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
 }
 
 // ------------------------------------------------------------------ CTA 1: P V issuer (warp 1, lane 0)
-__device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+__device__ void mixer_mma_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                uint32_t tbase, int u_begin, int u_end) {
+  Common& c = *sm.c;
   constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
   int it = 0, cmdn = 0, obn = 0;
   bool ok = true;
-  auto command = [&](uint32_t c) -> bool {
-    sm.cmd = c;
-    mbar_arrive(&sm.cmd_full);
-    const bool r = wait_bar(sm, &sm.cmd_done, cmdn & 1, a.status, 402);
+  auto command = [&](uint32_t cmd) -> bool {
+    c.cmd = cmd;
+    mbar_arrive(&c.cmd_full);
+    const bool r = wait_bar(c, &c.cmd_done, cmdn & 1, a.status, 402);
     ++cmdn;
     return r;
   };
   auto quiesce = [&]() -> bool {
-    mma_commit(&sm.obar);
-    const bool r = wait_bar(sm, &sm.obar, obn & 1, a.status, 403);
+    mma_commit(&c.obar);
+    const bool r = wait_bar(c, &c.obar, obn & 1, a.status, 403);
     ++obn;
     return r;
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 400)) {
+    for (int t = 0; t < 2 * ui.n_tiles; ++t, ++it) {
+      const int s = it & 1, ps = it % kSlots;
+      if (!wait_bar(c, &c.vfull[s], (it >> 1) & 1, a.status, 400)) {
         ok = false;
         break;
       }
       VTRACE(7, it);
-      if (!wait_bar(sm, &sm.pfull[s], ph, a.status, 401, true)) {
+      if (!wait_bar(c, &c.pfull[ps], (it / kSlots) & 1, a.status, 401, true)) {
         ok = false;
         break;
       }
       VTRACE(8, it);
-      if (t > 0 && (sm.msg[s].flags & 1u)) {
-        if (!quiesce() || !command(kCmdRescale | ((uint32_t)s << 8))) {
+      if (t > 0 && (sm.recv(ps)->flags & 1u)) {
+        if (!quiesce() || !command(kCmdRescale | ((uint32_t)ps << 8))) {
           ok = false;
           break;
         }
       }
       tc_fence_after();
-      const uint32_t pbase = smem_u32(sm.msg[s].p);
+      const uint32_t pbase = smem_u32(sm.recv(ps)->p);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint64_t adesc = smem_desc(pbase + k * 32, 16, 1024);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint64_t bdesc = smem_desc(smem_u32(&sm.kv[s][4 * hh][0]) + k * 16 * 128, kChunkBytes, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sm.vchunk(s, 4 * hh)) + k * 16 * 128, kVChunkBytes, 1024);
           mma_ss(tbase + (uint32_t)(256 * hh), adesc, bdesc, idesc, (t > 0 || k > 0) ? 1u : 0u);
         }
       }
-      mma_commit(&sm.kfree[s]);
-      mma_commit(&sm.pdone[s]);
+      mma_commit(&c.vfree[s]);
+      mma_commit(&c.pdone[ps]);
       VTRACE(9, it);
     }
     if (!ok) break;
     if (!quiesce() || !command(kCmdEpilogue)) ok = false;
   }
   if (!ok) quiesce();
-  sm.cmd = kCmdExit;
-  mbar_arrive(&sm.cmd_full);
+  c.cmd = kCmdExit;
+  mbar_arrive(&c.cmd_full);
 }
 
 // ------------------------------------------------------------------ CTA 1: P-slot release (warp 6, lane 0)
-__device__ void mixer_release_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+__device__ void mixer_release_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                    int u_begin, int u_end) {
+  Common& c = *sm.c;
   int total = 0;
-  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx) total += decode_unit(plan, sched.order[ui_idx]).n_tiles;
-  const uint32_t peer_pfree[2] = {mapa(smem_u32(&sm.pfree[0]), 0), mapa(smem_u32(&sm.pfree[1]), 0)};
+  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx) total += 2 * decode_unit(plan, sched.order[ui_idx]).n_tiles;
   for (int n = 0; n < total; ++n) {
-    const int s = n & 1;
-    if (!wait_bar(sm, &sm.pdone[s], (n >> 1) & 1, a.status, 500)) return;
+    const int ps = n % kSlots;
+    if (!wait_bar(c, &c.pdone[ps], (n / kSlots) & 1, a.status, 500)) return;
     VTRACE(10, n);
-    if (n + 2 < total) {
-      mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
-      mbar_arrive_remote(peer_pfree[s]);
+    if (n + kSlots < total) {
+      mbar_arrive_expect_tx(&c.pfull[ps], kMsgBytes);
+      mbar_arrive_remote(mapa(smem_u32(&c.pfree[ps]), 0));
     }
   }
 }
 
 // ------------------------------------------------------------------ CTA 1: rescale / epilogue (warps 2-5)
-__device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+__device__ void mixer_epilogue_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end) {
+  Common& c = *sm.c;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
@@ -498,33 +575,32 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     // the group learns it at a barrier, so a failed wait stops every thread
     if (tid == 0) {
       uint32_t cmd = kCmdExit;
-      if (wait_bar(sm, &sm.cmd_full, cmdn & 1, a.status, 600)) {
-        cmd = sm.cmd;
-        if ((cmd & 0xFF) == kCmdEpilogue &&
-            !wait_bar(sm, &sm.finfull[uu & 1], (uu >> 1) & 1, a.status, 601, true))
+      if (wait_bar(c, &c.cmd_full, cmdn & 1, a.status, 600)) {
+        cmd = c.cmd;
+        if ((cmd & 0xFF) == kCmdEpilogue && !wait_bar(c, &c.finfull[uu & 1], (uu >> 1) & 1, a.status, 601, true))
           cmd = kCmdExit;
       }
-      sm.wg_cmd = cmd;
+      c.wg_cmd = cmd;
     }
     ++cmdn;
     named_bar_sync(2, 128);
-    const uint32_t cmd = sm.wg_cmd;
+    const uint32_t cmd = c.wg_cmd;
     if ((cmd & 0xFF) == kCmdExit) return;
     __syncwarp();
     tc_fence_after();
     // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform
     if ((cmd & 0xFF) == kCmdRescale) {
-      const int s = (cmd >> 8) & 1;
-      const float alpha = sm.msg[s].alpha[row];
+      const int ps = (cmd >> 8) & 3;
+      const float alpha = sm.recv(ps)->alpha[row];
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
+        for (int ch = 0; ch < kDv / 32; ++ch) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_ld32(tbase + lane_base + (uint32_t)(ch * 32), v);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-          tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_st32(tbase + lane_base + (uint32_t)(ch * 32), v);
         }
         tmem_wait_st();
       }
@@ -532,8 +608,8 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       // epilogue of unit ui_idx: O / l -> output row (or fp32 partial)
       const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
       const SeqPlan& sp = plan.seq[ui.b];
-      const int f = uu & 1;
-      const float m = sm.fin[f].m[row], lsum = sm.fin[f].l[row];
+      const Finals* fin = sm.fin(uu & 1);
+      const float m = fin->m[row], lsum = fin->l[row];
       const int r = ui.rb * kRowsTC + row;
       const bool valid = r < ui.R;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -542,14 +618,14 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
         const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
         uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kDv);
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
+        for (int ch = 0; ch < kDv / 32; ++ch) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_ld32(tbase + lane_base + (uint32_t)(ch * 32), v);
           tmem_wait_ld();
           if (valid) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              dst[c * 4 + k] = make_uint4(
+              dst[ch * 4 + k] = make_uint4(
                   pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
@@ -562,15 +638,15 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
         const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + (valid ? r : 0);
         float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDv);
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
+        for (int ch = 0; ch < kDv / 32; ++ch) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_ld32(tbase + lane_base + (uint32_t)(ch * 32), v);
           tmem_wait_ld();
           if (valid) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              dst[c * 8 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                                           __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+              dst[ch * 8 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
           }
           __syncwarp();
         }
@@ -584,17 +660,20 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     if (tid == 0) {
       // a finals buffer is re-armed for the unit two ahead once it has been read
       if ((cmd & 0xFF) == kCmdEpilogue && ui_idx + 1 < u_end)
-        mbar_arrive_expect_tx(&sm.finfull[(uu + 1) & 1], sizeof(Finals));
-      mbar_arrive(&sm.cmd_done);
+        mbar_arrive_expect_tx(&c.finfull[(uu + 1) & 1], sizeof(Finals));
+      mbar_arrive(&c.cmd_done);
     }
   }
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ PlanParams plan,
-                 const __grid_constant__ TcSched sched, const RunArgs a) {
+tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem sm;
+  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  sm.c = reinterpret_cast<Common*>(sm.base + kCommonOff);
+  Common& c = *sm.c;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int cid = (int)cluster_id_x();
@@ -602,37 +681,41 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const int u_end = cid < sched.num_clusters ? sched.start[cid + 1] : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kfull[s], 1);
-      mbar_init(&sm.kfree[s], 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&c.cfull[s], 1);
+      mbar_init(&c.cfree[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.sfull[s], 1);
-      mbar_init(&sm.sfree[s], 256);
-      mbar_init(&sm.pfull[s], 1);
-      mbar_init(&sm.pfree[s], 1);
-      mbar_init(&sm.pdone[s], 1);
-      mbar_init(&sm.finfull[s], 1);
+      mbar_init(&c.vfull[s], 1);
+      mbar_init(&c.vfree[s], 1);
+      mbar_init(&c.sfull[s], 1);
+      mbar_init(&c.sfree[s], 256);
+      mbar_init(&c.finfull[s], 1);
     }
-    mbar_init(&sm.qfull, 1);
-    mbar_init(&sm.cmd_full, 1);
-    mbar_init(&sm.cmd_done, 1);
-    mbar_init(&sm.obar, 1);
-    sm.abort_flag = 0;
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&c.pfull[s], 1);
+      mbar_init(&c.pdone[s], 1);
+      mbar_init(&c.pfree[s], 1);
+    }
+    mbar_init(&c.qfull, 1);
+    mbar_init(&c.cmd_full, 1);
+    mbar_init(&c.cmd_done, 1);
+    mbar_init(&c.obar, 1);
+    c.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&kv_map);
+    prefetch_tensormap(rank == 0 ? &k_map : &v_map);
   }
   __syncwarp();
   if (warp == 0) {
-    tmem_alloc(&sm.tmem_base, 512);
+    tmem_alloc(&c.tmem_base, 512);
     tmem_relinquish();
   }
   if (rank == 1 && threadIdx.x == 64) {  // thread 0 of the epilogue group
     // receive slots and finals buffers armed before the partner can send
     int n_units = u_end - u_begin, total = 0;
-    for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.order[k]).n_tiles;
-    for (int s = 0; s < 2 && s < total; ++s) mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
-    for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&sm.finfull[s], sizeof(Finals));
+    for (int k = u_begin; k < u_end; ++k) total += 2 * decode_unit(plan, sched.order[k]).n_tiles;
+    for (int s = 0; s < kSlots && s < total; ++s) mbar_arrive_expect_tx(&c.pfull[s], kMsgBytes);
+    for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&c.finfull[s], sizeof(Finals));
   }
   __syncwarp();
   tc_fence_before();
@@ -640,11 +723,13 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   tc_fence_after();
   cluster_arrive();
   cluster_wait();
-  const uint32_t tbase = sm.tmem_base;
+  const uint32_t tbase = c.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0)
-      producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks, rank == 0);
+    if (lane == 0) {
+      if (rank == 0) scorer_producer_role(sm, &k_map, plan, sched, a, u_begin, u_end);
+      else mixer_producer_role(sm, &v_map, plan, sched, a, u_begin, u_end);
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
@@ -689,9 +774,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 2 * sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 }  // namespace
@@ -739,13 +822,18 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   static thread_local TcSched sched;
   rc = build_tc_schedule(plan, clusters, &sched);
   if (rc != VMLA_OK) return rc;
-  // 2-D map over the staged rows [total_kv x 576 bf16], boxes of 64 columns x 64 rows, 128-byte swizzle
-  CUtensorMap map;
+  // 2-D maps over the staged rows [total_kv x 576 bf16], 128-byte swizzle: boxes of
+  // 64 columns x 128 rows (K chunks of a score tile) and 64 columns x 64 rows (V chunks)
+  CUtensorMap kmap, vmap;
   cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(a.total_kv > 0 ? a.total_kv : 1)};
   cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
+  cuuint32_t kbox[2] = {64, (cuuint32_t)kKTile};
+  cuuint32_t vbox[2] = {64, (cuuint32_t)kVTile};
   cuuint32_t estride[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, box, estride,
+  if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, kbox, estride,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, vbox, estride,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return VMLA_ERR_CUDA;
@@ -761,7 +849,7 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, map, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 
