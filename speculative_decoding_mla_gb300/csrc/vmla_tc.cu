@@ -17,8 +17,10 @@
 //                     and its 64 rope dims in shared memory, computes S = Q K^T
 //                     for 128-key tiles (N = 128 MMAs) into double-buffered TMEM
 //                     columns, runs the online softmax (two threads per row),
-//                     and ships P (bf16) as two 64-key messages with per-row
-//                     rescale factors to CTA 1 by shared-memory bulk copies.
+//                     and writes P (bf16) as two 64-key messages with per-row
+//                     rescale factors straight into CTA 1's shared memory
+//                     (distributed shared-memory stores; no copy engine, so the
+//                     scorer's TMA queue carries only its own K loads).
 //   CTA 1 ("mixer")   keeps O [128 x 512] fp32 in tensor memory and computes
 //                     O = alpha * O + P V over 64-key tiles of the latent part
 //                     of the same rows, then normalises and writes the result.
@@ -49,14 +51,14 @@ constexpr int kChunks = kDqk / 64;    // 9 column chunks of 64 bf16 (128 bytes) 
 constexpr int kVChunks = kDv / 64;    // 8 of them are the latent / value part
 constexpr int kKTile = 128;           // keys per score tile (scorer)
 constexpr int kVTile = 64;            // keys per value tile (mixer) = keys per P message
-constexpr int kRing = 10;             // scorer K ring: column chunks of one 128-key tile (16 KB each)
+constexpr int kRing = 12;             // scorer K ring: column chunks of 128-key tiles (16 KB each)
 constexpr int kKChunkBytes = kKTile * 128;
 constexpr int kVChunkBytes = kVTile * 128;
 constexpr int kSlots = 4;             // mixer P receive slots
 constexpr uint32_t kSCol = 256;       // S buffers at TMEM columns 256 and 384 (Q latent uses 0..255)
 constexpr float kTau = 8.0f;          // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-constexpr int kPrefetchTiles = 3;     // 128-key tiles the scorer prefetches into L2 ahead of its loads
+constexpr int kPrefetchTiles = 0;     // 128-key tiles the scorer prefetches into L2 ahead of its loads (0: off)
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
@@ -74,8 +76,19 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
   }
 }
 #define VTRACE(ev, tile) vtrace(ev, tile)
+constexpr int kTraceChunks = 1024;
+__device__ uint64_t g_vmla_trace_chunks[3 * kTraceChunks];
+__device__ __forceinline__ void vtrace_chunk(int ev, int g) {
+  if (cluster_id_x() == 0 && g < kTraceChunks) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_vmla_trace_chunks[ev * kTraceChunks + g] = t;
+  }
+}
+#define VTRACE_CHUNK(ev, g) vtrace_chunk(ev, g)
 #else
 #define VTRACE(ev, tile) ((void)0)
+#define VTRACE_CHUNK(ev, g) ((void)0)
 #endif
 
 struct __align__(1024) PMsg {
@@ -84,7 +97,6 @@ struct __align__(1024) PMsg {
   uint32_t flags;            // bit 0: some alpha differs from 1
   uint32_t pad[3];
 };
-constexpr uint32_t kMsgBytes = kRowsTC * 128 + kRowsTC * 4 + 16;  // bytes shipped per message
 
 struct __align__(16) Finals {
   float m[kRowsTC];  // running max (log2 units)
@@ -96,9 +108,7 @@ struct __align__(16) Finals {
 // in both, so either CTA can address the other's copy through mapa.
 constexpr uint32_t kQRopeOff = 0;                                   // CTA 0: Q rope chunk, 16 KB
 constexpr uint32_t kKRingOff = kQRopeOff + kRowsTC * 128;           // CTA 0: 10 x 16 KB
-constexpr uint32_t kStageOff = kKRingOff + kRing * kKChunkBytes;    // CTA 0: 2 outgoing messages
-constexpr uint32_t kFinStageOff = kStageOff + 2 * sizeof(PMsg);     // CTA 0: 2 x Finals
-constexpr uint32_t kScorerEnd = kFinStageOff + 2 * sizeof(Finals);
+constexpr uint32_t kScorerEnd = kKRingOff + kRing * kKChunkBytes;
 constexpr uint32_t kVOff = 0;                                       // CTA 1: 2 stages x 8 x 8 KB
 constexpr uint32_t kRecvOff = kVOff + 2 * kVChunks * kVChunkBytes;  // CTA 1: 4 incoming messages
 constexpr uint32_t kFinOff = kRecvOff + kSlots * sizeof(PMsg);      // CTA 1: 2 x Finals
@@ -119,6 +129,7 @@ struct Common {
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   volatile uint32_t wg_stop;            // CTA 0 softmax group: stop after this tile
+  volatile uint32_t wg_go;              // CTA 0 softmax group: receive slots granted for this tile
   volatile uint32_t wg_cmd;             // CTA 1 epilogue group: command broadcast
   uint32_t warp_flags[8];
   float pmax[2][kRowsTC];               // CTA 0: per-half partial row maxima of the current tile
@@ -133,8 +144,6 @@ struct Smem {
   Common* c;
   __device__ uint8_t* qrope() const { return base + kQRopeOff; }
   __device__ uint8_t* kslot(int s) const { return base + kKRingOff + s * kKChunkBytes; }
-  __device__ PMsg* stage(int m) const { return reinterpret_cast<PMsg*>(base + kStageOff) + m; }
-  __device__ Finals* fin_stage(int f) const { return reinterpret_cast<Finals*>(base + kFinStageOff) + f; }
   __device__ uint8_t* vchunk(int s, int c) const { return base + kVOff + (s * kVChunks + c) * kVChunkBytes; }
   __device__ PMsg* recv(int s) const { return reinterpret_cast<PMsg*>(base + kRecvOff) + s; }
   __device__ Finals* fin(int f) const { return reinterpret_cast<Finals*>(base + kFinOff) + f; }
@@ -214,8 +223,11 @@ __device__ void scorer_producer_role(const Smem& sm, const CUtensorMap* map, con
           ok = false;
           break;
         }
+        VTRACE_CHUNK(0, g);
         mbar_arrive_expect_tx(&c.cfull[slot], (uint32_t)kKChunkBytes);
+        // two 64-row boxes per 128-row chunk (the TMA serves short boxes with lower latency)
         tma_load_2d(smem_u32(sm.kslot(slot)), map, 64 * ch, y, smem_u32(&c.cfull[slot]));
+        tma_load_2d(smem_u32(sm.kslot(slot)) + kVChunkBytes, map, 64 * ch, y + kVTile, smem_u32(&c.cfull[slot]));
       }
       prefetch_tile(sp, ui, t + kPrefetchTiles);
     }
@@ -275,6 +287,7 @@ __device__ void scorer_mma_role(const Smem& sm, const PlanParams& plan, const Tc
           break;
         }
         if (ch == 0) VTRACE(1, it);
+        VTRACE_CHUNK(1, g);
         tc_fence_after();
         const uint32_t kb = smem_u32(sm.kslot(slot));
 #pragma unroll
@@ -286,6 +299,7 @@ __device__ void scorer_mma_role(const Smem& sm, const PlanParams& plan, const Tc
             mma_ss(d, smem_desc(rope + k * 32, 16, 1024), bdesc, idesc, 1u);
         }
         mma_commit(&c.cfree[slot]);
+        VTRACE_CHUNK(2, g);
       }
       if (!ok) break;
       mma_commit(&c.sfull[sb]);
@@ -394,9 +408,18 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
       for (int j = 1; j < 64; ++j) mh = fmaxf(mh, x[j]);
       c.pmax[half][row] = mh;
       const bool last = t == ui.n_tiles - 1;
-      if (tid == 0) VTRACE(4, it);
-      if (tid == 0) bulk_wait_group_read<0>();  // the previous tile's messages have left the staging slots
-      named_bar_sync(1, 256);
+      if (tid == 0) {
+        VTRACE(4, it);
+        // both receive slots of this tile's messages free again on the mixer
+        bool go = !c.abort_flag;
+        for (int m = 0; m < 2 && go; ++m) {
+          const int n = 2 * it + m;
+          go = wait_bar(c, &c.pfree[n % kSlots], ((n / kSlots) & 1) ^ 1, a.status, 301, true);
+        }
+        c.wg_go = go ? 1u : 0u;
+      }
+      named_bar_sync(1, 256);  // partial maxima visible; slots granted
+      const bool go = c.wg_go != 0;
       const float mt = fmaxf(mh, c.pmax[half ^ 1][row]);
       float alpha = 1.f;
       if (mt > m_ref + kTau) {
@@ -418,53 +441,44 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
         }
       }
       l += lsum;
-      // P row -> message `half`, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7))
-      PMsg* msg = sm.stage(half);
-      uint8_t* prow = msg->p + row * 128;
+      // P row -> message `half` in the mixer's receive slot, 128-byte swizzle
+      // (16-byte granule g of row `row` at g ^ (row & 7))
+      const int slot = (2 * it + half) % kSlots;
+      PMsg* msg = sm.recv(slot);  // same offset in the mixer CTA
+      if (go) {
+        const uint32_t prow = mapa(smem_u32(msg->p + row * 128), 1);
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        *reinterpret_cast<uint4*>(prow + ((g ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-      // the rescale goes with the tile's first message; the second leaves O as it is
-      msg->alpha[row] = half == 0 ? alpha : 1.f;
+        for (int g = 0; g < 8; ++g)
+          st_cluster_v4(prow + ((g ^ (row & 7)) << 4), make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
+        // the rescale goes with the tile's first message; the second leaves O as it is
+        st_cluster_u32(mapa(smem_u32(&msg->alpha[row]), 1), __float_as_uint(half == 0 ? alpha : 1.f));
+      }
       const unsigned any = __ballot_sync(0xffffffffu, half == 0 && alpha != 1.f);
       if (lane == 0) c.warp_flags[wslot] = any ? 1u : 0u;
       if (last && half == 1) c.lpart[row] = l;
-      fence_proxy_async_smem();
+      fence_proxy_async_cluster();
       named_bar_sync(1, 256);
-      if (last) {
+      if (last && half == 0 && go) {
         // unit finals: running max and the row sum of both halves
-        if (half == 0) {
-          sm.fin_stage(uu & 1)->m[row] = m_ref;
-          sm.fin_stage(uu & 1)->l[row] = l + c.lpart[row];
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 256);
+        Finals* fin = sm.fin(uu & 1);
+        st_cluster_u32(mapa(smem_u32(&fin->m[row]), 1), __float_as_uint(m_ref));
+        st_cluster_u32(mapa(smem_u32(&fin->l[row]), 1), __float_as_uint(l + c.lpart[row]));
       }
+      if (last) named_bar_sync(1, 256);
       if (tid == 0) {
-        bool go = !c.abort_flag;
         if (go) {
           uint32_t f = 0;
 #pragma unroll
           for (int w = 0; w < 8; ++w) f |= c.warp_flags[w];
-          sm.stage(0)->flags = f;
-          sm.stage(1)->flags = 0;
-          fence_proxy_async_smem();
+          const int s0 = (2 * it) % kSlots, s1 = (2 * it + 1) % kSlots;
+          st_cluster_u32(mapa(smem_u32(&sm.recv(s0)->flags), 1), f);
+          st_cluster_u32(mapa(smem_u32(&sm.recv(s1)->flags), 1), 0u);
+          VTRACE(5, it);
+          // release: every store above is visible to the mixer once it sees the arrival
+          mbar_arrive_remote(mapa(smem_u32(&c.pfull[s0]), 1));
+          mbar_arrive_remote(mapa(smem_u32(&c.pfull[s1]), 1));
+          if (last) mbar_arrive_remote(mapa(smem_u32(&c.finfull[uu & 1]), 1));
         }
-        for (int m = 0; m < 2 && go; ++m) {
-          const int n = 2 * it + m;  // message index
-          const int slot = n % kSlots;
-          go = wait_bar(c, &c.pfree[slot], ((n / kSlots) & 1) ^ 1, a.status, 301, true);
-          if (go) {
-            if (m == 0) VTRACE(5, it);
-            bulk_s2s_cluster(mapa(smem_u32(sm.recv(slot)), 1), smem_u32(sm.stage(m)), kMsgBytes,
-                             mapa(smem_u32(&c.pfull[slot]), 1));
-          }
-        }
-        if (go && last)
-          bulk_s2s_cluster(mapa(smem_u32(sm.fin(uu & 1)), 1), smem_u32(sm.fin_stage(uu & 1)), sizeof(Finals),
-                           mapa(smem_u32(&c.finfull[uu & 1]), 1));
-        bulk_commit_group();
         c.wg_stop = go ? 0 : 1;
       }
       named_bar_sync(1, 256);
@@ -475,7 +489,6 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
     }
     if (stop) break;
   }
-  if (tid == 0) bulk_wait_group_read<0>();
 }
 
 // ------------------------------------------------------------------ CTA 1: P V issuer (warp 1, lane 0)
@@ -551,10 +564,7 @@ __device__ void mixer_release_role(const Smem& sm, const PlanParams& plan, const
     const int ps = n % kSlots;
     if (!wait_bar(c, &c.pdone[ps], (n / kSlots) & 1, a.status, 500)) return;
     VTRACE(10, n);
-    if (n + kSlots < total) {
-      mbar_arrive_expect_tx(&c.pfull[ps], kMsgBytes);
-      mbar_arrive_remote(mapa(smem_u32(&c.pfree[ps]), 0));
-    }
+    if (n + kSlots < total) mbar_arrive_remote(mapa(smem_u32(&c.pfree[ps]), 0));
   }
 }
 
@@ -657,12 +667,7 @@ __device__ void mixer_epilogue_role(const Smem& sm, const PlanParams& plan, cons
     }
     tc_fence_before();
     named_bar_sync(2, 128);
-    if (tid == 0) {
-      // a finals buffer is re-armed for the unit two ahead once it has been read
-      if ((cmd & 0xFF) == kCmdEpilogue && ui_idx + 1 < u_end)
-        mbar_arrive_expect_tx(&c.finfull[(uu + 1) & 1], sizeof(Finals));
-      mbar_arrive(&c.cmd_done);
-    }
+    if (tid == 0) mbar_arrive(&c.cmd_done);
   }
 }
 
@@ -703,19 +708,12 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     mbar_init(&c.obar, 1);
     c.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(rank == 0 ? &k_map : &v_map);
+    prefetch_tensormap(&v_map);
   }
   __syncwarp();
   if (warp == 0) {
     tmem_alloc(&c.tmem_base, 512);
     tmem_relinquish();
-  }
-  if (rank == 1 && threadIdx.x == 64) {  // thread 0 of the epilogue group
-    // receive slots and finals buffers armed before the partner can send
-    int n_units = u_end - u_begin, total = 0;
-    for (int k = u_begin; k < u_end; ++k) total += 2 * decode_unit(plan, sched.order[k]).n_tiles;
-    for (int s = 0; s < kSlots && s < total; ++s) mbar_arrive_expect_tx(&c.pfull[s], kMsgBytes);
-    for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&c.finfull[s], sizeof(Finals));
   }
   __syncwarp();
   tc_fence_before();
@@ -727,7 +725,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
   if (warp == 0) {
     if (lane == 0) {
-      if (rank == 0) scorer_producer_role(sm, &k_map, plan, sched, a, u_begin, u_end);
+      if (rank == 0) scorer_producer_role(sm, &v_map, plan, sched, a, u_begin, u_end);
       else mixer_producer_role(sm, &v_map, plan, sched, a, u_begin, u_end);
     }
   } else if (warp == 1) {
@@ -860,6 +858,11 @@ extern "C" int vmla_trace_read(uint64_t* host, int n) {
   const int total = vmla::kTraceEvents * vmla::kTraceTiles;
   if (n > total) n = total;
   return cudaMemcpyFromSymbol(host, vmla::g_vmla_trace, sizeof(uint64_t) * n) == cudaSuccess ? n : -1;
+}
+extern "C" int vmla_trace_chunks_read(uint64_t* host, int n) {
+  const int total = 3 * vmla::kTraceChunks;
+  if (n > total) n = total;
+  return cudaMemcpyFromSymbol(host, vmla::g_vmla_trace_chunks, sizeof(uint64_t) * n) == cudaSuccess ? n : -1;
 }
 extern "C" int vmla_trace_clear(void) {
   static uint64_t zeros[vmla::kTraceEvents * vmla::kTraceTiles] = {};
