@@ -26,7 +26,7 @@ PlanShape plan_shape(int kernel) {
     // about two units per cluster leave the greedy schedule room to balance
     s.rows_per_unit = 128;
     s.units_per_sm = 2;  // per pair of SMs; the caller halves the SM count
-    s.key_align = 128;   // the scorer's tile
+    s.key_align = 64;    // the kernel's tile
     s.min_chunk = 1024;
     s.max_splits = 64;
   }

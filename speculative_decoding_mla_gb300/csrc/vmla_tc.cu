@@ -13,22 +13,21 @@
 //
 // A work unit is 128 query rows (r = i*H + h) of one sequence over one
 // contiguous piece of its key range, and runs on a cluster of two CTAs:
-//   CTA 0 ("scorer")  keeps Q's 512 latent dims in tensor memory (A operand)
-//                     and its 64 rope dims in shared memory, computes S = Q K^T
-//                     for 128-key tiles (N = 128 MMAs) into double-buffered TMEM
-//                     columns, runs the online softmax (two threads per row),
-//                     and writes P (bf16) as two 64-key messages with per-row
-//                     rescale factors straight into CTA 1's shared memory
-//                     (distributed shared-memory stores; no copy engine, so the
-//                     scorer's TMA queue carries only its own K loads).
+//   CTA 0 ("scorer")  keeps Q [128 x 576] in tensor memory (A operand),
+//                     computes S = Q K^T for 64-key tiles into double-buffered
+//                     TMEM columns, runs the online softmax (two threads per
+//                     row), and writes P (bf16, 128 x 64) with per-row rescale
+//                     factors straight into CTA 1's shared memory (distributed
+//                     shared-memory stores: no staging copy, which leaves room
+//                     for three K stages).
 //   CTA 1 ("mixer")   keeps O [128 x 512] fp32 in tensor memory and computes
-//                     O = alpha * O + P V over 64-key tiles of the latent part
-//                     of the same rows, then normalises and writes the result.
+//                     O = alpha * O + P V with V the latent part of the same
+//                     rows, then normalises and writes the result.
 // The split of the work follows from tensor-memory capacity: O for 128 rows
 // fills one SM's 512 TMEM columns, so Q and S live on the partner SM.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer; CTA 0:
-// warps 2-9 softmax, two threads per row (each 64 of the tile's 128 keys);
+// warps 2-9 softmax, two threads per row (each 32 of the tile's 64 keys);
 // CTA 1: warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
 // status word, tells the partner CTA to stop, drains its own copies and MMAs,
@@ -49,16 +48,14 @@ constexpr int kRowsTC = 128;
 constexpr int kThreadsTC = 320;       // 10 warps
 constexpr int kChunks = kDqk / 64;    // 9 column chunks of 64 bf16 (128 bytes) per row
 constexpr int kVChunks = kDv / 64;    // 8 of them are the latent / value part
-constexpr int kKTile = 128;           // keys per score tile (scorer)
-constexpr int kVTile = 64;            // keys per value tile (mixer) = keys per P message
-constexpr int kRing = 12;             // scorer K ring: column chunks of 128-key tiles (16 KB each)
-constexpr int kKChunkBytes = kKTile * 128;
-constexpr int kVChunkBytes = kVTile * 128;
+constexpr int kTile = 64;             // keys per tile (one P message per tile)
+constexpr int kKStages = 3;           // scorer K stages (9 chunks each)
+constexpr int kVStages = 2;           // mixer V stages (8 chunks each)
+constexpr int kChunkBytes = kTile * 128;
 constexpr int kSlots = 4;             // mixer P receive slots
-constexpr uint32_t kSCol = 256;       // S buffers at TMEM columns 256 and 384 (Q latent uses 0..255)
+constexpr uint32_t kSCol = 384;       // S buffers at TMEM columns 384 and 448 (Q uses 0..287)
 constexpr float kTau = 8.0f;          // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-constexpr int kPrefetchTiles = 0;     // 128-key tiles the scorer prefetches into L2 ahead of its loads (0: off)
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
@@ -106,18 +103,17 @@ struct __align__(16) Finals {
 // Shared-memory map (byte offsets from the 1024-aligned base).  The two CTAs
 // use different regions; the barriers and small state sit at the same offset
 // in both, so either CTA can address the other's copy through mapa.
-constexpr uint32_t kQRopeOff = 0;                                   // CTA 0: Q rope chunk, 16 KB
-constexpr uint32_t kKRingOff = kQRopeOff + kRowsTC * 128;           // CTA 0: 10 x 16 KB
-constexpr uint32_t kScorerEnd = kKRingOff + kRing * kKChunkBytes;
+constexpr uint32_t kKOff = 0;                                       // CTA 0: 3 stages x 9 x 8 KB
+constexpr uint32_t kScorerEnd = kKOff + kKStages * kChunks * kChunkBytes;
 constexpr uint32_t kVOff = 0;                                       // CTA 1: 2 stages x 8 x 8 KB
-constexpr uint32_t kRecvOff = kVOff + 2 * kVChunks * kVChunkBytes;  // CTA 1: 4 incoming messages
+constexpr uint32_t kRecvOff = kVOff + kVStages * kVChunks * kChunkBytes;  // CTA 1: 4 incoming messages
 constexpr uint32_t kFinOff = kRecvOff + kSlots * sizeof(PMsg);      // CTA 1: 2 x Finals
 constexpr uint32_t kMixerEnd = kFinOff + 2 * sizeof(Finals);
 constexpr uint32_t kCommonOff = (kScorerEnd > kMixerEnd ? kScorerEnd : kMixerEnd);
 
 struct Common {
-  uint64_t cfull[kRing], cfree[kRing];  // CTA 0: K chunk ring
-  uint64_t vfull[2], vfree[2];          // CTA 1: V stages
+  uint64_t kfull[kKStages], kfree[kKStages];  // CTA 0: K stages
+  uint64_t vfull[kVStages], vfree[kVStages];  // CTA 1: V stages
   uint64_t sfull[2], sfree[2];          // CTA 0: S buffers
   uint64_t qfull;                       // CTA 0: Q of the unit in place
   uint64_t pfull[kSlots];               // CTA 1: message received
@@ -142,15 +138,14 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct Smem {
   uint8_t* base;
   Common* c;
-  __device__ uint8_t* qrope() const { return base + kQRopeOff; }
-  __device__ uint8_t* kslot(int s) const { return base + kKRingOff + s * kKChunkBytes; }
-  __device__ uint8_t* vchunk(int s, int c) const { return base + kVOff + (s * kVChunks + c) * kVChunkBytes; }
+  __device__ uint8_t* kchunk(int s, int c) const { return base + kKOff + (s * kChunks + c) * kChunkBytes; }
+  __device__ uint8_t* vchunk(int s, int c) const { return base + kVOff + (s * kVChunks + c) * kChunkBytes; }
   __device__ PMsg* recv(int s) const { return reinterpret_cast<PMsg*>(base + kRecvOff) + s; }
   __device__ Finals* fin(int f) const { return reinterpret_cast<Finals*>(base + kFinOff) + f; }
 };
 
 struct UnitInfo {
-  int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;  // n_tiles: 128-key tiles
+  int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;  // n_tiles: 64-key tiles
 };
 
 __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
@@ -164,7 +159,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
   ui.prefix = s.n_kv - s.n_q;
   ui.k_lo = ui.piece * s.chunk;
   ui.k_hi = min(s.n_kv, ui.k_lo + s.chunk);
-  ui.n_tiles = (ui.k_hi - ui.k_lo + kKTile - 1) / kKTile;
+  ui.n_tiles = (ui.k_hi - ui.k_lo + kTile - 1) / kTile;
   return ui;
 }
 
@@ -194,115 +189,82 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// ------------------------------------------------------------------ CTA 0: K producer (warp 0, lane 0)
-// Each 128-key tile is 9 column chunks (16 KB each: 128 rows x 64 columns,
-// 128-byte swizzle) of the staged rows, streamed through a 10-slot ring so a
-// chunk of the next tile loads as soon as the MMAs free a slot.
-__device__ void scorer_producer_role(const Smem& sm, const CUtensorMap* map, const PlanParams& plan,
-                                     const TcSched& sched, const RunArgs& a, int u_begin, int u_end) {
-  Common& c = *sm.c;
-  int g = 0;
-  bool ok = true;
-  auto prefetch_tile = [&](const SeqPlan& sp, const UnitInfo& ui, int t) {
-    if (t >= ui.n_tiles) return;
-    const int64_t row0 = (int64_t)sp.kv_off + ui.k_lo + (int64_t)t * kKTile;
-    int64_t rows = a.total_kv - row0;
-    if (rows > kKTile) rows = kKTile;
-    if (rows > 0) prefetch_l2_bulk(a.staged + row0 * kDqk, (uint32_t)(rows * kRowBytes));
-  };
-  for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    const SeqPlan& sp = plan.seq[ui.b];
-    for (int t = 0; t < kPrefetchTiles; ++t) prefetch_tile(sp, ui, t);
-    for (int t = 0; t < ui.n_tiles && ok; ++t) {
-      VTRACE(0, g / kChunks);
-      const int y = sp.kv_off + ui.k_lo + t * kKTile;
-      for (int ch = 0; ch < kChunks; ++ch, ++g) {
-        const int slot = g % kRing;
-        if (!wait_bar(c, &c.cfree[slot], ((g / kRing) & 1) ^ 1, a.status, 100)) {
-          ok = false;
-          break;
-        }
-        VTRACE_CHUNK(0, g);
-        mbar_arrive_expect_tx(&c.cfull[slot], (uint32_t)kKChunkBytes);
-        // two 64-row boxes per 128-row chunk (the TMA serves short boxes with lower latency)
-        tma_load_2d(smem_u32(sm.kslot(slot)), map, 64 * ch, y, smem_u32(&c.cfull[slot]));
-        tma_load_2d(smem_u32(sm.kslot(slot)) + kVChunkBytes, map, 64 * ch, y + kVTile, smem_u32(&c.cfull[slot]));
-      }
-      prefetch_tile(sp, ui, t + kPrefetchTiles);
-    }
-  }
-  // drain: every issued load has landed before the CTA may exit
-  for (int k = 1; k <= kRing && g - k >= 0; ++k) drain_wait(&c.cfull[(g - k) % kRing], ((g - k) / kRing) & 1);
-}
-
-// ------------------------------------------------------------------ CTA 1: V producer (warp 0, lane 0)
-__device__ void mixer_producer_role(const Smem& sm, const CUtensorMap* map, const PlanParams& plan,
-                                    const TcSched& sched, const RunArgs& a, int u_begin, int u_end) {
-  Common& c = *sm.c;
+// ------------------------------------------------------------------ producers (warp 0, lane 0)
+// Each 64-key tile of the unit's key range is loaded from the staged rows as
+// one 64-row x 64-column box (8 KB, 128-byte swizzle) per column chunk: 9 for
+// the scorer (K), 8 for the mixer (V).  Rows past the piece's end belong to
+// other keys and are masked by the softmax.
+__device__ bool load_tiles(Common& c, const Smem& sm, const CUtensorMap* map, const PlanParams& plan,
+                           const TcSched& sched, const RunArgs& a, int u_begin, int u_end, int nch, int stages,
+                           uint64_t* full, uint64_t* freeb, int* issued) {
   int it = 0;
   bool ok = true;
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
-    for (int t = 0; t < 2 * ui.n_tiles; ++t, ++it) {
-      const int s = it & 1;
-      if (!wait_bar(c, &c.vfree[s], ((it >> 1) & 1) ^ 1, a.status, 110)) {
+    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
+      const int s = it % stages;
+      if (!wait_bar(c, &freeb[s], ((it / stages) & 1) ^ 1, a.status, 100 + nch)) {
         ok = false;
         break;
       }
-      VTRACE(6, it);
-      const int y = sp.kv_off + ui.k_lo + t * kVTile;
-      mbar_arrive_expect_tx(&c.vfull[s], (uint32_t)(kVChunks * kVChunkBytes));
-      for (int ch = 0; ch < kVChunks; ++ch) tma_load_2d(smem_u32(sm.vchunk(s, ch)), map, 64 * ch, y, smem_u32(&c.vfull[s]));
+      VTRACE(nch == kChunks ? 0 : 6, it);
+      const int y = sp.kv_off + ui.k_lo + t * kTile;
+      mbar_arrive_expect_tx(&full[s], (uint32_t)(nch * kChunkBytes));
+      uint8_t* dst = nch == kChunks ? sm.kchunk(s, 0) : sm.vchunk(s, 0);
+      for (int ch = 0; ch < nch; ++ch) tma_load_2d(smem_u32(dst + ch * kChunkBytes), map, 64 * ch, y, smem_u32(&full[s]));
     }
   }
-  for (int k = 1; k <= 2 && it - k >= 0; ++k) drain_wait(&c.vfull[(it - k) & 1], ((it - k) >> 1) & 1);
+  *issued = it;
+  return ok;
+}
+
+__device__ void producer_role(const Smem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
+                              const RunArgs& a, int u_begin, int u_end, bool scorer) {
+  Common& c = *sm.c;
+  const int stages = scorer ? kKStages : kVStages;
+  uint64_t* full = scorer ? c.kfull : c.vfull;
+  uint64_t* freeb = scorer ? c.kfree : c.vfree;
+  int it = 0;
+  load_tiles(c, sm, map, plan, sched, a, u_begin, u_end, scorer ? kChunks : kVChunks, stages, full, freeb, &it);
+  // drain: every issued load has landed before the CTA may exit
+  for (int k = 1; k <= stages && it - k >= 0; ++k) drain_wait(&full[(it - k) % stages], ((it - k) / stages) & 1);
 }
 
 // ------------------------------------------------------------------ CTA 0: QK^T issuer (warp 1, lane 0)
 __device__ void scorer_mma_role(const Smem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                 uint32_t tbase, int u_begin, int u_end) {
   Common& c = *sm.c;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kKTile, 0, 0);
-  const uint32_t rope = smem_u32(sm.qrope());
-  int g = 0, it = 0, uu = 0;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, kTile, 0, 0);
+  int it = 0, uu = 0;
   bool ok = true;
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     if (!wait_bar(c, &c.qfull, uu & 1, a.status, 200)) break;
     tc_fence_after();
-    for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
-      const int sb = it & 1;
+    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
+      const int s = it % kKStages, sb = it & 1;
+      if (!wait_bar(c, &c.kfull[s], (it / kKStages) & 1, a.status, 201)) {
+        ok = false;
+        break;
+      }
+      VTRACE(1, it);
       if (!wait_bar(c, &c.sfree[sb], ((it >> 1) & 1) ^ 1, a.status, 202)) {
         ok = false;
         break;
       }
       VTRACE(2, it);
-      const uint32_t d = tbase + kSCol + (uint32_t)sb * kKTile;
-      for (int ch = 0; ch < kChunks; ++ch, ++g) {
-        const int slot = g % kRing;
-        if (!wait_bar(c, &c.cfull[slot], (g / kRing) & 1, a.status, 201)) {
-          ok = false;
-          break;
-        }
-        if (ch == 0) VTRACE(1, it);
-        VTRACE_CHUNK(1, g);
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sm.kslot(slot));
+      tc_fence_after();
+      const uint32_t d = tbase + kSCol + (uint32_t)sb * kTile;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bdesc = smem_desc(kb + k * 32, 16, 1024);
-          if (ch < kVChunks)
-            mma_ts(d, tbase + (uint32_t)(ch * 32 + k * 8), bdesc, idesc, (ch | k) != 0);
-          else
-            mma_ss(d, smem_desc(rope + k * 32, 16, 1024), bdesc, idesc, 1u);
-        }
-        mma_commit(&c.cfree[slot]);
-        VTRACE_CHUNK(2, g);
+      for (int ch = 0; ch < kChunks; ++ch) {
+        const uint32_t kb = smem_u32(sm.kchunk(s, ch));
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(d, tbase + (uint32_t)(ch * 32 + k * 8), smem_desc(kb + k * 32, 16, 1024), idesc, (ch | k) != 0);
       }
-      if (!ok) break;
       mma_commit(&c.sfull[sb]);
+      mma_commit(&c.kfree[s]);
     }
   }
   // all issued MMAs complete before the CTA may exit
@@ -311,8 +273,8 @@ __device__ void scorer_mma_role(const Smem& sm, const PlanParams& plan, const Tc
 }
 
 // ------------------------------------------------------------------ CTA 0: softmax (warps 2-9)
-// Thread (half, row): row = TMEM lane, keys [64*half, 64*half + 64) of each
-// 128-key tile; it builds message `half` of the tile (P for those 64 keys).
+// Thread (half, row): row = TMEM lane, keys [32*half, 32*half + 32) of each
+// 64-key tile; it writes granules 4*half .. 4*half + 3 of the row's P.
 // The two halves of a row agree on the tile max through shared memory, so both
 // keep the same running reference max m_ref (raised only when a tile exceeds it
 // by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
@@ -321,7 +283,7 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
   Common& c = *sm.c;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;                 // TMEM lane quarter this warp may access
-  const int half = (warp - 2) >> 2;        // 0: keys 0..63, 1: keys 64..127 of a tile
+  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a tile
   const int row = wq * 32 + lane;          // query row within the unit = TMEM lane
   const int tid = threadIdx.x - 64;        // 0..255 within the softmax group
   const int wslot = warp - 2;              // 0..7
@@ -334,14 +296,13 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsTC + row;
     const bool valid = r < ui.R;
-    // Q rows of this unit: latent chunks 0..7 into TMEM columns 0..255 (two
-    // bf16 per column, half 0 the even chunks, half 1 the odd ones); the rope
-    // chunk into shared memory (K-major, 128-byte swizzle) by half 1
+    // Q rows of this unit into TMEM columns 0..287 (two bf16 per column); each
+    // half of the group writes its own column chunks
     __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
-      for (int ch = half; ch < kVChunks; ch += 2) {
+      for (int ch = half; ch < kChunks; ch += 2) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -353,15 +314,7 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
         }
         tmem_st32(tbase + lane_base + (uint32_t)(ch * 32), v);
       }
-      if (half == 1) {
-        uint8_t* dst = sm.qrope() + row * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(dst + ((k ^ (row & 7)) << 4)) =
-              valid ? __ldg(qrow + kVChunks * 8 + k) : make_uint4(0, 0, 0, 0);
-      }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 256);
       if (tid == 0) mbar_arrive(&c.qfull);
@@ -379,24 +332,22 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
       if (tid == 0) VTRACE(3, it);
       __syncwarp();
       tc_fence_after();
-      uint32_t v[64];
-      const uint32_t scol = tbase + lane_base + kSCol + (uint32_t)sb * kKTile + (uint32_t)half * 64;
-      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      uint32_t v[32];
+      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)sb * kTile + (uint32_t)half * 32, v);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&c.sfree[sb]);
 
-      const int key0 = ui.k_lo + t * kKTile + half * 64;
-      float x[64];
+      const int key0 = ui.k_lo + t * kTile + half * 32;
+      float x[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(v[j]) * scale;
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * scale;
       if (!valid) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = -INFINITY;
-      } else if (key0 + 64 > mask_from) {
+        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
+      } else if (key0 + 32 > mask_from) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 32; ++j) {
           const int key = key0 + j;
           bool vis_j = key < ui.k_hi;
           if (vis_j && key >= ui.prefix) vis_j = ((vis >> (key - ui.prefix)) & 1ull) != 0;
@@ -405,17 +356,14 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
       }
       float mh = x[0];
 #pragma unroll
-      for (int j = 1; j < 64; ++j) mh = fmaxf(mh, x[j]);
+      for (int j = 1; j < 32; ++j) mh = fmaxf(mh, x[j]);
       c.pmax[half][row] = mh;
       const bool last = t == ui.n_tiles - 1;
       if (tid == 0) {
         VTRACE(4, it);
-        // both receive slots of this tile's messages free again on the mixer
+        // the receive slot of this tile's message free again on the mixer
         bool go = !c.abort_flag;
-        for (int m = 0; m < 2 && go; ++m) {
-          const int n = 2 * it + m;
-          go = wait_bar(c, &c.pfree[n % kSlots], ((n / kSlots) & 1) ^ 1, a.status, 301, true);
-        }
+        if (go) go = wait_bar(c, &c.pfree[it % kSlots], ((it / kSlots) & 1) ^ 1, a.status, 301, true);
         c.wg_go = go ? 1u : 0u;
       }
       named_bar_sync(1, 256);  // partial maxima visible; slots granted
@@ -427,31 +375,32 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
         l *= alpha;
         m_ref = mt;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
       float lsum = 0.f;
       if (m_ref == -INFINITY) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = 0u;
+        for (int k = 0; k < 16; ++k) pk[k] = 0u;
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 16; ++k) {
           const float p0 = ex2_approx(x[2 * k] - m_ref), p1 = ex2_approx(x[2 * k + 1] - m_ref);
           lsum += p0 + p1;
           pk[k] = pack_bf16x2(p0, p1);
         }
       }
       l += lsum;
-      // P row -> message `half` in the mixer's receive slot, 128-byte swizzle
-      // (16-byte granule g of row `row` at g ^ (row & 7))
-      const int slot = (2 * it + half) % kSlots;
+      // P row -> the mixer's receive slot, 128-byte swizzle (16-byte granule g of
+      // row `row` at g ^ (row & 7)); this half owns granules 4*half .. 4*half + 3
+      const int slot = it % kSlots;
       PMsg* msg = sm.recv(slot);  // same offset in the mixer CTA
       if (go) {
         const uint32_t prow = mapa(smem_u32(msg->p + row * 128), 1);
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-          st_cluster_v4(prow + ((g ^ (row & 7)) << 4), make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]));
-        // the rescale goes with the tile's first message; the second leaves O as it is
-        st_cluster_u32(mapa(smem_u32(&msg->alpha[row]), 1), __float_as_uint(half == 0 ? alpha : 1.f));
+        for (int k = 0; k < 4; ++k) {
+          const int g = 4 * half + k;
+          st_cluster_v4(prow + ((g ^ (row & 7)) << 4), make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]));
+        }
+        if (half == 0) st_cluster_u32(mapa(smem_u32(&msg->alpha[row]), 1), __float_as_uint(alpha));
       }
       const unsigned any = __ballot_sync(0xffffffffu, half == 0 && alpha != 1.f);
       if (lane == 0) c.warp_flags[wslot] = any ? 1u : 0u;
@@ -470,13 +419,10 @@ __device__ void scorer_softmax_role(const Smem& sm, const PlanParams& plan, cons
           uint32_t f = 0;
 #pragma unroll
           for (int w = 0; w < 8; ++w) f |= c.warp_flags[w];
-          const int s0 = (2 * it) % kSlots, s1 = (2 * it + 1) % kSlots;
-          st_cluster_u32(mapa(smem_u32(&sm.recv(s0)->flags), 1), f);
-          st_cluster_u32(mapa(smem_u32(&sm.recv(s1)->flags), 1), 0u);
+          st_cluster_u32(mapa(smem_u32(&sm.recv(slot)->flags), 1), f);
           VTRACE(5, it);
           // release: every store above is visible to the mixer once it sees the arrival
-          mbar_arrive_remote(mapa(smem_u32(&c.pfull[s0]), 1));
-          mbar_arrive_remote(mapa(smem_u32(&c.pfull[s1]), 1));
+          mbar_arrive_remote(mapa(smem_u32(&c.pfull[slot]), 1));
           if (last) mbar_arrive_remote(mapa(smem_u32(&c.finfull[uu & 1]), 1));
         }
         c.wg_stop = go ? 0 : 1;
@@ -513,9 +459,9 @@ __device__ void mixer_mma_role(const Smem& sm, const PlanParams& plan, const TcS
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    for (int t = 0; t < 2 * ui.n_tiles; ++t, ++it) {
-      const int s = it & 1, ps = it % kSlots;
-      if (!wait_bar(c, &c.vfull[s], (it >> 1) & 1, a.status, 400)) {
+    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
+      const int s = it % kVStages, ps = it % kSlots;
+      if (!wait_bar(c, &c.vfull[s], (it / kVStages) & 1, a.status, 400)) {
         ok = false;
         break;
       }
@@ -538,7 +484,7 @@ __device__ void mixer_mma_role(const Smem& sm, const PlanParams& plan, const TcS
         const uint64_t adesc = smem_desc(pbase + k * 32, 16, 1024);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint64_t bdesc = smem_desc(smem_u32(sm.vchunk(s, 4 * hh)) + k * 16 * 128, kVChunkBytes, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sm.vchunk(s, 4 * hh)) + k * 16 * 128, kChunkBytes, 1024);
           mma_ss(tbase + (uint32_t)(256 * hh), adesc, bdesc, idesc, (t > 0 || k > 0) ? 1u : 0u);
         }
       }
@@ -559,7 +505,7 @@ __device__ void mixer_release_role(const Smem& sm, const PlanParams& plan, const
                                    int u_begin, int u_end) {
   Common& c = *sm.c;
   int total = 0;
-  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx) total += 2 * decode_unit(plan, sched.order[ui_idx]).n_tiles;
+  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx) total += decode_unit(plan, sched.order[ui_idx]).n_tiles;
   for (int n = 0; n < total; ++n) {
     const int ps = n % kSlots;
     if (!wait_bar(c, &c.pdone[ps], (n / kSlots) & 1, a.status, 500)) return;
@@ -672,8 +618,8 @@ __device__ void mixer_epilogue_role(const Smem& sm, const PlanParams& plan, cons
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
-                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
+tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ PlanParams plan,
+                 const __grid_constant__ TcSched sched, const RunArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -686,13 +632,15 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
   const int u_end = cid < sched.num_clusters ? sched.start[cid + 1] : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&c.cfull[s], 1);
-      mbar_init(&c.cfree[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&c.kfull[s], 1);
+      mbar_init(&c.kfree[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&c.vfull[s], 1);
       mbar_init(&c.vfree[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&c.sfull[s], 1);
       mbar_init(&c.sfree[s], 256);
       mbar_init(&c.finfull[s], 1);
@@ -708,7 +656,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     mbar_init(&c.obar, 1);
     c.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&v_map);
+    prefetch_tensormap(&kv_map);
   }
   __syncwarp();
   if (warp == 0) {
@@ -725,8 +673,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
   if (warp == 0) {
     if (lane == 0) {
-      if (rank == 0) scorer_producer_role(sm, &v_map, plan, sched, a, u_begin, u_end);
-      else mixer_producer_role(sm, &v_map, plan, sched, a, u_begin, u_end);
+      producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -772,7 +719,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 2 * sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 }  // namespace
@@ -820,18 +767,13 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   static thread_local TcSched sched;
   rc = build_tc_schedule(plan, clusters, &sched);
   if (rc != VMLA_OK) return rc;
-  // 2-D maps over the staged rows [total_kv x 576 bf16], 128-byte swizzle: boxes of
-  // 64 columns x 128 rows (K chunks of a score tile) and 64 columns x 64 rows (V chunks)
-  CUtensorMap kmap, vmap;
+  // 2-D map over the staged rows [total_kv x 576 bf16], boxes of 64 columns x 64 rows, 128-byte swizzle
+  CUtensorMap map;
   cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(a.total_kv > 0 ? a.total_kv : 1)};
   cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  cuuint32_t kbox[2] = {64, (cuuint32_t)kKTile};
-  cuuint32_t vbox[2] = {64, (cuuint32_t)kVTile};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
   cuuint32_t estride[2] = {1, 1};
-  if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, kbox, estride,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, vbox, estride,
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, box, estride,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return VMLA_ERR_CUDA;
@@ -847,7 +789,7 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, map, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 
