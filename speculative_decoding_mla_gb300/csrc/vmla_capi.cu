@@ -54,7 +54,11 @@ int current_sm_count(int* sms, bool require_sm103) {
   return VMLA_OK;
 }
 
-int run(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+}  // namespace
+
+namespace vmla {
+
+int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
         const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask, const int32_t* parent,
         const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
         int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
@@ -132,7 +136,7 @@ int run(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, cons
   return rc;
 }
 
-}  // namespace
+}  // namespace vmla
 
 extern "C" {
 
@@ -171,7 +175,7 @@ int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, cons
                     const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch,
                     int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  return run(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
              kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
              workspace_bytes, stream);
 }
@@ -181,7 +185,7 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
                          const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
                          int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  return run(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
+  return run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
              kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
              workspace_bytes, stream);
 }

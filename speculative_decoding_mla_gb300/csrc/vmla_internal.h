@@ -96,6 +96,13 @@ struct RunArgs {
   uint32_t* status;
 };
 
+// One verify call on a caller-provided workspace (argument checks, plan, launches).
+int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+               const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask, const int32_t* parent,
+               const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
+               float sm_scale, int splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+               void* stream);
+
 int launch_simt(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_tc(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_gather(const RunArgs& args, void* stream);
