@@ -129,6 +129,9 @@ int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, cons
                     int batch, int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Fixed size of the scratch array behind verify_attn_mla_simt_static (32 MiB). */
+#define VMLA_STATIC_SCRATCH_BYTES (32u << 20)
+
 /* Same operation and arguments on the plain CUDA-core kernel (one warp per
  * four query rows, scores by FMA and warp shuffles).  A second, independent
  * GPU implementation used to cross-check the tensor-core kernel; its plan
@@ -138,6 +141,31 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
                          const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
                          int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* verify_attn_mla_simt without a workspace argument, for callers that cannot
+ * allocate device memory at call time (an engine whose free HBM is all handed
+ * to its KV cache, an allocator that must not be re-entered, a plugin host
+ * that allows cudaMalloc only during its own set-up).  This entry point has no
+ * counterpart in the pages; it exists only for such callers.
+ * Scratch (status word, ancestor masks, split partials) comes from a fixed
+ * VMLA_STATIC_SCRATCH_BYTES array in the library image, which every device
+ * that loads the library holds until the process exits.  The entry point
+ * allocates and frees nothing.  A plan whose workspace
+ * (verify_attn_mla_plan(VMLA_KERNEL_SIMT, ...).workspace_bytes) exceeds the
+ * array returns VMLA_ERR_WORKSPACE before any launch.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every call
+ * on a device shares the one array and leaves its contents behind: calls that
+ * may overlap on the GPU (different streams without ordering) race on it, so
+ * order them on one stream.  Faults a kernel detects (a slot outside the pool,
+ * malformed parents) are recorded in the array's status word but not reported
+ * by this entry point; diagnose them through verify_attn_mla_simt with a
+ * workspace. */
+int verify_attn_mla_simt_static(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                const int32_t* parent, const int32_t* kv_indptr_host,
+                                const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits,
+                                void* out, float* lse, void* stream);
 
 /* The split merge on its own: o_parts [num_splits, rows, 512] fp32 (each part
  * already normalised by its own softmax sum), lse_parts [num_splits, rows]

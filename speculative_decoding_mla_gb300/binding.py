@@ -37,6 +37,7 @@ EXPORTS = (
     "verify_attn_mla_merge", "verify_attn_mla_tree_mask", "verify_attn_mla_check",
     "verify_attn_mla_host_buffer_size", "verify_attn_mla_host", "verify_attn_mla_status_string",
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
+    "verify_attn_mla_simt_static",
 )
 
 
@@ -71,6 +72,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_version": [],
         "verify_attn_mla_timing_enable": [i32],
         "verify_attn_mla_timing_read": [vp, vp, vp, i32, ctypes.POINTER(i32)],
+        "verify_attn_mla_simt_static": [vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -227,3 +229,18 @@ def verify_attn_mla_timing_read(capacity: int):
     _check(_lib.verify_attn_mla_timing_read(g.ctypes.data, v.ctypes.data, m.ctypes.data, int(capacity),
                                             ctypes.byref(n)), "verify_attn_mla_timing_read")
     return g[: n.value].copy(), v[: n.value].copy(), m[: n.value].copy()
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def verify_attn_mla_simt_static(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out,
+                                lse, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    """CUDA-core verify with the library's fixed scratch array instead of a workspace (no allocation)."""
+    kvh = _host_i32(kv_indptr_host)
+    qoh = _host_i32(qo_indptr_host)
+    rc = _lib.verify_attn_mla_simt_static(_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(kv_indptr),
+                                          _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent),
+                                          kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, int(q.shape[1]),
+                                          float(sm_scale), int(splits), _ptr(out), _ptr(lse), _stream(stream))
+    _check(rc, "verify_attn_mla_simt_static")

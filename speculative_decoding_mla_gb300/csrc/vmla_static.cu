@@ -1,0 +1,58 @@
+// Allocation-free entry point: the CUDA-core verify path with its scratch in a
+// fixed array that lives in the library image on every device that loads it.
+//
+// Some callers cannot allocate device memory when they call in: code that runs
+// under a memory pool or arena it does not own (a serving engine that has
+// handed all free HBM to its KV cache), a custom allocator that must not be
+// re-entered from inside a callback, or a plugin host that forbids cudaMalloc
+// outside its own set-up phase.  They still own their inputs and outputs; this
+// entry point only removes the workspace argument.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "vmla_internal.h"
+
+namespace vmla {
+namespace {
+
+// Scratch for the status word, ancestor masks and split partials of one call.
+__device__ __align__(256) unsigned char g_vmla_static_scratch[VMLA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per
+// device (the host-side symbol is only a stand-in for it).
+int static_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VMLA_ERR_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return VMLA_ERR_DEVICE;
+  std::lock_guard<std::mutex> g(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_vmla_static_scratch) != cudaSuccess || !p) return VMLA_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return VMLA_OK;
+}
+
+}  // namespace
+}  // namespace vmla
+
+extern "C" int verify_attn_mla_simt_static(const void* q, const void* kv_pool, int64_t pool_slots,
+                                           const int32_t* kv_indptr, const int32_t* kv_indices,
+                                           const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                           const int32_t* parent, const int32_t* kv_indptr_host,
+                                           const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
+                                           int splits, void* out, float* lse, void* stream) {
+  void* scratch = nullptr;
+  int rc = vmla::static_scratch(&scratch);
+  if (rc != VMLA_OK) return rc;
+  // a plan that needs more than the array is refused (VMLA_ERR_WORKSPACE) before any launch
+  return vmla::run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask,
+                          parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse,
+                          scratch, VMLA_STATIC_SCRATCH_BYTES, stream);
+}
