@@ -253,7 +253,10 @@ def lognormal_prefixes(seed: int, n: int, median: float = 16384.0, sigma: float 
 #   long_185k       : B=1, P=185,000, 16 causal drafts, 200,000-slot pool, permuted slots
 #   tree_32k        : B=8, P=32,768, 64-node draft trees (depth <= 8), pool = sum N_b, permuted
 #   sweep_q{1,4,16} : B=32, lognormal P (median 16k, clipped 2k..128k), Q in {1,4,16}
-WORKLOADS = ("contiguous_1k", "paged_ragged", "long_185k", "tree_32k", "sweep_q1", "sweep_q4", "sweep_q16")
+#   long_120k       : B=1, P=120,000, 16 causal drafts, 130,000-slot pool (the profiling case: its 150 MB of
+#                     KV rows exceed the L2 while the device holds well under 1 GB)
+WORKLOADS = ("contiguous_1k", "paged_ragged", "long_185k", "tree_32k", "sweep_q1", "sweep_q4", "sweep_q16",
+             "long_120k")
 
 
 def workload(name: str, num_heads: int = NUM_HEADS) -> Case:
@@ -263,6 +266,8 @@ def workload(name: str, num_heads: int = NUM_HEADS) -> Case:
         return make_case(name, [4096, 8192, 16384, 32768], 16, num_heads=num_heads, pool_slots=65600, seed=2)
     if name == "long_185k":
         return make_case(name, [185000], 16, num_heads=num_heads, pool_slots=200000, seed=3)
+    if name == "long_120k":
+        return make_case(name, [120000], 16, num_heads=num_heads, pool_slots=130000, seed=9)
     if name == "tree_32k":
         return make_case(name, [32768] * 8, 64, num_heads=num_heads, tree_depth=8, seed=4)
     if name.startswith("sweep_q"):
@@ -280,6 +285,8 @@ def workload_sizes(name: str) -> dict:
         pre, q = [4096, 8192, 16384, 32768], [16] * 4
     elif name == "long_185k":
         pre, q = [185000], [16]
+    elif name == "long_120k":
+        pre, q = [120000], [16]
     elif name == "tree_32k":
         pre, q = [32768] * 8, [64] * 8
     elif name.startswith("sweep_q"):

@@ -1,0 +1,61 @@
+"""Host-side logic of bench.py without a GPU: algorithmic work counts, and the
+multi-rank aggregation (max time over ranks, summed tokens) on two gloo ranks."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from speculative_decoding_mla_gb300 import synth
+
+
+def test_algorithmic_work_causal_and_tree():
+    case = synth.make_case("w", [10, 3], [4, 2], num_heads=2, pool_slots=30, seed=1)
+    nbytes, flops, tokens = bench.algorithmic_work(case)
+    assert tokens == 14 + 5
+    # visible pairs: sum_b Q_b * P_b + causal triangles
+    V = (4 * 10 + 10) + (2 * 3 + 3)
+    assert flops == 2 * 2 * (576 + 512) * V
+    assert nbytes == (19 * 1156) + (6 * 2 * (1152 + 1024 + 4))
+    tree = synth.make_case("t", [5], [6], num_heads=1, pool_slots=11, tree_depth=2, seed=2)
+    depth = np.zeros(6, int)
+    for i in range(1, 6):
+        depth[i] = depth[tree.parent[i]] + 1
+    _, flops_t, _ = bench.algorithmic_work(tree)
+    assert flops_t == 2 * 1 * 1088 * (6 * 5 + int((depth + 1).sum()))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank), VMLA_BENCH_BACKEND="gloo")
+    r, local, w = bench.dist_setup(world)
+    assert (r, w) == (rank, world)
+    bench.barrier(w)
+    mx, sm = bench.reduce_max_sum(1.0 + rank, 10.0 * (rank + 1), w)
+    out[rank] = (mx, sm)
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_aggregate():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_rank, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
+    for rank in range(world):
+        assert out[rank] == (2.0, 30.0)
+
+
+def test_single_rank_is_identity():
+    assert bench.reduce_max_sum(3.5, 7.0, 1) == (3.5, 7.0)
