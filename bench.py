@@ -43,6 +43,23 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
+
+# DRAM bytes per verify launch from the committed ncu capture (profiles/tc_verify_long_120k_full.md),
+# scaled to the workload by keys; valid only while the kernel and planner sources are the ones profiled.
+PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
+PROFILED_FINGERPRINT = "eb17625cef8eb61d"
+PROFILED_TRAFFIC = {"long_185k": 263.6e6, "long_120k": 171.0e6}
+
+
+def traffic_per_launch(workload: str):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in PROFILED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != PROFILED_FINGERPRINT:
+        return None
+    return PROFILED_TRAFFIC.get(workload)
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -357,7 +374,8 @@ def run_ours(args, rank, local, world):
             "tflops": flops / (max_ms / 1e3) / 1e12,
             "hbm_gbs": nbytes / (max_ms / 1e3) / 1e9,
             "roofline": {"bound": "tensor", "achieved": achieved_tflops, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"], "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved_tflops / peaks["bf16_tflops"],
+                         "traffic": traffic_per_launch(args.workload),
                          "kernel": "verify", "peak_source": f"{peaks['source']} dense bf16 burst",
                          "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
                          "verify_ms": v_ms, "merge_ms": float(merge_ms.mean()), "gather_ms": float(gather_ms.mean()),
