@@ -69,7 +69,7 @@ typedef enum vmla_status {
 
 /* Description of the split plan a call would use (host only, no GPU needed). */
 typedef struct vmla_plan_info {
-  int32_t num_units;        /* work units (one CTA each, or one CTA pair for the tensor-core kernel) */
+  int32_t num_units;        /* work units (one CTA each; one four-CTA cluster each for the tensor-core kernel) */
   int32_t max_splits;       /* largest split count of any sequence */
   int64_t partial_rows;     /* fp32 partial (row, split) results kept in the workspace */
   int64_t merge_rows;       /* query rows whose splits the merge kernel combines */

@@ -76,9 +76,14 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   int sms = 0;
   rc = current_sm_count(&sms, true);
   if (rc != VMLA_OK) return rc;
+  int clusters = 0;
+  if (kernel == VMLA_KERNEL_TC) {
+    rc = tc_max_clusters(&clusters);
+    if (rc != VMLA_OK) return rc;
+  }
   static thread_local PlanParams plan;  // large (20 KB); kept off the stack
   vmla_plan_info info;
-  rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &plan, &info);
+  rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan, &info);
   if (rc != VMLA_OK) return rc;
   if (workspace_bytes < info.workspace_bytes) return VMLA_ERR_WORKSPACE;
   const WorkspaceLayout L = workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC ? total_kv : 0);
@@ -145,7 +150,7 @@ int verify_attn_mla_plan(int kernel, int batch, int num_heads, const int32_t* qo
                          int32_t* splits_out) {
   if (!info) return VMLA_ERR_NULL;
   static thread_local PlanParams plan;
-  int rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, num_sms, &plan, info);
+  int rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, num_sms, 0, &plan, info);
   if (rc == VMLA_OK && splits_out)
     for (int b = 0; b < batch; ++b) splits_out[b] = plan.seq[b].n_split;
   return rc;
@@ -157,9 +162,14 @@ int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_i
   int sms = 0;
   int rc = current_sm_count(&sms, false);
   if (rc != VMLA_OK) return rc;
+  // the tensor-core plan with this device's co-resident cluster count, as a call would make it
+  int clusters = 0;
+  rc = vmla::tc_max_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  static thread_local vmla::PlanParams plan;
   vmla_plan_info info;
-  rc = verify_attn_mla_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &info,
-                            nullptr);
+  rc = vmla::build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan,
+                        &info);
   if (rc != VMLA_OK) return rc;
   vmla_plan_info info2;
   rc = verify_attn_mla_plan(VMLA_KERNEL_SIMT, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, &info2,

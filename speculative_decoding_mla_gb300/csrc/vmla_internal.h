@@ -63,9 +63,16 @@ struct PlanShape {
 
 PlanShape plan_shape(int kernel);
 
-// Host planner: fills `pp` and `info`.  Returns a vmla_status.
+// Host planner: fills `pp` and `info`.  Returns a vmla_status.  For the
+// tensor-core kernel the units fill `tc_clusters` four-SM clusters (the
+// device's co-resident cluster count); tc_clusters <= 0 estimates it as
+// num_sms / 4.
 int build_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_host,
-               const int32_t* kv_indptr_host, int splits, int num_sms, PlanParams* pp, vmla_plan_info* info);
+               const int32_t* kv_indptr_host, int splits, int num_sms, int tc_clusters, PlanParams* pp,
+               vmla_plan_info* info);
+
+// Clusters of the tensor-core kernel that are co-resident on the current device.
+int tc_max_clusters(int* out);
 
 // Workspace layout (offsets in bytes from the workspace base, each 256 B aligned).
 struct WorkspaceLayout {

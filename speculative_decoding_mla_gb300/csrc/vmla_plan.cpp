@@ -22,11 +22,12 @@ PlanShape plan_shape(int kernel) {
     s.min_chunk = 256;
     s.max_splits = 64;
   } else {
-    // tensor-core kernel: one unit = 128 query rows on a pair of SMs (a cluster);
-    // about two units per cluster leave the greedy schedule room to balance
-    s.rows_per_unit = 128;
-    s.units_per_sm = 2;  // per pair of SMs; the caller halves the SM count
-    s.key_align = 64;    // the kernel's tile
+    // tensor-core kernel: one unit = 256 query rows on a cluster of four SMs
+    // (a scorer pair and a mixer pair); about two units per cluster leave the
+    // greedy schedule room to balance
+    s.rows_per_unit = 256;
+    s.units_per_sm = 2;  // per cluster of four SMs; the caller divides the SM count
+    s.key_align = 128;   // the kernel's tile
     s.min_chunk = 1024;
     s.max_splits = 64;
   }
@@ -48,7 +49,7 @@ WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t 
 }
 
 int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const int32_t* kv, int splits, int num_sms,
-               PlanParams* pp, vmla_plan_info* info) {
+               int tc_clusters, PlanParams* pp, vmla_plan_info* info) {
   if (!qo || !kv || !pp) return VMLA_ERR_NULL;
   if (kernel != VMLA_KERNEL_TC && kernel != VMLA_KERNEL_SIMT) return VMLA_ERR_SHAPE;
   if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
@@ -66,8 +67,8 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   pp->rows_per_unit = sh.rows_per_unit;
 
   // slots: units that run at once
-  int64_t slots = kernel == VMLA_KERNEL_TC ? (int64_t)std::max(1, num_sms / 2) * sh.units_per_sm
-                                           : (int64_t)num_sms * sh.units_per_sm;
+  const int clusters = tc_clusters > 0 ? tc_clusters : std::max(1, num_sms / 4);
+  int64_t slots = kernel == VMLA_KERNEL_TC ? (int64_t)clusters * sh.units_per_sm : (int64_t)num_sms * sh.units_per_sm;
   int64_t total_work = 0;  // (row block) x (keys)
   for (int b = 0; b < batch; ++b) {
     int64_t nq = qo[b + 1] - qo[b], nk = kv[b + 1] - kv[b];

@@ -1,35 +1,43 @@
-// Tensor-core verify attention for sm_103a: tcgen05 MMAs with TMEM
-// accumulators, KV rows gathered by TMA (tile::gather4) at page_size = 1.
+// Tensor-core verify attention for sm_103a: tcgen05 MMAs shared by pairs of
+// SMs (cta_group::2) with TMEM accumulators, KV tiles streamed by tiled TMA.
 //
 // The method is the KV-split flash-decode of "The Build That Unlocked 3-6x
 // Decode Speedup", section "The Context: A Custom Kernel for an Unsupported
 // Architecture": KV tiles streamed through shared memory, online softmax, and
 // one read of each KV tile shared by many query rows.  The pages share a tile
 // across a head tile of 8 heads (section "Context: The Long Road to a Custom
-// sm_120 Kernel" of "The Build Script Edit"); here a tile serves 128 query
-// rows (heads x draft positions of one sequence) in a single MMA.
+// sm_120 Kernel" of "The Build Script Edit"); here a tile serves 256 query
+// rows (heads x draft positions of one sequence) in one 2-SM MMA.  The KV rows
+// are read from the contiguous copy the gather kernel made of each sequence's
+// page_size = 1 slots.
 //
-// A work unit is 128 query rows (r = i*H + h) of one sequence over one
-// contiguous piece of its key range, and runs on a cluster of two CTAs:
-//   CTA 0 ("scorer")  keeps Q [128 x 576] in tensor memory (A operand),
-//                     computes S = Q K^T for 64-key tiles into double-buffered
-//                     TMEM columns, runs the online softmax (one thread per
-//                     row), and ships P (bf16, 128 x 64) plus per-row rescale
-//                     factors to CTA 1 by a shared-memory bulk copy.
-//   CTA 1 ("mixer")   keeps O [128 x 512] fp32 in tensor memory and computes
-//                     O = alpha * O + P V with V the latent part of the same
-//                     gathered rows, then normalises and writes the result.
-// The split of the work follows from tensor-memory capacity: O for 128 rows
-// fills one SM's 512 TMEM columns, so Q and S live on the partner SM.
+// A work unit is 256 query rows (r = i*H + h) of one sequence over one
+// contiguous piece of its key range, and runs on a cluster of four CTAs:
+//   ranks 0,1 ("scorer pair")  hold Q (latent part in tensor memory, rope part
+//       in shared memory), each for its 128 rows.  Per 128-key tile each CTA
+//       loads 64 of the keys (all 576 columns) and the pair computes
+//       S = Q K^T as M256 x N128 MMAs: every CTA receives the scores of its
+//       rows against all 128 keys.  Eight softmax warps per CTA run the online
+//       softmax and ship P (bf16, 128 x 128) plus per-row rescale factors to
+//       the matching mixer CTA by a shared-memory bulk copy.
+//   ranks 2,3 ("mixer pair")   hold O [128 x 512] fp32 in all 512 TMEM
+//       columns each.  Per tile each CTA loads half of the 512 value columns
+//       of all 128 keys and the pair computes O = alpha * O + P V as M256 x
+//       N256 MMAs, then normalises and writes the result.
+// Each SM thus streams half of every tile it needs; the split into scorer and
+// mixer follows from tensor-memory capacity (O for 128 rows fills an SM's
+// 512 columns).
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer; CTA 0:
-// warps 2-9 softmax, two threads per row (each 32 of the tile's 64 keys);
-// CTA 1: warps 2-5 rescale/epilogue, warp 6 P-slot release.
+// Warp roles (320 threads): warp 0 TMA producer (all ranks); warp 1: rank 0
+// score MMA issuer, rank 2 P V issuer, rank 3 relay of its P arrivals to
+// rank 2; scorer warps 2-9 softmax (two threads per row, 64 keys each);
+// mixer warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
-// status word, tells the partner CTA to stop, drains its own copies and MMAs,
+// status word, tells the other CTAs to stop, drains its own copies and MMAs,
 // frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #include <mutex>
 
@@ -40,17 +48,21 @@ namespace vmla {
 using namespace sm100;
 namespace {
 
-constexpr int kTileKeys = 64;
-constexpr int kChunks = kDqk / 64;   // 9 column chunks of 64 bf16 (128 bytes) per row
-constexpr int kVChunks = kDv / 64;   // 8 of them are the latent / value part
-constexpr int kChunkBytes = kTileKeys * 128;
-constexpr int kStages = 2;
-constexpr int kRowsTC = 128;
-constexpr int kThreadsTC = 320;      // 10 warps
-constexpr uint32_t kSCol = 384;      // S buffers at TMEM columns 384 and 448 (Q uses 0..287)
-constexpr float kTau = 8.0f;         // the running max is raised only when a tile exceeds it by 2^8
+constexpr int kTileKeys = 128;         // keys per tile (N of the score MMA)
+constexpr int kHalfKeys = 64;          // keys of a tile loaded by each scorer CTA
+constexpr int kChunks = kDqk / 64;     // 9 column chunks of 64 bf16 (128 bytes) per row
+constexpr int kQChunks = kDv / 64;     // 8 latent chunks (Q latent lives in TMEM columns 0..255)
+constexpr int kVChunksCta = kDv / 128; // 4 value chunks per mixer CTA (half of the 8)
+constexpr int kKBox = kHalfKeys * 128; // 8 KB: 64 rows x 128 bytes
+constexpr int kVBox = kTileKeys * 128; // 16 KB: 128 rows x 128 bytes
+constexpr int kRowsCta = 128;
+constexpr int kRowsUnit = 256;
+constexpr int kThreadsTC = 352;        // 11 warps
+constexpr int kClusterCtas = 4;
+constexpr uint32_t kSCol = 256;        // S buffers at TMEM columns 256 and 384
+constexpr float kTau = 8.0f;           // the running max is raised only when a tile exceeds it by 2^8
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-constexpr int kPrefetchTiles = 6;  // tiles the scorer's producer prefetches into L2 ahead of its loads
+constexpr uint16_t kScorerMask = 0x3, kMixerMask = 0xC;
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
@@ -58,7 +70,7 @@ enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 // each hand-off for the first kTraceTiles tiles of cluster 0.
 #ifdef VMLA_TRACE
 constexpr int kTraceTiles = 256;
-constexpr int kTraceEvents = 12;
+constexpr int kTraceEvents = 20;
 __device__ uint64_t g_vmla_trace[kTraceEvents * kTraceTiles];
 __device__ __forceinline__ void vtrace(int ev, int tile) {
   if (cluster_id_x() == 0 && tile < kTraceTiles) {
@@ -72,38 +84,65 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 #define VTRACE(ev, tile) ((void)0)
 #endif
 
+// One P message covers half a tile (64 keys): the scorer's outbound copies
+// are the slow path of the pipeline, and two staging buffers of this size let
+// one copy drain while the next half is computed.
+constexpr int kMsgKeys = 64;
+constexpr int kMsgsPerTile = kTileKeys / kMsgKeys;
+constexpr int kPSlots = 4;  // mixer receive slots
 struct __align__(1024) PMsg {
-  uint8_t p[kRowsTC * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
-  float alpha[kRowsTC];      // factor for O rows before this tile's product (1 = unchanged)
-  uint32_t flags;            // bit 0: some alpha differs from 1
+  uint8_t p[kRowsCta * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
+  float alpha[kRowsCta];      // factor for O rows before this message's product (1 = unchanged)
+  uint32_t flags;             // bit 0: some alpha differs from 1
   uint32_t pad[3];
 };
-constexpr uint32_t kMsgBytes = kRowsTC * 128 + kRowsTC * 4 + 16;  // bytes shipped per message
+constexpr uint32_t kMsgBytes = kRowsCta * 128 + kRowsCta * 4 + 16;  // bytes shipped per message
+static_assert(offsetof(PMsg, pad) + 12 == kMsgBytes, "message layout");
 
 struct __align__(16) Finals {
-  float m[kRowsTC];  // running max (log2 units)
-  float l[kRowsTC];  // softmax denominator relative to m
+  float m[kRowsCta];  // running max (log2 units)
+  float l[kRowsCta];  // softmax denominator relative to m
 };
 
-struct TcSmem {
-  uint8_t kv[kStages][kChunks][kChunkBytes];  // gathered rows, 128-byte swizzled chunks
-  PMsg msg[2];                                // CTA 0: staging; CTA 1: receive slots
-  Finals fin_stage[2];                        // CTA 0 staging of per-unit finals
-  Finals fin[2];                              // CTA 1 receive
-  uint64_t kfull[kStages], kfree[kStages];
-  uint64_t sfull[2], sfree[2];
-  uint64_t qfull;
-  uint64_t pfull[2], pfree[2], pdone[2];
+struct ScorerSmem {
+  uint8_t kv[2][kChunks][kKBox];  // this CTA's 64 keys of each tile, 128-byte swizzled column chunks
+  uint8_t qrope[kRowsCta * 128];  // Q rope part [128 rows x 64] bf16, K-major, 128-byte swizzle
+  PMsg stage[2];                  // P message staging (double-buffered)
+  Finals fin_stage[2];            // per-unit finals staging
+  float pmax[2][2][kRowsCta];     // per message parity and half: partial row maxima
+  float lpart[kRowsCta];          // second half's row sums at a unit's last tile
+};
+
+struct MixerSmem {
+  uint8_t v[2][kVChunksCta][kVBox];  // this CTA's value columns of each tile's 128 keys
+  PMsg msg[kPSlots];                 // P receive slots
+  Finals fin[2];                     // per-unit finals receive slots
+};
+
+struct Ctl {
+  uint64_t kfull[2], kfree[2];  // K stages (scorer) or V stages (mixer)
+  uint64_t sfull[2], sfree[2];  // S buffers (scorer; sfree counts on rank 0)
+  uint64_t sread[2];            // rank 1: its softmax warps have read S buffer s
+  uint64_t staged[2], stgfree[2];  // scorer: P staging buffer written / free again
+  uint64_t qfull;               // Q of both scorer CTAs written (rank 0)
+  uint64_t pfull[kPSlots], pfree[kPSlots], pdone[kPSlots];
   uint64_t finfull[2];
   uint64_t cmd_full, cmd_done, obar;
   uint32_t cmd;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
-  uint32_t warp_flags[8];
-  float pmax[2][kRowsTC];     // CTA 0: per-half partial row maxima of the current tile
-  float lpart[kRowsTC];       // CTA 0: second half's row sums at a unit's last tile
-  volatile uint32_t wg_stop;  // CTA 0 softmax group: stop after this tile
-  volatile uint32_t wg_cmd;   // CTA 1 epilogue group: command broadcast
+  uint32_t warp_flags[2][8];  // per staging buffer: softmax warp w saw some alpha != 1
+  uint32_t peer_flags[kPSlots];  // rank 2: flags of rank 3's half of message slot s
+  volatile uint32_t wg_stop[2];  // scorer softmax group: stop at this message (per message parity)
+  volatile uint32_t wg_cmd;   // mixer epilogue group: command broadcast
+};
+
+struct TcSmem {
+  union {
+    ScorerSmem s;
+    MixerSmem m;
+  } u;
+  Ctl c;
 };
 
 struct UnitInfo {
@@ -125,146 +164,180 @@ __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
   return ui;
 }
 
-// Bounded wait; false on expiry or when the CTA is aborting.
-__device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where,
-                                      bool cluster_scope = false) {
+// Sets the abort flag of every CTA of the cluster.
+__device__ __noinline__ void abort_cluster(TcSmem& sm) {
+  sm.c.abort_flag = 1;
+  const uint32_t me = cluster_ctarank();
+  const uint32_t local = smem_u32((const void*)const_cast<int32_t*>(&sm.c.abort_flag));
+  for (uint32_t r = 0; r < kClusterCtas; ++r)
+    if (r != me) st_cluster_u32(mapa(local, r), 1u);
+}
+
+// Bounded wait; false on expiry or when the cluster is aborting.
+__device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where) {
   long long t0 = clock64();
   for (;;) {
-    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (sm.abort_flag) return false;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (sm.c.abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
-      sm.abort_flag = 1;
-      // tell the partner CTA to stop too
-      const uint32_t peer = cluster_ctarank() ^ 1u;
-      const uint32_t remote = mapa(smem_u32((const void*)const_cast<int32_t*>(&sm.abort_flag)), peer);
-      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
+      abort_cluster(sm);
       return false;
     }
   }
 }
 
-// ------------------------------------------------------------------ producer (warp 0, lane 0, both CTAs)
-// Loads each 64-key tile of the unit's key range from the contiguous staged
-// copy of the KV rows: one 64-row x 64-column box (8 KB, 128-byte swizzle) per
-// column chunk, 9 chunks for the scorer (K), 8 for the mixer (V).  Rows past
-// the piece's end belong to other keys and are masked by the softmax.
-__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
-                              const RunArgs& a, int u_begin, int u_end, int nch, bool prefetch) {
-  int it = 0;
-  bool ok = true;
-  // L2 prefetch of the staged rows of tile t (contiguous: 64 rows x 1152 bytes), clamped to the staged area
-  auto prefetch_tile = [&](const SeqPlan& sp, const UnitInfo& ui, int t) {
-    if (!prefetch || t >= ui.n_tiles) return;
-    const int64_t row0 = (int64_t)sp.kv_off + ui.k_lo + (int64_t)t * kTileKeys;
-    int64_t rows = a.total_kv - row0;
-    if (rows > kTileKeys) rows = kTileKeys;
-    if (rows > 0) prefetch_l2_bulk(a.staged + row0 * kDqk, (uint32_t)(rows * kRowBytes));
-  };
-  for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    const SeqPlan& sp = plan.seq[ui.b];
-    for (int t = 0; t < kPrefetchTiles && t < ui.n_tiles; ++t) prefetch_tile(sp, ui, t);
-    for (int t = 0; t < ui.n_tiles; ++t) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfree[s], ph ^ 1, a.status, 100)) {
-        ok = false;
-        break;
-      }
-      VTRACE(prefetch ? 0 : 6, it);
-      const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
-      mbar_arrive_expect_tx(&sm.kfull[s], (uint32_t)(nch * kChunkBytes));
-      const uint32_t bar = smem_u32(&sm.kfull[s]);
-      for (int c = 0; c < nch; ++c) tma_load_2d(smem_u32(&sm.kv[s][c][0]), map, 64 * c, y, bar);
-      prefetch_tile(sp, ui, t + kPrefetchTiles);
-      ++it;
-    }
-  }
-  // drain: the loads of the last two stages have landed before the CTA may exit
-  for (int k = 1; k <= 2 && it - k >= 0; ++k) {
-    const int j = it - k;
-    long long t0 = clock64();
-    while (!mbar_try_wait(&sm.kfull[j & 1], (j >> 1) & 1) && clock64() - t0 < kWaitCycles) {
-    }
+// Bounded wait that ignores the abort flag (draining in-flight work before exit).
+__device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < kWaitCycles) {
   }
 }
 
-// ------------------------------------------------------------------ CTA 0: QK^T issuer (warp 1, lane 0)
+__device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched& sched, int u_begin, int u_end) {
+  int total = 0;
+  for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.order[k]).n_tiles;
+  return total;
+}
+
+// ------------------------------------------------------------------ producer (warp 0, lane 0, every CTA)
+// Scorer CTA q (q = 0, 1) loads keys [64q, 64q + 64) of each 128-key tile, all
+// nine column chunks (64-row x 64-column boxes); mixer CTA q loads value
+// chunks {2q, 2q+1, 2q+4, 2q+5} of all 128 keys (128-row boxes), which are the
+// N halves the pair's P V MMAs expect.  Both CTAs of a pair complete their
+// bytes on the even CTA's barrier, which that CTA arms for the pair.  Rows
+// past the piece's end belong to other keys (masked by the softmax) or lie
+// outside the staged rows (zero fill).
+__device__ void producer_role(TcSmem& sm, const CUtensorMap* kmap, const CUtensorMap* vmap, const PlanParams& plan,
+                              const TcSched& sched, const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
+  const bool scorer = rank < 2;
+  const uint32_t q = rank & 1;
+  const uint32_t leader = rank & 2u;
+  const uint32_t pair_bytes = scorer ? 2u * kChunks * kKBox : 2u * kVChunksCta * kVBox;
+  int it = 0;
+  bool ok = true;
+  for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
+    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const SeqPlan& sp = plan.seq[ui.b];
+    for (int t = 0; t < ui.n_tiles; ++t) {
+      const int s = it & 1;
+      if (!wait_bar(sm, &sm.c.kfree[s], ((it >> 1) & 1) ^ 1, a.status, 100)) {
+        ok = false;
+        break;
+      }
+      if (rank != 3) VTRACE(scorer ? (q ? 10 : 0) : 5, it);
+      const uint32_t bar = mapa(smem_u32(&sm.c.kfull[s]), leader);
+      if (q == 0) mbar_arrive_expect_tx(&sm.c.kfull[s], pair_bytes);
+      const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
+      if (scorer) {
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d_pair(smem_u32(&sm.u.s.kv[s][c][0]), kmap, 64 * c, y + kHalfKeys * (int)q, bar);
+      } else {
+#pragma unroll 1
+        for (int j = 0; j < kVChunksCta; ++j) {
+          const int g = (j & 1) + 2 * (int)q + 4 * (j >> 1);
+          tma_load_2d_pair(smem_u32(&sm.u.m.v[s][j][0]), vmap, 64 * g, y, bar);
+        }
+      }
+      ++it;
+    }
+  }
+  // the even CTA drains the last two stages (their barriers count both CTAs' bytes)
+  if (q == 0)
+    for (int k = 1; k <= 2 && it - k >= 0; ++k) drain_bar(&sm.c.kfull[(it - k) & 1], ((it - k) >> 1) & 1);
+}
+
+// ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
+// Per tile: 32 M256 N128 K16 MMAs with A = Q latent from TMEM, then 4 with
+// A = Q rope from shared memory; B = the pair's K rows (K-major).
 __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                 uint32_t tbase, int u_begin, int u_end) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kTileKeys, 0, 0);
+  constexpr uint32_t idesc = idesc_bf16_f32(kRowsUnit, kTileKeys, 0, 0);
+  ScorerSmem& S = sm.u.s;
   int it = 0, uu = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    if (!wait_bar(sm, &sm.qfull, uu & 1, a.status, 200)) break;
+    if (!wait_bar(sm, &sm.c.qfull, uu & 1, a.status, 200)) break;
     tc_fence_after();
     bool ok = true;
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 201)) {
+      if (!wait_bar(sm, &sm.c.kfull[s], ph, a.status, 201)) {
         ok = false;
         break;
       }
       VTRACE(1, it);
-      if (!wait_bar(sm, &sm.sfree[s], ph ^ 1, a.status, 202)) {
+      if (!wait_bar(sm, &sm.c.sfree[s], ph ^ 1, a.status, 202)) {
         ok = false;
         break;
       }
-      VTRACE(2, it);
+      VTRACE(12, it);
       tc_fence_after();
       const uint32_t d = tbase + kSCol + (uint32_t)s * kTileKeys;
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint32_t kbase = smem_u32(&sm.kv[s][c][0]);
+      for (int c = 0; c < kQChunks; ++c) {
+        const uint32_t kbase = smem_u32(&S.kv[s][c][0]);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(d, tbase + (uint32_t)(c * 32 + k * 8), smem_desc(kbase + k * 32, 16, 1024), idesc, (c | k) != 0);
+          mma_pair_ts(d, tbase + (uint32_t)(c * 32 + k * 8), smem_desc(kbase + k * 32, 16, 1024), idesc,
+                      (c | k) != 0);
       }
-      mma_commit(&sm.sfull[s]);
-      mma_commit(&sm.kfree[s]);
+      {
+        const uint32_t kbase = smem_u32(&S.kv[s][kQChunks][0]);
+        const uint32_t qbase = smem_u32(S.qrope);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_pair_ss(d, smem_desc(qbase + k * 32, 16, 1024), smem_desc(kbase + k * 32, 16, 1024), idesc, 1u);
+      }
+      mma_commit_pair(&sm.c.sfull[s], kScorerMask);
+      mma_commit_pair(&sm.c.kfree[s], kScorerMask);
+      VTRACE(2, it);
     }
     if (!ok) break;
   }
   // all issued MMAs complete before the CTA may exit
-  mma_commit(&sm.obar);
-  long long t0 = clock64();
-  while (!mbar_try_wait(&sm.obar, 0) && clock64() - t0 < kWaitCycles) {
-  }
+  mma_commit_pair(&sm.c.obar, kScorerMask);
+  drain_bar(&sm.c.obar, 0);
 }
 
-// ------------------------------------------------------------------ CTA 0: softmax (warps 2-9)
-// Thread (half, row): row = TMEM lane, keys [32*half, 32*half + 32) of each tile.
-// The two halves of a row agree on the tile max through shared memory, so
-// both keep the same running reference max m_ref (raised only when a tile
+// ------------------------------------------------------------------ ranks 0,1: softmax (warps 2-9)
+// A tile's 128 scores per row are processed as two 64-key messages.  Thread
+// (half, row): row = TMEM lane = query row of this CTA, keys
+// [32*half, 32*half + 32) of each message.  The two halves of a row agree on
+// the message max through shared memory (one group barrier per message), so
+// both keep the same running reference max m_ref (raised only when a message
 // exceeds it by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
+// The P message is staged in shared memory; the sender thread ships it.
 __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
-                                    uint32_t tbase, int u_begin, int u_end) {
+                                    uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;                 // TMEM lane quarter this warp may access
-  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a tile
-  const int row = wq * 32 + lane;          // query row within the unit = TMEM lane
+  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a message
+  const int row = wq * 32 + lane;          // query row within this CTA = TMEM lane
   const int tid = threadIdx.x - 64;        // 0..255 within the softmax group
   const int wslot = warp - 2;              // 0..7
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
   const float scale = a.scale_log2;
-  const uint32_t peer_pfull[2] = {mapa(smem_u32(&sm.pfull[0]), 1), mapa(smem_u32(&sm.pfull[1]), 1)};
-  const uint32_t peer_msg[2] = {mapa(smem_u32(&sm.msg[0]), 1), mapa(smem_u32(&sm.msg[1]), 1)};
-  int it = 0, uu = 0;
-  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
+  ScorerSmem& S = sm.u.s;
+  const uint32_t qfull_r = mapa(smem_u32(&sm.c.qfull), 0);
+  int it = 0, uu = 0, msg = 0;
+  bool stop = false;
+  for (int ui_idx = u_begin; ui_idx < u_end && !stop; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
-    const int r = ui.rb * kRowsTC + row;
+    const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
     const bool valid = r < ui.R;
-    // Q rows of this unit into TMEM columns 0..287 (two bf16 per column); each
-    // half of the group writes its own column chunks
+    // Q of this unit: latent part into TMEM columns 0..255 (two bf16 per column),
+    // rope part into shared memory; each half of the group writes its share.  The
+    // previous unit's MMAs are complete (its last S buffer was observed full).
     __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
-      for (int c = half; c < kChunks; c += 2) {
+      for (int c = half; c < kQChunks; c += 2) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -276,246 +349,323 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
         }
         tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
       }
+#pragma unroll
+      for (int g = 4 * half; g < 4 * half + 4; ++g) {
+        const uint4 x = valid ? __ldg(qrow + kQChunks * 8 + g) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(S.qrope + row * 128 + ((g ^ (row & 7)) << 4)) = x;
+      }
       tmem_wait_st();
+      fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 256);
-      if (tid == 0) mbar_arrive(&sm.qfull);
+      if (tid == 0) {
+        if (rank == 0) mbar_arrive(&sm.c.qfull);
+        else mbar_arrive_remote(qfull_r);
+      }
     }
     const int i = valid ? r / H : 0;
     const uint64_t vis = a.masks ? a.masks[sp.q_off + i] : causal_bits(i);
     const int mask_from = min(ui.prefix, ui.k_hi);  // keys below this are visible to every valid row
     float m_ref = -INFINITY, l = 0.f;
-    bool stop = false;
-    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      // a failed wait leaves garbage in this tile; the group still meets at every
-      // barrier below and stops together at the end of the tile
-      wait_bar(sm, &sm.sfull[s], ph, a.status, 300);
-      if (tid == 0) VTRACE(3, it);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tbase + lane_base + kSCol + (uint32_t)s * kTileKeys + (uint32_t)half * 32, v);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&sm.sfree[s]);
-
-      const int key0 = ui.k_lo + t * kTileKeys + half * 32;
-      float x[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]) * scale;
-      if (!valid) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
-      } else if (key0 + 32 > mask_from) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = key0 + j;
-          bool vis_j = key < ui.k_hi;
-          if (vis_j && key >= ui.prefix) vis_j = ((vis >> (key - ui.prefix)) & 1ull) != 0;
-          if (!vis_j) x[j] = -INFINITY;
+    for (int t = 0; t < ui.n_tiles && !stop; ++t, ++it) {
+      const int sb = it & 1;
+      // a failed wait leaves garbage in this tile; the group still meets at the
+      // barrier of each message and stops together there
+      wait_bar(sm, &sm.c.sfull[sb], (it >> 1) & 1, a.status, 300);
+      if (tid == 0) VTRACE(rank ? 11 : 3, it);
+#pragma unroll 1
+      for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
+        __syncwarp();
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_base + kSCol + (uint32_t)sb * kTileKeys + (uint32_t)(j * kMsgKeys + half * 32), v);
+        tmem_wait_ld();
+        if (j == kMsgsPerTile - 1) {
+          // this warp has read its part of the S buffer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(rank == 0 ? &sm.c.sfree[sb] : &sm.c.sread[sb]);
         }
-      }
-      float mh = x[0];
+        const int key0 = ui.k_lo + t * kTileKeys + j * kMsgKeys + half * 32;
+        float x[32];
 #pragma unroll
-      for (int j = 1; j < 32; ++j) mh = fmaxf(mh, x[j]);
-      sm.pmax[half][row] = mh;
-      const int ms = it & 1;  // message slot (one message per tile)
-      const bool last = t == ui.n_tiles - 1;
-      if (tid == 0) VTRACE(4, it);
-      if (tid == 0 && it >= 2) bulk_wait_group_read<1>();
-      named_bar_sync(1, 256);  // partial maxima visible; staging slot ms free
-      const float mt = fmaxf(mh, sm.pmax[half ^ 1][row]);
-      float alpha = 1.f;
-      if (mt > m_ref + kTau) {
-        alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
-        l *= alpha;
-        m_ref = mt;
-      }
-      uint32_t pk[16];
-      float lsum = 0.f;
-      if (m_ref == -INFINITY) {
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v[k]) * scale;
+        if (!valid) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = 0u;
-      } else {
+          for (int k = 0; k < 32; ++k) x[k] = -INFINITY;
+        } else if (key0 + 32 > mask_from) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2_approx(x[2 * k] - m_ref), p1 = ex2_approx(x[2 * k + 1] - m_ref);
-          lsum += p0 + p1;
-          pk[k] = pack_bf16x2(p0, p1);
+          for (int k = 0; k < 32; ++k) {
+            const int key = key0 + k;
+            bool vis_k = key < ui.k_hi;
+            if (vis_k && key >= ui.prefix) vis_k = ((vis >> (key - ui.prefix)) & 1ull) != 0;
+            if (!vis_k) x[k] = -INFINITY;
+          }
         }
-      }
-      l += lsum;
-      // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
-      // this half owns granules 4*half .. 4*half + 3
-      uint8_t* prow = sm.msg[ms].p + row * 128;
+        float mh = x[0];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int g = 4 * half + k;
-        *reinterpret_cast<uint4*>(prow + ((g ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-      }
-      if (half == 0) sm.msg[ms].alpha[row] = alpha;
-      const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
-      if (lane == 0) sm.warp_flags[wslot] = any ? 1u : 0u;
-      if (last && half == 1) sm.lpart[row] = l;
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (last) {
-        // unit finals: running max and the row sum of both halves
-        if (half == 0) {
-          sm.fin_stage[uu & 1].m[row] = m_ref;
-          sm.fin_stage[uu & 1].l[row] = l + sm.lpart[row];
+        for (int k = 1; k < 32; ++k) mh = fmaxf(mh, x[k]);
+        const int pb = msg & 1;  // double-buffered exchange slots (a thread may run one message ahead)
+        S.pmax[pb][half][row] = mh;
+        const bool last = t == ui.n_tiles - 1 && j == kMsgsPerTile - 1;
+        const int sg = msg & 1;  // staging buffer
+        if (tid == 0) {
+          // the copy of message msg - 2 has left this staging buffer
+          bool ok = msg < 2 || wait_bar(sm, &sm.c.stgfree[sg], ((msg - 2) >> 1) & 1, a.status, 302);
+          sm.c.wg_stop[pb] = (ok && !sm.c.abort_flag) ? 0u : 1u;
+        }
+        named_bar_sync(1, 256);  // partial maxima and the stop decision visible; staging free
+        if (sm.c.wg_stop[pb]) {
+          stop = true;
+          break;
+        }
+        if (tid == 0 && j == 0) VTRACE(rank ? 15 : 14, it);
+        const float mt = fmaxf(mh, S.pmax[pb][half ^ 1][row]);
+        float alpha = 1.f;
+        if (mt > m_ref + kTau) {
+          alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
+          l *= alpha;
+          m_ref = mt;
+        }
+        // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
+        // this half owns granules 4*half .. 4*half + 3
+        uint8_t* prow = S.stage[sg].p + row * 128;
+        const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // x = -inf there, so every p is 0
+        float lsum = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float p0 = ex2_approx(x[8 * g + 2 * k] - mref), p1 = ex2_approx(x[8 * g + 2 * k + 1] - mref);
+            lsum += p0 + p1;
+            w[k] = pack_bf16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(prow + (((4 * half + g) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l += lsum;
+        if (half == 0) S.stage[sg].alpha[row] = alpha;
+        const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
+        if (lane == 0) sm.c.warp_flags[sg][wslot] = any ? 1u : 0u;
+        if (last) {
+          // unit finals: running max and the row sum of both halves
+          if (half == 1) S.lpart[row] = l;
+          named_bar_sync(1, 256);
+          if (half == 0) {
+            S.fin_stage[uu & 1].m[row] = m_ref;
+            S.fin_stage[uu & 1].l[row] = l + S.lpart[row];
+          }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 256);
-      }
-      if (tid == 0) {
-        bool go = !sm.abort_flag;
-        if (go) {
-          uint32_t f = 0;
-#pragma unroll
-          for (int w = 0; w < 8; ++w) f |= sm.warp_flags[w];
-          sm.msg[ms].flags = f;
-          fence_proxy_async_smem();
-          go = wait_bar(sm, &sm.pfree[ms], ((it >> 1) & 1) ^ 1, a.status, 301, true);
-        }
-        if (go) {
-          VTRACE(5, it);
-          bulk_s2s_cluster(peer_msg[ms], smem_u32(&sm.msg[ms]), kMsgBytes, peer_pfull[ms]);
-          if (last)
-            bulk_s2s_cluster(mapa(smem_u32(&sm.fin[uu & 1]), 1), smem_u32(&sm.fin_stage[uu & 1]), sizeof(Finals),
-                             mapa(smem_u32(&sm.finfull[uu & 1]), 1));
-          bulk_commit_group();
-        }
-        sm.wg_stop = go ? 0 : 1;
-      }
-      named_bar_sync(1, 256);
-      if (sm.wg_stop) {
-        stop = true;
-        break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.c.staged[sg]);
       }
     }
-    if (stop) break;
   }
-  if (tid == 0) bulk_wait_group_read<0>();
 }
 
-// ------------------------------------------------------------------ CTA 1: P V issuer (warp 1, lane 0)
+// ------------------------------------------------------------------ ranks 0,1: P sender (warp 10, lane 0)
+// Ships each staged message (and, after a unit's last message, the unit's
+// finals) into the matching mixer CTA's receive slot, then reports when the
+// copy has left the staging buffer.
+__device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
+                                   int u_begin, int u_end, uint32_t rank) {
+  ScorerSmem& S = sm.u.s;
+  const uint32_t mixer = rank + 2;
+  int it = 0, uu = 0, msg = 0;
+  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
+    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
+      for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
+        const int sg = msg & 1;
+        const int ms = msg % kPSlots;
+        if (!wait_bar(sm, &sm.c.staged[sg], (msg >> 1) & 1, a.status, 310)) goto done;
+        {
+          uint32_t f = 0;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) f |= sm.c.warp_flags[sg][w];
+          S.stage[sg].flags = f;
+        }
+        fence_proxy_async_smem();
+        if (!wait_bar(sm, &sm.c.pfree[ms], ((msg / kPSlots) & 1) ^ 1, a.status, 311)) goto done;
+        if (j == 0) VTRACE(rank ? 18 : 4, it);
+        if (j == 1) VTRACE(rank ? 17 : 16, it);
+        // into the mixer's receive slot (same offset in its view of shared memory)
+        bulk_s2s_cluster(mapa(smem_u32(&sm.u.m.msg[ms]), mixer), smem_u32(&S.stage[sg]), kMsgBytes,
+                         mapa(smem_u32(&sm.c.pfull[ms]), mixer));
+        if (t == ui.n_tiles - 1 && j == kMsgsPerTile - 1)
+          bulk_s2s_cluster(mapa(smem_u32(&sm.u.m.fin[uu & 1]), mixer), smem_u32(&S.fin_stage[uu & 1]),
+                           sizeof(Finals), mapa(smem_u32(&sm.c.finfull[uu & 1]), mixer));
+        bulk_commit_group();
+        if (msg >= 1) {
+          // the previous message's copy has finished reading its staging buffer
+          bulk_wait_group_read<1>();
+          mbar_arrive(&sm.c.stgfree[(msg - 1) & 1]);
+        }
+      }
+    }
+  }
+done:
+  bulk_wait_group_read<0>();
+}
+
+// ------------------------------------------------------------------ rank 1: S-buffer release forwarder (warp 1, lane 0)
+// One remote arrive per tile on rank 0's S-buffer barrier once this CTA's
+// softmax warps have read the buffer (keeps the cluster-scope release off the
+// softmax warps).
+__device__ void scorer_forward_role(TcSmem& sm, const RunArgs& a, int total) {
+  for (int n = 0; n < total; ++n) {
+    if (!wait_bar(sm, &sm.c.sread[n & 1], (n >> 1) & 1, a.status, 320)) return;
+    mbar_arrive_remote(mapa(smem_u32(&sm.c.sfree[n & 1]), 0));
+  }
+}
+
+// ------------------------------------------------------------------ rank 2: P V issuer (warp 1, lane 0)
+// Per message (64 keys): 4 key steps x 2 value halves of M256 x N256 x K16
+// MMAs, A = P (K-major, 128 rows in each mixer CTA), B = value columns of the
+// message's 64 rows of the tile stage (MN-major view of the 128-byte-swizzled
+// chunks: leading byte offset = chunk stride).
 __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                uint32_t tbase, int u_begin, int u_end) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
-  int it = 0, cmdn = 0, obn = 0;
+  constexpr uint32_t idesc = idesc_bf16_f32(kRowsUnit, 256, 0, 1);
+  MixerSmem& M = sm.u.m;
+  const uint32_t peer_cmd = mapa(smem_u32(&sm.c.cmd), 3);
+  const uint32_t peer_cmd_full = mapa(smem_u32(&sm.c.cmd_full), 3);
+  int it = 0, msg = 0, cmdn = 0, obn = 0;
   bool ok = true;
+  auto post = [&](uint32_t c) {
+    sm.c.cmd = c;
+    st_cluster_u32(peer_cmd, c);
+    mbar_arrive(&sm.c.cmd_full);
+    mbar_arrive_remote(peer_cmd_full);
+  };
   auto command = [&](uint32_t c) -> bool {
-    sm.cmd = c;
-    mbar_arrive(&sm.cmd_full);
-    const bool r = wait_bar(sm, &sm.cmd_done, cmdn & 1, a.status, 402);
+    post(c);
+    const bool r = wait_bar(sm, &sm.c.cmd_done, cmdn & 1, a.status, 402);
     ++cmdn;
     return r;
   };
   auto quiesce = [&]() -> bool {
-    mma_commit(&sm.obar);
-    const bool r = wait_bar(sm, &sm.obar, obn & 1, a.status, 403);
+    mma_commit_pair(&sm.c.obar, kMixerMask);
+    const bool r = wait_bar(sm, &sm.c.obar, obn & 1, a.status, 403);
     ++obn;
     return r;
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
-    for (int t = 0; t < ui.n_tiles; ++t, ++it) {
+    for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
       const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!wait_bar(sm, &sm.kfull[s], ph, a.status, 400)) {
+      if (!wait_bar(sm, &sm.c.kfull[s], (it >> 1) & 1, a.status, 400)) {
         ok = false;
         break;
       }
-      VTRACE(7, it);
-      if (!wait_bar(sm, &sm.pfull[s], ph, a.status, 401, true)) {
-        ok = false;
-        break;
-      }
-      VTRACE(8, it);
-      if (t > 0 && (sm.msg[s].flags & 1u)) {
-        if (!quiesce() || !command(kCmdRescale | ((uint32_t)s << 8))) {
+      VTRACE(6, it);
+      for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
+        const int ps = msg % kPSlots;
+        if (!wait_bar(sm, &sm.c.pfull[ps], (msg / kPSlots) & 1, a.status, 401)) {
           ok = false;
           break;
         }
-      }
-      tc_fence_after();
-      const uint32_t pbase = smem_u32(sm.msg[s].p);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t adesc = smem_desc(pbase + k * 32, 16, 1024);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint64_t bdesc = smem_desc(smem_u32(&sm.kv[s][4 * hh][0]) + k * 16 * 128, kChunkBytes, 1024);
-          mma_ss(tbase + (uint32_t)(256 * hh), adesc, bdesc, idesc, (t > 0 || k > 0) ? 1u : 0u);
+        if (j == 0) VTRACE(7, it);
+        if (j == 1) VTRACE(19, it);
+        if ((t > 0 || j > 0) && ((M.msg[ps].flags | sm.c.peer_flags[ps]) & 1u)) {
+          if (!quiesce() || !command(kCmdRescale | ((uint32_t)ps << 8))) {
+            ok = false;
+            break;
+          }
         }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kMsgKeys / 16; ++k) {
+          const uint64_t adesc = smem_desc(smem_u32(M.msg[ps].p) + k * 32, 16, 1024);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t bdesc =
+                smem_desc(smem_u32(&M.v[s][2 * hh][0]) + (j * kMsgKeys + k * 16) * 128, kVBox, 1024);
+            mma_pair_ss(tbase + (uint32_t)(256 * hh), adesc, bdesc, idesc, (t > 0 || j > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit_pair(&sm.c.pdone[ps], kMixerMask);
       }
-      mma_commit(&sm.kfree[s]);
-      mma_commit(&sm.pdone[s]);
-      VTRACE(9, it);
+      if (!ok) break;
+      mma_commit_pair(&sm.c.kfree[s], kMixerMask);
+      VTRACE(8, it);
     }
     if (!ok) break;
     if (!quiesce() || !command(kCmdEpilogue)) ok = false;
   }
   if (!ok) quiesce();
-  sm.cmd = kCmdExit;
-  mbar_arrive(&sm.cmd_full);
+  post(kCmdExit);
 }
 
-// ------------------------------------------------------------------ CTA 1: P-slot release (warp 6, lane 0)
-__device__ void mixer_release_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
-                                   int u_begin, int u_end) {
-  int total = 0;
-  for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx) total += decode_unit(plan, sched.order[ui_idx]).n_tiles;
-  const uint32_t peer_pfree[2] = {mapa(smem_u32(&sm.pfree[0]), 0), mapa(smem_u32(&sm.pfree[1]), 0)};
-  for (int n = 0; n < total; ++n) {
-    const int s = n & 1;
-    if (!wait_bar(sm, &sm.pdone[s], (n >> 1) & 1, a.status, 500)) return;
-    VTRACE(10, n);
-    if (n + 2 < total) {
-      mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
-      mbar_arrive_remote(peer_pfree[s]);
+// ------------------------------------------------------------------ rank 3: relay (warp 1, lane 0)
+// Forwards each P arrival of this CTA (and its rescale flag) to rank 2, whose
+// MMA reads both CTAs' halves of the message.
+__device__ void mixer_relay_role(TcSmem& sm, const RunArgs& a, int total_msgs) {
+  for (int n = 0; n < total_msgs; ++n) {
+    const int s = n % kPSlots;
+    if (!wait_bar(sm, &sm.c.pfull[s], (n / kPSlots) & 1, a.status, 700)) return;
+    st_cluster_u32(mapa(smem_u32(&sm.c.peer_flags[s]), 2), sm.u.m.msg[s].flags);
+    mbar_arrive_remote(mapa(smem_u32(&sm.c.pfull[s]), 2));
+    VTRACE(13, n);
+  }
+}
+
+// ------------------------------------------------------------------ ranks 2,3: P-slot release (warp 6, lane 0)
+__device__ void mixer_release_role(TcSmem& sm, const RunArgs& a, int total_msgs, uint32_t rank) {
+  const uint32_t scorer = rank - 2;
+  for (int n = 0; n < total_msgs; ++n) {
+    const int s = n % kPSlots;
+    if (!wait_bar(sm, &sm.c.pdone[s], (n / kPSlots) & 1, a.status, 500)) return;
+    if (rank == 2) VTRACE(9, n);
+    if (n + kPSlots < total_msgs) {
+      mbar_arrive_expect_tx(&sm.c.pfull[s], kMsgBytes);
+      mbar_arrive_remote(mapa(smem_u32(&sm.c.pfree[s]), scorer));
     }
   }
 }
 
-// ------------------------------------------------------------------ CTA 1: rescale / epilogue (warps 2-5)
+// ------------------------------------------------------------------ ranks 2,3: rescale / epilogue (warps 2-5)
 __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
-                                    uint32_t tbase, int u_begin, int u_end) {
+                                    uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
   const int tid = threadIdx.x - 64;
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
-  int cmdn = 0, uu = 0;
+  MixerSmem& M = sm.u.m;
+  const uint32_t lead_cmd_done = mapa(smem_u32(&sm.c.cmd_done), 2);
+  int cmdn = 0, uu = 0, qn = 0;
   int ui_idx = u_begin;
   for (;;) {
-    // thread 0 waits for the command (and, for an epilogue, the unit's finals);
-    // the group learns it at a barrier, so a failed wait stops every thread
+    // thread 0 waits for the command, for the MMAs it follows (both CTAs'
+    // tensor memory is written by rank 2's MMAs) and, for an epilogue, for the
+    // unit's finals; the group learns the outcome at a barrier
     if (tid == 0) {
       uint32_t cmd = kCmdExit;
-      if (wait_bar(sm, &sm.cmd_full, cmdn & 1, a.status, 600)) {
-        cmd = sm.cmd;
-        if ((cmd & 0xFF) == kCmdEpilogue &&
-            !wait_bar(sm, &sm.finfull[uu & 1], (uu >> 1) & 1, a.status, 601, true))
+      if (wait_bar(sm, &sm.c.cmd_full, cmdn & 1, a.status, 600)) {
+        cmd = sm.c.cmd;
+        const uint32_t op = cmd & 0xFF;
+        if (op == kCmdRescale || op == kCmdEpilogue) {
+          if (!wait_bar(sm, &sm.c.obar, qn & 1, a.status, 602)) cmd = kCmdExit;
+          ++qn;
+        }
+        if ((cmd & 0xFF) == kCmdEpilogue && !wait_bar(sm, &sm.c.finfull[uu & 1], (uu >> 1) & 1, a.status, 601))
           cmd = kCmdExit;
       }
-      sm.wg_cmd = cmd;
+      sm.c.wg_cmd = cmd;
     }
     ++cmdn;
     named_bar_sync(2, 128);
-    const uint32_t cmd = sm.wg_cmd;
+    const uint32_t cmd = sm.c.wg_cmd;
     if ((cmd & 0xFF) == kCmdExit) return;
     __syncwarp();
     tc_fence_after();
     // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform
     if ((cmd & 0xFF) == kCmdRescale) {
-      const int s = (cmd >> 8) & 1;
-      const float alpha = sm.msg[s].alpha[row];
+      const int s = (cmd >> 8) & (kPSlots - 1);
+      const float alpha = M.msg[s].alpha[row];
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < kDv / 32; ++c) {
@@ -533,8 +683,8 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
       const SeqPlan& sp = plan.seq[ui.b];
       const int f = uu & 1;
-      const float m = sm.fin[f].m[row], lsum = sm.fin[f].l[row];
-      const int r = ui.rb * kRowsTC + row;
+      const float m = M.fin[f].m[row], lsum = M.fin[f].l[row];
+      const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
       const bool valid = r < ui.R;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
@@ -584,15 +734,16 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     if (tid == 0) {
       // a finals buffer is re-armed for the unit two ahead once it has been read
       if ((cmd & 0xFF) == kCmdEpilogue && ui_idx + 1 < u_end)
-        mbar_arrive_expect_tx(&sm.finfull[(uu + 1) & 1], sizeof(Finals));
-      mbar_arrive(&sm.cmd_done);
+        mbar_arrive_expect_tx(&sm.c.finfull[(uu + 1) & 1], sizeof(Finals));
+      if (rank == 2) mbar_arrive(&sm.c.cmd_done);
+      else mbar_arrive_remote(lead_cmd_done);
     }
   }
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ PlanParams plan,
-                 const __grid_constant__ TcSched sched, const RunArgs a) {
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -602,37 +753,42 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const int u_end = cid < sched.num_clusters ? sched.start[cid + 1] : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kfull[s], 1);
-      mbar_init(&sm.kfree[s], 1);
-    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.sfull[s], 1);
-      mbar_init(&sm.sfree[s], 256);
-      mbar_init(&sm.pfull[s], 1);
-      mbar_init(&sm.pfree[s], 1);
-      mbar_init(&sm.pdone[s], 1);
-      mbar_init(&sm.finfull[s], 1);
+      mbar_init(&sm.c.kfull[s], 1);
+      mbar_init(&sm.c.kfree[s], 1);
+      mbar_init(&sm.c.sfull[s], 1);
+      mbar_init(&sm.c.sfree[s], 9);  // rank 0's 8 softmax warps + rank 1's forwarder
+      mbar_init(&sm.c.sread[s], 8);
+      mbar_init(&sm.c.staged[s], 8);
+      mbar_init(&sm.c.stgfree[s], 1);
+      mbar_init(&sm.c.finfull[s], 1);
     }
-    mbar_init(&sm.qfull, 1);
-    mbar_init(&sm.cmd_full, 1);
-    mbar_init(&sm.cmd_done, 1);
-    mbar_init(&sm.obar, 1);
-    sm.abort_flag = 0;
+    for (int s = 0; s < kPSlots; ++s) {
+      mbar_init(&sm.c.pfull[s], rank == 2 ? 2 : 1);  // rank 2: own arming + rank 3's relay
+      mbar_init(&sm.c.pfree[s], 1);
+      mbar_init(&sm.c.pdone[s], 1);
+      sm.c.peer_flags[s] = 0;
+    }
+    mbar_init(&sm.c.qfull, 2);
+    mbar_init(&sm.c.cmd_full, 1);
+    mbar_init(&sm.c.cmd_done, 2);
+    mbar_init(&sm.c.obar, 1);
+    sm.c.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&kv_map);
+    prefetch_tensormap(rank < 2 ? &kmap : &vmap);
   }
   __syncwarp();
   if (warp == 0) {
-    tmem_alloc(&sm.tmem_base, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(&sm.c.tmem_base, 512);
+    tmem_relinquish_pair();
   }
-  if (rank == 1 && threadIdx.x == 64) {  // thread 0 of the epilogue group
+  const int n_tiles_all = total_tiles(plan, sched, u_begin, u_end);
+  const int total_msgs = kMsgsPerTile * n_tiles_all;
+  if (rank >= 2 && threadIdx.x == 64) {  // thread 0 of the epilogue group
     // receive slots and finals buffers armed before the partner can send
-    int n_units = u_end - u_begin, total = 0;
-    for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.order[k]).n_tiles;
-    for (int s = 0; s < 2 && s < total; ++s) mbar_arrive_expect_tx(&sm.pfull[s], kMsgBytes);
-    for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&sm.finfull[s], sizeof(Finals));
+    const int n_units = u_end - u_begin;
+    for (int s = 0; s < kPSlots && s < total_msgs; ++s) mbar_arrive_expect_tx(&sm.c.pfull[s], kMsgBytes);
+    for (int s = 0; s < 2 && s < n_units; ++s) mbar_arrive_expect_tx(&sm.c.finfull[s], sizeof(Finals));
   }
   __syncwarp();
   tc_fence_before();
@@ -640,34 +796,37 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   tc_fence_after();
   cluster_arrive();
   cluster_wait();
-  const uint32_t tbase = sm.tmem_base;
+  const uint32_t tbase = sm.c.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0)
-      producer_role(sm, &kv_map, plan, sched, a, u_begin, u_end, rank == 0 ? kChunks : kVChunks, rank == 0);
+    if (lane == 0) producer_role(sm, &kmap, &vmap, plan, sched, a, u_begin, u_end, rank);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
-      else mixer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
+      else if (rank == 2) mixer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
+      else if (rank == 3) mixer_relay_role(sm, a, total_msgs);
+      else scorer_forward_role(sm, a, n_tiles_all);
     }
-  } else if (rank == 0) {
-    scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end);
+  } else if (warp == 10) {
+    if (lane == 0 && rank < 2) scorer_sender_role(sm, plan, sched, a, u_begin, u_end, rank);
+  } else if (rank < 2) {
+    scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);
   } else if (warp < 6) {
-    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end);
+    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);
   } else if (warp == 6 && lane == 0) {
-    mixer_release_role(sm, plan, sched, a, u_begin, u_end);
+    mixer_release_role(sm, a, total_msgs, rank);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   __syncwarp();
-  // neither CTA leaves while the other may still address its shared memory
+  // no CTA leaves while another may still address its shared or tensor memory
   cluster_arrive();
   cluster_wait();
   __syncwarp();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tbase, 512);
+    tmem_dealloc_pair(tbase, 512);
   }
 }
 
@@ -691,8 +850,32 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 2 * sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
+
+cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterCtas * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreadsTC, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, uint32_t box_rows) {
+  cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -709,17 +892,8 @@ int tc_max_clusters(int* out) {
   if (cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
     return VMLA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreadsTC, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = cluster_config(1, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, tc_verify_kernel, &cfg) != cudaSuccess || n < 1) return VMLA_ERR_CUDA;
   if (dev < 64) cached[dev] = n;
@@ -739,29 +913,16 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   static thread_local TcSched sched;
   rc = build_tc_schedule(plan, clusters, &sched);
   if (rc != VMLA_OK) return rc;
-  // 2-D map over the staged rows [total_kv x 576 bf16], boxes of 64 columns x 64 rows, 128-byte swizzle
-  CUtensorMap map;
-  cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(a.total_kv > 0 ? a.total_kv : 1)};
-  cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTileKeys};
-  cuuint32_t estride[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.staged, gdim, gstride, box, estride,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  // 2-D maps over the staged rows [total_kv x 576 bf16], 64-column boxes with
+  // 128-byte swizzle: 64 rows (scorer half tiles) and 128 rows (mixer tiles)
+  CUtensorMap kmap, vmap;
+  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys) ||
+      !encode_rows(enc, &vmap, a.staged, a.total_kv, kTileKeys))
     return VMLA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * sched.num_clusters, 1, 1);
-  cfg.blockDim = dim3(kThreadsTC, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, map, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr);
+  cfg.stream = (cudaStream_t)stream;
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 
@@ -772,6 +933,10 @@ extern "C" int vmla_trace_read(uint64_t* host, int n) {
   const int total = vmla::kTraceEvents * vmla::kTraceTiles;
   if (n > total) n = total;
   return cudaMemcpyFromSymbol(host, vmla::g_vmla_trace, sizeof(uint64_t) * n) == cudaSuccess ? n : -1;
+}
+extern "C" int vmla_trace_clusters(void) {
+  int n = 0;
+  return vmla::tc_max_clusters(&n) == VMLA_OK ? n : -1;
 }
 extern "C" int vmla_trace_clear(void) {
   static uint64_t zeros[vmla::kTraceEvents * vmla::kTraceTiles] = {};

@@ -86,7 +86,7 @@ def _plan(B, kernel, prefixes, drafts, H=64, splits=0, sms=152):
 
 @pytest.mark.parametrize("kernel", [0, 1])
 def test_plan_covers_work(B, kernel):
-    rpu = 128 if kernel == 0 else 32
+    rpu = 256 if kernel == 0 else 32
     for prefixes, drafts in [([185000], [16]), ([4096, 8192, 16384, 32768], [16] * 4), ([1024], [16]),
                              ([32768] * 8, [64] * 8), ([3, 0, 70000], [1, 0, 4])]:
         info, per, qo, kv = _plan(B, kernel, prefixes, drafts)
@@ -112,10 +112,10 @@ def test_plan_covers_work(B, kernel):
 
 def test_plan_fills_the_gpu_for_one_long_sequence(B):
     info, per, _, _ = _plan(B, 0, [185000], [16])
-    # 8 row blocks of 128 rows on 76 SM pairs: several key pieces each
+    # 4 row blocks of 256 rows on 38 four-SM clusters: several key pieces each
     assert per[0] >= 8 and info.num_units >= 64
     info, per, _, _ = _plan(B, 0, [185000], [16], splits=3)
-    assert per[0] == 3 and info.num_units == 24
+    assert per[0] == 3 and info.num_units == 12
 
 
 def test_plan_rejects_bad_shapes(B):
