@@ -115,7 +115,7 @@ int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_i
  *               means causal among the drafts.
  *   kv_indptr_host, qo_indptr_host: host copies of the two indptr arrays; read
  *               during the call to build the plan, not retained.
- *   sm_scale    score scale (1/sqrt(192) for the target model)
+ *   sm_scale    score scale, finite and > 0 (1/sqrt(192) for the target model)
  *   splits      0 = planner's choice; k > 0 forces k pieces per sequence
  *   out         [T_q, H, 512] bf16 (16 B aligned);  lse [T_q, H] fp32
  *   workspace   >= verify_attn_mla_workspace_size() bytes, 256 B aligned.

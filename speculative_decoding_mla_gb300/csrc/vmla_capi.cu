@@ -3,6 +3,7 @@
 // include/verify_attn_mla.h.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -64,6 +65,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
         int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
   if (rc != VMLA_OK) return rc;
+  // a positive finite scale (the kernels take row maxima over unscaled scores)
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return VMLA_ERR_SHAPE;
   const int64_t total_q = qo_indptr_host[batch];
   const int64_t total_kv = kv_indptr_host[batch];
   if (!workspace) return VMLA_ERR_NULL;

@@ -57,7 +57,12 @@ constexpr int kKBox = kHalfKeys * 128; // 8 KB: 64 rows x 128 bytes
 constexpr int kVBox = kTileKeys * 128; // 16 KB: 128 rows x 128 bytes
 constexpr int kRowsCta = 128;
 constexpr int kRowsUnit = 256;
-constexpr int kThreadsTC = 352;        // 11 warps
+constexpr int kSoftWarps = 8;          // scorer softmax warps: two per TMEM lane quarter
+constexpr int kParts = kSoftWarps / 4; // threads per query row
+constexpr int kPartKeys = 64 / kParts; // keys of a 64-key message per thread
+constexpr int kSenderWarp = 2 + kSoftWarps;
+constexpr int kThreadsTC = 32 * (kSenderWarp + 1);  // 11 warps
+static_assert(kPartKeys == 16 || kPartKeys == 32, "TMEM load width per softmax thread");
 constexpr int kClusterCtas = 4;
 constexpr uint32_t kSCol = 256;        // S buffers at TMEM columns 256 and 384
 constexpr float kTau = 8.0f;           // the running max is raised only when a tile exceeds it by 2^8
@@ -90,6 +95,7 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 constexpr int kMsgKeys = 64;
 constexpr int kMsgsPerTile = kTileKeys / kMsgKeys;
 constexpr int kPSlots = 4;  // mixer receive slots
+constexpr int kStages = 2;  // scorer staging buffers (a copy drains while the next message is computed)
 struct __align__(1024) PMsg {
   uint8_t p[kRowsCta * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
   float alpha[kRowsCta];      // factor for O rows before this message's product (1 = unchanged)
@@ -107,10 +113,10 @@ struct __align__(16) Finals {
 struct ScorerSmem {
   uint8_t kv[2][kChunks][kKBox];  // this CTA's 64 keys of each tile, 128-byte swizzled column chunks
   uint8_t qrope[kRowsCta * 128];  // Q rope part [128 rows x 64] bf16, K-major, 128-byte swizzle
-  PMsg stage[2];                  // P message staging (double-buffered)
+  PMsg stage[kStages];            // P message staging
   Finals fin_stage[2];            // per-unit finals staging
-  float pmax[2][2][kRowsCta];     // per message parity and half: partial row maxima
-  float lpart[kRowsCta];          // second half's row sums at a unit's last tile
+  float pmax[2][kParts][kRowsCta];  // per message parity and part: partial row maxima
+  float lpart[kParts - 1][kRowsCta]; // parts 1.. row sums at a unit's last message
 };
 
 struct MixerSmem {
@@ -123,7 +129,7 @@ struct Ctl {
   uint64_t kfull[2], kfree[2];  // K stages (scorer) or V stages (mixer)
   uint64_t sfull[2], sfree[2];  // S buffers (scorer; sfree counts on rank 0)
   uint64_t sread[2];            // rank 1: its softmax warps have read S buffer s
-  uint64_t staged[2], stgfree[2];  // scorer: P staging buffer written / free again
+  uint64_t staged[kStages], stgfree[kStages];  // scorer: P staging buffer written / free again
   uint64_t qfull;               // Q of both scorer CTAs written (rank 0)
   uint64_t pfull[kPSlots], pfree[kPSlots], pdone[kPSlots];
   uint64_t finfull[2];
@@ -131,7 +137,7 @@ struct Ctl {
   uint32_t cmd;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
-  uint32_t warp_flags[2][8];  // per staging buffer: softmax warp w saw some alpha != 1
+  uint32_t warp_flags[kStages][kSoftWarps];  // per staging buffer: softmax warp w saw some alpha != 1
   uint32_t peer_flags[kPSlots];  // rank 2: flags of rank 3's half of message slot s
   volatile uint32_t wg_stop[2];  // scorer softmax group: stop at this message (per message parity)
   volatile uint32_t wg_cmd;   // mixer epilogue group: command broadcast
@@ -144,6 +150,10 @@ struct TcSmem {
   } u;
   Ctl c;
 };
+
+// TMEM load of a softmax thread's columns (overloads by width).
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
 
 struct UnitInfo {
   int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;
@@ -302,22 +312,23 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   drain_bar(&sm.c.obar, 0);
 }
 
-// ------------------------------------------------------------------ ranks 0,1: softmax (warps 2-9)
+// ------------------------------------------------------------------ ranks 0,1: softmax (warps 2 .. 2+kSoftWarps-1)
 // A tile's 128 scores per row are processed as two 64-key messages.  Thread
-// (half, row): row = TMEM lane = query row of this CTA, keys
-// [32*half, 32*half + 32) of each message.  The two halves of a row agree on
+// (part, row): row = TMEM lane = query row of this CTA, keys
+// [kPartKeys*part, kPartKeys*(part + 1)) of each message.  The parts of a row agree on
 // the message max through shared memory (one group barrier per message), so
-// both keep the same running reference max m_ref (raised only when a message
+// all keep the same running reference max m_ref (raised only when a message
 // exceeds it by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
 // The P message is staged in shared memory; the sender thread ships it.
 __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
+  constexpr int kGroup = 32 * kSoftWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sw = warp - 2;                 // 0 .. kSoftWarps-1
   const int wq = warp & 3;                 // TMEM lane quarter this warp may access
-  const int half = (warp - 2) >> 2;        // 0: keys 0..31, 1: keys 32..63 of a message
+  const int part = sw >> 2;                // keys [kPartKeys*part, kPartKeys*(part + 1)) of a message
   const int row = wq * 32 + lane;          // query row within this CTA = TMEM lane
-  const int tid = threadIdx.x - 64;        // 0..255 within the softmax group
-  const int wslot = warp - 2;              // 0..7
+  const int tid = threadIdx.x - 64;        // 0 .. kGroup-1 within the softmax group
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
   const float scale = a.scale_log2;
@@ -331,13 +342,13 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
     const bool valid = r < ui.R;
     // Q of this unit: latent part into TMEM columns 0..255 (two bf16 per column),
-    // rope part into shared memory; each half of the group writes its share.  The
-    // previous unit's MMAs are complete (its last S buffer was observed full).
+    // rope part into shared memory; each part writes its share.  The previous
+    // unit's MMAs are complete (its last S buffer was observed full).
     __syncwarp();
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
-      for (int c = half; c < kQChunks; c += 2) {
+      for (int c = part; c < kQChunks; c += kParts) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -350,14 +361,14 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
         tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
       }
 #pragma unroll
-      for (int g = 4 * half; g < 4 * half + 4; ++g) {
+      for (int g = (8 / kParts) * part; g < (8 / kParts) * (part + 1); ++g) {
         const uint4 x = valid ? __ldg(qrow + kQChunks * 8 + g) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(S.qrope + row * 128 + ((g ^ (row & 7)) << 4)) = x;
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, 256);
+      named_bar_sync(1, kGroup);
       if (tid == 0) {
         if (rank == 0) mbar_arrive(&sm.c.qfull);
         else mbar_arrive_remote(qfull_r);
@@ -377,8 +388,12 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
         __syncwarp();
         tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_base + kSCol + (uint32_t)sb * kTileKeys + (uint32_t)(j * kMsgKeys + half * 32), v);
+        uint32_t v[kPartKeys];
+        {
+          const uint32_t scol =
+              tbase + lane_base + kSCol + (uint32_t)sb * kTileKeys + (uint32_t)(j * kMsgKeys + part * kPartKeys);
+          tmem_ld_cols(scol, v);
+        }
         tmem_wait_ld();
         if (j == kMsgsPerTile - 1) {
           // this warp has read its part of the S buffer
@@ -386,16 +401,17 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
           __syncwarp();
           if (lane == 0) mbar_arrive(rank == 0 ? &sm.c.sfree[sb] : &sm.c.sread[sb]);
         }
-        const int key0 = ui.k_lo + t * kTileKeys + j * kMsgKeys + half * 32;
-        float x[32];
+        const int key0 = ui.k_lo + t * kTileKeys + j * kMsgKeys + part * kPartKeys;
+        // raw scores; the scale (> 0) is applied in the exponent's fused multiply-add
+        float x[kPartKeys];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v[k]) * scale;
+        for (int k = 0; k < kPartKeys; ++k) x[k] = __uint_as_float(v[k]);
         if (!valid) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = -INFINITY;
-        } else if (key0 + 32 > mask_from) {
+          for (int k = 0; k < kPartKeys; ++k) x[k] = -INFINITY;
+        } else if (key0 + kPartKeys > mask_from) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < kPartKeys; ++k) {
             const int key = key0 + k;
             bool vis_k = key < ui.k_hi;
             if (vis_k && key >= ui.prefix) vis_k = ((vis >> (key - ui.prefix)) & 1ull) != 0;
@@ -404,23 +420,26 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
         }
         float mh = x[0];
 #pragma unroll
-        for (int k = 1; k < 32; ++k) mh = fmaxf(mh, x[k]);
+        for (int k = 1; k < kPartKeys; ++k) mh = fmaxf(mh, x[k]);
         const int pb = msg & 1;  // double-buffered exchange slots (a thread may run one message ahead)
-        S.pmax[pb][half][row] = mh;
+        S.pmax[pb][part][row] = mh;
         const bool last = t == ui.n_tiles - 1 && j == kMsgsPerTile - 1;
-        const int sg = msg & 1;  // staging buffer
+        const int sg = msg % kStages;  // staging buffer
         if (tid == 0) {
-          // the copy of message msg - 2 has left this staging buffer
-          bool ok = msg < 2 || wait_bar(sm, &sm.c.stgfree[sg], ((msg - 2) >> 1) & 1, a.status, 302);
+          // the copy of message msg - kStages has left this staging buffer
+          bool ok = msg < kStages || wait_bar(sm, &sm.c.stgfree[sg], ((msg - kStages) / kStages) & 1, a.status, 302);
           sm.c.wg_stop[pb] = (ok && !sm.c.abort_flag) ? 0u : 1u;
         }
-        named_bar_sync(1, 256);  // partial maxima and the stop decision visible; staging free
+        named_bar_sync(1, kGroup);  // partial maxima and the stop decision visible; staging free
         if (sm.c.wg_stop[pb]) {
           stop = true;
           break;
         }
         if (tid == 0 && j == 0) VTRACE(rank ? 15 : 14, it);
-        const float mt = fmaxf(mh, S.pmax[pb][half ^ 1][row]);
+        float mraw = S.pmax[pb][0][row];
+#pragma unroll
+        for (int q = 1; q < kParts; ++q) mraw = fmaxf(mraw, S.pmax[pb][q][row]);
+        const float mt = mraw * scale;
         float alpha = 1.f;
         if (mt > m_ref + kTau) {
           alpha = ex2_approx(m_ref - mt);  // 0 when m_ref = -inf
@@ -428,32 +447,37 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
           m_ref = mt;
         }
         // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
-        // this half owns granules 4*half .. 4*half + 3
+        // this part owns granules kPartKeys/8 * part .. kPartKeys/8 * (part + 1) - 1
         uint8_t* prow = S.stage[sg].p + row * 128;
         const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // x = -inf there, so every p is 0
         float lsum = 0.f;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < kPartKeys / 8; ++g) {
           uint32_t w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float p0 = ex2_approx(x[8 * g + 2 * k] - mref), p1 = ex2_approx(x[8 * g + 2 * k + 1] - mref);
+            const float p0 = ex2_approx(fmaf(x[8 * g + 2 * k], scale, -mref));
+            const float p1 = ex2_approx(fmaf(x[8 * g + 2 * k + 1], scale, -mref));
             lsum += p0 + p1;
             w[k] = pack_bf16x2(p0, p1);
           }
-          *reinterpret_cast<uint4*>(prow + (((4 * half + g) ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(prow + ((((kPartKeys / 8) * part + g) ^ (row & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
         l += lsum;
-        if (half == 0) S.stage[sg].alpha[row] = alpha;
+        if (part == 0) S.stage[sg].alpha[row] = alpha;
         const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
-        if (lane == 0) sm.c.warp_flags[sg][wslot] = any ? 1u : 0u;
+        if (lane == 0) sm.c.warp_flags[sg][sw] = any ? 1u : 0u;
         if (last) {
-          // unit finals: running max and the row sum of both halves
-          if (half == 1) S.lpart[row] = l;
-          named_bar_sync(1, 256);
-          if (half == 0) {
+          // unit finals: running max and the row sum of all parts
+          if (part > 0) S.lpart[part - 1][row] = l;
+          named_bar_sync(1, kGroup);
+          if (part == 0) {
+            float lt = l;
+#pragma unroll
+            for (int q = 0; q < kParts - 1; ++q) lt += S.lpart[q][row];
             S.fin_stage[uu & 1].m[row] = m_ref;
-            S.fin_stage[uu & 1].l[row] = l + S.lpart[row];
+            S.fin_stage[uu & 1].l[row] = lt;
           }
         }
         fence_proxy_async_smem();
@@ -464,7 +488,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
   }
 }
 
-// ------------------------------------------------------------------ ranks 0,1: P sender (warp 10, lane 0)
+// ------------------------------------------------------------------ ranks 0,1: P sender (warp 2+kSoftWarps, lane 0)
 // Ships each staged message (and, after a unit's last message, the unit's
 // finals) into the matching mixer CTA's receive slot, then reports when the
 // copy has left the staging buffer.
@@ -477,13 +501,13 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
     const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
-        const int sg = msg & 1;
+        const int sg = msg % kStages;
         const int ms = msg % kPSlots;
-        if (!wait_bar(sm, &sm.c.staged[sg], (msg >> 1) & 1, a.status, 310)) goto done;
+        if (!wait_bar(sm, &sm.c.staged[sg], (msg / kStages) & 1, a.status, 310)) goto done;
         {
           uint32_t f = 0;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) f |= sm.c.warp_flags[sg][w];
+          for (int w = 0; w < kSoftWarps; ++w) f |= sm.c.warp_flags[sg][w];
           S.stage[sg].flags = f;
         }
         fence_proxy_async_smem();
@@ -497,10 +521,10 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
           bulk_s2s_cluster(mapa(smem_u32(&sm.u.m.fin[uu & 1]), mixer), smem_u32(&S.fin_stage[uu & 1]),
                            sizeof(Finals), mapa(smem_u32(&sm.c.finfull[uu & 1]), mixer));
         bulk_commit_group();
-        if (msg >= 1) {
-          // the previous message's copy has finished reading its staging buffer
-          bulk_wait_group_read<1>();
-          mbar_arrive(&sm.c.stgfree[(msg - 1) & 1]);
+        if (msg >= kStages - 1) {
+          // the copy issued kStages - 1 messages ago has finished reading its staging buffer
+          bulk_wait_group_read<kStages - 1>();
+          mbar_arrive(&sm.c.stgfree[(msg - (kStages - 1)) % kStages]);
         }
       }
     }
@@ -757,11 +781,13 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       mbar_init(&sm.c.kfull[s], 1);
       mbar_init(&sm.c.kfree[s], 1);
       mbar_init(&sm.c.sfull[s], 1);
-      mbar_init(&sm.c.sfree[s], 9);  // rank 0's 8 softmax warps + rank 1's forwarder
-      mbar_init(&sm.c.sread[s], 8);
-      mbar_init(&sm.c.staged[s], 8);
-      mbar_init(&sm.c.stgfree[s], 1);
+      mbar_init(&sm.c.sfree[s], kSoftWarps + 1);  // rank 0's softmax warps + rank 1's forwarder
+      mbar_init(&sm.c.sread[s], kSoftWarps);
       mbar_init(&sm.c.finfull[s], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.c.staged[s], kSoftWarps);
+      mbar_init(&sm.c.stgfree[s], 1);
     }
     for (int s = 0; s < kPSlots; ++s) {
       mbar_init(&sm.c.pfull[s], rank == 2 ? 2 : 1);  // rank 2: own arming + rank 3's relay
@@ -807,7 +833,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       else if (rank == 3) mixer_relay_role(sm, a, total_msgs);
       else scorer_forward_role(sm, a, n_tiles_all);
     }
-  } else if (warp == 10) {
+  } else if (warp == kSenderWarp) {
     if (lane == 0 && rank < 2) scorer_sender_role(sm, plan, sched, a, u_begin, u_end, rank);
   } else if (rank < 2) {
     scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);

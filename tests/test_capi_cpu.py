@@ -67,6 +67,10 @@ def test_argument_errors_before_any_launch(B):
     assert _run_raw(B, **{**good, "qoh": np.array([0, 9], np.int32)}) == B.VMLA_ERR_SHAPE  # drafts > keys
     assert _run_raw(B, **{**good, "kvh": np.array([1, 8], np.int32)}) == B.VMLA_ERR_SHAPE
     assert _run_raw(B, **{**good, "splits": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "scale": 0.0}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "scale": -0.1}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "scale": float("inf")}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "scale": float("nan")}) == B.VMLA_ERR_SHAPE
     assert _run_raw(B, **{**good, "q": fake + 2}) == B.VMLA_ERR_ALIGN
     assert _run_raw(B, **{**good, "ws": fake + 16}) == B.VMLA_ERR_ALIGN
     # valid arguments on a machine without an sm_103 device
