@@ -18,8 +18,9 @@
 //       loads 64 of the keys (all 576 columns) and the pair computes
 //       S = Q K^T as M256 x N128 MMAs: every CTA receives the scores of its
 //       rows against all 128 keys.  Eight softmax warps per CTA run the online
-//       softmax and ship P (bf16, 128 x 128) plus per-row rescale factors to
-//       the matching mixer CTA by a shared-memory bulk copy.
+//       softmax in two 64-key messages per tile; a sender thread ships each
+//       message (P bf16 128 x 64, per-row rescale factors) to the matching
+//       mixer CTA by a shared-memory bulk copy.
 //   ranks 2,3 ("mixer pair")   hold O [128 x 512] fp32 in all 512 TMEM
 //       columns each.  Per tile each CTA loads half of the 512 value columns
 //       of all 128 keys and the pair computes O = alpha * O + P V as M256 x
@@ -28,10 +29,11 @@
 // mixer follows from tensor-memory capacity (O for 128 rows fills an SM's
 // 512 columns).
 //
-// Warp roles (320 threads): warp 0 TMA producer (all ranks); warp 1: rank 0
-// score MMA issuer, rank 2 P V issuer, rank 3 relay of its P arrivals to
-// rank 2; scorer warps 2-9 softmax (two threads per row, 64 keys each);
-// mixer warps 2-5 rescale/epilogue, warp 6 P-slot release.
+// Warp roles (352 threads): warp 0 TMA producer (all ranks); warp 1: rank 0
+// score MMA issuer, rank 1 forwarder of its S-buffer releases to rank 0,
+// rank 2 P V issuer, rank 3 relay of its P arrivals to rank 2; scorer warps
+// 2-9 softmax (two threads per row, 32 keys each per 64-key message), warp 10
+// P sender; mixer warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
 // status word, tells the other CTAs to stop, drains its own copies and MMAs,
 // frees tensor memory and returns.
