@@ -38,19 +38,23 @@ struct PlanParams {
   SeqPlan seq[VMLA_MAX_BATCH];
 };
 
-// Work order of the tensor-core kernel: cluster c processes the units
+// Work order of one tensor-core launch: cluster c processes the units
 // order[start[c] .. start[c+1]) in that order (longest-first greedy balance).
+// A plan with more units is run as several launches of at most kMaxTcUnits.
 constexpr int kMaxTcUnits = 3072;
 constexpr int kMaxClusters = 128;
 struct TcSched {
   int32_t num_clusters;
-  int32_t total_units;
+  int32_t total_units;  // units of this launch
+  int32_t unit_base;    // plan unit of order value 0
+  int32_t pad;
   uint16_t start[kMaxClusters + 1];
-  uint16_t order[kMaxTcUnits];
+  uint16_t order[kMaxTcUnits];  // plan unit = unit_base + order[k]
 };
 
-// Builds the per-cluster unit lists for a plan (host).  Returns a vmla_status.
-int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched);
+// Builds the per-cluster unit lists for the plan's units [unit_begin, unit_end)
+// (at most kMaxTcUnits of them; host).  Returns a vmla_status.
+int build_tc_schedule(const PlanParams& plan, int num_clusters, int unit_begin, int unit_end, TcSched* sched);
 
 // Planner knobs of one kernel family.
 struct PlanShape {

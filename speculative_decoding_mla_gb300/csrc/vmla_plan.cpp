@@ -116,7 +116,6 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
     max_s = std::max<int>(max_s, (int)pieces);
   }
   if (unit > INT32_MAX || part > INT32_MAX / kDv) return VMLA_ERR_SHAPE;
-  if (kernel == VMLA_KERNEL_TC && unit > kMaxTcUnits) return VMLA_ERR_SHAPE;
   pp->total_units = (int32_t)unit;
   pp->merge_rows = (int32_t)merge;
   pp->max_splits = max_s;
@@ -131,13 +130,16 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   return VMLA_OK;
 }
 
-int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched) {
+int build_tc_schedule(const PlanParams& plan, int num_clusters, int unit_begin, int unit_end, TcSched* sched) {
   if (!sched || num_clusters < 1) return VMLA_ERR_SHAPE;
   if (num_clusters > kMaxClusters) num_clusters = kMaxClusters;
-  const int U = plan.total_units;
+  if (unit_begin < 0 || unit_end > plan.total_units || unit_end < unit_begin) return VMLA_ERR_SHAPE;
+  const int U = unit_end - unit_begin;
   if (U > kMaxTcUnits) return VMLA_ERR_SHAPE;
   sched->num_clusters = num_clusters;
   sched->total_units = U;
+  sched->unit_base = unit_begin;
+  sched->pad = 0;
   // cost of a unit: its keys plus a fixed charge for filling and draining the pipeline
   struct Item { int64_t cost; int unit; };
   std::vector<Item> items;
@@ -147,7 +149,10 @@ int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched) 
     for (int piece = 0; piece < s.n_split; ++piece) {
       const int64_t lo = (int64_t)piece * s.chunk;
       const int64_t hi = std::min<int64_t>(s.n_kv, lo + s.chunk);
-      for (int rb = 0; rb < s.n_rb; ++rb) items.push_back({(hi - lo) + 256, s.unit_start + piece * s.n_rb + rb});
+      for (int rb = 0; rb < s.n_rb; ++rb) {
+        const int u = s.unit_start + piece * s.n_rb + rb;
+        if (u >= unit_begin && u < unit_end) items.push_back({(hi - lo) + 256, u});
+      }
     }
   }
   // longest first, ties by unit id (deterministic)
@@ -166,7 +171,7 @@ int build_tc_schedule(const PlanParams& plan, int num_clusters, TcSched* sched) 
     sched->start[c] = (uint16_t)pos;
     // within a cluster, units of the same piece next to each other keep KV reuse in L2
     std::sort(lists[c].begin(), lists[c].end());
-    for (int u : lists[c]) sched->order[pos++] = (uint16_t)u;
+    for (int u : lists[c]) sched->order[pos++] = (uint16_t)(u - unit_begin);
   }
   sched->start[num_clusters] = (uint16_t)pos;
   return VMLA_OK;

@@ -134,7 +134,8 @@ struct Ctl {
   uint64_t staged[kStages], stgfree[kStages];  // scorer: P staging buffer written / free again
   uint64_t qfull;               // Q of both scorer CTAs written (rank 0)
   uint64_t pfull[kPSlots], pfree[kPSlots], pdone[kPSlots];
-  uint64_t finfull[2];
+  uint64_t finfull[2];          // mixer: unit finals received
+  uint64_t finfree[2];          // scorer: the mixer's epilogue has read finals buffer f
   uint64_t cmd_full, cmd_done, obar;
   uint32_t cmd;
   uint32_t tmem_base;
@@ -208,7 +209,7 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched& sched, int u_begin, int u_end) {
   int total = 0;
-  for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.order[k]).n_tiles;
+  for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.unit_base + sched.order[k]).n_tiles;
   return total;
 }
 
@@ -229,7 +230,7 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* kmap, const CUtenso
   int it = 0;
   bool ok = true;
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
     for (int t = 0; t < ui.n_tiles; ++t) {
       const int s = it & 1;
@@ -269,7 +270,7 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   ScorerSmem& S = sm.u.s;
   int it = 0, uu = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     if (!wait_bar(sm, &sm.c.qfull, uu & 1, a.status, 200)) break;
     tc_fence_after();
     bool ok = true;
@@ -339,7 +340,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
   int it = 0, uu = 0, msg = 0;
   bool stop = false;
   for (int ui_idx = u_begin; ui_idx < u_end && !stop; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
     const bool valid = r < ui.R;
@@ -500,7 +501,7 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
   const uint32_t mixer = rank + 2;
   int it = 0, uu = 0, msg = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
         const int sg = msg % kStages;
@@ -519,9 +520,16 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
         // into the mixer's receive slot (same offset in its view of shared memory)
         bulk_s2s_cluster(mapa(smem_u32(&sm.u.m.msg[ms]), mixer), smem_u32(&S.stage[sg]), kMsgBytes,
                          mapa(smem_u32(&sm.c.pfull[ms]), mixer));
-        if (t == ui.n_tiles - 1 && j == kMsgsPerTile - 1)
+        if (t == ui.n_tiles - 1 && j == kMsgsPerTile - 1) {
+          // the mixer's finals buffer uu & 1 was read for unit uu - 2 (short units let this
+          // thread run two units ahead of the mixer's epilogue)
+          if (uu >= 2 && !wait_bar(sm, &sm.c.finfree[uu & 1], ((uu - 2) >> 1) & 1, a.status, 312)) {
+            bulk_commit_group();
+            goto done;
+          }
           bulk_s2s_cluster(mapa(smem_u32(&sm.u.m.fin[uu & 1]), mixer), smem_u32(&S.fin_stage[uu & 1]),
                            sizeof(Finals), mapa(smem_u32(&sm.c.finfull[uu & 1]), mixer));
+        }
         bulk_commit_group();
         if (msg >= kStages - 1) {
           // the copy issued kStages - 1 messages ago has finished reading its staging buffer
@@ -578,7 +586,7 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     return r;
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
       const int s = it & 1;
       if (!wait_bar(sm, &sm.c.kfull[s], (it >> 1) & 1, a.status, 400)) {
@@ -706,7 +714,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       }
     } else {
       // epilogue of unit ui_idx: O / l -> output row (or fp32 partial)
-      const UnitInfo ui = decode_unit(plan, sched.order[ui_idx]);
+      const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
       const SeqPlan& sp = plan.seq[ui.b];
       const int f = uu & 1;
       const float m = M.fin[f].m[row], lsum = M.fin[f].l[row];
@@ -758,9 +766,12 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     tc_fence_before();
     named_bar_sync(2, 128);
     if (tid == 0) {
-      // a finals buffer is re-armed for the unit two ahead once it has been read
-      if ((cmd & 0xFF) == kCmdEpilogue && ui_idx + 1 < u_end)
-        mbar_arrive_expect_tx(&sm.c.finfull[(uu + 1) & 1], sizeof(Finals));
+      // a finals buffer is re-armed for the unit two ahead once it has been read,
+      // then handed back to the scorer
+      if ((cmd & 0xFF) == kCmdEpilogue) {
+        if (ui_idx + 1 < u_end) mbar_arrive_expect_tx(&sm.c.finfull[(uu + 1) & 1], sizeof(Finals));
+        mbar_arrive_remote(mapa(smem_u32(&sm.c.finfree[(uu + 1) & 1]), rank - 2));
+      }
       if (rank == 2) mbar_arrive(&sm.c.cmd_done);
       else mbar_arrive_remote(lead_cmd_done);
     }
@@ -786,6 +797,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       mbar_init(&sm.c.sfree[s], kSoftWarps + 1);  // rank 0's softmax warps + rank 1's forwarder
       mbar_init(&sm.c.sread[s], kSoftWarps);
       mbar_init(&sm.c.finfull[s], 1);
+      mbar_init(&sm.c.finfree[s], 1);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.c.staged[s], kSoftWarps);
@@ -937,20 +949,23 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   int rc = tc_max_clusters(&clusters);
   if (rc != VMLA_OK) return rc;
   clusters = clusters < kMaxClusters ? clusters : kMaxClusters;
-  if (clusters > plan.total_units) clusters = plan.total_units;
-  static thread_local TcSched sched;
-  rc = build_tc_schedule(plan, clusters, &sched);
-  if (rc != VMLA_OK) return rc;
   // 2-D maps over the staged rows [total_kv x 576 bf16], 64-column boxes with
   // 128-byte swizzle: 64 rows (scorer half tiles) and 128 rows (mixer tiles)
   CUtensorMap kmap, vmap;
   if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys) ||
       !encode_rows(enc, &vmap, a.staged, a.total_kv, kTileKeys))
     return VMLA_ERR_CUDA;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr);
-  cfg.stream = (cudaStream_t)stream;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  // units are independent: a plan with more than kMaxTcUnits runs as several launches
+  static thread_local TcSched sched;
+  for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
+    const int u1 = plan.total_units - u0 < kMaxTcUnits ? plan.total_units : u0 + kMaxTcUnits;
+    rc = build_tc_schedule(plan, clusters < u1 - u0 ? clusters : u1 - u0, u0, u1, &sched);
+    if (rc != VMLA_OK) return rc;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr);
+    cfg.stream = (cudaStream_t)stream;
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

@@ -122,6 +122,16 @@ def test_plan_fills_the_gpu_for_one_long_sequence(B):
     assert per[0] == 3 and info.num_units == 12
 
 
+def test_plan_accepts_more_units_than_one_launch(B):
+    # 16 x 4 row pairs x 64 forced pieces: more units than one tensor-core launch schedules
+    info, per, _, _ = _plan(B, 0, [8176] * 16, [16] * 16, splits=64)
+    assert info.num_units == 4096 and all(int(p) == 64 for p in per)
+    # the largest shapes the header allows plan on both kernels
+    for kernel in (0, 1):
+        info, per, _, _ = _plan(B, kernel, [2000] * 512, [64] * 512, H=128)
+        assert info.num_units > 0
+
+
 def test_plan_rejects_bad_shapes(B):
     with pytest.raises(B.VmlaError):
         _plan(B, 0, [10], [65])

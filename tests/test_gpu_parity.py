@@ -150,3 +150,29 @@ def test_full_size_sampled_rows(kernel, name):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
     pool = synth.bf16_bits_to_f64(case.kv_pool[:, :512])
     assert o.max() <= pool.max() + OUT_TOL and o.min() >= pool.min() - OUT_TOL
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_maximum_heads_and_drafts(kernel):
+    """128 heads x 64 drafts (8192 query rows per sequence): the largest row count a sequence can have."""
+    case = synth.make_case("max_rows", [300, 1500], 64, num_heads=128, pool_slots=2000, seed=211)
+    o, l, st = run_full(case, kernel)
+    assert st == 0
+    rows = sample_rows(case, n=300, seed=3)
+    ref_o, ref_l = oracle.verify_rows(case, rows)
+    compare(o.reshape(-1, o.shape[-1])[rows], l.reshape(-1)[rows], ref_o, ref_l, f"{kernel}/max_rows")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+
+
+def test_more_units_than_one_launch_holds():
+    """4096 tensor-core work units (16 sequences x 4 row pairs x 64 forced pieces) run as two launches."""
+    from speculative_decoding_mla_gb300 import binding
+    case = synth.make_case("many_units", [8176] * 16, 16, num_heads=64, pool_slots=16 * 8192 + 50, seed=212)
+    info, per = binding.verify_attn_mla_plan(binding.VMLA_KERNEL_TC, case.qo_indptr, case.kv_indptr, 64, 64)
+    assert info.num_units == 4096 and np.all(per == 64)
+    o, l, st = run_full(case, "tc", splits=64)
+    assert st == 0
+    rows = sample_rows(case, n=200, seed=4)
+    ref_o, ref_l = oracle.verify_rows(case, rows)
+    compare(o.reshape(-1, o.shape[-1])[rows], l.reshape(-1)[rows], ref_o, ref_l, "many_units")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
