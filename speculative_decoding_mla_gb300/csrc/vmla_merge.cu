@@ -5,7 +5,8 @@
 //   lse = log sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s,
 // the combination of partial softmaxes that the NSPLIT split-KV of "The Build
 // Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel",
-// implies.  One warp per row; pieces with lse = -inf carry no weight.
+// implies.  One warp per row, four pieces' loads in flight per lane; pieces
+// with lse = -inf carry no weight (their partial rows are zero).
 //
 // Tree masks: the q x q visibility matrix of "The Build That Bridged Design
 // and Deployment", section "What This Build Achieves: The paged+bf16 Kernel",
@@ -18,7 +19,8 @@
 namespace vmla {
 namespace {
 
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 4;
+constexpr int kMergeBatch = 4;  // pieces loaded together
 
 __global__ void __launch_bounds__(kMergeWarps * 32)
 merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ part_o,
@@ -58,18 +60,31 @@ merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ 
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-    if (ws == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + (int64_t)s * R + r) * kDv);
+  for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
+    float4 v[kMergeBatch][4];
+    float ws[kMergeBatch];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float4 v = __ldg(src + c * 32 + lane);
-      acc[4 * c + 0] = fmaf(ws, v.x, acc[4 * c + 0]);
-      acc[4 * c + 1] = fmaf(ws, v.y, acc[4 * c + 1]);
-      acc[4 * c + 2] = fmaf(ws, v.z, acc[4 * c + 2]);
-      acc[4 * c + 3] = fmaf(ws, v.w, acc[4 * c + 3]);
+    for (int b = 0; b < kMergeBatch; ++b) {
+      const int s = s0 + b;
+      // every lane takes part in the shuffle; pieces past S or without weight are not read
+      // (an empty piece's partial row may hold anything)
+      ws[b] = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (s >= S) ws[b] = 0.f;
+      const bool use = ws[b] != 0.f;  // warp-uniform
+      const float4* src =
+          reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + (int64_t)(use ? s : 0) * R + r) * kDv);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[b][c] = use ? __ldg(src + c * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int b = 0; b < kMergeBatch; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[4 * c + 0] = fmaf(ws[b], v[b][c].x, acc[4 * c + 0]);
+        acc[4 * c + 1] = fmaf(ws[b], v[b][c].y, acc[4 * c + 1]);
+        acc[4 * c + 2] = fmaf(ws[b], v[b][c].z, acc[4 * c + 2]);
+        acc[4 * c + 3] = fmaf(ws[b], v[b][c].w, acc[4 * c + 3]);
+      }
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c)

@@ -63,6 +63,7 @@ def test_merge_kernel_alone():
     lse_parts[2, :50] = -np.inf
     lse_parts[:, 7] = -np.inf  # a row with every part empty
     ref_o, ref_l = oracle.merge(o_parts.astype(np.float64), lse_parts.astype(np.float64))
+    o_parts[2, :50] = np.nan  # an empty piece's partial row carries no weight, whatever it holds
     out = torch.empty((R, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(R, dtype=torch.float32, device="cuda")
     binding.verify_attn_mla_merge(torch.from_numpy(o_parts).cuda(), torch.from_numpy(lse_parts).cuda(), out, lse)
