@@ -698,7 +698,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     tc_fence_after();
     // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform
     if ((cmd & 0xFF) == kCmdRescale) {
-      const int s = (cmd >> 8) & (kPSlots - 1);
+      const int s = (int)((cmd >> 8) & 0xFFu);
       const float alpha = M.msg[s].alpha[row];
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
