@@ -56,7 +56,7 @@ constexpr int kChunks = kDqk / 64;     // 9 column chunks of 64 bf16 (128 bytes)
 constexpr int kQChunks = kDv / 64;     // 8 latent chunks (Q latent lives in TMEM columns 0..255)
 constexpr int kVChunksCta = kDv / 128; // 4 value chunks per mixer CTA (half of the 8)
 constexpr int kKBox = kHalfKeys * 128; // 8 KB: 64 rows x 128 bytes
-constexpr int kVBox = kTileKeys * 128; // 16 KB: 128 rows x 128 bytes
+constexpr int kVStages = 4;            // mixer V stages, one per 64-key message
 constexpr int kRowsCta = 128;
 constexpr int kRowsUnit = 256;
 constexpr int kSoftWarps = 8;          // scorer softmax warps: two per TMEM lane quarter
@@ -122,13 +122,13 @@ struct ScorerSmem {
 };
 
 struct MixerSmem {
-  uint8_t v[2][kVChunksCta][kVBox];  // this CTA's value columns of each tile's 128 keys
+  uint8_t v[kVStages][kVChunksCta][kKBox];  // this CTA's value columns of one message's 64 keys
   PMsg msg[kPSlots];                 // P receive slots
   Finals fin[2];                     // per-unit finals receive slots
 };
 
 struct Ctl {
-  uint64_t kfull[2], kfree[2];  // K stages (scorer) or V stages (mixer)
+  uint64_t kfull[kVStages], kfree[kVStages];  // K stages (scorer: 2) or V stages (mixer: 4)
   uint64_t sfull[2], sfree[2];  // S buffers (scorer; sfree counts on rank 0)
   uint64_t sread[2];            // rank 1: its softmax warps have read S buffer s
   uint64_t staged[kStages], stgfree[kStages];  // scorer: P staging buffer written / free again
@@ -214,51 +214,53 @@ __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched
 }
 
 // ------------------------------------------------------------------ producer (warp 0, lane 0, every CTA)
-// Scorer CTA q (q = 0, 1) loads keys [64q, 64q + 64) of each 128-key tile, all
-// nine column chunks (64-row x 64-column boxes); mixer CTA q loads value
-// chunks {2q, 2q+1, 2q+4, 2q+5} of all 128 keys (128-row boxes), which are the
-// N halves the pair's P V MMAs expect.  Both CTAs of a pair complete their
-// bytes on the even CTA's barrier, which that CTA arms for the pair.  Rows
-// past the piece's end belong to other keys (masked by the softmax) or lie
-// outside the staged rows (zero fill).
-__device__ void producer_role(TcSmem& sm, const CUtensorMap* kmap, const CUtensorMap* vmap, const PlanParams& plan,
-                              const TcSched& sched, const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
+// Scorer CTA q loads keys [64q, 64q + 64) of each 128-key tile, all nine
+// column chunks (64-row x 64-column boxes), into two tile stages; mixer CTA q
+// loads value chunks {2q, 2q+1, 2q+4, 2q+5} of each 64-key message (the N
+// halves the pair's P V MMAs expect) into four message stages.  Both CTAs of
+// a pair complete their bytes on the even CTA's barrier, which that CTA arms
+// for the pair.  Rows past the piece's end belong to other keys (masked by the
+// softmax) or lie outside the staged rows (zero fill).
+__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
+                              const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
   const bool scorer = rank < 2;
   const uint32_t q = rank & 1;
   const uint32_t leader = rank & 2u;
-  const uint32_t pair_bytes = scorer ? 2u * kChunks * kKBox : 2u * kVChunksCta * kVBox;
-  int it = 0;
+  const int nst = scorer ? 2 : kVStages;
+  const uint32_t pair_bytes = scorer ? 2u * kChunks * kKBox : 2u * kVChunksCta * kKBox;
+  int it = 0;  // loads issued (tiles for the scorer, messages for the mixer)
   bool ok = true;
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
-    for (int t = 0; t < ui.n_tiles; ++t) {
-      const int s = it & 1;
-      if (!wait_bar(sm, &sm.c.kfree[s], ((it >> 1) & 1) ^ 1, a.status, 100)) {
+    const int loads = scorer ? ui.n_tiles : ui.n_tiles * kMsgsPerTile;
+    for (int n = 0; n < loads; ++n) {
+      const int s = it % nst;
+      if (!wait_bar(sm, &sm.c.kfree[s], ((it / nst) & 1) ^ 1, a.status, 100)) {
         ok = false;
         break;
       }
       if (rank != 3) VTRACE(scorer ? (q ? 10 : 0) : 5, it);
       const uint32_t bar = mapa(smem_u32(&sm.c.kfull[s]), leader);
       if (q == 0) mbar_arrive_expect_tx(&sm.c.kfull[s], pair_bytes);
-      const int y = sp.kv_off + ui.k_lo + t * kTileKeys;
       if (scorer) {
+        const int y = sp.kv_off + ui.k_lo + n * kTileKeys + kHalfKeys * (int)q;
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d_pair(smem_u32(&sm.u.s.kv[s][c][0]), kmap, 64 * c, y + kHalfKeys * (int)q, bar);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d_pair(smem_u32(&sm.u.s.kv[s][c][0]), map, 64 * c, y, bar);
       } else {
+        const int y = sp.kv_off + ui.k_lo + n * kMsgKeys;
 #pragma unroll 1
         for (int j = 0; j < kVChunksCta; ++j) {
           const int g = (j & 1) + 2 * (int)q + 4 * (j >> 1);
-          tma_load_2d_pair(smem_u32(&sm.u.m.v[s][j][0]), vmap, 64 * g, y, bar);
+          tma_load_2d_pair(smem_u32(&sm.u.m.v[s][j][0]), map, 64 * g, y, bar);
         }
       }
       ++it;
     }
   }
-  // the even CTA drains the last two stages (their barriers count both CTAs' bytes)
+  // the even CTA drains its last loads (their barriers count both CTAs' bytes)
   if (q == 0)
-    for (int k = 1; k <= 2 && it - k >= 0; ++k) drain_bar(&sm.c.kfull[(it - k) & 1], ((it - k) >> 1) & 1);
+    for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(&sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1);
 }
 
 // ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
@@ -588,13 +590,13 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
-      const int s = it & 1;
-      if (!wait_bar(sm, &sm.c.kfull[s], (it >> 1) & 1, a.status, 400)) {
-        ok = false;
-        break;
-      }
-      VTRACE(6, it);
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
+        const int s = msg % kVStages;  // V stage of this message
+        if (!wait_bar(sm, &sm.c.kfull[s], (msg / kVStages) & 1, a.status, 400)) {
+          ok = false;
+          break;
+        }
+        if (j == 0) VTRACE(6, it);
         const int ps = msg % kPSlots;
         if (!wait_bar(sm, &sm.c.pfull[ps], (msg / kPSlots) & 1, a.status, 401)) {
           ok = false;
@@ -614,15 +616,14 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
           const uint64_t adesc = smem_desc(smem_u32(M.msg[ps].p) + k * 32, 16, 1024);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const uint64_t bdesc =
-                smem_desc(smem_u32(&M.v[s][2 * hh][0]) + (j * kMsgKeys + k * 16) * 128, kVBox, 1024);
+            const uint64_t bdesc = smem_desc(smem_u32(&M.v[s][2 * hh][0]) + k * 16 * 128, kKBox, 1024);
             mma_pair_ss(tbase + (uint32_t)(256 * hh), adesc, bdesc, idesc, (t > 0 || j > 0 || k > 0) ? 1u : 0u);
           }
         }
         mma_commit_pair(&sm.c.pdone[ps], kMixerMask);
+        mma_commit_pair(&sm.c.kfree[s], kMixerMask);
       }
       if (!ok) break;
-      mma_commit_pair(&sm.c.kfree[s], kMixerMask);
       VTRACE(8, it);
     }
     if (!ok) break;
@@ -779,8 +780,8 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ PlanParams plan,
+                 const __grid_constant__ TcSched sched, const RunArgs a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -790,9 +791,11 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const int u_end = cid < sched.num_clusters ? sched.start[cid + 1] : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&sm.c.kfull[s], 1);
       mbar_init(&sm.c.kfree[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.c.sfull[s], 1);
       mbar_init(&sm.c.sfree[s], kSoftWarps + 1);  // rank 0's softmax warps + rank 1's forwarder
       mbar_init(&sm.c.sread[s], kSoftWarps);
@@ -815,7 +818,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     mbar_init(&sm.c.obar, 1);
     sm.c.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(rank < 2 ? &kmap : &vmap);
+    prefetch_tensormap(&kmap);
   }
   __syncwarp();
   if (warp == 0) {
@@ -839,7 +842,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   const uint32_t tbase = sm.c.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sm, &kmap, &vmap, plan, sched, a, u_begin, u_end, rank);
+    if (lane == 0) producer_role(sm, &kmap, plan, sched, a, u_begin, u_end, rank);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
@@ -890,7 +893,7 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 2 * sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
@@ -949,12 +952,10 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   int rc = tc_max_clusters(&clusters);
   if (rc != VMLA_OK) return rc;
   clusters = clusters < kMaxClusters ? clusters : kMaxClusters;
-  // 2-D maps over the staged rows [total_kv x 576 bf16], 64-column boxes with
-  // 128-byte swizzle: 64 rows (scorer half tiles) and 128 rows (mixer tiles)
-  CUtensorMap kmap, vmap;
-  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys) ||
-      !encode_rows(enc, &vmap, a.staged, a.total_kv, kTileKeys))
-    return VMLA_ERR_CUDA;
+  // 2-D map over the staged rows [total_kv x 576 bf16]: boxes of 64 rows x 64
+  // columns with 128-byte swizzle (scorer half tiles, mixer message chunks)
+  CUtensorMap kmap;
+  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys)) return VMLA_ERR_CUDA;
   // units are independent: a plan with more than kMaxTcUnits runs as several launches
   static thread_local TcSched sched;
   for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
@@ -964,7 +965,7 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr);
     cfg.stream = (cudaStream_t)stream;
-    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
