@@ -261,6 +261,10 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   // the even CTA drains its last loads (their barriers count both CTAs' bytes)
   if (q == 0)
     for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(&sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1);
+  // tail: the releases of the last stages arrive on this CTA's barriers from the
+  // tensor core (a commit multicast to both CTAs of the pair); this CTA may not
+  // exit while one is still in flight
+  for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(&sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1);
 }
 
 // ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
@@ -312,8 +316,9 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
     }
     if (!ok) break;
   }
-  // all issued MMAs complete before the CTA may exit
-  mma_commit_pair(&sm.c.obar, kScorerMask);
+  // all issued MMAs complete before the CTA may exit (this arrive goes to rank 0
+  // only: nothing in rank 1 waits for it)
+  mma_commit_pair(&sm.c.obar, (uint16_t)0x1);
   drain_bar(&sm.c.obar, 0);
 }
 
@@ -685,6 +690,11 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
         if (op == kCmdRescale || op == kCmdEpilogue) {
           if (!wait_bar(sm, &sm.c.obar, qn & 1, a.status, 602)) cmd = kCmdExit;
           ++qn;
+        }
+        if ((cmd & 0xFF) == kCmdEpilogue && ui_idx >= u_end) {
+          // an epilogue with no unit left in this cluster's list: the command protocol is broken
+          record_status(a.status, VMLA_ERR_TIMEOUT, 603u);
+          cmd = kCmdExit;
         }
         if ((cmd & 0xFF) == kCmdEpilogue && !wait_bar(sm, &sm.c.finfull[uu & 1], (uu >> 1) & 1, a.status, 601))
           cmd = kCmdExit;
