@@ -44,11 +44,11 @@ if ROOT not in sys.path:
 
 METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
 
-# DRAM bytes per verify launch from the committed ncu capture (profiles/tc_verify_long_120k_full.md),
+# DRAM bytes per verify launch from the committed ncu capture (profiles/tc_verify_long_120k_sections.md),
 # scaled to the workload by keys; valid only while the kernel and planner sources are the ones profiled.
 PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
-PROFILED_FINGERPRINT = "eb17625cef8eb61d"
-PROFILED_TRAFFIC = {"long_185k": 263.6e6, "long_120k": 171.0e6}
+PROFILED_FINGERPRINT = "9ce68f03bf7260a2"
+PROFILED_TRAFFIC = {"long_185k": 240.3e6, "long_120k": 155.9e6}
 
 
 def traffic_per_launch(workload: str):
