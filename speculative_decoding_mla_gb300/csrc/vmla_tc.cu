@@ -634,7 +634,13 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     if (!ok) break;
     if (!quiesce() || !command(kCmdEpilogue)) ok = false;
   }
-  if (!ok) quiesce();
+  if (!ok) {
+    // after a failed wait: the last commit goes to this CTA only and is waited for
+    // regardless of the abort flag, so no arrival of this pair's earlier commits is
+    // still travelling when the cluster leaves
+    mma_commit_pair(&sm.c.obar, (uint16_t)0x4);
+    drain_bar(&sm.c.obar, obn & 1);
+  }
   post(kCmdExit);
 }
 
