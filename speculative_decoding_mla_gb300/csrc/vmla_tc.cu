@@ -142,7 +142,7 @@ struct Ctl {
   volatile int32_t abort_flag;
   uint32_t warp_flags[kStages][kSoftWarps];  // per staging buffer: softmax warp w saw some alpha != 1
   uint32_t peer_flags[kPSlots];  // rank 2: flags of rank 3's half of message slot s
-  volatile uint32_t wg_stop[2];  // scorer softmax group: stop at this message (per message parity)
+  volatile uint32_t wg_stop[4][2];  // scorer softmax warp pair (lane quarter): stop at this message (per parity)
   volatile uint32_t wg_cmd;   // mixer epilogue group: command broadcast
 };
 
@@ -326,19 +326,20 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
 // A tile's 128 scores per row are processed as two 64-key messages.  Thread
 // (part, row): row = TMEM lane = query row of this CTA, keys
 // [kPartKeys*part, kPartKeys*(part + 1)) of each message.  The parts of a row agree on
-// the message max through shared memory (one group barrier per message), so
+// the message max through shared memory (one barrier of the lane quarter's two
+// warps per message; the four quarters run independently), so
 // all keep the same running reference max m_ref (raised only when a message
 // exceeds it by 2^kTau, which bounds P by 2^kTau and makes rescales rare).
 // The P message is staged in shared memory; the sender thread ships it.
 __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
-  constexpr int kGroup = 32 * kSoftWarps;
+  constexpr int kPairThreads = 32 * kParts;  // the warps of one TMEM lane quarter (both parts of its rows)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sw = warp - 2;                 // 0 .. kSoftWarps-1
   const int wq = warp & 3;                 // TMEM lane quarter this warp may access
   const int part = sw >> 2;                // keys [kPartKeys*part, kPartKeys*(part + 1)) of a message
   const int row = wq * 32 + lane;          // query row within this CTA = TMEM lane
-  const int tid = threadIdx.x - 64;        // 0 .. kGroup-1 within the softmax group
+  const int tid = threadIdx.x - 64;        // 0 .. 32*kSoftWarps-1 within the softmax warps
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const int H = plan.num_heads;
   const float scale = a.scale_log2;
@@ -378,8 +379,8 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, kGroup);
-      if (tid == 0) {
+      __syncwarp();
+      if (lane == 0) {
         if (rank == 0) mbar_arrive(&sm.c.qfull);
         else mbar_arrive_remote(qfull_r);
       }
@@ -390,7 +391,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     float m_ref = -INFINITY, l = 0.f;
     for (int t = 0; t < ui.n_tiles && !stop; ++t, ++it) {
       const int sb = it & 1;
-      // a failed wait leaves garbage in this tile; the group still meets at the
+      // a failed wait leaves garbage in this tile; each warp pair still meets at the
       // barrier of each message and stops together there
       wait_bar(sm, &sm.c.sfull[sb], (it >> 1) & 1, a.status, 300);
       if (tid == 0) VTRACE(rank ? 11 : 3, it);
@@ -428,20 +429,18 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
             if (!vis_k) x[k] = -INFINITY;
           }
         }
-        float mh = x[0];
+        // row max over this thread's keys: four independent chains
+        float mc[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int k = 1; k < kPartKeys; ++k) mh = fmaxf(mh, x[k]);
+        for (int k = 4; k < kPartKeys; ++k) mc[k & 3] = fmaxf(mc[k & 3], x[k]);
+        const float mh = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
         const int pb = msg & 1;  // double-buffered exchange slots (a thread may run one message ahead)
         S.pmax[pb][part][row] = mh;
         const bool last = t == ui.n_tiles - 1 && j == kMsgsPerTile - 1;
         const int sg = msg % kStages;  // staging buffer
-        if (tid == 0) {
-          // the copy of message msg - kStages has left this staging buffer
-          bool ok = msg < kStages || wait_bar(sm, &sm.c.stgfree[sg], ((msg - kStages) / kStages) & 1, a.status, 302);
-          sm.c.wg_stop[pb] = (ok && !sm.c.abort_flag) ? 0u : 1u;
-        }
-        named_bar_sync(1, kGroup);  // partial maxima and the stop decision visible; staging free
-        if (sm.c.wg_stop[pb]) {
+        if (part == 0 && lane == 0) sm.c.wg_stop[wq][pb] = sm.c.abort_flag ? 1u : 0u;
+        named_bar_sync(1 + wq, kPairThreads);  // the pair's partial maxima and stop decision visible
+        if (sm.c.wg_stop[wq][pb]) {
           stop = true;
           break;
         }
@@ -456,32 +455,42 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
           l *= alpha;
           m_ref = mt;
         }
-        // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
-        // this part owns granules kPartKeys/8 * part .. kPartKeys/8 * (part + 1) - 1
-        uint8_t* prow = S.stage[sg].p + row * 128;
+        // P of this thread's keys into registers (bf16 pairs) while the copy of message
+        // msg - kStages may still be reading the staging buffer
         const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // x = -inf there, so every p is 0
-        float lsum = 0.f;
+        uint32_t w[kPartKeys / 2];
+        float ls[2] = {0.f, 0.f};
 #pragma unroll
-        for (int g = 0; g < kPartKeys / 8; ++g) {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float p0 = ex2_approx(fmaf(x[8 * g + 2 * k], scale, -mref));
-            const float p1 = ex2_approx(fmaf(x[8 * g + 2 * k + 1], scale, -mref));
-            lsum += p0 + p1;
-            w[k] = pack_bf16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + ((((kPartKeys / 8) * part + g) ^ (row & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < kPartKeys / 2; ++k) {
+          const float p0 = ex2_approx(fmaf(x[2 * k], scale, -mref));
+          const float p1 = ex2_approx(fmaf(x[2 * k + 1], scale, -mref));
+          ls[k & 1] += p0 + p1;
+          w[k] = pack_bf16x2(p0, p1);
         }
-        l += lsum;
-        if (part == 0) S.stage[sg].alpha[row] = alpha;
+        l += ls[0] + ls[1];
+        // each warp waits for the staging buffer itself (lane 0); after a failed wait it
+        // writes nothing, and its pair stops at the next message's barrier (the abort
+        // flag is raised by the failed wait)
+        bool free_ok = true;
+        if (lane == 0 && msg >= kStages)
+          free_ok = wait_bar(sm, &sm.c.stgfree[sg], ((msg - kStages) / kStages) & 1, a.status, 302);
+        free_ok = __shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0) != 0;
+        if (free_ok) {
+          // P row -> staging, 128-byte swizzle (16-byte granule g of row `row` at g ^ (row & 7));
+          // this part owns granules kPartKeys/8 * part .. kPartKeys/8 * (part + 1) - 1
+          uint8_t* prow = S.stage[sg].p + row * 128;
+#pragma unroll
+          for (int g = 0; g < kPartKeys / 8; ++g)
+            *reinterpret_cast<uint4*>(prow + ((((kPartKeys / 8) * part + g) ^ (row & 7)) << 4)) =
+                make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          if (part == 0) S.stage[sg].alpha[row] = alpha;
+        }
         const unsigned any = __ballot_sync(0xffffffffu, alpha != 1.f);
         if (lane == 0) sm.c.warp_flags[sg][sw] = any ? 1u : 0u;
         if (last) {
           // unit finals: running max and the row sum of all parts
           if (part > 0) S.lpart[part - 1][row] = l;
-          named_bar_sync(1, kGroup);
+          named_bar_sync(1 + wq, kPairThreads);
           if (part == 0) {
             float lt = l;
 #pragma unroll
@@ -828,7 +837,7 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
       mbar_init(&sm.c.pdone[s], 1);
       sm.c.peer_flags[s] = 0;
     }
-    mbar_init(&sm.c.qfull, 2);
+    mbar_init(&sm.c.qfull, 2 * kSoftWarps);  // every softmax warp of both scorer CTAs
     mbar_init(&sm.c.cmd_full, 1);
     mbar_init(&sm.c.cmd_done, 2);
     mbar_init(&sm.c.obar, 1);
