@@ -852,6 +852,9 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   }
   const int n_tiles_all = total_tiles(plan, sched, u_begin, u_end);
   const int total_msgs = kMsgsPerTile * n_tiles_all;
+  // every barrier object is initialised before any thread of this CTA arms or
+  // waits on one (the arming below runs in another warp than the initialisation)
+  __syncthreads();
   if (rank >= 2 && threadIdx.x == 64) {  // thread 0 of the epilogue group
     // receive slots and finals buffers armed before the partner can send
     const int n_units = u_end - u_begin;
