@@ -129,6 +129,37 @@ int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, cons
                     int batch, int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Stream-capture-safe form of verify_attn_mla.  The pages make the verify
+ * kernel CUDA-graph capture-safe once it works ("The Build That Unlocked 3-6x
+ * Decode Speedup", section "The Broader Significance"); a captured graph
+ * replays every launch with its captured parameters, so here nothing depends
+ * on host copies of the lengths: a planner kernel reads kv_indptr / qo_indptr
+ * on the device at run time and writes the split plan (the same pieces as
+ * verify_attn_mla's host planner, hence the same results bit for bit) and the
+ * cluster schedule into the workspace, and every later kernel reads them from
+ * there.  Capture one call per batch size; each replay may change the lengths,
+ * the indices and the contents of every input buffer, within the bounds.
+ *   batch, num_heads, sm_scale, splits, q .. lse: as for verify_attn_mla (the
+ *               pointers are captured; their contents are read at replay)
+ *   max_total_q   upper bound on qo_indptr[batch] at every replay, <= 64 * batch;
+ *                 q holds max_total_q rows, out / lse hold max_total_q rows
+ *   max_total_kv  upper bound on kv_indptr[batch] at every replay; kv_indices
+ *                 holds max_total_kv entries
+ *   workspace   >= verify_attn_mla_device_plan_workspace_size() bytes for the
+ *               same batch, num_heads, bounds and splits, 256 B aligned.
+ * Lengths that are inconsistent or exceed a bound are found by the planner on
+ * the device: the call then computes nothing (out and lse keep their contents)
+ * and verify_attn_mla_check returns VMLA_ERR_SHAPE.  Other argument errors are
+ * returned before any launch.  No host synchronisation, allocation or host
+ * read of device data happens inside the call. */
+int verify_attn_mla_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv,
+                                               int splits, size_t* bytes);
+int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                                int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Fixed size of the scratch array behind verify_attn_mla_simt_static (32 MiB). */
 #define VMLA_STATIC_SCRATCH_BYTES (32u << 20)
 

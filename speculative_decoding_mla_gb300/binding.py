@@ -37,7 +37,7 @@ EXPORTS = (
     "verify_attn_mla_merge", "verify_attn_mla_tree_mask", "verify_attn_mla_check",
     "verify_attn_mla_host_buffer_size", "verify_attn_mla_host", "verify_attn_mla_status_string",
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
-    "verify_attn_mla_simt_static",
+    "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
 )
 
 
@@ -73,6 +73,9 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_timing_enable": [i32],
         "verify_attn_mla_timing_read": [vp, vp, vp, i32, ctypes.POINTER(i32)],
         "verify_attn_mla_simt_static": [vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp],
+        "verify_attn_mla_device_plan_workspace_size": [i32, i32, i64, i64, i32, ctypes.POINTER(sz)],
+        "verify_attn_mla_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp, vp,
+                                        sz, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -159,6 +162,29 @@ def verify_attn_mla(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host
     """Tensor-core verify attention into `out` [T,H,512] bf16 and `lse` [T,H] fp32."""
     _run(_lib.verify_attn_mla, "verify_attn_mla", q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host,
          qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+
+
+def verify_attn_mla_device_plan_workspace_size(batch: int, num_heads: int, max_total_q: int, max_total_kv: int,
+                                               splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.verify_attn_mla_device_plan_workspace_size(int(batch), int(num_heads), int(max_total_q),
+                                                           int(max_total_kv), int(splits), ctypes.byref(n)),
+           "verify_attn_mla_device_plan_workspace_size")
+    return int(n.value)
+
+
+def verify_attn_mla_device_plan(q, kv_pool, kv_indptr, kv_indices, qo_indptr, batch: int, max_total_q: int,
+                                max_total_kv: int, out, lse, workspace, sm_scale, draft_mask=None, parent=None,
+                                splits=0, stream=None, num_heads=None, pool_slots=None):
+    """Stream-capture-safe verify attention: the plan is built on the device from the device indptr arrays."""
+    H = int(num_heads if num_heads is not None else q.shape[1])
+    S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
+    rc = _lib.verify_attn_mla_device_plan(_ptr(q), _ptr(kv_pool), S, _ptr(kv_indptr), _ptr(kv_indices),
+                                          _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent), int(batch), H,
+                                          int(max_total_q), int(max_total_kv), float(sm_scale), int(splits),
+                                          _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "verify_attn_mla_device_plan")
 
 
 def verify_attn_mla_simt(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libvmla.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["vmla_capi.cu", "vmla_plan.cpp", "vmla_simt.cu", "vmla_merge.cu", "vmla_gather.cu", "vmla_tc.cu", "vmla_static.cu"]
+SOURCES = ["vmla_capi.cu", "vmla_plan.cpp", "vmla_simt.cu", "vmla_merge.cu", "vmla_gather.cu", "vmla_tc.cu", "vmla_static.cu",
+           "vmla_dplan.cu"]
 
 
 def nvcc() -> str:

@@ -326,6 +326,99 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   return verify_attn_mla_check(d_ws, stream);
 }
 
+namespace {
+// Bounds of a device-planned call (host values only).
+int check_dplan_bounds(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits) {
+  if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
+  if (splits < 0 || splits > 64) return VMLA_ERR_SHAPE;
+  if (max_total_q < 0 || max_total_q > (int64_t)batch * VMLA_MAX_DRAFT) return VMLA_ERR_SHAPE;
+  if (max_total_kv < 0 || max_total_kv > INT32_MAX) return VMLA_ERR_SHAPE;
+  return VMLA_OK;
+}
+
+int dplan_clusters(int* clusters) {
+  int rc = tc_max_clusters(clusters);
+  if (rc == VMLA_OK && *clusters > kMaxClusters) *clusters = kMaxClusters;
+  return rc;
+}
+}  // namespace
+
+int verify_attn_mla_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv,
+                                               int splits, size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int rc = check_dplan_bounds(batch, num_heads, max_total_q, max_total_kv, splits);
+  if (rc != VMLA_OK) return rc;
+  int sms = 0, clusters = 0;
+  rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  rc = dplan_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  *bytes = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters).total;
+  return VMLA_OK;
+}
+
+int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                                int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_dplan_bounds(batch, num_heads, max_total_q, max_total_kv, splits);
+  if (rc != VMLA_OK) return rc;
+  if (pool_slots < 0 || pool_slots > INT32_MAX) return VMLA_ERR_SHAPE;
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return VMLA_ERR_SHAPE;
+  if (!workspace) return VMLA_ERR_NULL;
+  if (batch > 0 && (!kv_indptr || !qo_indptr)) return VMLA_ERR_NULL;
+  if (max_total_q > 0 && (!q || !kv_pool || !kv_indices || !out || !lse)) return VMLA_ERR_NULL;
+  if (max_total_kv > 0 && pool_slots == 0) return VMLA_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, VMLA_WORKSPACE_ALIGN) || !aligned(draft_mask, 8) || !aligned(parent, 4))
+    return VMLA_ERR_ALIGN;
+  int sms = 0, clusters = 0;
+  rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  rc = dplan_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  const DplanLayout L = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters);
+  if (workspace_bytes < L.total) return VMLA_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
+  PlanParams* plan = reinterpret_cast<PlanParams*>(ws + L.plan_off);
+  TcSched* sched = reinterpret_cast<TcSched*>(ws + L.sched_off);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(status, 0, 16, st) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (batch == 0 || max_total_q == 0) return VMLA_OK;
+  rc = launch_device_plan(qo_indptr, kv_indptr, batch, num_heads, splits, clusters, max_total_q, max_total_kv,
+                          L.part_cap, plan, sched, status, stream);
+  if (rc != VMLA_OK) return rc;
+  const uint64_t* masks = draft_mask;
+  if (!masks && parent) {
+    uint64_t* m = reinterpret_cast<uint64_t*>(ws + L.masks_off);
+    rc = launch_tree_mask_dplan(parent, qo_indptr, batch, max_total_q, status + 3, m, status, stream);
+    if (rc != VMLA_OK) return rc;
+    masks = m;
+  }
+  RunArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint16_t*>(kv_pool);
+  a.pool_slots = pool_slots;
+  a.kv_indices = kv_indices;
+  a.masks = masks;
+  a.sm_scale = sm_scale;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
+  a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
+  a.total_kv = max_total_kv;  // the staged capacity; the planner's count is in status word 2
+  a.status = status;
+  rc = launch_gather_dplan(a, status + 2, stream);
+  if (rc != VMLA_OK) return rc;
+  rc = launch_tc_dplan(plan, sched, clusters, a, stream);
+  if (rc != VMLA_OK) return rc;
+  return launch_merge_dplan(plan, max_total_q * num_heads, a.part_o, a.part_lse, a.out, a.lse, stream);
+}
+
 int verify_attn_mla_timing_enable(int capacity) {
   std::lock_guard<std::mutex> g(g_timing.mu);
   for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);

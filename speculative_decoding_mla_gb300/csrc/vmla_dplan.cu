@@ -1,0 +1,205 @@
+// Device-side planner for stream-captured calls.
+//
+// The pages make the verify kernel CUDA-graph capture-safe after it first
+// runs ("The Build That Unlocked 3-6x Decode Speedup", section "The Broader
+// Significance").  A captured graph replays its launches with the parameters
+// they were captured with, so a plan built on the host from one step's lengths
+// would be stale at the next.  Here the plan is computed by a kernel from the
+// device indptr arrays at run time: the same split arithmetic as the host
+// planner (vmla_plan_core.h, so both give identical pieces and results), and
+// a cluster schedule for the tensor-core kernel (units sorted by cost, dealt
+// to the clusters in a snake order, then in unit order within each cluster).
+// The areas of the workspace are sized for caller-given upper bounds on the
+// query and key totals.
+#include <cuda_runtime.h>
+
+#include "vmla_device.cuh"
+#include "vmla_plan_core.h"
+
+namespace vmla {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kSortKeys = 4096;  // power of two, at least kMaxTcUnits
+static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
+static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
+
+// Ascending bitonic sort of kSortKeys keys in shared memory (whole block).
+__device__ void block_sort(uint64_t* k) {
+  for (int size = 2; size <= kSortKeys; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < kSortKeys / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t a = k[lo], b = k[hi];
+        if ((a > b) == up) {
+          k[lo] = b;
+          k[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+}
+
+// Inclusive prefix sum of v[0, n) in place (whole block, n <= blockDim.x).
+__device__ void block_scan(int64_t* v, int n) {
+  for (int off = 1; off < n; off <<= 1) {
+    int64_t t = 0;
+    const int i = threadIdx.x;
+    if (i < n && i >= off) t = v[i - off];
+    __syncthreads();
+    if (i < n && i >= off) v[i] += t;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ kv, int batch, int num_heads,
+                   int splits, int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
+                   PlanParams* __restrict__ pp, TcSched* __restrict__ sched, uint32_t* status) {
+  __shared__ int64_t s_units[VMLA_MAX_BATCH], s_part[VMLA_MAX_BATCH], s_merge[VMLA_MAX_BATCH];
+  __shared__ uint64_t keys[kSortKeys];
+  __shared__ unsigned long long s_work;
+  __shared__ int s_bad, s_maxs;
+  const int tid = threadIdx.x;
+  const PlanShape sh = plan_shape(VMLA_KERNEL_TC);
+  if (tid == 0) {
+    s_work = 0;
+    s_bad = 0;
+    s_maxs = 0;
+  }
+  __syncthreads();
+  // lengths: each thread checks one sequence and adds its work
+  int64_t nq = 0, nk = 0;
+  if (tid < batch) {
+    nq = (int64_t)qo[tid + 1] - qo[tid];
+    nk = (int64_t)kv[tid + 1] - kv[tid];
+    if (plan_check_seq(nq, nk) != VMLA_OK)
+      atomicOr(&s_bad, 1);
+    else
+      atomicAdd(&s_work, (unsigned long long)plan_seq_work(sh, nq, nk, num_heads));
+  }
+  if (tid == 0 && (qo[0] != 0 || kv[0] != 0 || (int64_t)qo[batch] > max_total_q || (int64_t)kv[batch] > max_total_kv))
+    atomicOr(&s_bad, 2);
+  __syncthreads();
+  const bool lengths_ok = s_bad == 0;
+  const int64_t chunk_target = plan_chunk_target(sh, (int64_t)s_work, (int64_t)clusters * sh.units_per_sm);
+  SeqPlan sp = {};
+  int64_t u = 0, pr = 0, mr = 0;
+  if (tid < batch) {
+    sp.kv_off = kv[tid];
+    sp.n_kv = (int32_t)nk;
+    sp.q_off = qo[tid];
+    sp.n_q = (int32_t)nq;
+    if (lengths_ok) u = plan_split_seq(sh, sp, num_heads, splits, chunk_target, &pr, &mr);
+    s_units[tid] = u;
+    s_part[tid] = pr;
+    s_merge[tid] = mr;
+    if (lengths_ok && nq > 0) atomicMax(&s_maxs, sp.n_split);
+  }
+  __syncthreads();
+  block_scan(s_units, batch);
+  block_scan(s_part, batch);
+  block_scan(s_merge, batch);
+  const int64_t units = batch > 0 ? s_units[batch - 1] : 0;
+  const int64_t part = batch > 0 ? s_part[batch - 1] : 0;
+  const int64_t merge = batch > 0 ? s_merge[batch - 1] : 0;
+  const bool ok = lengths_ok && units <= kMaxTcUnits && part <= part_cap;
+  if (tid < batch) {
+    sp.unit_start = (int32_t)(s_units[tid] - u);
+    sp.part_off = (int32_t)(s_part[tid] - pr);
+    sp.merge_off = (int32_t)(s_merge[tid] - mr);
+    pp->seq[tid] = sp;
+  }
+  if (tid == 0) {
+    pp->batch = batch;
+    pp->num_heads = num_heads;
+    pp->rows_per_unit = sh.rows_per_unit;
+    pp->total_units = ok ? (int32_t)units : 0;
+    pp->merge_rows = ok ? (int32_t)merge : 0;
+    pp->max_splits = ok ? s_maxs : 0;
+    pp->partial_rows = ok ? (int32_t)part : 0;
+    pp->pad = 0;
+    status[2] = ok ? (uint32_t)kv[batch] : 0u;  // rows the gather stages
+    status[3] = ok ? (uint32_t)qo[batch] : 0u;  // draft rows the mask kernel expands
+    if (!ok) record_status(status, VMLA_ERR_SHAPE, lengths_ok ? 2u : (uint32_t)s_bad);
+  }
+  __syncthreads();
+  // schedule: units by decreasing cost (ties by unit), dealt to the clusters
+  // in a snake order, then in unit order within each cluster
+  const int U = ok ? (int)units : 0;
+  for (int k = tid; k < kSortKeys; k += blockDim.x) {
+    uint64_t key = ~0ull;
+    if (k < U) {
+      const int64_t cost = plan_unit_cost(pp->seq[seq_of_unit(*pp, k)], k);
+      key = ((uint64_t)(0x7FFFFFFFll - cost) << 32) | (uint32_t)k;
+    }
+    keys[k] = key;
+  }
+  __syncthreads();
+  block_sort(keys);
+  const int C = clusters;
+  for (int p = tid; p < U; p += blockDim.x) {
+    const int round = p / C, j = p - round * C;
+    const int c = (round & 1) ? C - 1 - j : j;
+    keys[p] = ((uint64_t)c << 32) | (keys[p] & 0xFFFFFFFFull);
+  }
+  __syncthreads();
+  block_sort(keys);
+  for (int p = tid; p < U; p += blockDim.x) sched->order[p] = (uint16_t)(keys[p] & 0xFFFFu);
+  for (int c = tid; c <= C; c += blockDim.x) {
+    int lo = 0, hi = U;  // first position whose cluster is >= c
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int)(keys[mid] >> 32) < c) lo = mid + 1; else hi = mid;
+    }
+    sched->start[c] = (uint16_t)lo;
+  }
+  if (tid == 0) {
+    sched->num_clusters = ok ? C : 0;
+    sched->total_units = U;
+    sched->unit_base = 0;
+    sched->pad = 0;
+  }
+}
+
+}  // namespace
+
+DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits,
+                         int clusters) {
+  auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
+  const PlanShape sh = plan_shape(VMLA_KERNEL_TC);
+  // units are at most slots + (row blocks) with the planner's own piece count
+  // (each sequence's pieces exceed its share of the slots by less than one),
+  // or splits x (row blocks) when the count is forced; 256 partial rows each
+  const int64_t row_blocks = plan_ceil_div(max_total_q * num_heads, sh.rows_per_unit) + batch;
+  const int64_t units =
+      splits > 0 ? (int64_t)splits * row_blocks : (int64_t)clusters * sh.units_per_sm + row_blocks;
+  int64_t cap = units * sh.rows_per_unit;
+  const int64_t all = max_total_q * num_heads * sh.max_splits;
+  if (cap > all) cap = all;
+  DplanLayout L;
+  L.status_off = 0;
+  L.plan_off = up(16);
+  L.sched_off = L.plan_off + up(sizeof(PlanParams));
+  L.masks_off = L.sched_off + up(sizeof(TcSched));
+  L.part_o_off = L.masks_off + up((size_t)max_total_q * 8);
+  L.part_lse_off = L.part_o_off + up((size_t)cap * kDv * 4);
+  L.staged_off = L.part_lse_off + up((size_t)cap * 4);
+  L.total = L.staged_off + up((size_t)max_total_kv * kRowBytes);
+  L.part_cap = cap;
+  return L;
+}
+
+int launch_device_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads, int splits,
+                       int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
+                       PlanParams* plan, TcSched* sched, uint32_t* status, void* stream) {
+  if (batch < 0 || batch > VMLA_MAX_BATCH || clusters < 1 || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
+  device_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(qo_indptr, kv_indptr, batch, num_heads, splits,
+                                                                   clusters, max_total_q, max_total_kv, part_cap,
+                                                                   plan, sched, status);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+}  // namespace vmla

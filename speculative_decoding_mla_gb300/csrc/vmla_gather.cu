@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kGatherWarps = 8;
 constexpr int kRowU4 = kRowBytes / 16;  // 72
+constexpr int kTileRows = 128;           // rows one tile of the tensor-core kernel covers
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -30,10 +31,26 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int32_t* __restrict__ kv_indices,
-                   int64_t total_kv, uint4* __restrict__ staged, uint32_t* status) {
+                   int64_t total_kv, const uint32_t* __restrict__ rows_dev, uint4* __restrict__ staged,
+                   uint32_t* status) {
   const int lane = threadIdx.x & 31;
+  int64_t end = total_kv;
+  if (rows_dev) {
+    // device-planned call: total_kv is the staged capacity and the planner
+    // counted the rows; the tile after the last row is zeroed too, as the tile
+    // loads' out-of-range fill would be, since it holds an earlier call's rows
+    const int64_t cap = total_kv, r = *rows_dev;
+    total_kv = r < cap ? r : cap;
+    end = total_kv + kTileRows < cap ? total_kv + kTileRows : cap;
+  }
   const int64_t warp0 = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kGatherWarps;
+  for (int64_t j = warp0 + total_kv; j < end; j += nwarps) {
+    uint4* dst = staged + j * kRowU4;
+    dst[lane] = make_uint4(0, 0, 0, 0);
+    dst[lane + 32] = make_uint4(0, 0, 0, 0);
+    if (lane < kRowU4 - 64) dst[lane + 64] = make_uint4(0, 0, 0, 0);
+  }
   for (int64_t j = warp0; j < total_kv; j += nwarps) {
     const int32_t slot = kv_indices[j];
     const bool ok = slot >= 0 && (int64_t)slot < pool_slots;
@@ -52,7 +69,8 @@ gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int
 
 }  // namespace
 
-int launch_gather(const RunArgs& a, void* stream) {
+namespace {
+int launch_gather_impl(const RunArgs& a, const uint32_t* rows_dev, void* stream) {
   if (a.total_kv == 0) return VMLA_OK;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -62,9 +80,17 @@ int launch_gather(const RunArgs& a, void* stream) {
   const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM keep enough rows in flight
   const int blocks = (int)(need < cap ? need : cap);
   gather_rows_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_indices, a.total_kv, reinterpret_cast<uint4*>(a.staged),
-      a.status);
+      reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_indices, a.total_kv, rows_dev,
+      reinterpret_cast<uint4*>(a.staged), a.status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+}  // namespace
+
+int launch_gather(const RunArgs& a, void* stream) { return launch_gather_impl(a, nullptr, stream); }
+
+// a.total_kv is the staged capacity; the kernel gathers *rows_dev rows of it
+int launch_gather_dplan(const RunArgs& a, const uint32_t* rows_dev, void* stream) {
+  return launch_gather_impl(a, rows_dev, stream);
 }
 
 }  // namespace vmla

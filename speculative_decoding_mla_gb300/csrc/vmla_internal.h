@@ -65,7 +65,7 @@ struct PlanShape {
   int max_splits;
 };
 
-PlanShape plan_shape(int kernel);
+// plan_shape(kernel): vmla_plan_core.h (host and device)
 
 // Host planner: fills `pp` and `info`.  Returns a vmla_status.  For the
 // tensor-core kernel the units fill `tc_clusters` four-SM clusters (the
@@ -113,6 +113,39 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
                const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
                float sm_scale, int splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
                void* stream);
+
+// Device-planned calls (stream-capture safe): the plan and the cluster
+// schedule are computed on the device from the device indptr arrays.  The
+// workspace holds, after the status words, the plan, the schedule, and areas
+// sized for upper bounds on the lengths fixed by the caller.
+struct DplanLayout {
+  size_t status_off;  // uint32 status, info, rows to gather, draft rows to mask
+  size_t plan_off;    // PlanParams
+  size_t sched_off;   // TcSched
+  size_t masks_off;   // uint64 [max_total_q]
+  size_t part_o_off;  // float [part_cap, 512]
+  size_t part_lse_off;// float [part_cap]  (log2 domain)
+  size_t staged_off;  // bf16 [max_total_kv, 576]
+  size_t total;
+  int64_t part_cap;   // partial rows the area holds
+};
+DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits,
+                         int clusters);
+
+// Planner kernel: reads qo_indptr / kv_indptr [batch+1] on the device, writes
+// the plan and the schedule into the workspace, the gather and mask row counts
+// into status words 2 and 3, and VMLA_ERR_SHAPE into the status word (with an
+// empty plan) when the lengths are inconsistent or exceed the bounds.
+int launch_device_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads, int splits,
+                       int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
+                       PlanParams* plan, TcSched* sched, uint32_t* status, void* stream);
+int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, const RunArgs& args, void* stream);
+// Gather of the rows counted in *rows_dev (at most args.total_kv, the staged capacity).
+int launch_gather_dplan(const RunArgs& args, const uint32_t* rows_dev, void* stream);
+int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* part_o, const float* part_lse,
+                       uint16_t* out, float* lse, void* stream);
+int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,
+                           const uint32_t* rows_dev, uint64_t* mask_out, uint32_t* status, void* stream);
 
 int launch_simt(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_tc(const PlanParams& plan, const RunArgs& args, void* stream);

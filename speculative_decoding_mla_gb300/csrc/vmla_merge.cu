@@ -22,10 +22,9 @@ namespace {
 constexpr int kMergeWarps = 4;
 constexpr int kMergeBatch = 4;  // pieces loaded together
 
-__global__ void __launch_bounds__(kMergeWarps * 32)
-merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ part_o,
-             const float* __restrict__ part_lse, int lse_is_log2, uint16_t* __restrict__ out,
-             float* __restrict__ lse) {
+__device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
+                                           const float* __restrict__ part_lse, int lse_is_log2,
+                                           uint16_t* __restrict__ out, float* __restrict__ lse) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mrow = blockIdx.x * kMergeWarps + warp;
   if (mrow >= plan.merge_rows) return;
@@ -93,9 +92,28 @@ merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ 
   if (lane == 0) lse[orow] = (M + log2f(W)) * 0.6931471805599453f;
 }
 
+__global__ void __launch_bounds__(kMergeWarps * 32)
+merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ part_o,
+             const float* __restrict__ part_lse, int lse_is_log2, uint16_t* __restrict__ out,
+             float* __restrict__ lse) {
+  merge_body(plan, part_o, part_lse, lse_is_log2, out, lse);
+}
+
+// The plan in the workspace (device-planned calls); rows past its merge rows exit.
+__global__ void __launch_bounds__(kMergeWarps * 32)
+merge_kernel_dplan(const PlanParams* __restrict__ plan, const float* __restrict__ part_o,
+                   const float* __restrict__ part_lse, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  merge_body(*plan, part_o, part_lse, 1, out, lse);
+}
+
 __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ qo_indptr,
-                                 int batch, int total_q, uint64_t* __restrict__ mask_out, uint32_t* status) {
+                                 int batch, int total_q, const uint32_t* __restrict__ rows_dev,
+                                 uint64_t* __restrict__ mask_out, uint32_t* status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (rows_dev) {  // device-planned call: the planner's count of draft rows (0 when the lengths are bad)
+    const int r = (int)*rows_dev;
+    total_q = r < total_q ? r : total_q;
+  }
   if (t >= total_q) return;
   int lo = 0, hi = batch;
   while (hi - lo > 1) {
@@ -137,7 +155,26 @@ int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch,
                      uint32_t* status, void* stream) {
   if (total_q == 0) return VMLA_OK;
   tree_mask_kernel<<<(total_q + 127) / 128, 128, 0, (cudaStream_t)stream>>>(parent, qo_indptr, batch, total_q,
-                                                                             mask_out, status);
+                                                                             nullptr, mask_out, status);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* part_o, const float* part_lse,
+                       uint16_t* out, float* lse, void* stream) {
+  if (max_rows <= 0) return VMLA_OK;
+  const int64_t blocks = (max_rows + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > INT32_MAX) return VMLA_ERR_SHAPE;
+  merge_kernel_dplan<<<(int)blocks, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, out, lse);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,
+                           const uint32_t* rows_dev, uint64_t* mask_out, uint32_t* status, void* stream) {
+  if (max_total_q <= 0) return VMLA_OK;
+  if (max_total_q > INT32_MAX) return VMLA_ERR_SHAPE;
+  const int total_q = (int)max_total_q;
+  tree_mask_kernel<<<(total_q + 127) / 128, 128, 0, (cudaStream_t)stream>>>(parent, qo_indptr, batch, total_q,
+                                                                             rows_dev, mask_out, status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

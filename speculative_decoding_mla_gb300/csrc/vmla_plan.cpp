@@ -10,31 +10,9 @@
 #include <vector>
 
 #include "vmla_internal.h"
+#include "vmla_plan_core.h"
 
 namespace vmla {
-
-PlanShape plan_shape(int kernel) {
-  PlanShape s;
-  if (kernel == VMLA_KERNEL_SIMT) {
-    s.rows_per_unit = 32;
-    s.units_per_sm = 2;
-    s.key_align = 32;
-    s.min_chunk = 256;
-    s.max_splits = 64;
-  } else {
-    // tensor-core kernel: one unit = 256 query rows on a cluster of four SMs
-    // (a scorer pair and a mixer pair); about two units per cluster leave the
-    // greedy schedule room to balance
-    s.rows_per_unit = 256;
-    s.units_per_sm = 2;  // per cluster of four SMs; the caller divides the SM count
-    s.key_align = 128;   // the kernel's tile
-    s.min_chunk = 1024;
-    s.max_splits = 64;
-  }
-  return s;
-}
-
-static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
@@ -55,11 +33,8 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
   if (splits < 0 || num_sms < 1) return VMLA_ERR_SHAPE;
   if (qo[0] != 0 || kv[0] != 0) return VMLA_ERR_SHAPE;
-  for (int b = 0; b < batch; ++b) {
-    int64_t nq = (int64_t)qo[b + 1] - qo[b];
-    int64_t nk = (int64_t)kv[b + 1] - kv[b];
-    if (nq < 0 || nq > VMLA_MAX_DRAFT || nk < nq) return VMLA_ERR_SHAPE;
-  }
+  for (int b = 0; b < batch; ++b)
+    if (plan_check_seq((int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b]) != VMLA_OK) return VMLA_ERR_SHAPE;
   const PlanShape sh = plan_shape(kernel);
   std::memset(pp, 0, sizeof(PlanParams));
   pp->batch = batch;
@@ -70,12 +45,8 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   const int clusters = tc_clusters > 0 ? tc_clusters : std::max(1, num_sms / 4);
   int64_t slots = kernel == VMLA_KERNEL_TC ? (int64_t)clusters * sh.units_per_sm : (int64_t)num_sms * sh.units_per_sm;
   int64_t total_work = 0;  // (row block) x (keys)
-  for (int b = 0; b < batch; ++b) {
-    int64_t nq = qo[b + 1] - qo[b], nk = kv[b + 1] - kv[b];
-    if (nq == 0) continue;
-    total_work += ceil_div(nq * num_heads, sh.rows_per_unit) * nk;
-  }
-  int64_t chunk_target = std::max<int64_t>(sh.min_chunk, ceil_div(std::max<int64_t>(total_work, 1), slots));
+  for (int b = 0; b < batch; ++b) total_work += plan_seq_work(sh, qo[b + 1] - qo[b], kv[b + 1] - kv[b], num_heads);
+  const int64_t chunk_target = plan_chunk_target(sh, total_work, slots);
 
   int64_t unit = 0, part = 0, merge = 0;
   int max_s = 0;
@@ -88,32 +59,11 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
     s.unit_start = (int32_t)unit;
     s.merge_off = (int32_t)merge;
     s.part_off = (int32_t)part;
-    if (s.n_q == 0) {
-      s.n_rb = 0;
-      s.n_split = 1;
-      s.chunk = std::max(1, s.n_kv);
-      continue;
-    }
-    int64_t rows = (int64_t)s.n_q * num_heads;
-    s.n_rb = (int32_t)ceil_div(rows, sh.rows_per_unit);
-    int64_t pieces;
-    if (splits > 0) {
-      pieces = splits;
-    } else {
-      pieces = ceil_div(s.n_kv, chunk_target);
-    }
-    pieces = std::max<int64_t>(1, std::min<int64_t>(pieces, sh.max_splits));
-    // piece length rounded to the key alignment, then the count that leaves no piece empty
-    int64_t chunk = ceil_div(ceil_div(s.n_kv, pieces), sh.key_align) * sh.key_align;
-    pieces = ceil_div(s.n_kv, chunk);
-    s.chunk = (int32_t)chunk;
-    s.n_split = (int32_t)pieces;
-    unit += (int64_t)s.n_rb * pieces;
-    if (pieces > 1) {
-      part += rows * pieces;
-      merge += rows;
-    }
-    max_s = std::max<int>(max_s, (int)pieces);
+    int64_t prows = 0, mrows = 0;
+    unit += plan_split_seq(sh, s, num_heads, splits, chunk_target, &prows, &mrows);
+    part += prows;
+    merge += mrows;
+    if (s.n_q > 0) max_s = std::max<int>(max_s, s.n_split);
   }
   if (unit > INT32_MAX || part > INT32_MAX / kDv) return VMLA_ERR_SHAPE;
   pp->total_units = (int32_t)unit;
@@ -146,14 +96,11 @@ int build_tc_schedule(const PlanParams& plan, int num_clusters, int unit_begin, 
   items.reserve(U);
   for (int b = 0; b < plan.batch; ++b) {
     const SeqPlan& s = plan.seq[b];
-    for (int piece = 0; piece < s.n_split; ++piece) {
-      const int64_t lo = (int64_t)piece * s.chunk;
-      const int64_t hi = std::min<int64_t>(s.n_kv, lo + s.chunk);
+    for (int piece = 0; piece < s.n_split; ++piece)
       for (int rb = 0; rb < s.n_rb; ++rb) {
         const int u = s.unit_start + piece * s.n_rb + rb;
-        if (u >= unit_begin && u < unit_end) items.push_back({(hi - lo) + 256, u});
+        if (u >= unit_begin && u < unit_end) items.push_back({plan_unit_cost(s, u), u});
       }
-    }
   }
   // longest first, ties by unit id (deterministic)
   std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) { return x.cost > y.cost; });

@@ -804,9 +804,10 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
   }
 }
 
-__global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ PlanParams plan,
-                 const __grid_constant__ TcSched sched, const RunArgs a) {
+// The kernel body; `plan` and `sched` are kernel parameters (host-planned
+// calls) or live in the workspace (device-planned calls).
+__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const PlanParams& plan, const TcSched& sched,
+                                               const RunArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -901,6 +902,20 @@ tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
   }
 }
 
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ PlanParams plan,
+                 const __grid_constant__ TcSched sched, const RunArgs a) {
+  tc_verify_body(kmap, plan, sched, a);
+}
+
+// Same kernel with the plan and the cluster schedule read from the workspace,
+// where the device planner wrote them (stream-capture-safe calls).
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const PlanParams* __restrict__ plan,
+                       const TcSched* __restrict__ sched, const RunArgs a) {
+  tc_verify_body(kmap, *plan, *sched, a);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -961,7 +976,9 @@ int tc_max_clusters(int* out) {
     return VMLA_OK;
   }
   if (cudaFuncSetAttribute(tc_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(tc_verify_kernel_dplan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+          cudaSuccess)
     return VMLA_ERR_CUDA;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(1, attr);
@@ -996,6 +1013,23 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, const RunArgs& a, void* stream) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return VMLA_ERR_DEVICE;
+  int dev_clusters = 0;
+  int rc = tc_max_clusters(&dev_clusters);
+  if (rc != VMLA_OK) return rc;
+  if (clusters < 1 || clusters > dev_clusters || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
+  // the map spans the staged area's capacity; the planned keys lie inside it
+  CUtensorMap kmap;
+  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys)) return VMLA_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(clusters, attr);
+  cfg.stream = (cudaStream_t)stream;
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  return VMLA_OK;
 }
 
 }  // namespace vmla

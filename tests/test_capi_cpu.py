@@ -79,6 +79,47 @@ def test_argument_errors_before_any_launch(B):
         assert _run_raw(B, **good) == B.VMLA_ERR_DEVICE
 
 
+def _run_dplan(B, **kw):
+    args = dict(q=None, kv=None, S=16, kvp=None, kvi=None, qop=None, dm=None, par=None, batch=1, H=4, maxq=2,
+                maxkv=8, scale=0.1, splits=0, out=None, lse=None, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    return B.lib().verify_attn_mla_device_plan(args["q"], args["kv"], args["S"], args["kvp"], args["kvi"],
+                                               args["qop"], args["dm"], args["par"], args["batch"], args["H"],
+                                               args["maxq"], args["maxkv"], args["scale"], args["splits"],
+                                               args["out"], args["lse"], args["ws"], args["wsb"], args["stream"])
+
+
+def test_device_plan_argument_errors_before_any_launch(B):
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    good = dict(q=fake, kv=fake, kvp=fake, kvi=fake, qop=fake, out=fake, lse=fake, ws=fake * 2, wsb=1 << 20)
+    assert _run_dplan(B, **{**good, "ws": None}) == B.VMLA_ERR_NULL
+    assert _run_dplan(B, **{**good, "kvp": None}) == B.VMLA_ERR_NULL
+    assert _run_dplan(B, **{**good, "q": None}) == B.VMLA_ERR_NULL
+    assert _run_dplan(B, **{**good, "batch": -1}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "batch": 513}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "H": 0}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "maxq": 65}) == B.VMLA_ERR_SHAPE  # more than 64 drafts per sequence
+    assert _run_dplan(B, **{**good, "maxq": -1}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "maxkv": -1}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "maxkv": 1 << 31}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "splits": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "scale": 0.0}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "scale": float("nan")}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "S": 0}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, **{**good, "q": fake + 2}) == B.VMLA_ERR_ALIGN
+    assert _run_dplan(B, **{**good, "ws": fake + 16}) == B.VMLA_ERR_ALIGN
+    import ctypes
+    n = ctypes.c_size_t(0)
+    assert B.lib().verify_attn_mla_device_plan_workspace_size(1, 64, 16, 1000, 0, None) == B.VMLA_ERR_NULL
+    assert B.lib().verify_attn_mla_device_plan_workspace_size(1, 64, 65, 1000, 0, ctypes.byref(n)) == \
+        B.VMLA_ERR_SHAPE
+    import torch
+    if not torch.cuda.is_available():
+        assert _run_dplan(B, **good) == B.VMLA_ERR_DEVICE
+        assert B.lib().verify_attn_mla_device_plan_workspace_size(1, 64, 16, 1000, 0, ctypes.byref(n)) == \
+            B.VMLA_ERR_DEVICE
+
+
 def _plan(B, kernel, prefixes, drafts, H=64, splits=0, sms=152):
     qo = np.zeros(len(prefixes) + 1, np.int32)
     qo[1:] = np.cumsum(drafts)

@@ -1,0 +1,140 @@
+"""GPU tests of the device-planned (stream-capture-safe) entry point: its
+results equal the host-planned call's bit for bit (both cut the same pieces),
+and one captured CUDA graph replayed with other lengths, indices and contents
+matches the oracle each time; lengths past the bounds are refused on the
+device."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_mla_gb300 import synth
+from tests.test_gpu_parity import compare, run_full, small
+
+pytestmark = pytest.mark.gpu
+
+
+def _mods():
+    import torch
+    from speculative_decoding_mla_gb300 import build as vbuild
+    vbuild.build()
+    from speculative_decoding_mla_gb300 import binding, device
+    return torch, binding, device
+
+
+def run_dplan(case, splits=0, slack_q=0, slack_kv=0):
+    """One device-planned call on buffers sized for the case plus slack; returns (out, lse, status)."""
+    torch, binding, device = _mods()
+    dc = device.to_device(case)
+    T, H = dc.total_q, dc.num_heads
+    maxq, maxkv = T + slack_q, int(case.kv_indptr[-1]) + slack_kv
+    q = torch.zeros((max(maxq, 1), H, 576), dtype=torch.bfloat16, device="cuda")
+    q[:T] = dc.q
+    kvi = torch.zeros(max(maxkv, 1), dtype=torch.int32, device="cuda")
+    kvi[:dc.kv_indices.numel()] = dc.kv_indices
+    out = torch.full((max(maxq, 1), H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((max(maxq, 1), H), float("nan"), dtype=torch.float32, device="cuda")
+    n = binding.verify_attn_mla_device_plan_workspace_size(case.batch, H, maxq, maxkv, splits)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    binding.verify_attn_mla_device_plan(q, dc.kv_pool, dc.kv_indptr, kvi, dc.qo_indptr, case.batch, maxq, maxkv,
+                                        out, lse, ws, dc.sm_scale, parent=dc.parent, splits=splits)
+    st = binding.verify_attn_mla_check(ws)
+    torch.cuda.synchronize()
+    return device.bf16_to_f64(out[:T]), lse[:T].cpu().numpy().astype(np.float64), st
+
+
+@pytest.mark.parametrize("name", ["one_seq", "ragged", "tree", "heads_odd", "decode_q1"])
+def test_device_plan_equals_host_plan_bitwise(name):
+    case = small(name, seed=410)
+    o1, l1, s1 = run_full(case, "tc")
+    o2, l2, s2 = run_dplan(case, slack_q=5, slack_kv=300)
+    assert s1 == 0 and s2 == 0
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 7])
+def test_device_plan_forced_splits_bitwise(splits):
+    case = small("ragged", seed=411)
+    o1, l1, _ = run_full(case, "tc", splits=splits)
+    o2, l2, st = run_dplan(case, splits=splits)
+    assert st == 0
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_device_plan_contiguous_1k_against_oracle():
+    case = synth.workload("contiguous_1k")
+    ref_o, ref_l = oracle.verify(case)
+    o, l, st = run_dplan(case)
+    assert st == 0
+    compare(o, l, ref_o, ref_l, "device plan / contiguous_1k")
+
+
+def _step(name, prefixes, drafts, seed, H, pool):
+    return synth.make_case(name, prefixes, drafts, num_heads=H, pool_slots=pool, seed=seed)
+
+
+def test_captured_graph_replays_with_new_lengths():
+    torch, binding, device = _mods()
+    H, B, pool = 16, 3, 9000
+    steps = [_step("a", [1000, 2000, 300], [16, 8, 4], 421, H, pool),
+             _step("b", [700, 4100, 50], [4, 16, 12], 422, H, pool),
+             _step("c", [0, 130, 5000], [1, 64, 2], 423, H, pool)]
+    maxq = max(s.q.shape[0] for s in steps)
+    maxkv = max(int(s.kv_indptr[-1]) for s in steps)
+    q = torch.zeros((maxq, H, 576), dtype=torch.bfloat16, device="cuda")
+    kv_pool = torch.zeros((pool, 576), dtype=torch.bfloat16, device="cuda")
+    kvp = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
+    qop = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
+    kvi = torch.zeros(maxkv, dtype=torch.int32, device="cuda")
+    out = torch.zeros((maxq, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((maxq, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.verify_attn_mla_device_plan_workspace_size(B, H, maxq, maxkv, 0), dtype=torch.uint8,
+                     device="cuda")
+
+    def load(case):
+        dc = device.to_device(case)
+        T, N = dc.total_q, dc.kv_indices.numel()
+        q[:T].copy_(dc.q)
+        kv_pool.copy_(dc.kv_pool)
+        kvp.copy_(dc.kv_indptr)
+        qop.copy_(dc.qo_indptr)
+        kvi[:N].copy_(dc.kv_indices)
+        torch.cuda.synchronize()
+        return dc
+
+    def call(stream):
+        binding.verify_attn_mla_device_plan(q, kv_pool, kvp, kvi, qop, B, maxq, maxkv, out, lse, ws,
+                                            steps[0].sm_scale, stream=stream)
+
+    load(steps[0])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(side)  # outside the capture: device set-up and the cluster count are looked up once
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for case in steps:
+        dc = load(case)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.verify_attn_mla_check(ws) == 0
+        T = dc.total_q
+        o = device.bf16_to_f64(out[:T])
+        l = lse[:T].cpu().numpy().astype(np.float64)
+        ref_o, ref_l = oracle.verify(case)
+        compare(o, l, ref_o, ref_l, f"graph replay {case.name}")
+        o_host, l_host, _ = run_full(case, "tc")
+        assert np.array_equal(o, o_host) and np.array_equal(l, l_host)
+    # lengths past the bounds: nothing is computed and the status says why
+    big = np.array(steps[1].kv_indptr, np.int32)
+    big[-1] = maxkv + 1
+    kvp.copy_(torch.from_numpy(big))
+    out.fill_(0.5)
+    g.replay()
+    torch.cuda.synchronize()
+    assert binding.verify_attn_mla_check(ws) == binding.VMLA_ERR_SHAPE
+    assert bool(torch.all(out == 0.5))
