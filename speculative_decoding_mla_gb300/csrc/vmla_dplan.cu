@@ -24,11 +24,12 @@ constexpr int kSortKeys = 4096;  // power of two, at least kMaxTcUnits
 static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
 static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
 
-// Ascending bitonic sort of kSortKeys keys in shared memory (whole block).
-__device__ void block_sort(uint64_t* k) {
-  for (int size = 2; size <= kSortKeys; size <<= 1)
+// Ascending bitonic sort of the first n keys in shared memory (n a power of
+// two, at most kSortKeys; whole block).
+__device__ void block_sort(uint64_t* k, int n) {
+  for (int size = 2; size <= n; size <<= 1)
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < kSortKeys / 2; i += blockDim.x) {
+      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool up = (lo & size) == 0;
@@ -129,7 +130,9 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   // schedule: units by decreasing cost (ties by unit), dealt to the clusters
   // in a snake order, then in unit order within each cluster
   const int U = ok ? (int)units : 0;
-  for (int k = tid; k < kSortKeys; k += blockDim.x) {
+  int n_sort = 2;  // sort only as many keys as there are units (rounded up to a power of two)
+  while (n_sort < U) n_sort <<= 1;
+  for (int k = tid; k < n_sort; k += blockDim.x) {
     uint64_t key = ~0ull;
     if (k < U) {
       const int64_t cost = plan_unit_cost(pp->seq[seq_of_unit(*pp, k)], k);
@@ -138,7 +141,7 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     keys[k] = key;
   }
   __syncthreads();
-  block_sort(keys);
+  block_sort(keys, n_sort);
   const int C = clusters;
   for (int p = tid; p < U; p += blockDim.x) {
     const int round = p / C, j = p - round * C;
@@ -146,7 +149,7 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     keys[p] = ((uint64_t)c << 32) | (keys[p] & 0xFFFFFFFFull);
   }
   __syncthreads();
-  block_sort(keys);
+  block_sort(keys, n_sort);
   for (int p = tid; p < U; p += blockDim.x) sched->order[p] = (uint16_t)(keys[p] & 0xFFFFu);
   for (int c = tid; c <= C; c += blockDim.x) {
     int lo = 0, hi = U;  // first position whose cluster is >= c
