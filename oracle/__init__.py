@@ -15,6 +15,7 @@ Parity status of each function (what pins it is listed in the tests):
   verify_split          pinned: equals the unsplit result (merge identity)
   merge                 pinned: closed forms, equals the unsplit result
   tree_masks            pinned: graph-library ancestor sets
+  tree_accept           pinned: hand-worked trees, brute force over all root paths
 """
 from __future__ import annotations
 
@@ -153,3 +154,61 @@ def tree_masks(parent: np.ndarray, qo_indptr: np.ndarray, lib_=None) -> np.ndarr
     if rc != 0:
         raise ValueError("oracle_tree_masks: parents must precede their children")
     return out
+
+
+def tree_accept(qo_indptr: np.ndarray, parent: Optional[np.ndarray], draft_token: np.ndarray,
+                target_token: np.ndarray, root_token: np.ndarray):
+    """Greedy acceptance of a verified draft tree (plain Python; small trees).
+
+    The pages name a tree_accept kernel run after the verify attention but do
+    not describe it; this is the plain reading of greedy tree verification.
+    Draft node i of a sequence proposes draft_token[i] after its parent (the
+    prefix for a root, parent -1); the target's greedy token after node j is
+    target_token[j], and after the prefix root_token.  A node is accepted when
+    its parent is accepted (the prefix always is) and its token equals the
+    target's token after the parent.  The chosen path ends at the deepest
+    accepted node (the smallest index among equally deep ones).
+
+    Returns accept_len [B] (nodes on the path), accept_path [T] (each
+    sequence's path, root first, from its first position; -1 after it),
+    next_token [B] (the target's token after the path's last node, or after
+    the prefix) and bad [B] (parents not in [-1, i); nothing accepted).
+    parent None means the chain parent[i] = i - 1.
+    """
+    qo = np.asarray(qo_indptr, np.int64)
+    B = len(qo) - 1
+    T = int(qo[-1])
+    accept_len = np.zeros(B, np.int32)
+    accept_path = np.full(T, -1, np.int32)
+    next_token = np.zeros(B, np.int32)
+    bad = np.zeros(B, bool)
+    for b in range(B):
+        q0, n = int(qo[b]), int(qo[b + 1] - qo[b])
+        par = [int(parent[q0 + i]) if parent is not None else i - 1 for i in range(n)]
+        if any(p < -1 or p >= i for i, p in enumerate(par)):
+            bad[b] = True
+            next_token[b] = root_token[b]
+            continue
+        accepted = [False] * n
+        depth = [0] * n
+        best = -1
+        for i in range(n):
+            p = par[i]
+            expected = root_token[b] if p < 0 else target_token[q0 + p]
+            accepted[i] = (p < 0 or accepted[p]) and draft_token[q0 + i] == expected
+            depth[i] = 0 if p < 0 else depth[p] + 1
+            if accepted[i] and (best < 0 or depth[i] > depth[best]):
+                best = i
+        if best < 0:
+            next_token[b] = root_token[b]
+            continue
+        path = []
+        node = best
+        while node >= 0:
+            path.append(node)
+            node = par[node]
+        path.reverse()
+        accept_len[b] = len(path)
+        accept_path[q0:q0 + len(path)] = path
+        next_token[b] = target_token[q0 + best]
+    return accept_len, accept_path, next_token, bad

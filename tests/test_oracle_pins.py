@@ -332,3 +332,92 @@ def test_rejects_bad_inputs():
         oracle.verify(bad)
     with pytest.raises(ValueError):
         oracle.tree_masks(np.array([-1, 1], np.int32), np.array([0, 2], np.int32))
+
+
+# ---------------------------------------------------------------- tree acceptance
+
+def _accept_one(parent, draft, target, root):
+    qo = np.array([0, len(draft)])
+    par = None if parent is None else np.array(parent, np.int32)
+    return oracle.tree_accept(qo, par, np.array(draft, np.int32), np.array(target, np.int32),
+                              np.array([root], np.int32))
+
+
+def test_tree_accept_hand_worked():
+    # chain, every draft matches the target's token after its predecessor
+    n, path, nxt, bad = _accept_one(None, [10, 11, 12, 13], [11, 12, 13, 14], 10)
+    assert n[0] == 4 and list(path) == [0, 1, 2, 3] and nxt[0] == 14 and not bad[0]
+    # chain, the first draft is already wrong: nothing accepted, the prefix's token is next
+    n, path, nxt, _ = _accept_one(None, [9, 11, 12, 13], [11, 12, 13, 14], 10)
+    assert n[0] == 0 and list(path) == [-1] * 4 and nxt[0] == 10
+    # chain, wrong at the third node: two accepted, the second node's target token is next
+    n, path, nxt, _ = _accept_one(None, [10, 11, 99, 13], [11, 12, 13, 14], 10)
+    assert n[0] == 2 and list(path) == [0, 1, -1, -1] and nxt[0] == 12
+    # tree: roots 0 and 1 (only 1 matches the prefix's token 5), 2 under 1 matches, 3 under 0 would
+    # match its parent's token but 0 was rejected, 4 under 2 is wrong
+    parent = [-1, -1, 1, 0, 2]
+    draft = [4, 5, 7, 8, 0]
+    target = [8, 7, 6, 1, 2]
+    n, path, nxt, _ = _accept_one(parent, draft, target, 5)
+    assert n[0] == 2 and list(path) == [1, 2, -1, -1, -1] and nxt[0] == 6
+    # equal depths: the smaller index wins (nodes 1 and 2 are both accepted children of 0)
+    n, path, nxt, _ = _accept_one([-1, 0, 0], [3, 4, 4], [4, 9, 8], 3)
+    assert n[0] == 2 and list(path) == [0, 1, -1] and nxt[0] == 9
+    # a deeper accepted node beats a shallower one with a smaller index
+    n, path, nxt, _ = _accept_one([-1, 0, 0, 2], [3, 4, 4, 8], [4, 9, 8, 1], 3)
+    assert n[0] == 3 and list(path) == [0, 2, 3, -1] and nxt[0] == 1
+    # malformed parent (a parent after its child): flagged, nothing accepted
+    n, path, nxt, bad = _accept_one([-1, 2, 0], [3, 4, 4], [4, 9, 8], 3)
+    assert bad[0] and n[0] == 0 and nxt[0] == 3
+
+
+def test_tree_accept_empty_sequences_and_parent_none_is_chain():
+    qo = np.array([0, 0, 3, 3])
+    draft = np.array([7, 8, 1], np.int32)
+    target = np.array([8, 2, 5], np.int32)
+    root = np.array([1, 7, 4], np.int32)
+    n, path, nxt, bad = oracle.tree_accept(qo, None, draft, target, root)
+    assert list(n) == [0, 2, 0] and list(nxt) == [1, 2, 4] and not bad.any()
+    n2, path2, nxt2, _ = oracle.tree_accept(qo, np.array([-1, 0, 1], np.int32), draft, target, root)
+    assert np.array_equal(n, n2) and np.array_equal(path, path2) and np.array_equal(nxt, nxt2)
+
+
+def _brute_force_accept(parent, draft, target, root):
+    """Every root-to-node path, accepted when each token equals the target's token after its
+    predecessor; the longest accepted path, ties by the smaller last node."""
+    n = len(draft)
+    best = []
+    for end in range(n):
+        path = [end]
+        while parent[path[-1]] >= 0:
+            path.append(parent[path[-1]])
+        path.reverse()
+        prev_tok = root
+        ok = True
+        for node in path:
+            if draft[node] != prev_tok:
+                ok = False
+                break
+            prev_tok = target[node]
+        if ok and len(path) > len(best):
+            best = path
+    return best, (target[best[-1]] if best else root)
+
+
+def test_tree_accept_matches_brute_force_on_random_trees():
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        n = int(rng.integers(1, 20))
+        parent = synth.tree_parents(trial, n, int(rng.integers(1, 8)), 0)
+        target = rng.integers(0, 4, n).astype(np.int32)
+        root = int(rng.integers(0, 4))
+        # drafts that often (not always) follow the target, so paths of every length occur
+        draft = np.empty(n, np.int32)
+        for i in range(n):
+            follow = root if parent[i] < 0 else target[parent[i]]
+            draft[i] = follow if rng.random() < 0.7 else int(rng.integers(0, 4))
+        path, nxt = _brute_force_accept(list(parent), list(draft), list(target), root)
+        n_acc, p_acc, nxt_acc, bad = _accept_one(parent, draft, target, root)
+        assert not bad[0]
+        assert n_acc[0] == len(path) and list(p_acc[:len(path)]) == path and nxt_acc[0] == nxt
+        assert (p_acc[len(path):] == -1).all()
