@@ -355,6 +355,7 @@ def run_ours(args, rank, local, world):
     # the stream-capture-safe entry point (plan computed on the device) captured
     # once in a CUDA graph and replayed on the same workload, one replay per step
     graph = device_plan_graph(args, case, dc, stream, flush_buf, tokens)
+    accept = tree_accept_timing()
 
     peaks = load_peaks()
     v_ms = float(verify_ms.mean())
@@ -394,9 +395,41 @@ def run_ours(args, rank, local, world):
                             "the KV cache stays resident in HBM"},
             "gpu_launches": int(launches_per_step * args.steps),
             "device_plan_graph": graph,
+            "tree_accept": accept,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
+
+
+def tree_accept_timing(batch=32, nodes=64, calls=200):
+    """Times the tree-acceptance kernel on seeded random trees of `nodes` drafts per sequence."""
+    import torch
+    from speculative_decoding_mla_gb300 import binding, synth
+    rng = np.random.default_rng(5)
+    qo = np.arange(batch + 1, dtype=np.int32) * nodes
+    parent = np.concatenate([synth.tree_parents(5, nodes, 8, b) for b in range(batch)]).astype(np.int32)
+    target = rng.integers(0, 8, batch * nodes).astype(np.int32)
+    root = rng.integers(0, 8, batch).astype(np.int32)
+    follow = np.where(parent < 0, root[np.arange(batch * nodes) // nodes], target[np.maximum(parent, 0) +
+                                                                              (np.arange(batch * nodes) // nodes) * nodes])
+    draft = np.where(rng.random(batch * nodes) < 0.8, follow, rng.integers(0, 8, batch * nodes)).astype(np.int32)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    qo_d, par_d, dr_d, tg_d, rt_d = d(qo), d(parent), d(draft), d(target), d(root)
+    acc = torch.empty(batch, dtype=torch.int32, device="cuda")
+    path = torch.empty(batch * nodes, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(batch, dtype=torch.int32, device="cuda")
+    for _ in range(5):
+        binding.verify_attn_mla_tree_accept(qo_d, par_d, dr_d, tg_d, rt_d, acc, path, nxt)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls):
+        binding.verify_attn_mla_tree_accept(qo_d, par_d, dr_d, tg_d, rt_d, acc, path, nxt)
+    e1.record()
+    torch.cuda.synchronize()
+    return {"us_per_call": e0.elapsed_time(e1) * 1e3 / calls, "batch": batch, "nodes_per_sequence": nodes,
+            "mean_accepted": float(acc.float().mean()),
+            "note": "one thread per sequence; back-to-back launches on one stream (launch-bound)"}
 
 
 def device_plan_graph(args, case, dc, stream, flush_buf, tokens):

@@ -160,6 +160,36 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
                                 int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Greedy acceptance of the verified draft tree, the step after the verify
+ * attention.  "The Build That Unlocked 3-6x Decode Speedup" lists a
+ * tree_accept kernel (section "The Context: A Custom Kernel for an
+ * Unsupported Architecture") without describing it; this is the plain reading:
+ * draft node i of a sequence proposes draft_token[i] after its parent (the
+ * prefix for a root) and is accepted when its parent is accepted and the token
+ * equals the target model's greedy token after the parent.  The chosen path
+ * ends at the deepest accepted node (the smallest index among equally deep
+ * ones).  All arrays are device arrays; one thread per sequence.
+ *   qo_indptr    [batch+1] int32; Q_b = qo_indptr[b+1] - qo_indptr[b] <= 64 nodes
+ *   parent       [T_q] int32 local parent (-1 = root, parent[i] < i), or NULL for
+ *                the chain parent[i] = i - 1
+ *   draft_token  [T_q] int32: the token each node proposes
+ *   target_token [T_q] int32: the target's greedy token after each node
+ *   root_token   [batch] int32: the target's greedy token after the prefix
+ *   accept_len   [batch] int32 out: nodes on the chosen path (0 .. Q_b)
+ *   accept_path  [T_q] int32 out: from qo_indptr[b], the path's local node
+ *                indices, root first, then -1 up to the sequence's end
+ *   next_token   [batch] int32 out: the target's token after the path's last
+ *                node, or root_token[b] when nothing is accepted
+ *   status_word  optional (the first word of a workspace): a parent outside
+ *                [-1, i) or a sequence outside [0, total_q) records
+ *                VMLA_ERR_PARENT with the sequence index; that sequence
+ *                accepts nothing.
+ * Argument errors return before the launch.  No host synchronisation. */
+int verify_attn_mla_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft_token,
+                                const int32_t* target_token, const int32_t* root_token, int batch, int total_q,
+                                int32_t* accept_len, int32_t* accept_path, int32_t* next_token, uint32_t* status_word,
+                                void* stream);
+
 /* Fixed size of the scratch array behind verify_attn_mla_simt_static (32 MiB). */
 #define VMLA_STATIC_SCRATCH_BYTES (32u << 20)
 

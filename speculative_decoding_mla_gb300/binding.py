@@ -38,6 +38,7 @@ EXPORTS = (
     "verify_attn_mla_host_buffer_size", "verify_attn_mla_host", "verify_attn_mla_status_string",
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
     "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
+    "verify_attn_mla_tree_accept",
 )
 
 
@@ -76,6 +77,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_device_plan_workspace_size": [i32, i32, i64, i64, i32, ctypes.POINTER(sz)],
         "verify_attn_mla_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp, vp,
                                         sz, vp],
+        "verify_attn_mla_tree_accept": [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -185,6 +187,16 @@ def verify_attn_mla_device_plan(q, kv_pool, kv_indptr, kv_indices, qo_indptr, ba
                                           _ptr(out), _ptr(lse), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "verify_attn_mla_device_plan")
+
+
+def verify_attn_mla_tree_accept(qo_indptr, parent, draft_token, target_token, root_token, accept_len, accept_path,
+                                next_token, status_word=None, stream=None):
+    """Greedy acceptance of the verified draft tree (device int32 arrays; parent None = chain)."""
+    batch = int(qo_indptr.numel()) - 1
+    rc = _lib.verify_attn_mla_tree_accept(_ptr(qo_indptr), _ptr(parent), _ptr(draft_token), _ptr(target_token),
+                                          _ptr(root_token), batch, int(draft_token.numel()), _ptr(accept_len),
+                                          _ptr(accept_path), _ptr(next_token), _ptr(status_word), _stream(stream))
+    _check(rc, "verify_attn_mla_tree_accept")
 
 
 def verify_attn_mla_simt(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,

@@ -419,6 +419,25 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   return launch_merge_dplan(plan, max_total_q * num_heads, a.part_o, a.part_lse, a.out, a.lse, stream);
 }
 
+int verify_attn_mla_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft_token,
+                                const int32_t* target_token, const int32_t* root_token, int batch, int total_q,
+                                int32_t* accept_len, int32_t* accept_path, int32_t* next_token, uint32_t* status_word,
+                                void* stream) {
+  if (batch < 0 || batch > VMLA_MAX_BATCH || total_q < 0 || total_q > batch * VMLA_MAX_DRAFT) return VMLA_ERR_SHAPE;
+  if (batch == 0) return VMLA_OK;
+  if (!qo_indptr || !root_token || !accept_len || !next_token) return VMLA_ERR_NULL;
+  if (total_q > 0 && (!draft_token || !target_token || !accept_path)) return VMLA_ERR_NULL;
+  if (!aligned(qo_indptr, 4) || !aligned(parent, 4) || !aligned(draft_token, 4) || !aligned(target_token, 4) ||
+      !aligned(root_token, 4) || !aligned(accept_len, 4) || !aligned(accept_path, 4) || !aligned(next_token, 4) ||
+      !aligned(status_word, 4))
+    return VMLA_ERR_ALIGN;
+  int sms = 0;
+  int rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  return launch_tree_accept(qo_indptr, parent, draft_token, target_token, root_token, batch, total_q, accept_len,
+                            accept_path, next_token, status_word, stream);
+}
+
 int verify_attn_mla_timing_enable(int capacity) {
   std::lock_guard<std::mutex> g(g_timing.mu);
   for (cudaEvent_t e : g_timing.ev) cudaEventDestroy(e);

@@ -147,6 +147,10 @@ int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* pa
 int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,
                            const uint32_t* rows_dev, uint64_t* mask_out, uint32_t* status, void* stream);
 
+int launch_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft, const int32_t* target,
+                       const int32_t* root, int batch, int total_q, int32_t* accept_len, int32_t* path,
+                       int32_t* next_token, uint32_t* status, void* stream);
+
 int launch_simt(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_tc(const PlanParams& plan, const RunArgs& args, void* stream);
 int launch_gather(const RunArgs& args, void* stream);

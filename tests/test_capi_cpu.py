@@ -120,6 +120,29 @@ def test_device_plan_argument_errors_before_any_launch(B):
             B.VMLA_ERR_DEVICE
 
 
+def test_tree_accept_argument_errors_before_any_launch(B):
+    fake = 1 << 20
+    L = B.lib()
+    good = [fake, fake, fake, fake, fake, 2, 10, fake, fake, fake, None, None]
+    def call(i=None, v=None):
+        a = list(good)
+        if i is not None:
+            a[i] = v
+        return L.verify_attn_mla_tree_accept(*a)
+    assert call(5, -1) == B.VMLA_ERR_SHAPE
+    assert call(6, 129) == B.VMLA_ERR_SHAPE  # more than 64 nodes per sequence
+    assert call(6, -1) == B.VMLA_ERR_SHAPE
+    assert call(0, None) == B.VMLA_ERR_NULL
+    assert call(4, None) == B.VMLA_ERR_NULL
+    assert call(2, None) == B.VMLA_ERR_NULL
+    assert call(8, None) == B.VMLA_ERR_NULL
+    assert call(2, fake + 2) == B.VMLA_ERR_ALIGN
+    assert L.verify_attn_mla_tree_accept(None, None, None, None, None, 0, 0, None, None, None, None, None) == B.VMLA_OK
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == B.VMLA_ERR_DEVICE
+
+
 def _plan(B, kernel, prefixes, drafts, H=64, splits=0, sms=152):
     qo = np.zeros(len(prefixes) + 1, np.int32)
     qo[1:] = np.cumsum(drafts)

@@ -92,3 +92,40 @@ def test_mutant_is_caught(tmp_path, name):
 def test_unmutated_passes_battery():
     results = dict(_battery(oracle.lib()))
     assert all(results.values()), results
+
+
+# ---------------------------------------------------------------- tree acceptance (Python oracle)
+
+ACCEPT_MUTANTS = {
+    "expects_own_target": ("expected = root_token[b] if p < 0 else target_token[q0 + p]",
+                           "expected = root_token[b] if p < 0 else target_token[q0 + i]"),
+    "parent_acceptance_ignored": ("accepted[i] = (p < 0 or accepted[p]) and", "accepted[i] = True and"),
+    "ties_to_larger_index": ("depth[i] > depth[best]", "depth[i] >= depth[best]"),
+    "next_after_parent": ("next_token[b] = target_token[q0 + best]",
+                          "next_token[b] = target_token[q0 + max(par[best], 0)]"),
+    "depth_not_accumulated": ("depth[i] = 0 if p < 0 else depth[p] + 1", "depth[i] = 0 if p < 0 else 1"),
+}
+
+
+def _accept_mutant(old, new):
+    import inspect
+    from typing import Optional
+    src = inspect.getsource(oracle.tree_accept)
+    assert src.count(old) == 1, f"pattern must occur exactly once: {old}"
+    ns = {"np": np, "Optional": Optional}
+    exec(src.replace(old, new), ns)
+    return ns["tree_accept"]
+
+
+@pytest.mark.parametrize("name", sorted(ACCEPT_MUTANTS))
+def test_tree_accept_mutant_breaks_a_pin(name, monkeypatch):
+    mutant = _accept_mutant(*ACCEPT_MUTANTS[name])
+    monkeypatch.setattr(oracle, "tree_accept", mutant)
+    failed = []
+    for pin in (pins.test_tree_accept_hand_worked, pins.test_tree_accept_empty_sequences_and_parent_none_is_chain,
+                pins.test_tree_accept_matches_brute_force_on_random_trees):
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passes every tree-acceptance pin"
