@@ -429,7 +429,7 @@ def tree_accept_timing(batch=32, nodes=64, calls=200):
     torch.cuda.synchronize()
     return {"us_per_call": e0.elapsed_time(e1) * 1e3 / calls, "batch": batch, "nodes_per_sequence": nodes,
             "mean_accepted": float(acc.float().mean()),
-            "note": "one thread per sequence; back-to-back launches on one stream (launch-bound)"}
+            "note": "one warp per sequence; back-to-back launches on one stream"}
 
 
 def device_plan_graph(args, case, dc, stream, flush_buf, tokens):
