@@ -160,6 +160,43 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
                                 int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Persistent KV defragmentation ("The Build That Unlocked 3-6x Decode
+ * Speedup" names the compaction of scattered page_size = 1 slots into
+ * contiguous runs as the plan's next phase, section "The Context: A Custom
+ * Kernel for an Unsupported Architecture").  Copies the rows of sequence b,
+ * src_pool[kv_indices[kv_indptr[b] + j]] for j < N_b, to dst_pool slots
+ * run_base[b] + j, and zeroes the run's following slots up to a multiple of
+ * 128 rows (inside dst_slots), which verify_attn_mla_runs reads with no weight.
+ *   src_pool [src_slots, 576] bf16, dst_pool [dst_slots, 576] bf16 (may be the
+ *            same pool; a run must not overlap rows that are still being read)
+ *   kv_indptr, kv_indices  device arrays as for verify_attn_mla;
+ *   kv_indptr_host         host copy of kv_indptr (sizes the launch)
+ *   run_base [batch] int32 device: each sequence's first destination slot;
+ *            runs must not overlap one another
+ *   status_word  optional: a source slot outside the pool or a run outside
+ *            [0, dst_slots) records VMLA_ERR_INDEX (row or sequence index).
+ * Argument errors return before the launch.  No host synchronisation. */
+int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
+                           const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
+                           int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream);
+
+/* verify_attn_mla on rows that lie in runs of the pool: the rows of sequence b
+ * are kv_pool slots run_base[b] .. run_base[b] + N_b - 1 (its last Q_b rows
+ * being the drafts), and the slots after each run up to a multiple of 128 hold
+ * finite values (verify_attn_mla_defrag writes zeros there).  No gather runs:
+ * the tensor-core kernel streams each run as tile loads straight from the pool.
+ * Arguments as for verify_attn_mla with run_base [batch] int32 (device) in
+ * place of kv_indices; workspace >= verify_attn_mla_runs_workspace_size()
+ * bytes (no staged rows).  A run outside the pool records VMLA_ERR_INDEX
+ * (sequence index) in the status word; its keys then read zeros. */
+int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                         const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                         const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
+                         int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream);
+int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                        const int32_t* kv_indptr_host, int splits, size_t* bytes);
+
 /* Greedy acceptance of the verified draft tree, the step after the verify
  * attention.  "The Build That Unlocked 3-6x Decode Speedup" lists a
  * tree_accept kernel (section "The Context: A Custom Kernel for an

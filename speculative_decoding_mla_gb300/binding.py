@@ -38,7 +38,8 @@ EXPORTS = (
     "verify_attn_mla_host_buffer_size", "verify_attn_mla_host", "verify_attn_mla_status_string",
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
     "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
-    "verify_attn_mla_tree_accept",
+    "verify_attn_mla_tree_accept", "verify_attn_mla_defrag", "verify_attn_mla_runs",
+    "verify_attn_mla_runs_workspace_size",
 )
 
 
@@ -78,6 +79,9 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp, vp,
                                         sz, vp],
         "verify_attn_mla_tree_accept": [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp],
+        "verify_attn_mla_defrag": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, vp],
+        "verify_attn_mla_runs": run,
+        "verify_attn_mla_runs_workspace_size": [i32, i32, vp, vp, i32, ctypes.POINTER(sz)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -187,6 +191,32 @@ def verify_attn_mla_device_plan(q, kv_pool, kv_indptr, kv_indices, qo_indptr, ba
                                           _ptr(out), _ptr(lse), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "verify_attn_mla_device_plan")
+
+
+def verify_attn_mla_defrag(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, status_word=None,
+                           stream=None):
+    """Copies every sequence's rows into its run of dst_pool (runs start at run_base) and zeroes each run's tail."""
+    kvh = _host_i32(kv_indptr_host)
+    rc = _lib.verify_attn_mla_defrag(_ptr(src_pool), int(src_pool.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
+                                     kvh.ctypes.data, len(kvh) - 1, _ptr(dst_pool), int(dst_pool.shape[0]),
+                                     _ptr(run_base), _ptr(status_word), _stream(stream))
+    _check(rc, "verify_attn_mla_defrag")
+
+
+def verify_attn_mla_runs_workspace_size(qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0) -> int:
+    qo = _host_i32(qo_indptr_host)
+    kv = _host_i32(kv_indptr_host)
+    n = ctypes.c_size_t(0)
+    _check(_lib.verify_attn_mla_runs_workspace_size(len(qo) - 1, num_heads, qo.ctypes.data, kv.ctypes.data, splits,
+                                                    ctypes.byref(n)), "verify_attn_mla_runs_workspace_size")
+    return int(n.value)
+
+
+def verify_attn_mla_runs(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+                         workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    """Tensor-core verify attention on rows that lie in per-sequence runs of the pool (no gather)."""
+    _run(_lib.verify_attn_mla_runs, "verify_attn_mla_runs", q, kv_pool, kv_indptr, run_base, qo_indptr,
+         kv_indptr_host, qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
 
 
 def verify_attn_mla_tree_accept(qo_indptr, parent, draft_token, target_token, root_token, accept_len, accept_path,

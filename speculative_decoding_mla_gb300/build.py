@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libvmla.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["vmla_capi.cu", "vmla_plan.cpp", "vmla_simt.cu", "vmla_merge.cu", "vmla_gather.cu", "vmla_tc.cu", "vmla_static.cu",
-           "vmla_dplan.cu", "vmla_accept.cu"]
+           "vmla_dplan.cu", "vmla_accept.cu", "vmla_defrag.cu"]
 
 
 def nvcc() -> str:

@@ -60,7 +60,8 @@ int current_sm_count(int* sms, bool require_sm103) {
 namespace vmla {
 
 int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
-        const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask, const int32_t* parent,
+        const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+        const int32_t* parent,
         const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
         int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
@@ -70,8 +71,11 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   const int64_t total_q = qo_indptr_host[batch];
   const int64_t total_kv = kv_indptr_host[batch];
   if (!workspace) return VMLA_ERR_NULL;
-  if (total_q > 0 && (!q || !kv_pool || !kv_indptr || !kv_indices || !qo_indptr || !out || !lse))
+  const bool runs = run_base != nullptr;  // rows in per-sequence pool runs: no gather
+  if (runs && kernel != VMLA_KERNEL_TC) return VMLA_ERR_SHAPE;
+  if (total_q > 0 && (!q || !kv_pool || !kv_indptr || (!runs && !kv_indices) || !qo_indptr || !out || !lse))
     return VMLA_ERR_NULL;
+  if (!aligned(run_base, 4)) return VMLA_ERR_ALIGN;
   if (total_kv > 0 && pool_slots == 0) return VMLA_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(workspace, VMLA_WORKSPACE_ALIGN) || !aligned(draft_mask, 8) || !aligned(parent, 4))
@@ -89,7 +93,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan, &info);
   if (rc != VMLA_OK) return rc;
   if (workspace_bytes < info.workspace_bytes) return VMLA_ERR_WORKSPACE;
-  const WorkspaceLayout L = workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC ? total_kv : 0);
+  const WorkspaceLayout L =
+      workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC && !runs ? total_kv : 0);
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
   cudaStream_t st = (cudaStream_t)stream;
@@ -115,15 +120,23 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   a.lse = lse;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
-  a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
-  a.total_kv = total_kv;
+  a.staged = runs ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_pool))
+                  : reinterpret_cast<uint16_t*>(ws + L.staged_off);
+  a.total_kv = runs ? pool_slots : total_kv;
+  a.run_base = run_base;
   a.status = status;
   int slot = -1;
   {
     std::lock_guard<std::mutex> g(g_timing.mu);
     if (g_timing.n < g_timing.cap) slot = g_timing.n++;
   }
-  if (kernel == VMLA_KERNEL_TC) {
+  if (runs) {
+    // the runs must lie in the pool (the kernel reads whatever the tile loads
+    // return; this check reports a run outside it)
+    rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, batch, total_kv, nullptr, pool_slots, run_base, true, status,
+                       stream);
+    if (rc != VMLA_OK) return rc;
+  } else if (kernel == VMLA_KERNEL_TC) {
     // KV rows of every sequence gathered once into a contiguous staging area, so
     // that the verify kernel streams them with tiled TMA loads
     if (slot >= 0) cudaEventRecord(timing_event(slot, 4), st);
@@ -188,9 +201,61 @@ int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, cons
                     const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch,
                     int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
-             kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask,
+             parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
              workspace_bytes, stream);
+}
+
+int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                         const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                         const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
+                         int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch > 0 && !run_base) return VMLA_ERR_NULL;
+  static const int32_t kNone = 0;  // any non-null pointer selects the runs mode when batch is 0
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, nullptr, run_base ? run_base : &kNone,
+                    qo_indptr, draft_mask, parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits,
+                    out, lse, workspace, workspace_bytes, stream);
+}
+
+int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                        const int32_t* kv_indptr_host, int splits, size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, 0, splits);
+  if (rc != VMLA_OK) return rc;
+  int sms = 0, clusters = 0;
+  rc = current_sm_count(&sms, false);
+  if (rc != VMLA_OK) return rc;
+  rc = vmla::tc_max_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  static thread_local PlanParams plan;
+  vmla_plan_info info;
+  rc = build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan,
+                  &info);
+  if (rc != VMLA_OK) return rc;
+  *bytes = workspace_layout(qo_indptr_host[batch], info.partial_rows, 0).total;
+  return VMLA_OK;
+}
+
+int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
+                           const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
+                           int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream) {
+  if (!kv_indptr_host) return VMLA_ERR_NULL;
+  if (batch < 0 || batch > VMLA_MAX_BATCH || src_slots < 0 || src_slots > INT32_MAX || dst_slots < 0 ||
+      dst_slots > INT32_MAX || kv_indptr_host[0] != 0)
+    return VMLA_ERR_SHAPE;
+  for (int b = 0; b < batch; ++b)
+    if (kv_indptr_host[b + 1] < kv_indptr_host[b]) return VMLA_ERR_SHAPE;
+  const int64_t total_kv = batch > 0 ? kv_indptr_host[batch] : 0;
+  if (total_kv == 0) return VMLA_OK;
+  if (!src_pool || !dst_pool || !kv_indptr || !kv_indices || !run_base) return VMLA_ERR_NULL;
+  if (!aligned(src_pool, 16) || !aligned(dst_pool, 16) || !aligned(status_word, 4) || !aligned(run_base, 4))
+    return VMLA_ERR_ALIGN;
+  int sms = 0;
+  int rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  return launch_defrag(static_cast<const uint16_t*>(src_pool), src_slots, kv_indptr, kv_indices, batch, total_kv,
+                       static_cast<uint16_t*>(dst_pool), dst_slots, run_base, false, status_word, stream);
 }
 
 int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
@@ -198,7 +263,8 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
                          const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
                          int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  return run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, qo_indptr, draft_mask, parent,
+  return run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask,
+             parent,
              kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
              workspace_bytes, stream);
 }
@@ -411,6 +477,7 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
   a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
   a.total_kv = max_total_kv;  // the staged capacity; the planner's count is in status word 2
+  a.run_base = nullptr;
   a.status = status;
   rc = launch_gather_dplan(a, status + 2, stream);
   if (rc != VMLA_OK) return rc;

@@ -1,0 +1,122 @@
+// Persistent KV defragmentation.
+//
+// "The Build That Unlocked 3-6x Decode Speedup" names the compaction of
+// scattered page_size = 1 slots into contiguous runs as the plan's next phase
+// (section "The Context: A Custom Kernel for an Unsupported Architecture"), so
+// that the verify kernel streams a sequence's rows as plain tile loads.  The
+// per-call gather (vmla_gather.cu) does this into the workspace at every call;
+// this kernel does it once into the caller's pool: the rows of sequence b go
+// to slots run_base[b] .. run_base[b] + N_b - 1, and the slots after the run up
+// to a multiple of 128 are zeroed, because the verify kernel's last tile of a
+// run reads them (with no weight) and stale contents could hold non-finite
+// bf16 values.  verify_attn_mla_runs then reads the runs with no gather.
+//
+// One warp per row, as in the gather: lane l moves 16-byte granules l, l+32
+// and l+64 (< 72).  A source slot outside the pool records VMLA_ERR_INDEX and
+// writes a zero row; a run outside the destination records VMLA_ERR_INDEX
+// (with the sequence index) and is skipped.
+#include <cuda_runtime.h>
+
+#include "vmla_device.cuh"
+
+namespace vmla {
+namespace {
+
+constexpr int kDefragWarps = 8;
+constexpr int kRowU4 = kRowBytes / 16;  // 72
+constexpr int kRunAlign = 128;          // rows one tile of the tensor-core kernel covers
+
+__device__ __forceinline__ int64_t round_run(int64_t n) { return (n + kRunAlign - 1) / kRunAlign * kRunAlign; }
+
+__device__ __forceinline__ bool run_ok(const int32_t* kv_indptr, const int32_t* run_base, int b, int64_t slots) {
+  const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+  const int64_t base = run_base[b];
+  return n >= 0 && base >= 0 && base + n <= slots;
+}
+
+__global__ void __launch_bounds__(kDefragWarps * 32)
+defrag_kernel(const uint4* __restrict__ src, int64_t src_slots, const int32_t* __restrict__ kv_indptr,
+              const int32_t* __restrict__ kv_indices, int batch, int64_t total_kv, uint4* __restrict__ dst,
+              int64_t dst_slots, const int32_t* __restrict__ run_base, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kDefragWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kDefragWarps;
+  const int64_t items = total_kv + (int64_t)batch * kRunAlign;  // rows, then each run's tail candidates
+  for (int64_t it = warp0; it < items; it += nwarps) {
+    int b;
+    int64_t r;
+    bool zero;
+    if (it < total_kv) {
+      int lo = 0, hi = batch;  // sequence owning row it: last b with kv_indptr[b] <= it
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (kv_indptr[mid] <= it) lo = mid; else hi = mid;
+      }
+      b = lo;
+      r = it - kv_indptr[b];
+      zero = false;
+    } else {
+      b = (int)((it - total_kv) / kRunAlign);
+      const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+      r = n + (it - total_kv) % kRunAlign;
+      if (r >= round_run(n)) continue;  // warp-uniform
+      zero = true;
+    }
+    if (!run_ok(kv_indptr, run_base, b, dst_slots)) {
+      if (lane == 0 && r == 0 && !zero) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
+      continue;
+    }
+    const int64_t row = (int64_t)run_base[b] + r;
+    if (row >= dst_slots) continue;  // a tail past the pool: the tile loads read zeros there
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0;
+    if (!zero) {
+      const int32_t slot = kv_indices[it];
+      const bool ok = slot >= 0 && (int64_t)slot < src_slots;
+      if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)it);
+      if (ok) {
+        const uint4* s = src + (int64_t)slot * kRowU4;
+        v0 = s[lane];
+        v1 = s[lane + 32];
+        if (lane < kRowU4 - 64) v2 = s[lane + 64];
+      }
+    }
+    uint4* d = dst + row * kRowU4;
+    d[lane] = v0;
+    d[lane + 32] = v1;
+    if (lane < kRowU4 - 64) d[lane + 64] = v2;
+  }
+}
+
+// Runs read by verify_attn_mla_runs must lie in the pool.
+__global__ void run_check_kernel(const int32_t* __restrict__ kv_indptr, const int32_t* __restrict__ run_base,
+                                 int batch, int64_t slots, uint32_t* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch && !run_ok(kv_indptr, run_base, b, slots)) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
+}
+
+}  // namespace
+
+int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
+                  int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots, const int32_t* run_base,
+                  bool check_only, uint32_t* status, void* stream) {
+  if (batch == 0) return VMLA_OK;
+  if (check_only) {
+    run_check_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(kv_indptr, run_base, batch, dst_slots,
+                                                                           status);
+    return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return VMLA_ERR_CUDA;
+  const int64_t items = total_kv + (int64_t)batch * kRunAlign;
+  const int64_t need = (items + kDefragWarps - 1) / kDefragWarps;
+  const int64_t cap = (int64_t)sms * 8;
+  const int blocks = (int)(need < cap ? need : cap);
+  defrag_kernel<<<blocks, kDefragWarps * 32, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const uint4*>(src_pool), src_slots, kv_indptr, kv_indices, batch, total_kv,
+      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, status);
+  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+}
+
+}  // namespace vmla

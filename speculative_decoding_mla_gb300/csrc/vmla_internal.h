@@ -102,14 +102,19 @@ struct RunArgs {
   float* lse;
   float* part_o;
   float* part_lse;  // log2 domain
-  uint16_t* staged; // contiguous copy of the gathered KV rows, [total_kv, 576] (tensor-core kernel)
-  int64_t total_kv;
+  uint16_t* staged; // contiguous copy of the gathered KV rows, [total_kv, 576] (tensor-core kernel),
+                    // or the pool itself when the rows lie in runs
+  int64_t total_kv; // rows of `staged`
+  const int32_t* run_base;  // [batch] first pool slot of each sequence's run, or NULL (staged rows)
   uint32_t* status;
 };
 
 // One verify call on a caller-provided workspace (argument checks, plan, launches).
+// kv_indices NULL and run_base given: the rows of sequence b are the pool's
+// slots run_base[b] .. run_base[b] + N_b - 1 (tensor-core kernel only).
 int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
-               const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask, const int32_t* parent,
+               const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
+               const uint64_t* draft_mask, const int32_t* parent,
                const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
                float sm_scale, int splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
                void* stream);
@@ -146,6 +151,13 @@ int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* pa
                        uint16_t* out, float* lse, void* stream);
 int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,
                            const uint32_t* rows_dev, uint64_t* mask_out, uint32_t* status, void* stream);
+
+// Copies the rows of every sequence into its run of dst_pool and zeroes each
+// run's tail up to a multiple of 128 rows; with check_only, records
+// VMLA_ERR_INDEX for runs outside [0, dst_slots) without copying.
+int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
+                  int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots, const int32_t* run_base,
+                  bool check_only, uint32_t* status, void* stream);
 
 int launch_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft, const int32_t* target,
                        const int32_t* root, int batch, int total_q, int32_t* accept_len, int32_t* path,

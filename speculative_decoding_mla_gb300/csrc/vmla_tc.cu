@@ -233,6 +233,9 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
+    // first row of the sequence in the tensor map: its staged offset, or its pool run
+    // (a run outside the pool only reads the out-of-range fill; a check kernel reports it)
+    const int row0 = a.run_base ? a.run_base[ui.b] : sp.kv_off;
     const int loads = scorer ? ui.n_tiles : ui.n_tiles * kMsgsPerTile;
     for (int n = 0; n < loads; ++n) {
       const int s = it % nst;
@@ -244,11 +247,11 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
       const uint32_t bar = mapa(smem_u32(&sm.c.kfull[s]), leader);
       if (q == 0) mbar_arrive_expect_tx(&sm.c.kfull[s], pair_bytes);
       if (scorer) {
-        const int y = sp.kv_off + ui.k_lo + n * kTileKeys + kHalfKeys * (int)q;
+        const int y = row0 + ui.k_lo + n * kTileKeys + kHalfKeys * (int)q;
 #pragma unroll 1
         for (int c = 0; c < kChunks; ++c) tma_load_2d_pair(smem_u32(&sm.u.s.kv[s][c][0]), map, 64 * c, y, bar);
       } else {
-        const int y = sp.kv_off + ui.k_lo + n * kMsgKeys;
+        const int y = row0 + ui.k_lo + n * kMsgKeys;
 #pragma unroll 1
         for (int j = 0; j < kVChunksCta; ++j) {
           const int g = (j & 1) + 2 * (int)q + 4 * (j >> 1);

@@ -120,6 +120,42 @@ def test_device_plan_argument_errors_before_any_launch(B):
             B.VMLA_ERR_DEVICE
 
 
+def test_defrag_and_runs_argument_errors_before_any_launch(B):
+    fake = 1 << 20
+    L = B.lib()
+    kvh = np.array([0, 8], np.int32)
+    def defrag(**kw):
+        a = dict(src=fake, ss=16, kvp=fake, kvi=fake, kvh=kvh.ctypes.data, batch=1, dst=fake, ds=64, base=fake,
+                 st=None, stream=None)
+        a.update(kw)
+        return L.verify_attn_mla_defrag(*a.values())
+    assert defrag(kvh=None) == B.VMLA_ERR_NULL
+    assert defrag(batch=-1) == B.VMLA_ERR_SHAPE
+    assert defrag(ds=-1) == B.VMLA_ERR_SHAPE
+    assert defrag(kvh=np.array([0, -3], np.int32).ctypes.data) == B.VMLA_ERR_SHAPE
+    assert defrag(kvh=np.array([2, 8], np.int32).ctypes.data) == B.VMLA_ERR_SHAPE
+    assert defrag(dst=None) == B.VMLA_ERR_NULL
+    assert defrag(base=None) == B.VMLA_ERR_NULL
+    assert defrag(src=fake + 4) == B.VMLA_ERR_ALIGN
+    assert defrag(kvh=np.array([0, 0], np.int32).ctypes.data) == B.VMLA_OK  # nothing to copy
+    qoh = np.array([0, 2], np.int32)
+    def runs(**kw):
+        a = dict(q=fake, kv=fake, S=16, kvp=fake, base=fake, qop=fake, dm=None, par=None, kvh=kvh.ctypes.data,
+                 qoh=qoh.ctypes.data, batch=1, H=4, scale=0.1, splits=0, out=fake, lse=fake, ws=fake * 2,
+                 wsb=1 << 20, stream=None)
+        a.update(kw)
+        return L.verify_attn_mla_runs(*a.values())
+    assert runs(base=None) == B.VMLA_ERR_NULL
+    assert runs(kvp=None) == B.VMLA_ERR_NULL
+    assert runs(H=0) == B.VMLA_ERR_SHAPE
+    assert runs(scale=0.0) == B.VMLA_ERR_SHAPE
+    assert runs(base=fake + 2) == B.VMLA_ERR_ALIGN
+    import torch
+    if not torch.cuda.is_available():
+        assert defrag() == B.VMLA_ERR_DEVICE
+        assert runs() == B.VMLA_ERR_DEVICE
+
+
 def test_tree_accept_argument_errors_before_any_launch(B):
     fake = 1 << 20
     L = B.lib()
