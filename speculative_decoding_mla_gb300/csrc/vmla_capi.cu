@@ -92,9 +92,9 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   vmla_plan_info info;
   rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan, &info);
   if (rc != VMLA_OK) return rc;
-  if (workspace_bytes < info.workspace_bytes) return VMLA_ERR_WORKSPACE;
   const WorkspaceLayout L =
       workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC && !runs ? total_kv : 0);
+  if (workspace_bytes < L.total) return VMLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
   cudaStream_t st = (cudaStream_t)stream;
