@@ -5,8 +5,9 @@
 //   lse = log sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s,
 // the combination of partial softmaxes that the NSPLIT split-KV of "The Build
 // Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel",
-// implies.  One warp per row, four pieces' loads in flight per lane; pieces
-// with lse = -inf carry no weight (their partial rows are zero).
+// implies.  One block per row, each of its four warps a quarter of the
+// columns with eight pieces' loads in flight per lane; pieces with
+// lse = -inf carry no weight (their partial rows are not read).
 //
 // Tree masks: the q x q visibility matrix of "The Build That Bridged Design
 // and Deployment", section "What This Build Achieves: The paged+bf16 Kernel",
@@ -19,14 +20,15 @@
 namespace vmla {
 namespace {
 
-constexpr int kMergeWarps = 4;
-constexpr int kMergeBatch = 4;  // pieces loaded together
+constexpr int kMergeWarps = 4;  // one per quarter of a 512-column row
+constexpr int kMergeBatch = 8;  // pieces loaded together
 
 __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
                                            const float* __restrict__ part_lse, int lse_is_log2,
                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mrow = blockIdx.x * kMergeWarps + warp;
+  // block = one merge row; warp c = its columns 4 * (32 c + lane) .. + 3
+  const int c = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mrow = blockIdx.x;
   if (mrow >= plan.merge_rows) return;
   // sequence owning merge row mrow: last b with merge_off <= mrow
   int lo = 0, hi = plan.batch;
@@ -46,21 +48,18 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
   if (lane + 32 < S) l1 = part_lse[(int64_t)sp.part_off + (int64_t)(lane + 32) * R + r] * to2;
   const float M = warp_max(fmaxf(l0, l1));
   const int64_t orow = (int64_t)sp.q_off * H + r;
-  uint2* dst = reinterpret_cast<uint2*>(out + orow * kDv);
+  uint2* dst = reinterpret_cast<uint2*>(out + orow * kDv) + c * 32 + lane;
   if (M == -INFINITY) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) dst[c * 32 + lane] = make_uint2(0u, 0u);
-    if (lane == 0) lse[orow] = -INFINITY;
+    *dst = make_uint2(0u, 0u);
+    if (c == 0 && lane == 0) lse[orow] = -INFINITY;
     return;
   }
   const float w0 = exp2f(l0 - M), w1 = exp2f(l1 - M);
   const float W = warp_sum(w0 + w1);
   const float invW = 1.f / W;
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
-    float4 v[kMergeBatch][4];
+    float4 v[kMergeBatch];
     float ws[kMergeBatch];
 #pragma unroll
     for (int b = 0; b < kMergeBatch; ++b) {
@@ -72,24 +71,18 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
       const bool use = ws[b] != 0.f;  // warp-uniform
       const float4* src =
           reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + (int64_t)(use ? s : 0) * R + r) * kDv);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) v[b][c] = use ? __ldg(src + c * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[b] = use ? __ldg(src + c * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int b = 0; b < kMergeBatch; ++b)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[4 * c + 0] = fmaf(ws[b], v[b][c].x, acc[4 * c + 0]);
-        acc[4 * c + 1] = fmaf(ws[b], v[b][c].y, acc[4 * c + 1]);
-        acc[4 * c + 2] = fmaf(ws[b], v[b][c].z, acc[4 * c + 2]);
-        acc[4 * c + 3] = fmaf(ws[b], v[b][c].w, acc[4 * c + 3]);
-      }
+    for (int b = 0; b < kMergeBatch; ++b) {
+      acc.x = fmaf(ws[b], v[b].x, acc.x);
+      acc.y = fmaf(ws[b], v[b].y, acc.y);
+      acc.z = fmaf(ws[b], v[b].z, acc.z);
+      acc.w = fmaf(ws[b], v[b].w, acc.w);
+    }
   }
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    dst[c * 32 + lane] = make_uint2(pack_bf16x2(acc[4 * c] * invW, acc[4 * c + 1] * invW),
-                                    pack_bf16x2(acc[4 * c + 2] * invW, acc[4 * c + 3] * invW));
-  if (lane == 0) lse[orow] = (M + log2f(W)) * 0.6931471805599453f;
+  *dst = make_uint2(pack_bf16x2(acc.x * invW, acc.y * invW), pack_bf16x2(acc.z * invW, acc.w * invW));
+  if (c == 0 && lane == 0) lse[orow] = (M + log2f(W)) * 0.6931471805599453f;
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -145,8 +138,7 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32
 int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
                  uint16_t* out, float* lse, void* stream) {
   if (plan.merge_rows == 0) return VMLA_OK;
-  const int blocks = (plan.merge_rows + kMergeWarps - 1) / kMergeWarps;
-  merge_kernel<<<blocks, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, lse_is_log2, out,
+  merge_kernel<<<plan.merge_rows, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, lse_is_log2, out,
                                                                        lse);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
@@ -162,9 +154,8 @@ int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch,
 int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* part_o, const float* part_lse,
                        uint16_t* out, float* lse, void* stream) {
   if (max_rows <= 0) return VMLA_OK;
-  const int64_t blocks = (max_rows + kMergeWarps - 1) / kMergeWarps;
-  if (blocks > INT32_MAX) return VMLA_ERR_SHAPE;
-  merge_kernel_dplan<<<(int)blocks, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, out, lse);
+  if (max_rows > INT32_MAX) return VMLA_ERR_SHAPE;
+  merge_kernel_dplan<<<(int)max_rows, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, out, lse);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 
