@@ -197,6 +197,16 @@ int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots,
 int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
                                         const int32_t* kv_indptr_host, int splits, size_t* bytes);
 
+/* Failure test only.  For the calling thread's later calls of the tensor-core
+ * entry points: fault 1 makes the kernel's softmax warps withhold the signal
+ * that Q is in place, so no score MMA starts, a bounded wait expires, the
+ * kernel records VMLA_ERR_TIMEOUT in the status word, stops every CTA of the
+ * cluster and returns (no trap, no hang; the context stays usable); fault 0
+ * restores normal operation.  wait_cycles sets the budget of every bounded
+ * wait in clock cycles (0 = about a second).  Returns VMLA_ERR_SHAPE for other
+ * values. */
+int verify_attn_mla_test_fault(int fault, int64_t wait_cycles);
+
 /* Greedy acceptance of the verified draft tree, the step after the verify
  * attention.  "The Build That Unlocked 3-6x Decode Speedup" lists a
  * tree_accept kernel (section "The Context: A Custom Kernel for an

@@ -39,7 +39,7 @@ EXPORTS = (
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
     "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
     "verify_attn_mla_tree_accept", "verify_attn_mla_defrag", "verify_attn_mla_runs",
-    "verify_attn_mla_runs_workspace_size",
+    "verify_attn_mla_runs_workspace_size", "verify_attn_mla_test_fault",
 )
 
 
@@ -82,6 +82,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_defrag": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, vp],
         "verify_attn_mla_runs": run,
         "verify_attn_mla_runs_workspace_size": [i32, i32, vp, vp, i32, ctypes.POINTER(sz)],
+        "verify_attn_mla_test_fault": [i32, i64],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -217,6 +218,11 @@ def verify_attn_mla_runs(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_h
     """Tensor-core verify attention on rows that lie in per-sequence runs of the pool (no gather)."""
     _run(_lib.verify_attn_mla_runs, "verify_attn_mla_runs", q, kv_pool, kv_indptr, run_base, qo_indptr,
          kv_indptr_host, qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+
+
+def verify_attn_mla_test_fault(fault: int, wait_cycles: int = 0):
+    """Failure test only: fault 1 makes the next tensor-core calls on this thread time out; 0 restores."""
+    _check(_lib.verify_attn_mla_test_fault(int(fault), int(wait_cycles)), "verify_attn_mla_test_fault")
 
 
 def verify_attn_mla_tree_accept(qo_indptr, parent, draft_token, target_token, root_token, accept_len, accept_path,

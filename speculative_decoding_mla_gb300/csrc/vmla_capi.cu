@@ -57,7 +57,18 @@ int current_sm_count(int* sms, bool require_sm103) {
 
 }  // namespace
 
+namespace {
+// failure-test settings of this thread (verify_attn_mla_test_fault)
+thread_local int32_t g_test_fault = 0;
+thread_local long long g_test_wait_cycles = 0;
+}  // namespace
+
 namespace vmla {
+
+void test_fault_settings(int32_t* fault, long long* wait_cycles) {
+  *fault = g_test_fault;
+  *wait_cycles = g_test_wait_cycles > 0 ? g_test_wait_cycles : kWaitCyclesDefault;
+}
 
 int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
         const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
@@ -109,6 +120,7 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
     masks = m;
   }
   RunArgs a;
+  test_fault_settings(&a.test_fault, &a.wait_cycles);
   a.q = static_cast<const uint16_t*>(q);
   a.kv = static_cast<const uint16_t*>(kv_pool);
   a.pool_slots = pool_slots;
@@ -464,6 +476,7 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
     masks = m;
   }
   RunArgs a;
+  test_fault_settings(&a.test_fault, &a.wait_cycles);
   a.q = static_cast<const uint16_t*>(q);
   a.kv = static_cast<const uint16_t*>(kv_pool);
   a.pool_slots = pool_slots;
@@ -503,6 +516,13 @@ int verify_attn_mla_tree_accept(const int32_t* qo_indptr, const int32_t* parent,
   if (rc != VMLA_OK) return rc;
   return launch_tree_accept(qo_indptr, parent, draft_token, target_token, root_token, batch, total_q, accept_len,
                             accept_path, next_token, status_word, stream);
+}
+
+int verify_attn_mla_test_fault(int fault, int64_t wait_cycles) {
+  if ((fault != 0 && fault != kFaultNoQReady) || wait_cycles < 0) return VMLA_ERR_SHAPE;
+  g_test_fault = fault;
+  g_test_wait_cycles = wait_cycles;
+  return VMLA_OK;
 }
 
 int verify_attn_mla_timing_enable(int capacity) {

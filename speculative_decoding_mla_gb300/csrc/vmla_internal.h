@@ -89,6 +89,14 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows);
 
+// Bounded waits of the tensor-core kernel: about a second at 2 GHz, or the
+// failure test's budget.
+constexpr long long kWaitCyclesDefault = 2000000000LL;
+// Failure test: the softmax warps never report Q ready, so a bounded wait expires.
+constexpr int32_t kFaultNoQReady = 1;
+// Failure-test settings for the calls that follow on this thread (verify_attn_mla_test_fault).
+void test_fault_settings(int32_t* fault, long long* wait_cycles);
+
 // Device-side entry points implemented in the .cu files (launch only; no sync).
 struct RunArgs {
   const uint16_t* q;
@@ -106,6 +114,8 @@ struct RunArgs {
                     // or the pool itself when the rows lie in runs
   int64_t total_kv; // rows of `staged`
   const int32_t* run_base;  // [batch] first pool slot of each sequence's run, or NULL (staged rows)
+  long long wait_cycles;    // budget of every bounded wait in the tensor-core kernel (clock64 cycles)
+  int32_t test_fault;       // 0; kFaultNoQReady only in the failure test
   uint32_t* status;
 };
 

@@ -68,7 +68,6 @@ static_assert(kPartKeys == 16 || kPartKeys == 32, "TMEM load width per softmax t
 constexpr int kClusterCtas = 4;
 constexpr uint32_t kSCol = 256;        // S buffers at TMEM columns 256 and 384
 constexpr float kTau = 8.0f;           // the running max is raised only when a tile exceeds it by 2^8
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr uint16_t kScorerMask = 0x3, kMixerMask = 0xC;
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
@@ -140,6 +139,7 @@ struct Ctl {
   uint32_t cmd;
   uint32_t tmem_base;
   volatile int32_t abort_flag;
+  long long wait_cycles;        // budget of every bounded wait (clock64 cycles)
   uint32_t warp_flags[kStages][kSoftWarps];  // per staging buffer: softmax warp w saw some alpha != 1
   uint32_t peer_flags[kPSlots];  // rank 2: flags of rank 3's half of message slot s
   volatile uint32_t wg_stop[4][2];  // scorer softmax warp pair (lane quarter): stop at this message (per parity)
@@ -192,7 +192,7 @@ __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity
   for (;;) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (sm.c.abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > sm.c.wait_cycles) {
       record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
       abort_cluster(sm);
       return false;
@@ -201,9 +201,9 @@ __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity
 }
 
 // Bounded wait that ignores the abort flag (draining in-flight work before exit).
-__device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ void drain_bar(TcSmem& sm, uint64_t* bar, uint32_t parity) {
   long long t0 = clock64();
-  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < kWaitCycles) {
+  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < sm.c.wait_cycles) {
   }
 }
 
@@ -263,11 +263,11 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   }
   // the even CTA drains its last loads (their barriers count both CTAs' bytes)
   if (q == 0)
-    for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(&sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1);
+    for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(sm, &sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1);
   // tail: the releases of the last stages arrive on this CTA's barriers from the
   // tensor core (a commit multicast to both CTAs of the pair); this CTA may not
   // exit while one is still in flight
-  for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(&sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1);
+  for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(sm, &sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1);
 }
 
 // ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
@@ -322,7 +322,7 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   // all issued MMAs complete before the CTA may exit (this arrive goes to rank 0
   // only: nothing in rank 1 waits for it)
   mma_commit_pair(&sm.c.obar, (uint16_t)0x1);
-  drain_bar(&sm.c.obar, 0);
+  drain_bar(sm, &sm.c.obar, 0);
 }
 
 // ------------------------------------------------------------------ ranks 0,1: softmax (warps 2 .. 2+kSoftWarps-1)
@@ -383,7 +383,9 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
+      // (the failure test withholds this signal: the score MMAs then never start and a
+      // bounded wait expires)
+      if (lane == 0 && a.test_fault != kFaultNoQReady) {
         if (rank == 0) mbar_arrive(&sm.c.qfull);
         else mbar_arrive_remote(qfull_r);
       }
@@ -651,7 +653,7 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     // regardless of the abort flag, so no arrival of this pair's earlier commits is
     // still travelling when the cluster leaves
     mma_commit_pair(&sm.c.obar, (uint16_t)0x4);
-    drain_bar(&sm.c.obar, obn & 1);
+    drain_bar(sm, &sm.c.obar, obn & 1);
   }
   post(kCmdExit);
 }
@@ -846,6 +848,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
     mbar_init(&sm.c.cmd_done, 2);
     mbar_init(&sm.c.obar, 1);
     sm.c.abort_flag = 0;
+    sm.c.wait_cycles = a.wait_cycles;
     fence_mbar_init();
     prefetch_tensormap(&kmap);
   }

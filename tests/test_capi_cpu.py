@@ -156,6 +156,14 @@ def test_defrag_and_runs_argument_errors_before_any_launch(B):
         assert runs() == B.VMLA_ERR_DEVICE
 
 
+def test_test_fault_hook_arguments(B):
+    L = B.lib()
+    assert L.verify_attn_mla_test_fault(2, 0) == B.VMLA_ERR_SHAPE
+    assert L.verify_attn_mla_test_fault(0, -1) == B.VMLA_ERR_SHAPE
+    assert L.verify_attn_mla_test_fault(1, 1000) == B.VMLA_OK
+    assert L.verify_attn_mla_test_fault(0, 0) == B.VMLA_OK
+
+
 def test_tree_accept_argument_errors_before_any_launch(B):
     fake = 1 << 20
     L = B.lib()

@@ -152,3 +152,23 @@ def test_small_workspace_is_rejected():
         binding.verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
                                 dc.qo_indptr_host, out, lse, ws, dc.sm_scale, splits=7)
     assert e.value.status == binding.VMLA_ERR_WORKSPACE
+
+
+def test_bounded_wait_expiry_reports_timeout_and_context_stays_usable():
+    """A signal that never comes (the test flag withholds Q-ready): the kernel's bounded wait
+    expires, the status word says VMLA_ERR_TIMEOUT, and the next call works normally."""
+    torch, binding, device = _mods()
+    case = small("one_seq", seed=320)
+    dc = device.to_device(case)
+    try:
+        binding.verify_attn_mla_test_fault(1, 20_000_000)  # ~10 ms per bounded wait
+        _, _, ws = device.run(dc, kernel="tc")
+        st = binding.verify_attn_mla_check(ws)  # the outputs of this call are not defined
+    finally:
+        binding.verify_attn_mla_test_fault(0, 0)
+    assert st == binding.VMLA_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.verify(case)
+    o, l, st = run_full(case, "tc")
+    assert st == 0
+    compare(o, l, ref_o, ref_l, "after the failure test")
