@@ -188,11 +188,13 @@ __device__ __noinline__ void abort_cluster(TcSmem& sm) {
 
 // Bounded wait; false on expiry or when the cluster is aborting.
 __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where) {
-  long long t0 = clock64();
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long budget = sm.c.wait_cycles;
+  const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (sm.c.abort_flag) return false;
-    if (clock64() - t0 > sm.c.wait_cycles) {
+    if (clock64() - t0 > budget) {
       record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
       abort_cluster(sm);
       return false;
@@ -202,8 +204,9 @@ __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity
 
 // Bounded wait that ignores the abort flag (draining in-flight work before exit).
 __device__ __noinline__ void drain_bar(TcSmem& sm, uint64_t* bar, uint32_t parity) {
-  long long t0 = clock64();
-  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < sm.c.wait_cycles) {
+  const long long budget = sm.c.wait_cycles;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < budget) {
   }
 }
 
