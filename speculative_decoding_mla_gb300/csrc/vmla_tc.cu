@@ -186,9 +186,9 @@ __device__ __noinline__ void abort_cluster(TcSmem& sm) {
     if (r != me) st_cluster_u32(mapa(local, r), 1u);
 }
 
-// Bounded wait; false on expiry or when the cluster is aborting.
-__device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+// Bounded wait after a first try failed; false on expiry or when the cluster is aborting.
+__device__ __noinline__ bool wait_bar_slow(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status,
+                                           int where) {
   const long long budget = sm.c.wait_cycles;
   const long long t0 = clock64();
   for (;;) {
@@ -200,6 +200,13 @@ __device__ __noinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+
+// Bounded wait; false on expiry or when the cluster is aborting.  The first try
+// is inline (it suspends the thread until the phase completes or the hardware's
+// time limit passes); the clocked loop is out of line.
+__device__ __forceinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where) {
+  return mbar_try_wait_cluster(bar, parity) || wait_bar_slow(sm, bar, parity, status, where);
 }
 
 // Bounded wait that ignores the abort flag (draining in-flight work before exit).
