@@ -90,9 +90,9 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 #define VTRACE(ev, tile) ((void)0)
 #endif
 
-// One P message covers half a tile (64 keys): the scorer's outbound copies
-// are the slow path of the pipeline, and two staging buffers of this size let
-// one copy drain while the next half is computed.
+// One P message covers half a tile (64 keys): two staging buffers of this
+// size let one copy drain while the next half is computed, and the mixer
+// starts its products as soon as each half has arrived.
 constexpr int kMsgKeys = 64;
 constexpr int kMsgsPerTile = kTileKeys / kMsgKeys;
 constexpr int kPSlots = 4;  // mixer receive slots
