@@ -16,6 +16,8 @@ Parity status of each function (what pins it is listed in the tests):
   merge                 pinned: closed forms, equals the unsplit result
   tree_masks            pinned: graph-library ancestor sets
   tree_accept           pinned: hand-worked trees, brute force over all root paths
+  e4m3_value /          pinned: torch's float8_e4m3fn for all 256 codes; RNE ties
+  dequantize_e4m3
 """
 from __future__ import annotations
 
@@ -212,3 +214,32 @@ def tree_accept(qo_indptr: np.ndarray, parent: Optional[np.ndarray], draft_token
         accept_path[q0:q0 + len(path)] = path
         next_token[b] = target_token[q0 + best]
     return accept_len, accept_path, next_token, bad
+
+
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    """Exact value of 8-bit e4m3 codes (OCP FP8 "E4M3": 1 sign, 4 exponent bits
+    with bias 7, 3 mantissa bits; exponent field 0 is subnormal, 2^-6 * m/8;
+    S.1111.111 is NaN; no infinities), as float64."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def _bf16_rne_bits(x32: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit pattern, round to nearest, ties to even (finite inputs)."""
+    b = np.asarray(x32, np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def dequantize_e4m3(codes: np.ndarray, scale: float) -> np.ndarray:
+    """An fp8 latent row's bf16 value: the code's value times the pool's scale,
+    rounded to float32 and then to bf16 (both round to nearest even), as bf16
+    bit patterns.  This is the reading used for fp8 KV storage: the pages do
+    not describe one."""
+    v32 = e4m3_value(codes).astype(np.float32) * np.float32(scale)
+    return _bf16_rne_bits(v32)

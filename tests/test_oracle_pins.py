@@ -421,3 +421,31 @@ def test_tree_accept_matches_brute_force_on_random_trees():
         assert not bad[0]
         assert n_acc[0] == len(path) and list(p_acc[:len(path)]) == path and nxt_acc[0] == nxt
         assert (p_acc[len(path):] == -1).all()
+
+
+# ---------------------------------------------------------------- fp8 (e4m3) storage
+
+def test_e4m3_values_match_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_value(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert oracle.e4m3_value(np.array([0x7E], np.uint8))[0] == 448.0
+    assert oracle.e4m3_value(np.array([0x01], np.uint8))[0] == 2.0 ** -9
+
+
+def test_dequantize_e4m3_rounds_to_nearest_even():
+    rng = np.random.default_rng(4)
+    codes = rng.integers(0, 256, 4096).astype(np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    for scale in (1.0, 0.0037, 1.0 / 3.0, 2.0 ** -5):
+        bits = oracle.dequantize_e4m3(codes, scale)
+        # the product in float32, then float32 -> bf16 by torch (round to nearest even)
+        prod = torch.from_numpy(oracle.e4m3_value(codes).astype(np.float32)) * torch.tensor(scale, dtype=torch.float32)
+        ref = prod.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(bits, ref)
+    # a tie: 1 + 2^-8 is halfway between two bf16 values and goes to the even one (1.0)
+    tie = np.array([1.0 + 2.0 ** -8], np.float32)
+    assert oracle._bf16_rne_bits(tie)[0] == 0x3F80
