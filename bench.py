@@ -357,6 +357,7 @@ def run_ours(args, rank, local, world):
     graph = device_plan_graph(args, case, dc, stream, flush_buf, tokens)
     accept = tree_accept_timing()
     runs = defragmented_runs(args, case, dc, flush_buf, tokens)
+    fp8 = fp8_pool_timing(args, case, dc, flush_buf, tokens)
 
     peaks = load_peaks()
     v_ms = float(verify_ms.mean())
@@ -398,6 +399,7 @@ def run_ours(args, rank, local, world):
             "device_plan_graph": graph,
             "tree_accept": accept,
             "defragmented": runs,
+            "fp8_kv": fp8,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -452,6 +454,45 @@ def defragmented_runs(args, case, dc, flush_buf, tokens):
     return {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "KV tokens/s", "defrag_ms_once": defrag_ms,
             "note": "rows compacted once into 128-aligned pool runs (verify_attn_mla_defrag), then "
                     "verify_attn_mla_runs each step: no per-call gather; events around each call"}
+
+
+def fp8_pool_timing(args, case, dc, flush_buf, tokens):
+    """The same workload with the latent pool stored as e4m3 codes and one scale (verify_attn_mla_fp8)."""
+    import torch
+    from speculative_decoding_mla_gb300 import binding
+    vals = dc.kv_pool.float()
+    scale = float(vals.abs().max()) / 400.0
+    pool8 = (vals / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    del vals
+    out = torch.empty((dc.total_q, dc.num_heads, 512), dtype=torch.bfloat16, device=dc.q.device)
+    lse = torch.empty((dc.total_q, dc.num_heads), dtype=torch.float32, device=dc.q.device)
+    ws = torch.empty(binding.verify_attn_mla_workspace_size(dc.qo_indptr_host, dc.kv_indptr_host, dc.num_heads,
+                                                            args.splits), dtype=torch.uint8, device=dc.q.device)
+
+    def call():
+        binding.verify_attn_mla_fp8(dc.q, pool8, scale, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
+                                    dc.qo_indptr_host, out, lse, ws, dc.sm_scale, parent=dc.parent, splits=args.splits)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        times.append((a, b))
+    torch.cuda.synchronize()
+    status = binding.verify_attn_mla_check(ws)
+    if status != 0:
+        raise RuntimeError(f"fp8 pool: {binding.status_string(status)}")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    return {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "KV tokens/s", "pool_bytes_per_key": 576,
+            "note": "latent pool as e4m3 codes with one scale; the gather dequantizes into the bf16 staged rows; "
+                    "events around each call"}
 
 
 def tree_accept_timing(batch=32, nodes=64, calls=200):

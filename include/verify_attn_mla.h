@@ -237,6 +237,22 @@ int verify_attn_mla_tree_accept(const int32_t* qo_indptr, const int32_t* parent,
                                 int32_t* accept_len, int32_t* accept_path, int32_t* next_token, uint32_t* status_word,
                                 void* stream);
 
+/* verify_attn_mla on an fp8 latent pool: kv_pool_e4m3 [pool_slots, 576]
+ * bytes, each an OCP FP8 E4M3 code (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; codes S.1111.111 are NaN and must not occur), with one scale
+ * for the pool: the value of a code is its e4m3 value times kv_scale, rounded
+ * to float32 and then to bf16 (nearest even).  The pages do not describe an
+ * fp8 cache; this is the plainest storage reading.  The gather dequantizes the
+ * rows it copies into the workspace (the pool read is 576 B per key instead of
+ * 1152), and everything after it is verify_attn_mla on those bf16 rows, so the
+ * result equals verify_attn_mla on the dequantized pool bit for bit.
+ * kv_scale: finite and > 0.  Workspace: verify_attn_mla_workspace_size(). */
+int verify_attn_mla_fp8(const void* q, const void* kv_pool_e4m3, int64_t pool_slots, float kv_scale,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* qo_indptr,
+                        const uint64_t* draft_mask, const int32_t* parent, const int32_t* kv_indptr_host,
+                        const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Fixed size of the scratch array behind verify_attn_mla_simt_static (32 MiB). */
 #define VMLA_STATIC_SCRATCH_BYTES (32u << 20)
 

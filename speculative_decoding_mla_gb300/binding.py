@@ -39,7 +39,7 @@ EXPORTS = (
     "verify_attn_mla_version", "verify_attn_mla_timing_enable", "verify_attn_mla_timing_read",
     "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
     "verify_attn_mla_tree_accept", "verify_attn_mla_defrag", "verify_attn_mla_runs",
-    "verify_attn_mla_runs_workspace_size", "verify_attn_mla_test_fault",
+    "verify_attn_mla_runs_workspace_size", "verify_attn_mla_test_fault", "verify_attn_mla_fp8",
 )
 
 
@@ -83,6 +83,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_runs": run,
         "verify_attn_mla_runs_workspace_size": [i32, i32, vp, vp, i32, ctypes.POINTER(sz)],
         "verify_attn_mla_test_fault": [i32, i64],
+        "verify_attn_mla_fp8": [vp, vp, i64, f32, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -218,6 +219,19 @@ def verify_attn_mla_runs(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_h
     """Tensor-core verify attention on rows that lie in per-sequence runs of the pool (no gather)."""
     _run(_lib.verify_attn_mla_runs, "verify_attn_mla_runs", q, kv_pool, kv_indptr, run_base, qo_indptr,
          kv_indptr_host, qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+
+
+def verify_attn_mla_fp8(q, kv_pool_e4m3, kv_scale, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host,
+                        out, lse, workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    """verify_attn_mla on an e4m3 latent pool ([S, 576] uint8 codes) with one scale."""
+    kvh = _host_i32(kv_indptr_host)
+    qoh = _host_i32(qo_indptr_host)
+    rc = _lib.verify_attn_mla_fp8(_ptr(q), _ptr(kv_pool_e4m3), int(kv_pool_e4m3.shape[0]), float(kv_scale),
+                                  _ptr(kv_indptr), _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent),
+                                  kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, int(q.shape[1]), float(sm_scale),
+                                  int(splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "verify_attn_mla_fp8")
 
 
 def verify_attn_mla_test_fault(fault: int, wait_cycles: int = 0):

@@ -70,8 +70,8 @@ void test_fault_settings(int32_t* fault, long long* wait_cycles) {
   *wait_cycles = g_test_wait_cycles > 0 ? g_test_wait_cycles : kWaitCyclesDefault;
 }
 
-int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
-        const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, float kv_scale,
+        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
         const int32_t* parent,
         const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
         int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
@@ -84,6 +84,9 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   if (!workspace) return VMLA_ERR_NULL;
   const bool runs = run_base != nullptr;  // rows in per-sequence pool runs: no gather
   if (runs && kernel != VMLA_KERNEL_TC) return VMLA_ERR_SHAPE;
+  // an e4m3 pool (kv_scale > 0, finite) is dequantized by the gather of the tensor-core path
+  if (kv_scale != 0.f && (!(kv_scale > 0.f) || !(kv_scale < INFINITY) || runs || kernel != VMLA_KERNEL_TC))
+    return VMLA_ERR_SHAPE;
   if (total_q > 0 && (!q || !kv_pool || !kv_indptr || (!runs && !kv_indices) || !qo_indptr || !out || !lse))
     return VMLA_ERR_NULL;
   if (!aligned(run_base, 4)) return VMLA_ERR_ALIGN;
@@ -136,6 +139,7 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
                   : reinterpret_cast<uint16_t*>(ws + L.staged_off);
   a.total_kv = runs ? pool_slots : total_kv;
   a.run_base = run_base;
+  a.kv_scale = kv_scale;
   a.status = status;
   int slot = -1;
   {
@@ -213,9 +217,20 @@ int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, cons
                     const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch,
                     int num_heads, float sm_scale, int splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask,
-             parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
-             workspace_bytes, stream);
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, 0.f, kv_indptr, kv_indices, nullptr, qo_indptr,
+             draft_mask, parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse,
+             workspace, workspace_bytes, stream);
+}
+
+int verify_attn_mla_fp8(const void* q, const void* kv_pool_e4m3, int64_t pool_slots, float kv_scale,
+                        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* qo_indptr,
+                        const uint64_t* draft_mask, const int32_t* parent, const int32_t* kv_indptr_host,
+                        const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!(kv_scale > 0.f) || !(kv_scale < INFINITY)) return VMLA_ERR_SHAPE;
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool_e4m3, pool_slots, kv_scale, kv_indptr, kv_indices, nullptr, qo_indptr,
+                    draft_mask, parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse,
+                    workspace, workspace_bytes, stream);
 }
 
 int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
@@ -225,7 +240,7 @@ int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots,
                          void* workspace, size_t workspace_bytes, void* stream) {
   if (batch > 0 && !run_base) return VMLA_ERR_NULL;
   static const int32_t kNone = 0;  // any non-null pointer selects the runs mode when batch is 0
-  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, kv_indptr, nullptr, run_base ? run_base : &kNone,
+  return run_verify(VMLA_KERNEL_TC, q, kv_pool, pool_slots, 0.f, kv_indptr, nullptr, run_base ? run_base : &kNone,
                     qo_indptr, draft_mask, parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits,
                     out, lse, workspace, workspace_bytes, stream);
 }
@@ -275,7 +290,7 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
                          const int32_t* parent, const int32_t* kv_indptr_host, const int32_t* qo_indptr_host,
                          int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  return run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask,
+  return run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, 0.f, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask,
              parent,
              kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse, workspace,
              workspace_bytes, stream);
@@ -491,6 +506,7 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
   a.total_kv = max_total_kv;  // the staged capacity; the planner's count is in status word 2
   a.run_base = nullptr;
+  a.kv_scale = 0.f;
   a.status = status;
   rc = launch_gather_dplan(a, status + 2, stream);
   if (rc != VMLA_OK) return rc;

@@ -10,6 +10,7 @@
 // One warp per row: lane l moves 16-byte granules l, l+32 and l+64 (< 72), so
 // every warp instruction reads and writes 512 contiguous bytes.  A slot outside
 // [0, pool_slots) records VMLA_ERR_INDEX and stages a zero row.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "vmla_device.cuh"
@@ -67,6 +68,52 @@ gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int
   }
 }
 
+// Two e4m3 codes (low byte first) -> two bf16 (low half first): exact to
+// half precision, times the pool's scale in float32, rounded to bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes, float scale) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(two_codes));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  return pack_bf16x2(lo * scale, hi * scale);
+}
+
+// The same gather from a pool of e4m3 rows (576 bytes): lane l reads code
+// granules l and, for l < 4, l + 32 (16 codes each) and writes their 16 bf16
+// values as two granules of the staged row.
+__global__ void __launch_bounds__(kGatherWarps * 32)
+gather_rows_fp8_kernel(const uint4* __restrict__ pool, int64_t pool_slots, float scale,
+                       const int32_t* __restrict__ kv_indices, int64_t total_kv, uint4* __restrict__ staged,
+                       uint32_t* status) {
+  constexpr int kCodeU4 = kDqk / 16;  // 36 granules of 16 codes
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kGatherWarps;
+  for (int64_t j = warp0; j < total_kv; j += nwarps) {
+    const int32_t slot = kv_indices[j];
+    const bool ok = slot >= 0 && (int64_t)slot < pool_slots;
+    if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)j);
+    const uint4* src = pool + (int64_t)(ok ? slot : 0) * kCodeU4;
+    uint4* dst = staged + j * kRowU4;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int g = lane + 32 * pass;
+      if (g < kCodeU4) {
+        const uint4 c = ok ? ld_stream(src + g) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          o[2 * k] = e4m3x2_to_bf16x2(w[k] & 0xFFFFu, scale);
+          o[2 * k + 1] = e4m3x2_to_bf16x2(w[k] >> 16, scale);
+        }
+        dst[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -79,6 +126,13 @@ int launch_gather_impl(const RunArgs& a, const uint32_t* rows_dev, void* stream)
   const int64_t need = (a.total_kv + kGatherWarps - 1) / kGatherWarps;
   const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM keep enough rows in flight
   const int blocks = (int)(need < cap ? need : cap);
+  if (a.kv_scale > 0.f) {
+    if (rows_dev) return VMLA_ERR_SHAPE;  // e4m3 pools are read by host-planned calls only
+    gather_rows_fp8_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_scale, a.kv_indices, a.total_kv,
+        reinterpret_cast<uint4*>(a.staged), a.status);
+    return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  }
   gather_rows_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
       reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_indices, a.total_kv, rows_dev,
       reinterpret_cast<uint4*>(a.staged), a.status);

@@ -115,6 +115,7 @@ struct RunArgs {
   int64_t total_kv; // rows of `staged`
   const int32_t* run_base;  // [batch] first pool slot of each sequence's run, or NULL (staged rows)
   long long wait_cycles;    // budget of every bounded wait in the tensor-core kernel (clock64 cycles)
+  float kv_scale;           // 0: kv is bf16 [S, 576]; > 0: kv is e4m3 [S, 576] bytes, value = code * kv_scale
   int32_t test_fault;       // 0; kFaultNoQReady only in the failure test
   uint32_t* status;
 };
@@ -122,8 +123,9 @@ struct RunArgs {
 // One verify call on a caller-provided workspace (argument checks, plan, launches).
 // kv_indices NULL and run_base given: the rows of sequence b are the pool's
 // slots run_base[b] .. run_base[b] + N_b - 1 (tensor-core kernel only).
-int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
-               const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
+// kv_scale > 0: kv_pool holds e4m3 codes; the gather dequantizes them (tensor-core kernel only).
+int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, float kv_scale,
+               const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
                const uint64_t* draft_mask, const int32_t* parent,
                const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
                float sm_scale, int splits, void* out, float* lse, void* workspace, size_t workspace_bytes,

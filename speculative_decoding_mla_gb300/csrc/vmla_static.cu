@@ -52,7 +52,7 @@ extern "C" int verify_attn_mla_simt_static(const void* q, const void* kv_pool, i
   int rc = vmla::static_scratch(&scratch);
   if (rc != VMLA_OK) return rc;
   // a plan that needs more than the array is refused (VMLA_ERR_WORKSPACE) before any launch
-  return vmla::run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr,
+  return vmla::run_verify(VMLA_KERNEL_SIMT, q, kv_pool, pool_slots, 0.f, kv_indptr, kv_indices, nullptr, qo_indptr,
                           draft_mask,
                           parent, kv_indptr_host, qo_indptr_host, batch, num_heads, sm_scale, splits, out, lse,
                           scratch, VMLA_STATIC_SCRATCH_BYTES, stream);

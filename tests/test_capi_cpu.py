@@ -156,6 +156,25 @@ def test_defrag_and_runs_argument_errors_before_any_launch(B):
         assert runs() == B.VMLA_ERR_DEVICE
 
 
+def test_fp8_argument_errors_before_any_launch(B):
+    fake = 1 << 20
+    L = B.lib()
+    kvh, qoh = np.array([0, 8], np.int32), np.array([0, 2], np.int32)
+    def call(scale=0.05, **kw):
+        a = dict(q=fake, kv=fake, S=16, scale=scale, kvp=fake, kvi=fake, qop=fake, dm=None, par=None,
+                 kvh=kvh.ctypes.data, qoh=qoh.ctypes.data, batch=1, H=4, sm=0.1, splits=0, out=fake, lse=fake,
+                 ws=fake * 2, wsb=1 << 20, stream=None)
+        a.update(kw)
+        return L.verify_attn_mla_fp8(*a.values())
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert call(scale=bad) == B.VMLA_ERR_SHAPE
+    assert call(kvi=None) == B.VMLA_ERR_NULL
+    assert call(q=fake + 2) == B.VMLA_ERR_ALIGN
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == B.VMLA_ERR_DEVICE
+
+
 def test_test_fault_hook_arguments(B):
     L = B.lib()
     assert L.verify_attn_mla_test_fault(2, 0) == B.VMLA_ERR_SHAPE
