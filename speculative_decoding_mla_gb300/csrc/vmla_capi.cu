@@ -71,10 +71,10 @@ void test_fault_settings(int32_t* fault, long long* wait_cycles) {
 }
 
 int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, float kv_scale,
-        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
-        const int32_t* parent,
-        const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale,
-        int splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+        const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
+        const uint64_t* draft_mask, const int32_t* parent, const int32_t* kv_indptr_host,
+        const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
+        void* workspace, size_t workspace_bytes, void* stream, void* q_ready) {
   int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
   if (rc != VMLA_OK) return rc;
   // a positive finite scale (the kernels take row maxima over unscaled scores)
@@ -160,6 +160,7 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
     if (rc != VMLA_OK) return rc;
     if (slot >= 0) cudaEventRecord(timing_event(slot, 5), st);
   }
+  if (q_ready && cudaStreamWaitEvent(st, (cudaEvent_t)q_ready, 0) != cudaSuccess) return VMLA_ERR_CUDA;
   if (slot >= 0) cudaEventRecord(timing_event(slot, 0), st);
   rc = kernel == VMLA_KERNEL_SIMT ? launch_simt(plan, a, stream) : launch_tc(plan, a, stream);
   if (rc != VMLA_OK) return rc;
@@ -340,6 +341,30 @@ int verify_attn_mla_check(const void* workspace, void* stream) {
   return (int)(int32_t)word[0];
 }
 
+namespace {
+// Side stream and events of the host-buffer entry point, one set per thread and device.
+struct HostSide {
+  cudaStream_t side = nullptr;
+  cudaEvent_t start = nullptr, q_done = nullptr;
+};
+int host_side(HostSide** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VMLA_ERR_DEVICE;
+  thread_local HostSide sides[64];
+  HostSide& h = sides[dev];
+  if (!h.side) {
+    if (cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h.q_done, cudaEventDisableTiming) != cudaSuccess) {
+      h = HostSide();
+      return VMLA_ERR_CUDA;
+    }
+  }
+  *out = &h;
+  return VMLA_OK;
+}
+}  // namespace
+
 int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,
                                      const int32_t* kv_indptr_host, int splits, int has_mask, int has_parent,
                                      size_t* bytes) {
@@ -397,20 +422,37 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   char* d_lse = p;           p += up(T * num_heads * 4);
   cudaStream_t st = (cudaStream_t)stream;
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  // q crosses on a side stream while the gather runs; only the kernels after the
+  // gather read q, and they wait for its copy
+  HostSide* hs = nullptr;
+  if (T > 0) {
+    rc = host_side(&hs);
+    if (rc != VMLA_OK) return rc;
+  }
   bool ok = true;
   ok = ok && cudaMemcpyAsync(d_kvp, kv_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(d_qop, qo_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
   if (T > 0) {
-    ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, st) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(d_kvi, kv_indices_host, N * 4, h2d, st) == cudaSuccess;
     if (d_mask) ok = ok && cudaMemcpyAsync(d_mask, draft_mask_host, T * 8, h2d, st) == cudaSuccess;
     if (d_par) ok = ok && cudaMemcpyAsync(d_par, parent_host, T * 4, h2d, st) == cudaSuccess;
   }
-  if (!ok) return VMLA_ERR_CUDA;
-  rc = verify_attn_mla(d_q, kv_pool, pool_slots, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
-                       (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
-                       qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream);
-  if (rc != VMLA_OK) return rc;
+  if (hs) {
+    // starts once the indices have crossed, so that it shares the link with no other copy
+    ok = ok && cudaEventRecord(hs->start, st) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(hs->side, hs->start, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, hs->side) == cudaSuccess;
+    ok = ok && cudaEventRecord(hs->q_done, hs->side) == cudaSuccess;
+  }
+  if (ok)
+    rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
+                    nullptr, (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
+                    qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream,
+                    hs ? (void*)hs->q_done : nullptr);
+  if (!ok || rc != VMLA_OK) {
+    if (hs) cudaStreamSynchronize(hs->side);  // the buffer is the caller's again when this returns
+    return ok ? rc : VMLA_ERR_CUDA;
+  }
   if (T > 0) {
     ok = ok && cudaMemcpyAsync(out_host, d_out, T * num_heads * VMLA_D_V * 2, d2h, st) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(lse_host, d_lse, T * num_heads * 4, d2h, st) == cudaSuccess;
