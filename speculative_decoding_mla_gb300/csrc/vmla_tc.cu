@@ -95,7 +95,7 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 // starts its products as soon as each half has arrived.
 constexpr int kMsgKeys = 64;
 constexpr int kMsgsPerTile = kTileKeys / kMsgKeys;
-constexpr int kPSlots = 4;  // mixer receive slots
+constexpr int kPSlots = 5;  // mixer receive slots
 constexpr int kStages = 2;  // scorer staging buffers (a copy drains while the next message is computed)
 struct __align__(1024) PMsg {
   uint8_t p[kRowsCta * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
