@@ -47,8 +47,8 @@ METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
 # DRAM bytes per verify launch from the committed ncu capture (profiles/tc_verify_long_120k_sections.md),
 # scaled to the workload by keys; valid only while the kernel and planner sources are the ones profiled.
 PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
-PROFILED_FINGERPRINT = "b2bb6933996ffe8e"
-PROFILED_TRAFFIC = {"long_185k": 251.6e6, "long_120k": 163.2e6}
+PROFILED_FINGERPRINT = "5c3902caa46e9cdf"
+PROFILED_TRAFFIC = {"long_185k": 241.4e6, "long_120k": 156.6e6}
 
 
 def traffic_per_launch(workload: str):

@@ -56,7 +56,8 @@ constexpr int kChunks = kDqk / 64;     // 9 column chunks of 64 bf16 (128 bytes)
 constexpr int kQChunks = kDv / 64;     // 8 latent chunks (Q latent lives in TMEM columns 0..255)
 constexpr int kVChunksCta = kDv / 128; // 4 value chunks per mixer CTA (half of the 8)
 constexpr int kKBox = kHalfKeys * 128; // 8 KB: 64 rows x 128 bytes
-constexpr int kVStages = 4;            // mixer V stages, one per 64-key message
+constexpr int kVStages = 3;            // mixer V stages, one per 64-key message
+static_assert(kVStages >= 2, "the scorer's two K stages use the first two stage barriers");
 constexpr int kRowsCta = 128;
 constexpr int kRowsUnit = 256;
 constexpr int kSoftWarps = 8;          // scorer softmax warps: two per TMEM lane quarter
@@ -95,7 +96,7 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
 // starts its products as soon as each half has arrived.
 constexpr int kMsgKeys = 64;
 constexpr int kMsgsPerTile = kTileKeys / kMsgKeys;
-constexpr int kPSlots = 5;  // mixer receive slots
+constexpr int kPSlots = 6;  // mixer receive slots (an even count measured faster than an odd one)
 constexpr int kStages = 2;  // scorer staging buffers (a copy drains while the next message is computed)
 struct __align__(1024) PMsg {
   uint8_t p[kRowsCta * 128];  // P [128 rows][64 keys] bf16, K-major, 128-byte swizzle
@@ -127,7 +128,7 @@ struct MixerSmem {
 };
 
 struct Ctl {
-  uint64_t kfull[kVStages], kfree[kVStages];  // K stages (scorer: 2) or V stages (mixer: 4)
+  uint64_t kfull[kVStages], kfree[kVStages];  // K stages (scorer: 2) or V stages (mixer: kVStages)
   uint64_t sfull[2], sfree[2];  // S buffers (scorer; sfree counts on rank 0)
   uint64_t sread[2];            // rank 1: its softmax warps have read S buffer s
   uint64_t staged[kStages], stgfree[kStages];  // scorer: P staging buffer written / free again
@@ -227,7 +228,7 @@ __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched
 // Scorer CTA q loads keys [64q, 64q + 64) of each 128-key tile, all nine
 // column chunks (64-row x 64-column boxes), into two tile stages; mixer CTA q
 // loads value chunks {2q, 2q+1, 2q+4, 2q+5} of each 64-key message (the N
-// halves the pair's P V MMAs expect) into four message stages.  Both CTAs of
+// halves the pair's P V MMAs expect) into kVStages message stages.  Both CTAs of
 // a pair complete their bytes on the even CTA's barrier, which that CTA arms
 // for the pair.  Rows past the piece's end belong to other keys (masked by the
 // softmax) or lie outside the staged rows (zero fill).
