@@ -47,17 +47,26 @@ METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
 # DRAM bytes per verify launch from the committed ncu capture (profiles/tc_verify_long_120k_sections.md),
 # scaled to the workload by keys; valid only while the kernel and planner sources are the ones profiled.
 PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
-PROFILED_FINGERPRINT = "5c3902caa46e9cdf"
+PROFILED_FINGERPRINT = "9076164ff3f00a32"
 PROFILED_TRAFFIC = {"long_185k": 241.4e6, "long_120k": 156.6e6}
 
 
-def traffic_per_launch(workload: str):
+def source_fingerprint(paths=None) -> str:
+    """First 16 hex digits of the sha256 of the profiled sources' code (or of `paths`): each line
+    cut at `//`, trailing blanks and empty lines dropped, so that comment edits keep the fingerprint."""
     import hashlib
     h = hashlib.sha256()
-    for rel in PROFILED_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest()[:16] != PROFILED_FINGERPRINT:
+    for rel in paths if paths is not None else PROFILED_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(workload: str):
+    if source_fingerprint() != PROFILED_FINGERPRINT:
         return None
     return PROFILED_TRAFFIC.get(workload)
 L2_BYTES = 129 * 1024 * 1024

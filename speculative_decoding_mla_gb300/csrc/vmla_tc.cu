@@ -9,7 +9,8 @@
 // sm_120 Kernel" of "The Build Script Edit"); here a tile serves 256 query
 // rows (heads x draft positions of one sequence) in one 2-SM MMA.  The KV rows
 // are read from the contiguous copy the gather kernel made of each sequence's
-// page_size = 1 slots.
+// page_size = 1 slots, or from each sequence's run of the pool after a
+// persistent defragmentation.
 //
 // A work unit is 256 query rows (r = i*H + h) of one sequence over one
 // contiguous piece of its key range, and runs on a cluster of four CTAs:

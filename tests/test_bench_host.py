@@ -59,3 +59,19 @@ def test_two_gloo_ranks_aggregate():
 
 def test_single_rank_is_identity():
     assert bench.reduce_max_sum(3.5, 7.0, 1) == (3.5, 7.0)
+
+
+def test_source_fingerprint_ignores_comments_only(tmp_path):
+    base = "int a = 1;  // one\n\n// a note\nint b = a + 1;\n"
+    comment_edit = "int a = 1;   // the first\n// another note\n\nint b = a + 1;\n"
+    code_edit = "int a = 2;  // one\n\n// a note\nint b = a + 1;\n"
+    paths = []
+    for name, text in (("base.cu", base), ("comment.cu", comment_edit), ("code.cu", code_edit)):
+        p = tmp_path / name
+        p.write_text(text)
+        paths.append(str(p))
+    fp = [bench.source_fingerprint([p]) for p in paths]
+    assert fp[0] == fp[1] and fp[0] != fp[2]
+    # the committed traffic figures apply exactly when the profiled code is unchanged
+    assert (bench.traffic_per_launch("long_185k") is not None) == (bench.source_fingerprint() ==
+                                                                   bench.PROFILED_FINGERPRINT)
