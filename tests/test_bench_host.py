@@ -75,3 +75,15 @@ def test_source_fingerprint_ignores_comments_only(tmp_path):
     # the committed traffic figures apply exactly when the profiled code is unchanged
     assert (bench.traffic_per_launch("long_185k") is not None) == (bench.source_fingerprint() ==
                                                                    bench.PROFILED_FINGERPRINT)
+
+
+def test_roofline_picks_the_bound_of_the_work():
+    peaks = {"bf16_tflops": 1912.5, "hbm_gbs": 6789.3, "source": "measured"}
+    # 185k-key prefix, 16 drafts, 64 heads: about 1900 flop per byte, above the ridge
+    r = bench.roofline_entry(412.24e9, 216.1e6, 0.3313, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 412.24e9 / 0.3313e-3 / 1e12) < 1e-9 and abs(r["frac"] - r["achieved"] / 1912.5) < 1e-12
+    # one draft per sequence: about 120 flop per byte, below the ridge, so the HBM copy rate bounds it
+    r = bench.roofline_entry(89.23e9, 745.1e6, 0.3359, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 745.1e6 / 0.3359e-3 / 1e9) < 1e-9 and abs(r["frac"] - r["achieved"] / 6789.3) < 1e-12
