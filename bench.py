@@ -1,16 +1,16 @@
 #!/usr/bin/env python
 """Benchmark of the MLA speculative-decoding verify attention on GB300.
 
-One step = one verify call (mask expansion when a tree is given, the verify
-kernel, the split merge) over one batch of seeded synthetic inputs resident in
-HBM.  Prints ONE JSON line (rank 0).
+One step = one verify call (mask expansion when a tree is given, the KV row
+gather, the verify kernel, the split merge) over one batch of seeded synthetic
+inputs resident in HBM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 Default workload: long_185k (1 sequence, 185,000-token prefix + 16 causal draft
 positions, 64 heads, 576-dim bf16 latent rows at page_size = 1 with permuted
-slots in a 200,000-slot pool), the shape the >= 60 % roofline target is stated
-on.  Every workload whose KV rows are under twice the 129 MB L2 (this one's
+slots in a 200,000-slot pool), the long-context shape of the pages' decode
+workload.  Every workload whose KV rows are under twice the 129 MB L2 (this one's
 are 213 MB) gets a 512 MB L2 flush before each step (outside the kernel
 events, inside the step); larger ones need none.
 
@@ -18,8 +18,10 @@ Metric: KV tokens per second (sum over sequences of N_b, per step), plus
 algorithmic TFLOP/s and HBM GB/s.  Algorithmic work per launch:
   bytes = sum_b [N_b * (1152 + 4) + Q_b * H * (1152 + 1024 + 4)]
   flops = 2 * H * (576 + 512) * V,   V = sum_b (Q_b * P_b + sum_i |mask_i|)
-Roofline: the verify kernel's achieved TFLOP/s (algorithmic flops / its mean
-event-timed duration) against the measured dense bf16 peak.
+Roofline: the verify kernel's achieved rate (algorithmic work / its mean
+event-timed duration) against the roof that bounds the work: TFLOP/s against the
+measured dense bf16 peak when the flops take longer there than the bytes at the
+measured HBM copy rate, GB/s against that copy rate otherwise.
 
 --impl reference times the CPU fp64 oracle on the host cores on a bounded
 sample of the same workload (a subset of query rows), scaled to the metric.
