@@ -62,7 +62,7 @@ typedef enum vmla_status {
   VMLA_ERR_WORKSPACE = -4, /* workspace smaller than verify_attn_mla_workspace_size() */
   VMLA_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed */
   VMLA_ERR_TIMEOUT = -6,   /* a kernel's bounded wait expired (kernel returned early) */
-  VMLA_ERR_INDEX = -7,     /* a kv slot index was outside [0, pool_slots) (key skipped) */
+  VMLA_ERR_INDEX = -7,     /* a kv slot index was outside [0, pool_slots) (its row reads as zeros) */
   VMLA_ERR_DEVICE = -8,    /* no usable sm_103 device for this library */
   VMLA_ERR_PARENT = -9     /* a parent index was not in [-1, i) (mask left empty) */
 } vmla_status;
@@ -215,7 +215,7 @@ int verify_attn_mla_test_fault(int fault, int64_t wait_cycles);
  * prefix for a root) and is accepted when its parent is accepted and the token
  * equals the target model's greedy token after the parent.  The chosen path
  * ends at the deepest accepted node (the smallest index among equally deep
- * ones).  All arrays are device arrays; one thread per sequence.
+ * ones).  All arrays are device arrays; one warp per sequence.
  *   qo_indptr    [batch+1] int32; Q_b = qo_indptr[b+1] - qo_indptr[b] <= 64 nodes
  *   parent       [T_q] int32 local parent (-1 = root, parent[i] < i), or NULL for
  *                the chain parent[i] = i - 1
@@ -335,8 +335,9 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
 
 /* Measurement aid.  verify_attn_mla_timing_enable(n) creates host-side CUDA
  * events for the next n run calls (0 turns it off and frees them); while it is
- * on, every verify_attn_mla / verify_attn_mla_simt call records events on its
- * stream around each kernel it launches.  verify_attn_mla_timing_read() waits
+ * on, every verify_attn_mla, _simt, _runs, _fp8 and _host call (not the
+ * device-planned form) records events on its stream around each kernel it
+ * launches.  verify_attn_mla_timing_read() waits
  * for those events and writes, per call in launch order, the device time in ms
  * of the KV gather kernel, the verify kernel and the merge kernel (0 for a
  * kernel the call did not launch) into arrays of `capacity` entries, sets
