@@ -264,3 +264,29 @@ def test_plan_rejects_bad_shapes(B):
         _plan(B, 0, [10], [65])
     with pytest.raises(B.VmlaError):
         B.verify_attn_mla_plan(0, np.array([0, 4], np.int32), np.array([0, 2], np.int32), 64)
+
+
+def test_plan_units_within_the_device_plan_bound(B):
+    """The device-planned call sizes its partial area for caller bounds before any length is known:
+    with C clusters (two units each) the automatic plan makes at most 2C units plus one per row
+    block, each of 256 rows, and never more than 64 pieces of every query row.  The host planner
+    runs the same split arithmetic; check that bound on random length sets."""
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        batch = int(rng.integers(1, 40))
+        H = int(rng.choice([8, 16, 64, 128]))
+        drafts = rng.integers(0, 65, batch)
+        prefixes = np.where(rng.random(batch) < 0.5, rng.integers(0, 3000, batch), rng.integers(0, 200000, batch))
+        clusters = int(rng.integers(1, 40))
+        info, per, qo, kv = _plan(B, 0, prefixes.tolist(), drafts.tolist(), H=H, sms=4 * clusters)
+        rows = int(qo[-1]) * H
+        row_blocks = -(-rows // 256) + batch
+        cap = min(256 * (2 * clusters + row_blocks), rows * 64)
+        assert info.num_units <= 2 * clusters + row_blocks
+        assert info.partial_rows <= cap
+    # forced piece counts: at most `splits` pieces of every row block
+    for splits in (1, 3, 17, 64):
+        info, per, qo, kv = _plan(B, 0, [5000, 100, 70000], [16, 3, 64], H=64, splits=splits, sms=144)
+        row_blocks = -(-int(qo[-1]) * 64 // 256) + 3
+        assert info.num_units <= splits * row_blocks
+        assert info.partial_rows <= min(256 * splits * row_blocks, int(qo[-1]) * 64 * 64)
