@@ -239,7 +239,12 @@ def cpu_oracle_sample(case, budget_s: float = 15.0, max_rows: int = 4096):
         done_keys += int(keys_per_row[rows].sum())
         if spent >= budget_s or done_rows >= min(total_rows, max_rows):
             break
-        n = int(min(total_rows - done_rows, max(len(rows), len(rows) * max(1.0, (budget_s - spent) / max(dt, 1e-3)))))
+        # next batch: most of the remaining budget at the last batch's rate, at most 4x that batch
+        # (small batches are dominated by thread start-up); stop when less than a batch of one row
+        # per core still fits
+        n = int(min(total_rows - done_rows, 4 * len(rows), 0.8 * (budget_s - spent) * len(rows) / max(dt, 1e-3)))
+        if n < cores:
+            break
     # whole-job time estimate: (all rows' keys) / (keys per second achieved on the sample)
     keys_per_s = done_keys / spent
     all_keys = int(keys_per_row.sum())
