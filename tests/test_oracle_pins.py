@@ -324,6 +324,16 @@ def test_sampled_rows_equal_full():
         assert np.array_equal(o[k], out[r // H, r % H]) and l[k] == lse[r // H, r % H]
 
 
+def test_thread_count_does_not_change_any_row():
+    """Rows are independent: every split of the rows over threads gives the same bits (a row skipped
+    or computed twice at a thread boundary would show here)."""
+    case = small_case(73, [37, 0, 12, 5], [7, 3, 1, 8], heads=5)
+    out1, lse1 = oracle.verify(case, threads=1)
+    for threads in (2, 3, 7, 64):
+        out, lse = oracle.verify(case, threads=threads)
+        assert np.array_equal(out, out1) and np.array_equal(lse, lse1)
+
+
 def test_rejects_bad_inputs():
     case = small_case(81, [3], 2, heads=1)
     bad = synth.Case(name="bad", q=case.q, kv_pool=case.kv_pool, kv_indptr=case.kv_indptr,
