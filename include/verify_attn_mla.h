@@ -320,8 +320,10 @@ int verify_attn_mla_check(const void* workspace, void* stream);
  * synchronises `stream` before returning (so the returned status includes the
  * device status word).  Host buffers should be pinned for asynchronous copies.
  * q crosses on a side stream after the indices, while the gather runs (the
- * kernels after the gather wait for it); the library keeps one such stream and
- * two events per calling thread and device, created at the first call.
+ * kernels after the gather wait for it); out, lse and the status words return
+ * by asynchronous copies on `stream` before its one synchronisation.  The
+ * library keeps one such side stream, two events and an 8-byte pinned status
+ * slot per calling thread and device, created at the first call.
  * device_buffer must hold verify_attn_mla_host_buffer_size() bytes (256 B
  * aligned). */
 int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,

@@ -342,10 +342,12 @@ int verify_attn_mla_check(const void* workspace, void* stream) {
 }
 
 namespace {
-// Side stream and events of the host-buffer entry point, one set per thread and device.
+// Side stream, events and a pinned status slot of the host-buffer entry point,
+// one set per thread and device.
 struct HostSide {
   cudaStream_t side = nullptr;
   cudaEvent_t start = nullptr, q_done = nullptr;
+  uint32_t* status = nullptr;  // pinned host copy of the workspace status words
 };
 int host_side(HostSide** out) {
   int dev = 0;
@@ -355,7 +357,8 @@ int host_side(HostSide** out) {
   if (!h.side) {
     if (cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h.q_done, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&h.q_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaMallocHost(reinterpret_cast<void**>(&h.status), 2 * sizeof(uint32_t)) != cudaSuccess) {
       h = HostSide();
       return VMLA_ERR_CUDA;
     }
@@ -453,12 +456,14 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     if (hs) cudaStreamSynchronize(hs->side);  // the buffer is the caller's again when this returns
     return ok ? rc : VMLA_ERR_CUDA;
   }
-  if (T > 0) {
-    ok = ok && cudaMemcpyAsync(out_host, d_out, T * num_heads * VMLA_D_V * 2, d2h, st) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(lse_host, d_lse, T * num_heads * 4, d2h, st) == cudaSuccess;
-  }
+  if (!hs) return verify_attn_mla_check(d_ws, stream);  // nothing to compute
+  // out, lse and the status words come back in stream order, then one synchronisation
+  ok = ok && cudaMemcpyAsync(out_host, d_out, T * num_heads * VMLA_D_V * 2, d2h, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(lse_host, d_lse, T * num_heads * 4, d2h, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(hs->status, d_ws, 2 * sizeof(uint32_t), d2h, st) == cudaSuccess;
+  ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
   if (!ok) return VMLA_ERR_CUDA;
-  return verify_attn_mla_check(d_ws, stream);
+  return (int)(int32_t)hs->status[0];
 }
 
 namespace {

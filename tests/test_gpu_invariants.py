@@ -123,6 +123,32 @@ def test_host_entry_point_matches_device_path():
     assert np.array_equal(o1, o2) and np.array_equal(l1, lse_h.numpy().astype(np.float64))
 
 
+def test_host_entry_point_reports_a_bad_slot():
+    """The host-buffer call returns the device status word (read back with its results): a slot
+    outside the pool gives VMLA_ERR_INDEX, and the next good call on the same buffers returns 0."""
+    torch, binding, device = _mods()
+    case = small("ragged", seed=308)
+    kv = device.to_device(case).kv_pool
+    T, H = case.q.shape[0], case.num_heads
+    q_h = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    out_h = torch.empty((T, H, 512), dtype=torch.int16).pin_memory()
+    lse_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    bad = case.kv_indices.copy()
+    bad[3] = case.pool_slots + 7
+    kvi_h = torch.from_numpy(bad).pin_memory()
+    n = binding.verify_attn_mla_host_buffer_size(case.qo_indptr, case.kv_indptr, H)
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.VmlaError) as err:
+        binding.verify_attn_mla_host(q_h, kv, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, buf,
+                                     case.sm_scale)
+    assert err.value.status == binding.VMLA_ERR_INDEX
+    kvi_h.copy_(torch.from_numpy(case.kv_indices))
+    binding.verify_attn_mla_host(q_h, kv, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, buf, case.sm_scale)
+    o1, l1, _ = run_full(case, "tc")
+    o2 = synth.bf16_bits_to_f64(out_h.numpy().view(np.uint16))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, lse_h.numpy().astype(np.float64))
+
+
 def test_empty_batch_and_empty_sequences():
     torch, binding, device = _mods()
     case = synth.make_case("empties", [0, 40, 0], [0, 3, 0], num_heads=8, pool_slots=60, seed=306)
