@@ -108,12 +108,35 @@ def _check(rc: int, where: str):
         raise VmlaError(rc, where)
 
 
-def _ptr(t) -> Optional[int]:
+def _arg(t, itemsize: int, name: str, on_device: bool) -> Optional[int]:
+    """Pointer of an array argument after the checks the C ABI cannot make from a bare pointer:
+    contiguous storage, the element size of the type the entry point reads (0: any) and device or
+    host memory as the entry point expects.  Raises ValueError before any call."""
     if t is None:
         return None
     if isinstance(t, np.ndarray):
+        if on_device:
+            raise ValueError(f"{name}: device memory expected, got a numpy array")
+        if not t.flags.c_contiguous:
+            raise ValueError(f"{name}: not contiguous")
+        if itemsize and t.itemsize != itemsize:
+            raise ValueError(f"{name}: {itemsize}-byte elements expected, got {t.dtype}")
         return t.ctypes.data
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: not contiguous")
+    if itemsize and t.element_size() != itemsize:
+        raise ValueError(f"{name}: {itemsize}-byte elements expected, got {t.dtype}")
+    if bool(t.is_cuda) != on_device:
+        raise ValueError(f"{name}: {'device' if on_device else 'host'} memory expected, got {t.device}")
     return t.data_ptr()
+
+
+def _d(t, itemsize: int, name: str) -> Optional[int]:
+    return _arg(t, itemsize, name, True)
+
+
+def _h(t, itemsize: int, name: str) -> Optional[int]:
+    return _arg(t, itemsize, name, False)
 
 
 def _host_i32(a) -> np.ndarray:
@@ -159,9 +182,11 @@ def _run(fn, name, q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host,
     qoh = _host_i32(qo_indptr_host)
     H = int(num_heads if num_heads is not None else q.shape[1])
     S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
-    rc = fn(_ptr(q), _ptr(kv_pool), S, _ptr(kv_indptr), _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask),
-            _ptr(parent), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, H, float(sm_scale), int(splits), _ptr(out),
-            _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    rc = fn(_d(q, 2, "q"), _d(kv_pool, 2, "kv_pool"), S, _d(kv_indptr, 4, "kv_indptr"),
+            _d(kv_indices, 4, "kv_indices"), _d(qo_indptr, 4, "qo_indptr"), _d(draft_mask, 8, "draft_mask"),
+            _d(parent, 4, "parent"), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, H, float(sm_scale), int(splits),
+            _d(out, 2, "out"), _d(lse, 4, "lse"), _d(workspace, 0, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, name)
 
 
@@ -187,10 +212,11 @@ def verify_attn_mla_device_plan(q, kv_pool, kv_indptr, kv_indices, qo_indptr, ba
     """Stream-capture-safe verify attention: the plan is built on the device from the device indptr arrays."""
     H = int(num_heads if num_heads is not None else q.shape[1])
     S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
-    rc = _lib.verify_attn_mla_device_plan(_ptr(q), _ptr(kv_pool), S, _ptr(kv_indptr), _ptr(kv_indices),
-                                          _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent), int(batch), H,
+    rc = _lib.verify_attn_mla_device_plan(_d(q, 2, "q"), _d(kv_pool, 2, "kv_pool"), S, _d(kv_indptr, 4, "kv_indptr"),
+                                          _d(kv_indices, 4, "kv_indices"), _d(qo_indptr, 4, "qo_indptr"),
+                                          _d(draft_mask, 8, "draft_mask"), _d(parent, 4, "parent"), int(batch), H,
                                           int(max_total_q), int(max_total_kv), float(sm_scale), int(splits),
-                                          _ptr(out), _ptr(lse), _ptr(workspace),
+                                          _d(out, 2, "out"), _d(lse, 4, "lse"), _d(workspace, 0, "workspace"),
                                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "verify_attn_mla_device_plan")
 
@@ -199,9 +225,11 @@ def verify_attn_mla_defrag(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_
                            stream=None):
     """Copies every sequence's rows into its run of dst_pool (runs start at run_base) and zeroes each run's tail."""
     kvh = _host_i32(kv_indptr_host)
-    rc = _lib.verify_attn_mla_defrag(_ptr(src_pool), int(src_pool.shape[0]), _ptr(kv_indptr), _ptr(kv_indices),
-                                     kvh.ctypes.data, len(kvh) - 1, _ptr(dst_pool), int(dst_pool.shape[0]),
-                                     _ptr(run_base), _ptr(status_word), _stream(stream))
+    rc = _lib.verify_attn_mla_defrag(_d(src_pool, 2, "src_pool"), int(src_pool.shape[0]),
+                                     _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
+                                     kvh.ctypes.data, len(kvh) - 1, _d(dst_pool, 2, "dst_pool"),
+                                     int(dst_pool.shape[0]), _d(run_base, 4, "run_base"),
+                                     _d(status_word, 4, "status_word"), _stream(stream))
     _check(rc, "verify_attn_mla_defrag")
 
 
@@ -226,11 +254,13 @@ def verify_attn_mla_fp8(q, kv_pool_e4m3, kv_scale, kv_indptr, kv_indices, qo_ind
     """verify_attn_mla on an e4m3 latent pool ([S, 576] uint8 codes) with one scale."""
     kvh = _host_i32(kv_indptr_host)
     qoh = _host_i32(qo_indptr_host)
-    rc = _lib.verify_attn_mla_fp8(_ptr(q), _ptr(kv_pool_e4m3), int(kv_pool_e4m3.shape[0]), float(kv_scale),
-                                  _ptr(kv_indptr), _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent),
-                                  kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, int(q.shape[1]), float(sm_scale),
-                                  int(splits), _ptr(out), _ptr(lse), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    rc = _lib.verify_attn_mla_fp8(_d(q, 2, "q"), _d(kv_pool_e4m3, 1, "kv_pool_e4m3"), int(kv_pool_e4m3.shape[0]),
+                                  float(kv_scale), _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
+                                  _d(qo_indptr, 4, "qo_indptr"), _d(draft_mask, 8, "draft_mask"),
+                                  _d(parent, 4, "parent"), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1,
+                                  int(q.shape[1]), float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
+                                  _d(workspace, 0, "workspace"), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
     _check(rc, "verify_attn_mla_fp8")
 
 
@@ -243,9 +273,12 @@ def verify_attn_mla_tree_accept(qo_indptr, parent, draft_token, target_token, ro
                                 next_token, status_word=None, stream=None):
     """Greedy acceptance of the verified draft tree (device int32 arrays; parent None = chain)."""
     batch = int(qo_indptr.numel()) - 1
-    rc = _lib.verify_attn_mla_tree_accept(_ptr(qo_indptr), _ptr(parent), _ptr(draft_token), _ptr(target_token),
-                                          _ptr(root_token), batch, int(draft_token.numel()), _ptr(accept_len),
-                                          _ptr(accept_path), _ptr(next_token), _ptr(status_word), _stream(stream))
+    rc = _lib.verify_attn_mla_tree_accept(_d(qo_indptr, 4, "qo_indptr"), _d(parent, 4, "parent"),
+                                          _d(draft_token, 4, "draft_token"), _d(target_token, 4, "target_token"),
+                                          _d(root_token, 4, "root_token"), batch, int(draft_token.numel()),
+                                          _d(accept_len, 4, "accept_len"), _d(accept_path, 4, "accept_path"),
+                                          _d(next_token, 4, "next_token"), _d(status_word, 4, "status_word"),
+                                          _stream(stream))
     _check(rc, "verify_attn_mla_tree_accept")
 
 
@@ -258,20 +291,21 @@ def verify_attn_mla_simt(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr
 
 def verify_attn_mla_merge(o_parts, lse_parts, out, lse, stream=None):
     S, R = int(o_parts.shape[0]), int(o_parts.shape[1])
-    _check(_lib.verify_attn_mla_merge(_ptr(o_parts), _ptr(lse_parts), S, R, _ptr(out), _ptr(lse), _stream(stream)),
-           "verify_attn_mla_merge")
+    _check(_lib.verify_attn_mla_merge(_d(o_parts, 4, "o_parts"), _d(lse_parts, 4, "lse_parts"), S, R,
+                                      _d(out, 2, "out"), _d(lse, 4, "lse"), _stream(stream)), "verify_attn_mla_merge")
 
 
 def verify_attn_mla_tree_mask(parent, qo_indptr, mask_out, status_word=None, stream=None):
     B = int(qo_indptr.shape[0]) - 1
     T = int(parent.shape[0])
-    _check(_lib.verify_attn_mla_tree_mask(_ptr(parent), _ptr(qo_indptr), B, T, _ptr(mask_out), _ptr(status_word),
+    _check(_lib.verify_attn_mla_tree_mask(_d(parent, 4, "parent"), _d(qo_indptr, 4, "qo_indptr"), B, T,
+                                          _d(mask_out, 8, "mask_out"), _d(status_word, 4, "status_word"),
                                           _stream(stream)), "verify_attn_mla_tree_mask")
 
 
 def verify_attn_mla_check(workspace, stream=None) -> int:
     """Device status of the last call on `workspace` (synchronises the stream)."""
-    return int(_lib.verify_attn_mla_check(_ptr(workspace), _stream(stream)))
+    return int(_lib.verify_attn_mla_check(_d(workspace, 0, "workspace"), _stream(stream)))
 
 
 def verify_attn_mla_host_buffer_size(qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0,
@@ -292,11 +326,12 @@ def verify_attn_mla_host(q_host, kv_pool, kv_indptr_host, kv_indices_host, qo_in
     kvh = _host_i32(kv_indptr_host)
     qoh = _host_i32(qo_indptr_host)
     H = int(num_heads if num_heads is not None else q_host.shape[1])
-    rc = _lib.verify_attn_mla_host(_ptr(q_host), _ptr(kv_pool), int(kv_pool.shape[0]), kvh.ctypes.data,
-                                   _ptr(kv_indices_host), qoh.ctypes.data, _ptr(draft_mask_host), _ptr(parent_host),
-                                   len(kvh) - 1, H, float(sm_scale), int(splits), _ptr(out_host), _ptr(lse_host),
-                                   _ptr(device_buffer), device_buffer.numel() * device_buffer.element_size(),
-                                   _stream(stream))
+    rc = _lib.verify_attn_mla_host(_h(q_host, 2, "q_host"), _d(kv_pool, 2, "kv_pool"), int(kv_pool.shape[0]),
+                                   kvh.ctypes.data, _h(kv_indices_host, 4, "kv_indices_host"), qoh.ctypes.data,
+                                   _h(draft_mask_host, 8, "draft_mask_host"), _h(parent_host, 4, "parent_host"),
+                                   len(kvh) - 1, H, float(sm_scale), int(splits), _h(out_host, 2, "out_host"),
+                                   _h(lse_host, 4, "lse_host"), _d(device_buffer, 0, "device_buffer"),
+                                   device_buffer.numel() * device_buffer.element_size(), _stream(stream))
     _check(rc, "verify_attn_mla_host")
 
 
@@ -327,8 +362,11 @@ def verify_attn_mla_simt_static(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv
     """CUDA-core verify with the library's fixed scratch array instead of a workspace (no allocation)."""
     kvh = _host_i32(kv_indptr_host)
     qoh = _host_i32(qo_indptr_host)
-    rc = _lib.verify_attn_mla_simt_static(_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(kv_indptr),
-                                          _ptr(kv_indices), _ptr(qo_indptr), _ptr(draft_mask), _ptr(parent),
+    rc = _lib.verify_attn_mla_simt_static(_d(q, 2, "q"), _d(kv_pool, 2, "kv_pool"), int(kv_pool.shape[0]),
+                                          _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
+                                          _d(qo_indptr, 4, "qo_indptr"), _d(draft_mask, 8, "draft_mask"),
+                                          _d(parent, 4, "parent"),
                                           kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1, int(q.shape[1]),
-                                          float(sm_scale), int(splits), _ptr(out), _ptr(lse), _stream(stream))
+                                          float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
+                                          _stream(stream))
     _check(rc, "verify_attn_mla_simt_static")

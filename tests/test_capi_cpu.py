@@ -290,3 +290,42 @@ def test_plan_units_within_the_device_plan_bound(B):
         row_blocks = -(-int(qo[-1]) * 64 // 256) + 3
         assert info.num_units <= splits * row_blocks
         assert info.partial_rows <= min(256 * splits * row_blocks, int(qo[-1]) * 64 * 64)
+
+
+def test_binding_checks_array_arguments_before_the_call(B):
+    """The binding refuses, before calling the library, arrays the C ABI cannot check from a bare
+    pointer: host memory where device memory is read, the wrong element size, strided views."""
+    import torch
+    T, H, N = 2, 8, 40
+    kvp = np.array([0, N], np.int32)
+    qop = np.array([0, T], np.int32)
+    kv = torch.zeros((N, 576), dtype=torch.bfloat16)
+    kvi = torch.arange(N, dtype=torch.int32)
+    out = torch.zeros((T, H, 512), dtype=torch.bfloat16)
+    lse = torch.zeros((T, H), dtype=torch.float32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+
+    def call(q):
+        B.verify_attn_mla(q, kv, torch.from_numpy(kvp), kvi, torch.from_numpy(qop), kvp, qop, out, lse, ws, 0.07)
+
+    # through an entry point (its first array argument is checked first)
+    with pytest.raises(ValueError, match="q: device memory expected, got cpu"):
+        call(torch.zeros((T, H, 576), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="q: device memory expected, got a numpy array"):
+        call(np.zeros((T, H, 576), np.uint16))
+    with pytest.raises(ValueError, match="q: 2-byte elements expected"):
+        call(torch.zeros((T, H, 576), dtype=torch.float32))
+    with pytest.raises(ValueError, match="q_host: 2-byte elements expected"):
+        B.verify_attn_mla_host(torch.zeros((T, H, 576), dtype=torch.float32), kv, kvp, kvi, qop, out, lse, ws, 0.07)
+    # each rule of the check
+    with pytest.raises(ValueError, match="kv_pool: not contiguous"):
+        B._arg(torch.zeros((576, N), dtype=torch.bfloat16).t(), 2, "kv_pool", False)
+    with pytest.raises(ValueError, match="kv_indices: not contiguous"):
+        B._arg(np.zeros((8, 2), np.int32)[:, 0], 4, "kv_indices", False)
+    with pytest.raises(ValueError, match="kv_indices: 4-byte elements expected"):
+        B._arg(torch.zeros(4, dtype=torch.int64), 4, "kv_indices", False)
+    assert B._arg(None, 4, "parent", True) is None
+    a = np.zeros(3, np.int32)
+    assert B._arg(a, 4, "kv_indices_host", False) == a.ctypes.data
+    t = torch.zeros(5, dtype=torch.uint8)
+    assert B._arg(t, 0, "workspace", False) == t.data_ptr()
