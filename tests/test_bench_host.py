@@ -87,3 +87,11 @@ def test_roofline_picks_the_bound_of_the_work():
     r = bench.roofline_entry(89.23e9, 745.1e6, 0.3359, peaks)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert abs(r["achieved"] - 745.1e6 / 0.3359e-3 / 1e9) < 1e-9 and abs(r["frac"] - r["achieved"] / 6789.3) < 1e-12
+
+
+def test_side_leg_records_a_failure_in_its_place():
+    assert bench.side_leg(lambda a, b: {"ms": a + b}, 1, 2) == {"ms": 3}
+
+    def broken():
+        raise RuntimeError("device-planned call: bad shape")
+    assert bench.side_leg(broken) == {"error": "RuntimeError: device-planned call: bad shape"}
