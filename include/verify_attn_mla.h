@@ -62,7 +62,8 @@ typedef enum vmla_status {
   VMLA_ERR_WORKSPACE = -4, /* workspace smaller than verify_attn_mla_workspace_size() */
   VMLA_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed */
   VMLA_ERR_TIMEOUT = -6,   /* a kernel's bounded wait expired (kernel returned early) */
-  VMLA_ERR_INDEX = -7,     /* a kv slot index was outside [0, pool_slots) (its row reads as zeros) */
+  VMLA_ERR_INDEX = -7,     /* a kv slot index was outside [0, pool_slots); that key still takes part,
+                              with a row of zeros (score 0, value 0), in every kernel */
   VMLA_ERR_DEVICE = -8,    /* no usable sm_103 device for this library */
   VMLA_ERR_PARENT = -9     /* a parent index was not in [-1, i) (mask left empty) */
 } vmla_status;
@@ -282,14 +283,23 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
  * on a device shares the one array and leaves its contents behind: calls that
  * may overlap on the GPU (different streams without ordering) race on it, so
  * order them on one stream.  Faults a kernel detects (a slot outside the pool,
- * malformed parents) are recorded in the array's status word but not reported
- * by this entry point; diagnose them through verify_attn_mla_simt with a
- * workspace. */
+ * malformed parents) are recorded in the array's status word, which
+ * verify_attn_mla_simt_static_check() reads.  The device address of the array
+ * is looked up once per device and kept; after cudaDeviceReset the library's
+ * module is loaded again and that address is stale, so a process that resets a
+ * device must not call this entry point on it afterwards. */
 int verify_attn_mla_simt_static(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
                                 const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
                                 const int32_t* parent, const int32_t* kv_indptr_host,
                                 const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits,
                                 void* out, float* lse, void* stream);
+
+/* Synchronises `stream` and returns the status word that the calls of
+ * verify_attn_mla_simt_static on the current device left in the library's
+ * scratch array (VMLA_OK when no kernel recorded a fault).  It copies 8 bytes
+ * from the array to the host and allocates nothing.  Test and debugging aid;
+ * it blocks the host. */
+int verify_attn_mla_simt_static_check(void* stream);
 
 /* The split merge on its own: o_parts [num_splits, rows, 512] fp32 (each part
  * already normalised by its own softmax sum), lse_parts [num_splits, rows]

@@ -40,6 +40,7 @@ EXPORTS = (
     "verify_attn_mla_simt_static", "verify_attn_mla_device_plan_workspace_size", "verify_attn_mla_device_plan",
     "verify_attn_mla_tree_accept", "verify_attn_mla_defrag", "verify_attn_mla_runs",
     "verify_attn_mla_runs_workspace_size", "verify_attn_mla_test_fault", "verify_attn_mla_fp8",
+    "verify_attn_mla_simt_static_check",
 )
 
 
@@ -75,6 +76,7 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_timing_enable": [i32],
         "verify_attn_mla_timing_read": [vp, vp, vp, i32, ctypes.POINTER(i32)],
         "verify_attn_mla_simt_static": [vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp, vp, vp],
+        "verify_attn_mla_simt_static_check": [vp],
         "verify_attn_mla_device_plan_workspace_size": [i32, i32, i64, i64, i32, ctypes.POINTER(sz)],
         "verify_attn_mla_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp, vp,
                                         sz, vp],
@@ -370,3 +372,8 @@ def verify_attn_mla_simt_static(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv
                                           float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
                                           _stream(stream))
     _check(rc, "verify_attn_mla_simt_static")
+
+
+def verify_attn_mla_simt_static_check(stream=None) -> int:
+    """Synchronises the stream and returns the status word the static-scratch calls left (0 = ok)."""
+    return int(_lib.verify_attn_mla_simt_static_check(_stream(stream)))

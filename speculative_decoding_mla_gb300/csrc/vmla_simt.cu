@@ -124,7 +124,9 @@ simt_verify_kernel(const __grid_constant__ PlanParams plan, const RunArgs a) {
         }
       }
       const int j = base + lane;
-      bool visible = j < k_hi && slot_s[lane] >= 0;
+      // a slot outside the pool reads as a zero row (score 0, value 0) and stays visible,
+      // as in the tensor-core kernel
+      bool visible = j < k_hi;
       if (visible && j >= prefix) visible = ((vis[rr] >> (j - prefix)) & 1ull) != 0;
       const float s2 = visible ? part[0] * a.scale_log2 : -INFINITY;
       const float mx = warp_max(s2);

@@ -162,6 +162,12 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_cluster, uint32_t 
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Wait until at most N committed bulk groups are still incomplete (writes included).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Wait until at most N committed bulk groups still read their source.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {

@@ -42,6 +42,18 @@ int static_scratch(void** ptr) {
 }  // namespace
 }  // namespace vmla
 
+extern "C" int verify_attn_mla_simt_static_check(void* stream) {
+  void* scratch = nullptr;
+  int rc = vmla::static_scratch(&scratch);
+  if (rc != VMLA_OK) return rc;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return VMLA_ERR_CUDA;
+  // the status words open the scratch layout (offset 0), as they open a workspace
+  uint32_t word[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(word, vmla::g_vmla_static_scratch, sizeof word, 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return VMLA_ERR_CUDA;
+  return (int)(int32_t)word[0];
+}
+
 extern "C" int verify_attn_mla_simt_static(const void* q, const void* kv_pool, int64_t pool_slots,
                                            const int32_t* kv_indptr, const int32_t* kv_indices,
                                            const int32_t* qo_indptr, const uint64_t* draft_mask,

@@ -36,8 +36,9 @@
 // 2-9 softmax (two threads per row, 32 keys each per 64-key message), warp 10
 // P sender; mixer warps 2-5 rescale/epilogue, warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
-// status word, tells the other CTAs to stop, drains its own copies and MMAs,
-// frees tensor memory and returns.
+// status word, tells the other CTAs to stop, and every CTA leaves only after
+// what was issued into it has landed (see the end of tc_verify_body), frees
+// tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -211,11 +212,49 @@ __device__ __forceinline__ bool wait_bar(TcSmem& sm, uint64_t* bar, uint32_t par
   return mbar_try_wait_cluster(bar, parity) || wait_bar_slow(sm, bar, parity, status, where);
 }
 
-// Bounded wait that ignores the abort flag (draining in-flight work before exit).
-__device__ __noinline__ void drain_bar(TcSmem& sm, uint64_t* bar, uint32_t parity) {
+// Bounded wait that ignores the abort flag, for a phase that completes once
+// what this CTA itself issued has landed (draining before exit).  Should the
+// budget run out, the kernel records VMLA_ERR_TIMEOUT and aborts the cluster,
+// so that every CTA waits out the settle period before it leaves.
+__device__ __noinline__ void drain_bar(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status, int where) {
   const long long budget = sm.c.wait_cycles;
   const long long t0 = clock64();
-  while (!mbar_try_wait_cluster(bar, parity) && clock64() - t0 < budget) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - t0 > budget) {
+      record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
+      abort_cluster(sm);
+      return;
+    }
+  }
+}
+
+// Bounded wait for a phase that another CTA's work completes; it may never
+// come once the cluster is aborting (the settle period at the end of the
+// kernel then covers whatever had been issued).
+__device__ __noinline__ void drain_bar_live(TcSmem& sm, uint64_t* bar, uint32_t parity, uint32_t* status,
+                                            int where) {
+  const long long budget = sm.c.wait_cycles;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity) && !sm.c.abort_flag) {
+    if (clock64() - t0 > budget) {
+      record_status(status, VMLA_ERR_TIMEOUT, (uint32_t)where);
+      abort_cluster(sm);
+      return;
+    }
+  }
+}
+
+// After a failed wait: every CTA of the cluster has stopped issuing work, but
+// tile loads, bulk copies, tensor-core commits and MMAs issued before may still
+// be on their way into this CTA's shared and tensor memory.  Each of them takes
+// microseconds; this waits half a millisecond of the global timer (and at most
+// 2^26 reads of it).
+__device__ __noinline__ void settle_after_abort() {
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int k = 0; k < (1 << 26); ++k) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 500000ull) break;
   }
 }
 
@@ -275,11 +314,13 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   }
   // the even CTA drains its last loads (their barriers count both CTAs' bytes)
   if (q == 0)
-    for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(sm, &sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1);
+    for (int k = 1; k <= nst && it - k >= 0; ++k)
+      drain_bar_live(sm, &sm.c.kfull[(it - k) % nst], ((it - k) / nst) & 1, a.status, 120);
   // tail: the releases of the last stages arrive on this CTA's barriers from the
   // tensor core (a commit multicast to both CTAs of the pair); this CTA may not
   // exit while one is still in flight
-  for (int k = 1; k <= nst && it - k >= 0; ++k) drain_bar(sm, &sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1);
+  for (int k = 1; k <= nst && it - k >= 0; ++k)
+    drain_bar_live(sm, &sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1, a.status, 121);
 }
 
 // ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
@@ -334,7 +375,7 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   // all issued MMAs complete before the CTA may exit (this arrive goes to rank 0
   // only: nothing in rank 1 waits for it)
   mma_commit_pair(&sm.c.obar, (uint16_t)0x1);
-  drain_bar(sm, &sm.c.obar, 0);
+  drain_bar(sm, &sm.c.obar, 0, a.status, 204);
 }
 
 // ------------------------------------------------------------------ ranks 0,1: softmax (warps 2 .. 2+kSoftWarps-1)
@@ -573,7 +614,9 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
     }
   }
 done:
-  bulk_wait_group_read<0>();
+  // every copy this thread issued has been written into the mixer (not only read
+  // from the staging buffer) before the CTA may reach the final cluster barrier
+  bulk_wait_group<0>();
 }
 
 // ------------------------------------------------------------------ rank 1: S-buffer release forwarder (warp 1, lane 0)
@@ -665,7 +708,7 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     // regardless of the abort flag, so no arrival of this pair's earlier commits is
     // still travelling when the cluster leaves
     mma_commit_pair(&sm.c.obar, (uint16_t)0x4);
-    drain_bar(sm, &sm.c.obar, obn & 1);
+    drain_bar(sm, &sm.c.obar, obn & 1, a.status, 405);
   }
   post(kCmdExit);
 }
@@ -910,9 +953,19 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
   tc_fence_before();
   __syncthreads();
   __syncwarp();
-  // no CTA leaves while another may still address its shared or tensor memory
+  // no CTA leaves while another may still address its shared or tensor memory.
+  // Past this barrier no thread of the cluster issues anything.  On the normal
+  // path every arrival into this CTA has been waited for by now (tile loads,
+  // stage releases, P and finals copies, MMA commits).  After a failed wait some
+  // of those waits were cut short, so the CTA first lets whatever was issued
+  // land; all four CTAs read the same abort flag here, since a failed wait
+  // raises it in every CTA of the cluster before the barrier.
   cluster_arrive();
   cluster_wait();
+  if (sm.c.abort_flag) {
+    if (threadIdx.x == 0) settle_after_abort();
+    __syncthreads();
+  }
   __syncwarp();
   if (warp == 0) {
     tc_fence_after();
