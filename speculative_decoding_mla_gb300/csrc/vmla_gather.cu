@@ -7,9 +7,12 @@
 // Decode Speedup" names as the plan's next phase (section "The Context: A
 // Custom Kernel for an Unsupported Architecture"), done per call.
 //
-// One warp per row: lane l moves 16-byte granules l, l+32 and l+64 (< 72), so
-// every warp instruction reads and writes 512 contiguous bytes.  A slot outside
-// [0, pool_slots) records VMLA_ERR_INDEX and stages a zero row.
+// One warp per four rows at a time: lane l moves 16-byte granules l, l+32 and
+// l+64 (< 72) of each, so every warp instruction reads and writes 512
+// contiguous bytes; the four slots are read in one load and all twelve row
+// loads are in flight before the stores, so a warp waits out one index read
+// and one row read per four rows.  A slot outside [0, pool_slots) records
+// VMLA_ERR_INDEX and stages a zero row.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -29,6 +32,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
                : "l"(p));
   return v;
 }
+
+constexpr int kRowsPerWarp = 4;  // rows a gather warp has in flight
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int32_t* __restrict__ kv_indices,
@@ -52,19 +57,34 @@ gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int
     dst[lane + 32] = make_uint4(0, 0, 0, 0);
     if (lane < kRowU4 - 64) dst[lane + 64] = make_uint4(0, 0, 0, 0);
   }
-  for (int64_t j = warp0; j < total_kv; j += nwarps) {
-    const int32_t slot = kv_indices[j];
-    const bool ok = slot >= 0 && (int64_t)slot < pool_slots;
-    if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)j);
-    const uint4* src = pool + (int64_t)(ok ? slot : 0) * kRowU4;
-    uint4* dst = staged + j * kRowU4;
-    uint4 v0 = ok ? ld_stream(src + lane) : make_uint4(0, 0, 0, 0);
-    uint4 v1 = ok ? ld_stream(src + lane + 32) : make_uint4(0, 0, 0, 0);
-    uint4 v2 = make_uint4(0, 0, 0, 0);
-    if (lane < kRowU4 - 64 && ok) v2 = ld_stream(src + lane + 64);
-    dst[lane] = v0;
-    dst[lane + 32] = v1;
-    if (lane < kRowU4 - 64) dst[lane + 64] = v2;
+  for (int64_t j0 = warp0 * kRowsPerWarp; j0 < total_kv; j0 += nwarps * kRowsPerWarp) {
+    // lane k < kRowsPerWarp reads the slot of row j0 + k
+    int32_t my = 0;
+    if (lane < kRowsPerWarp && j0 + lane < total_kv) {
+      my = kv_indices[j0 + lane];
+      if (my < 0 || (int64_t)my >= pool_slots) {
+        record_status(status, VMLA_ERR_INDEX, (uint32_t)(j0 + lane));
+        my = -1;
+      }
+    }
+    uint4 v[kRowsPerWarp][3];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int32_t slot = __shfl_sync(0xffffffffu, my, k);
+      const bool ok = slot >= 0 && j0 + k < total_kv;
+      const uint4* src = pool + (int64_t)(ok ? slot : 0) * kRowU4;
+      v[k][0] = ok ? ld_stream(src + lane) : make_uint4(0, 0, 0, 0);
+      v[k][1] = ok ? ld_stream(src + lane + 32) : make_uint4(0, 0, 0, 0);
+      v[k][2] = (ok && lane < kRowU4 - 64) ? ld_stream(src + lane + 64) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      if (j0 + k >= total_kv) break;
+      uint4* dst = staged + (j0 + k) * kRowU4;
+      dst[lane] = v[k][0];
+      dst[lane + 32] = v[k][1];
+      if (lane < kRowU4 - 64) dst[lane + 64] = v[k][2];
+    }
   }
 }
 
@@ -123,7 +143,7 @@ int launch_gather_impl(const RunArgs& a, const uint32_t* rows_dev, void* stream)
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess)
     return VMLA_ERR_CUDA;
-  const int64_t need = (a.total_kv + kGatherWarps - 1) / kGatherWarps;
+  const int64_t need = (a.total_kv + kGatherWarps * kRowsPerWarp - 1) / (kGatherWarps * kRowsPerWarp);
   const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM keep enough rows in flight
   const int blocks = (int)(need < cap ? need : cap);
   if (a.kv_scale > 0.f) {

@@ -329,3 +329,14 @@ def test_binding_checks_array_arguments_before_the_call(B):
     assert B._arg(a, 4, "kv_indices_host", False) == a.ctypes.data
     t = torch.zeros(5, dtype=torch.uint8)
     assert B._arg(t, 0, "workspace", False) == t.data_ptr()
+
+
+def test_prepared_call_marshals_once_and_reports_errors(B):
+    # a prepared call converts its arguments to the entry point's C types once and repeats the call
+    ok = B.Prepared(B.lib().verify_attn_mla_test_fault, "verify_attn_mla_test_fault", (0, 0), ())
+    ok()
+    ok()
+    bad = B.Prepared(B.lib().verify_attn_mla_test_fault, "verify_attn_mla_test_fault", (5, 0), ())
+    with pytest.raises(B.VmlaError) as e:
+        bad()
+    assert e.value.status == B.VMLA_ERR_SHAPE
