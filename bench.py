@@ -49,11 +49,12 @@ if ROOT not in sys.path:
 
 METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
 
-# DRAM bytes per verify launch from a committed ncu capture of the long_120k case, scaled to the
-# workload by keys; valid only while the kernel and planner sources are the ones profiled.
+# DRAM bytes (read + write) per verify launch from committed ncu captures of each workload's
+# first timed launch; valid only while the kernel and planner sources are the ones profiled.
 PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
-PROFILED_FINGERPRINT = "9076164ff3f00a32"
-PROFILED_TRAFFIC = {"long_185k": 241.4e6, "long_120k": 156.6e6}
+PROFILED_FINGERPRINT = "6e349c8de2df3f4c"
+PROFILED_TRAFFIC = {"contiguous_1k": 2.460e6, "paged_ragged": 82.29e6, "long_185k": 238.36e6, "tree_32k": 485.32e6,
+                    "sweep_q1": 756.03e6, "sweep_q4": 793.42e6, "sweep_q16": 825.56e6}
 
 
 def source_fingerprint(paths=None) -> str:

@@ -138,3 +138,18 @@ def test_captured_graph_replays_with_new_lengths():
     torch.cuda.synchronize()
     assert binding.verify_attn_mla_check(ws) == binding.VMLA_ERR_SHAPE
     assert bool(torch.all(out == 0.5))
+
+
+@pytest.mark.slow
+def test_device_plan_long_185k_sampled_rows():
+    """The device-planned call on the full 185,000-token workload (the bench's graph-replayed path):
+    bit-equal to the host-planned call, and sampled rows against the oracle."""
+    from tests.test_gpu_parity import full_case, oracle_rows, sample_rows
+    case = full_case("long_185k")
+    o1, l1, s1 = run_full(case, "tc")
+    o2, l2, s2 = run_dplan(case)
+    assert s1 == 0 and s2 == 0
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    rows = sample_rows(case)
+    ref_o, ref_l = oracle_rows(case, rows, "long_185k/sampled")
+    compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, "device plan / long_185k")

@@ -72,3 +72,20 @@ def test_fp8_bad_slot_is_reported():
     case.kv_indices[5] = case.pool_slots + 3
     _, l, st = run_fp8(case, codes, scale)
     assert st == binding.VMLA_ERR_INDEX and np.all(np.isfinite(l))
+
+
+@pytest.mark.slow
+def test_fp8_long_185k_sampled_rows():
+    """The e4m3 pool path on the full 185,000-token workload: sampled rows against the oracle on the
+    dequantized pool, and bit-equal to the bf16 call on that pool."""
+    from tests.test_gpu_parity import full_case, run_full, sample_rows
+    case = full_case("long_185k")
+    codes, scale, case2 = quantize(case)
+    o, l, st = run_fp8(case, codes, scale)
+    assert st == 0
+    o2, l2, s2 = run_full(case2, "tc")
+    assert s2 == 0
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
+    rows = sample_rows(case)
+    ref_o, ref_l = oracle.verify_rows(case2, rows)
+    compare(o.reshape(-1, o.shape[-1])[rows], l.reshape(-1)[rows], ref_o, ref_l, "fp8 / long_185k")

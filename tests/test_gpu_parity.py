@@ -3,8 +3,10 @@
 Tolerances (the target's own): max |out_gpu - out_oracle| <= 1e-2 on the bf16
 output and max |lse_gpu - lse_oracle| <= 1e-3 on the fp32 log-sum-exp.
 Small cases are compared element by element over every row; the full-size
-workloads, in the launch configuration the bench times, on sampled rows the
-oracle evaluates one by one.
+workloads run in the launch configuration the bench times and are compared
+on every row of the 185,000-token workload, every row of one 256-row unit per
+sequence of the tree and Q=4 sweep workloads, and sampled rows of all of them,
+which the oracle evaluates one by one.
 """
 import numpy as np
 import pytest
@@ -176,3 +178,49 @@ def test_more_units_than_one_launch_holds():
     ref_o, ref_l = oracle.verify_rows(case, rows)
     compare(o.reshape(-1, o.shape[-1])[rows], l.reshape(-1)[rows], ref_o, ref_l, "many_units")
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+
+
+_ORACLE_ROWS = {}
+
+
+def oracle_rows(case, rows, key):
+    """The oracle's result for `rows` of a full-size case, computed once per test session."""
+    if key not in _ORACLE_ROWS:
+        _ORACLE_ROWS[key] = oracle.verify_rows(case, rows)
+    return _ORACLE_ROWS[key]
+
+
+def unit_rows(case, rows_per_unit=256):
+    """Every row of the first 256-row unit (row block 0) of each sequence."""
+    H = case.num_heads
+    out = []
+    for b in range(case.batch):
+        q0, q1 = int(case.qo_indptr[b]), int(case.qo_indptr[b + 1])
+        n = (q1 - q0) * H
+        out.append(q0 * H + np.arange(min(n, rows_per_unit), dtype=np.int64))
+    return np.concatenate(out)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_long_185k_every_row(kernel):
+    """All 1024 query rows (16 drafts x 64 heads) of the 185,000-token workload, in the bench's launch
+    configuration, against the oracle row by row."""
+    case = full_case("long_185k")
+    rows = np.arange(case.q.shape[0] * case.num_heads, dtype=np.int64)
+    ref_o, ref_l = oracle_rows(case, rows, "long_185k/all")
+    o, l, st = run_full(case, kernel)
+    assert st == 0
+    compare(o.reshape(-1, o.shape[-1]), l.reshape(-1), ref_o, ref_l, f"{kernel}/long_185k every row")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["tree_32k", "sweep_q4"])
+def test_full_unit_every_row(name):
+    """Every row of one full 256-row unit (row block 0) of every sequence, tensor-core path."""
+    case = full_case(name)
+    rows = unit_rows(case)
+    ref_o, ref_l = oracle_rows(case, rows, f"{name}/unit0")
+    o, l, st = run_full(case, "tc")
+    assert st == 0
+    compare(o.reshape(-1, o.shape[-1])[rows], l.reshape(-1)[rows], ref_o, ref_l, f"tc/{name} unit rows")

@@ -103,3 +103,18 @@ def test_runs_and_slots_outside_their_pools_are_reported():
     binding.verify_attn_mla_runs(dc.q, dst, dc.kv_indptr, torch.from_numpy(far).cuda(), dc.qo_indptr,
                                  dc.kv_indptr_host, dc.qo_indptr_host, out, lse, ws, dc.sm_scale)
     assert binding.verify_attn_mla_check(ws) == binding.VMLA_ERR_INDEX
+
+
+@pytest.mark.slow
+def test_runs_long_185k_sampled_rows():
+    """The runs path on the full 185,000-token workload (as the bench times it): bit-equal to the
+    per-call gather path, and sampled rows against the oracle."""
+    from tests.test_gpu_parity import full_case, oracle_rows, sample_rows
+    case = full_case("long_185k")
+    o1, l1, s1 = run_full(case, "tc")
+    o2, l2, s2 = run_runs(case)
+    assert s1 == 0 and s2 == 0
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    rows = sample_rows(case)
+    ref_o, ref_l = oracle_rows(case, rows, "long_185k/sampled")
+    compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, "runs / long_185k")
