@@ -25,6 +25,23 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream still runs
+// (once every block of that kernel has signalled, or exited); it must wait for
+// that kernel's completion and memory before it reads anything the kernel
+// wrote.  Without such a launch the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Launch attribute that lets a kernel start under the tail of the one before it
+// (it then calls grid_dependency_wait before reading that kernel's output).
+inline cudaLaunchAttribute early_start_attribute() {
+  cudaLaunchAttribute a = {};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // First fault wins: records code and info in the workspace status word.
 __device__ __forceinline__ void record_status(uint32_t* status, int code, uint32_t info) {
   if (!status) return;

@@ -39,6 +39,9 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int32_t* __restrict__ kv_indices,
                    int64_t total_kv, const uint32_t* __restrict__ rows_dev, uint4* __restrict__ staged,
                    uint32_t* status) {
+  // the verify kernel may be scheduled as this grid's blocks retire (it waits for
+  // the staged rows before it reads them)
+  grid_dependents_launch();
   const int lane = threadIdx.x & 31;
   int64_t end = total_kv;
   if (rows_dev) {
@@ -105,6 +108,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_fp8_kernel(const uint4* __restrict__ pool, int64_t pool_slots, float scale,
                        const int32_t* __restrict__ kv_indices, int64_t total_kv, uint4* __restrict__ staged,
                        uint32_t* status) {
+  grid_dependents_launch();
   constexpr int kCodeU4 = kDqk / 16;  // 36 granules of 16 codes
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);

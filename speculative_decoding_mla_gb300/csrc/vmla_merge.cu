@@ -28,6 +28,8 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
   // block = one merge row; warp c = its columns 4 * (32 c + lane) .. + 3
   const int c = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched to start under the verify kernel's tail: its partials first
+  grid_dependency_wait();
   const int mrow = blockIdx.x;
   if (mrow >= plan.merge_rows) return;
   // sequence owning merge row mrow: last b with merge_off <= mrow
@@ -138,9 +140,16 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32
 int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
                  uint16_t* out, float* lse, void* stream) {
   if (plan.merge_rows == 0) return VMLA_OK;
-  merge_kernel<<<plan.merge_rows, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, lse_is_log2, out,
-                                                                       lse);
-  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {early_start_attribute()};
+  cfg.gridDim = dim3(plan.merge_rows, 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel, plan, part_o, part_lse, lse_is_log2, out, lse) != cudaSuccess)
+    return VMLA_ERR_CUDA;
+  return VMLA_OK;
 }
 
 int launch_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_q, uint64_t* mask_out,
@@ -155,8 +164,16 @@ int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* pa
                        uint16_t* out, float* lse, void* stream) {
   if (max_rows <= 0) return VMLA_OK;
   if (max_rows > INT32_MAX) return VMLA_ERR_SHAPE;
-  merge_kernel_dplan<<<(int)max_rows, kMergeWarps * 32, 0, (cudaStream_t)stream>>>(plan, part_o, part_lse, out, lse);
-  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {early_start_attribute()};
+  cfg.gridDim = dim3((unsigned)max_rows, 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel_dplan, plan, part_o, part_lse, out, lse) != cudaSuccess)
+    return VMLA_ERR_CUDA;
+  return VMLA_OK;
 }
 
 int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,

@@ -34,7 +34,7 @@ VMLA_HD PlanShape plan_shape(int kernel) {
     s.rows_per_unit = 256;
     s.units_per_sm = 2;  // per cluster of four SMs; the caller divides the SM count
     s.key_align = 128;   // the kernel's tile
-    s.min_chunk = 1024;
+    s.min_chunk = 128;   // one tile: a small workload is spread over every cluster
     s.max_splits = 64;
   }
   return s;

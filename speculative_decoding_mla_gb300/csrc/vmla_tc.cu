@@ -281,6 +281,8 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   const uint32_t pair_bytes = scorer ? 2u * kChunks * kKBox : 2u * kVChunksCta * kKBox;
   int it = 0;  // loads issued (tiles for the scorer, messages for the mixer)
   bool ok = true;
+  // the kernel may start under the gather's tail: the staged rows are complete past this wait
+  grid_dependency_wait();
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
     const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
@@ -403,6 +405,9 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
   const uint32_t qfull_r = mapa(smem_u32(&sm.c.qfull), 0);
   int it = 0, uu = 0, msg = 0;
   bool stop = false;
+  // q and the ancestor masks are read only once everything before the kernel in the
+  // stream is complete (the kernel may start under the gather's tail)
+  grid_dependency_wait();
   for (int ui_idx = u_begin; ui_idx < u_end && !stop; ++ui_idx, ++uu) {
     const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
     const SeqPlan& sp = plan.seq[ui.b];
@@ -952,6 +957,9 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // this CTA's work is done: the merge may be scheduled as CTAs retire (it waits
+  // for the whole grid before it reads the partials)
+  grid_dependents_launch();
   __syncwarp();
   // no CTA leaves while another may still address its shared or tensor memory.
   // Past this barrier no thread of the cluster issues anything.  On the normal
@@ -1010,7 +1018,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
-cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
+// attr: room for two attributes (the cluster shape, and an early start under
+// the previous kernel's tail when `early` is set)
+cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr, bool early = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kClusterCtas * clusters, 1, 1);
   cfg.blockDim = dim3(kThreadsTC, 1, 1);
@@ -1019,8 +1029,9 @@ cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
   attr[0].val.clusterDim.x = kClusterCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  if (early) attr[1] = early_start_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early ? 2 : 1;
   return cfg;
 }
 
@@ -1078,8 +1089,8 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     const int u1 = plan.total_units - u0 < kMaxTcUnits ? plan.total_units : u0 + kMaxTcUnits;
     rc = build_tc_schedule(plan, clusters < u1 - u0 ? clusters : u1 - u0, u0, u1, &sched);
     if (rc != VMLA_OK) return rc;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr, true);
     cfg.stream = (cudaStream_t)stream;
     if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   }
@@ -1096,8 +1107,8 @@ int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, 
   // the map spans the staged area's capacity; the planned keys lie inside it
   CUtensorMap kmap;
   if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys)) return VMLA_ERR_CUDA;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config(clusters, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config(clusters, attr, true);
   cfg.stream = (cudaStream_t)stream;
   if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
   return VMLA_OK;
