@@ -127,6 +127,7 @@ struct MixerSmem {
   uint8_t v[kVStages][kVChunksCta][kKBox];  // this CTA's value columns of one message's 64 keys
   PMsg msg[kPSlots];                 // P receive slots
   Finals fin[2];                     // per-unit finals receive slots
+  float4 ep[4][32][8];               // epilogue: each warp's 32 rows x 32 columns (16-byte XOR swizzle)
 };
 
 struct Ctl {
@@ -815,37 +816,63 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
       if (sp.n_split == 1) {
         const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
-        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kDv);
+        // as for the partials below: two 32-column chunks (128 bytes of bf16 per row)
+        // at a time through the warp's tile, whole rows per store instruction
+        uint4(*tile)[8] = reinterpret_cast<uint4(*)[8]>(M.ep[wq]);
+        const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
+        const int64_t orow_w = (int64_t)sp.q_off * H + r_w;
+        const int sub = lane >> 3, k4 = lane & 7;
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
-          tmem_wait_ld();
-          if (valid) {
+        for (int c = 0; c < kDv / 32; c += 2) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_base + (uint32_t)((c + h) * 32), v);
+            tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              dst[c * 4 + k] = make_uint4(
+              tile[lane][(4 * h + k) ^ (lane & 7)] = make_uint4(
                   pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
                   pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
           }
           __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + sub;
+            if (r_w + rr < ui.R)
+              reinterpret_cast<uint4*>(a.out + (orow_w + rr) * kDv + c * 32)[k4] = tile[rr][k4 ^ (rr & 7)];
+          }
+          __syncwarp();
         }
         if (valid) a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
       } else {
         const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + (valid ? r : 0);
-        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDv);
+        // Each 32-column chunk of the warp's 32 rows goes through shared memory (row
+        // `lane`'s 16-byte piece k at k ^ (lane & 7), conflict-free both ways), so that
+        // every store instruction writes four whole 128-byte rows instead of one
+        // 16-byte piece of each of 32 rows.
+        float4(*tile)[8] = M.ep[wq];
+        const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
+        const int64_t prow_w = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + r_w;
+        const int sub = lane >> 3, k4 = lane & 7;  // store phase: rows 4i + sub, piece k4
 #pragma unroll 1
         for (int c = 0; c < kDv / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
           tmem_wait_ld();
-          if (valid) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[c * 8 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                                           __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+          for (int k = 0; k < 8; ++k)
+            tile[lane][k ^ (lane & 7)] =
+                make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + sub;
+            if (r_w + rr < ui.R)
+              reinterpret_cast<float4*>(a.part_o + (prow_w + rr) * kDv + c * 32)[k4] = tile[rr][k4 ^ (rr & 7)];
           }
           __syncwarp();
         }
