@@ -34,7 +34,8 @@
 // score MMA issuer, rank 1 forwarder of its S-buffer releases to rank 0,
 // rank 2 P V issuer, rank 3 relay of its P arrivals to rank 2; scorer warps
 // 2-9 softmax (two threads per row, 32 keys each per 64-key message), warp 10
-// P sender; mixer warps 2-5 rescale/epilogue, warp 6 P-slot release.
+// P sender; mixer warps 2-5 and 7-10 rescale/epilogue (two warps per TMEM
+// lane quarter, each for half of the value columns), warp 6 P-slot release.
 // Every wait is bounded; on expiry the kernel records VMLA_ERR_TIMEOUT in the
 // status word, tells the other CTAs to stop, and every CTA leaves only after
 // what was issued into it has landed (see the end of tc_verify_body), frees
@@ -79,10 +80,10 @@ enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 // each hand-off for the first kTraceTiles tiles of cluster 0.
 #ifdef VMLA_TRACE
 constexpr int kTraceTiles = 256;
-constexpr int kTraceEvents = 20;
+constexpr int kTraceEvents = 32;
 __device__ uint64_t g_vmla_trace[kTraceEvents * kTraceTiles];
 __device__ __forceinline__ void vtrace(int ev, int tile) {
-  if (cluster_id_x() == 0 && tile < kTraceTiles) {
+  if (cluster_id_x() == 0 && ev >= 0 && ev < kTraceEvents && tile >= 0 && tile < kTraceTiles) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     g_vmla_trace[ev * kTraceTiles + tile] = t;
@@ -127,7 +128,7 @@ struct MixerSmem {
   uint8_t v[kVStages][kVChunksCta][kKBox];  // this CTA's value columns of one message's 64 keys
   PMsg msg[kPSlots];                 // P receive slots
   Finals fin[2];                     // per-unit finals receive slots
-  float4 ep[4][32][8];               // epilogue: each warp's 32 rows x 32 columns (16-byte XOR swizzle)
+  uint4 ep[8][32][4];                // epilogue: each warp's 32 rows x 64 bytes (16-byte granules, swizzled)
 };
 
 struct Ctl {
@@ -707,7 +708,11 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
       VTRACE(8, it);
     }
     if (!ok) break;
-    if (!quiesce() || !command(kCmdEpilogue)) ok = false;
+    // the epilogue group waits for this commit itself, so the command travels
+    // while the unit's last products finish
+    mma_commit_pair(&sm.c.obar, kMixerMask);
+    ++obn;
+    if (!command(kCmdEpilogue)) ok = false;
   }
   if (!ok) {
     // after a failed wait: the last commit goes to this CTA only and is waited for
@@ -746,14 +751,23 @@ __device__ void mixer_release_role(TcSmem& sm, const RunArgs& a, int total_msgs,
   }
 }
 
-// ------------------------------------------------------------------ ranks 2,3: rescale / epilogue (warps 2-5)
+// ------------------------------------------------------------------ ranks 2,3: rescale / epilogue (warps 2-5, 7-10)
+// Two groups of four warps, one warp of each per TMEM lane quarter; group g
+// owns value columns [256g, 256g + 256).  Thread 0 of group 0 takes each
+// command and broadcasts it to the 256 threads.
+constexpr int kEpiThreads = 256;
+__device__ __forceinline__ int epi_gran(int row, int k) { return k ^ ((row >> 1) & 3); }  // conflict-free both ways
+
 __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
                                     uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp >= 7 ? 1 : 0;
   const int wq = warp & 3;
   const int row = wq * 32 + lane;
-  const int tid = threadIdx.x - 64;
+  const int tid = grp ? threadIdx.x - 224 + 128 : threadIdx.x - 64;
+  const int ew = grp * 4 + (warp - (grp ? 7 : 2));  // epilogue warp 0..7 (its staging tile)
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t col0 = (uint32_t)grp * (kDv / 2);
   const int H = plan.num_heads;
   MixerSmem& M = sm.u.m;
   const uint32_t lead_cmd_done = mapa(smem_u32(&sm.c.cmd_done), 2);
@@ -783,7 +797,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       sm.c.wg_cmd = cmd;
     }
     ++cmdn;
-    named_bar_sync(2, 128);
+    named_bar_sync(2, kEpiThreads);
     const uint32_t cmd = sm.c.wg_cmd;
     if ((cmd & 0xFF) == kCmdExit) return;
     __syncwarp();
@@ -794,18 +808,22 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const float alpha = M.msg[s].alpha[row];
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
+        for (int c = 0; c < kDv / 64; ++c) {
+          const uint32_t col = col0 + (uint32_t)(c * 32);
           uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_ld32(tbase + lane_base + col, v);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-          tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_st32(tbase + lane_base + col, v);
         }
         tmem_wait_st();
       }
     } else {
-      // epilogue of unit ui_idx: O / l -> output row (or fp32 partial)
+      // epilogue of unit ui_idx: O / l -> output row (or fp32 partial).  Each chunk
+      // of the warp's 32 rows goes through its shared-memory tile so that every
+      // store instruction writes eight rows' 64 contiguous bytes instead of one
+      // 16-byte piece of each of 32 rows.
       const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
       const SeqPlan& sp = plan.seq[ui.b];
       const int f = uu & 1;
@@ -814,75 +832,66 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const bool valid = r < ui.R;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
+      uint4(*tile)[4] = M.ep[ew];
+      const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
+      const int sub = lane >> 2, k4 = lane & 3;  // store phase: rows 8i + sub, granule k4
       if (sp.n_split == 1) {
         const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
-        // as for the partials below: two 32-column chunks (128 bytes of bf16 per row)
-        // at a time through the warp's tile, whole rows per store instruction
-        uint4(*tile)[8] = reinterpret_cast<uint4(*)[8]>(M.ep[wq]);
-        const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
         const int64_t orow_w = (int64_t)sp.q_off * H + r_w;
-        const int sub = lane >> 3, k4 = lane & 7;
 #pragma unroll 1
-        for (int c = 0; c < kDv / 32; c += 2) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_base + (uint32_t)((c + h) * 32), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tile[lane][(4 * h + k) ^ (lane & 7)] = make_uint4(
-                  pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                  pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                  pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                  pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + sub;
-            if (r_w + rr < ui.R)
-              reinterpret_cast<uint4*>(a.out + (orow_w + rr) * kDv + c * 32)[k4] = tile[rr][k4 ^ (rr & 7)];
-          }
-          __syncwarp();
-        }
-        if (valid) a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
-      } else {
-        const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + (valid ? r : 0);
-        // Each 32-column chunk of the warp's 32 rows goes through shared memory (row
-        // `lane`'s 16-byte piece k at k ^ (lane & 7), conflict-free both ways), so that
-        // every store instruction writes four whole 128-byte rows instead of one
-        // 16-byte piece of each of 32 rows.
-        float4(*tile)[8] = M.ep[wq];
-        const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
-        const int64_t prow_w = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + r_w;
-        const int sub = lane >> 3, k4 = lane & 7;  // store phase: rows 4i + sub, piece k4
-#pragma unroll 1
-        for (int c = 0; c < kDv / 32; ++c) {
+        for (int c = 0; c < kDv / 64; ++c) {  // 32 columns = 64 bytes of bf16 per row
+          const uint32_t col = col0 + (uint32_t)(c * 32);
           uint32_t v[32];
-          tmem_ld32(tbase + lane_base + (uint32_t)(c * 32), v);
+          tmem_ld32(tbase + lane_base + col, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            tile[lane][k ^ (lane & 7)] =
-                make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+          for (int k = 0; k < 4; ++k)
+            tile[lane][epi_gran(lane, k)] = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
+                pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
           __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + sub;
+          for (int i = 0; i < 4; ++i) {
+            const int rr = 8 * i + sub;
             if (r_w + rr < ui.R)
-              reinterpret_cast<float4*>(a.part_o + (prow_w + rr) * kDv + c * 32)[k4] = tile[rr][k4 ^ (rr & 7)];
+              reinterpret_cast<uint4*>(a.out + (orow_w + rr) * kDv + col)[k4] = tile[rr][epi_gran(rr, k4)];
           }
           __syncwarp();
         }
-        if (valid) a.part_lse[prow] = lse2;
+        if (valid && grp == 0) a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
+      } else {
+        const int64_t prow = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + (valid ? r : 0);
+        const int64_t prow_w = (int64_t)sp.part_off + (int64_t)ui.piece * ui.R + r_w;
+#pragma unroll 1
+        for (int c = 0; c < kDv / 32; ++c) {  // 16 columns = 64 bytes of fp32 per row
+          const uint32_t col = col0 + (uint32_t)(c * 16);
+          uint32_t v[16];
+          tmem_ld16(tbase + lane_base + col, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tile[lane][epi_gran(lane, k)] = make_uint4(__float_as_uint(__uint_as_float(v[4 * k]) * inv),
+                                                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * inv),
+                                                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * inv),
+                                                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * inv));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = 8 * i + sub;
+            if (r_w + rr < ui.R)
+              reinterpret_cast<uint4*>(a.part_o + (prow_w + rr) * kDv + col)[k4] = tile[rr][epi_gran(rr, k4)];
+          }
+          __syncwarp();
+        }
+        if (valid && grp == 0) a.part_lse[prow] = lse2;
       }
       ++uu;
       ++ui_idx;
     }
     tc_fence_before();
-    named_bar_sync(2, 128);
+    named_bar_sync(2, kEpiThreads);
     if (tid == 0) {
       // a finals buffer is re-armed for the unit two ahead once it has been read,
       // then handed back to the scorer
@@ -972,14 +981,16 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
       else if (rank == 3) mixer_relay_role(sm, a, total_msgs);
       else scorer_forward_role(sm, a, n_tiles_all);
     }
-  } else if (warp == kSenderWarp) {
-    if (lane == 0 && rank < 2) scorer_sender_role(sm, plan, sched, a, u_begin, u_end, rank);
   } else if (rank < 2) {
-    scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);
-  } else if (warp < 6) {
-    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);
-  } else if (warp == 6 && lane == 0) {
-    mixer_release_role(sm, a, total_msgs, rank);
+    if (warp == kSenderWarp) {
+      if (lane == 0) scorer_sender_role(sm, plan, sched, a, u_begin, u_end, rank);
+    } else {
+      scorer_softmax_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);
+    }
+  } else if (warp == 6) {
+    if (lane == 0) mixer_release_role(sm, a, total_msgs, rank);
+  } else {
+    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);  // warps 2-5 and 7-10
   }
   __syncwarp();
   tc_fence_before();
