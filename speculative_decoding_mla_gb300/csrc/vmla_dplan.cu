@@ -9,6 +9,8 @@
 // planner (vmla_plan_core.h, so both give identical pieces and results), and
 // a cluster schedule for the tensor-core kernel (units sorted by cost, dealt
 // to the clusters in a snake order, then in unit order within each cluster).
+// The piece size is the host planner's choice among the same candidates,
+// scored with the same integer arithmetic, one warp per candidate.
 // The areas of the workspace are sized for caller-given upper bounds on the
 // query and key totals.
 #include <cuda_runtime.h>
@@ -23,6 +25,78 @@ constexpr int kPlanThreads = 1024;
 constexpr int kSortKeys = 4096;  // power of two, at least kMaxTcUnits
 static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
 static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
+static_assert(kPlanThreads / 32 == kChunkCands, "one warp per piece-size candidate");
+static_assert(kChunkCands * kRunsPerSeq * kSearchMaxBatch <= kSortKeys, "candidate runs fit the sort keys");
+
+__device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const int64_t x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = x > v ? x : v;
+  }
+  return v;
+}
+
+// Score of candidate k (plan_pick_chunk_host's, for one warp): the longest
+// cluster load of the snake deal of its units plus the merge's charge, or -1
+// when they exceed one launch.  runs: this warp's kRunsPerSeq * kSearchMaxBatch words, each run
+// packed as cost << 32 | sort position << 16 | count (costs are below 2^32,
+// counts below 2^12 and positions below kMaxTcUnits).
+__device__ int64_t candidate_score(const PlanShape& sh, const int32_t* qo, const int32_t* kv, int batch,
+                                   int num_heads, int clusters, int64_t total_work, int k, uint64_t* runs) {
+  const int ln = threadIdx.x & 31;
+  const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
+  const int R = kRunsPerSeq * batch;
+  int64_t units = 0, part = 0;
+  for (int b = ln; b < batch; b += 32) {
+    int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
+    part += plan_seq_runs(sh, (int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b], num_heads, ct, c2, n2);
+    for (int t = 0; t < kRunsPerSeq; ++t) {
+      runs[kRunsPerSeq * b + t] = ((uint64_t)c2[t] << 32) | (uint64_t)n2[t];
+      units += n2[t];
+    }
+  }
+  units = warp_sum_i64(units);
+  part = warp_sum_i64(part);
+  __syncwarp();
+  if (units > kMaxTcUnits) return -1;
+  // sort positions (each lane holds those of its runs until every lane has read the costs)
+  constexpr int kPerLane = kRunsPerSeq * kSearchMaxBatch / 32;
+  int64_t rank[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int r = ln + 32 * i;
+    rank[i] = 0;
+    if (r < R) {
+      const int64_t cr = (int64_t)(runs[r] >> 32);
+      for (int r2 = 0; r2 < R; ++r2) {
+        const uint64_t x = runs[r2];
+        if (plan_run_before((int64_t)(x >> 32), r2, cr, r)) rank[i] += (int64_t)(x & 0xFFFFu);
+      }
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int r = ln + 32 * i;
+    if (r < R) runs[r] |= (uint64_t)rank[i] << 16;
+  }
+  __syncwarp();
+  int64_t worst = 0;
+  for (int j = ln; j < clusters; j += 32) {
+    int64_t load = 0;
+    for (int r = 0; r < R; ++r) {
+      const uint64_t x = runs[r];
+      const int64_t cost = (int64_t)(x >> 32), pos = (int64_t)((x >> 16) & 0xFFFFu), n = (int64_t)(x & 0xFFFFu);
+      load += cost * (plan_snake_share(pos + n, j, clusters) - plan_snake_share(pos, j, clusters));
+    }
+    worst = load > worst ? load : worst;
+  }
+  return warp_max_i64(worst) + plan_merge_score(part);
+}
 
 // Ascending bitonic sort of the first n keys in shared memory (n a power of
 // two, at most kSortKeys; whole block).
@@ -63,6 +137,8 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   __shared__ uint64_t keys[kSortKeys];
   __shared__ unsigned long long s_work;
   __shared__ int s_bad, s_maxs;
+  __shared__ int64_t s_score[kChunkCands];
+  __shared__ int64_t s_chunk;
   const int tid = threadIdx.x;
   const PlanShape sh = plan_shape(VMLA_KERNEL_TC);
   if (tid == 0) {
@@ -85,7 +161,20 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     atomicOr(&s_bad, 2);
   __syncthreads();
   const bool lengths_ok = s_bad == 0;
-  const int64_t chunk_target = plan_chunk_target(sh, (int64_t)s_work, (int64_t)clusters * sh.units_per_sm);
+  const int64_t total_work = (int64_t)s_work;
+  const bool search = lengths_ok && splits == 0 && batch >= 1 && batch <= kSearchMaxBatch;
+  if (search) {
+    const int w = tid >> 5;
+    const int64_t sc = candidate_score(sh, qo, kv, batch, num_heads, clusters, total_work, w,
+                                       keys + w * (kRunsPerSeq * kSearchMaxBatch));
+    if ((tid & 31) == 0) s_score[w] = sc;
+  }
+  __syncthreads();
+  if (tid == 0)
+    s_chunk = search ? plan_choose_cand(sh, total_work, clusters, s_score)
+                     : plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
+  __syncthreads();
+  const int64_t chunk_target = s_chunk;
   SeqPlan sp = {};
   int64_t u = 0, pr = 0, mr = 0;
   if (tid < batch) {
@@ -173,12 +262,13 @@ DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t 
                          int clusters) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   const PlanShape sh = plan_shape(VMLA_KERNEL_TC);
-  // units are at most slots + (row blocks) with the planner's own piece count
-  // (each sequence's pieces exceed its share of the slots by less than one),
-  // or splits x (row blocks) when the count is forced; 256 partial rows each
+  // units are at most clusters x m / 16 + (row blocks) with the planner's own
+  // piece count (the largest candidate m; each sequence's pieces exceed its
+  // share by less than one), or splits x (row blocks) when the count is
+  // forced; 256 partial rows each
   const int64_t row_blocks = plan_ceil_div(max_total_q * num_heads, sh.rows_per_unit) + batch;
-  const int64_t units =
-      splits > 0 ? (int64_t)splits * row_blocks : (int64_t)clusters * sh.units_per_sm + row_blocks;
+  const int64_t units = splits > 0 ? (int64_t)splits * row_blocks
+                                   : plan_ceil_div((int64_t)clusters * plan_cand_m(kChunkCands - 1), 16) + row_blocks;
   int64_t cap = units * sh.rows_per_unit;
   const int64_t all = max_total_q * num_heads * sh.max_splits;
   if (cap > all) cap = all;

@@ -46,7 +46,10 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   int64_t slots = kernel == VMLA_KERNEL_TC ? (int64_t)clusters * sh.units_per_sm : (int64_t)num_sms * sh.units_per_sm;
   int64_t total_work = 0;  // (row block) x (keys)
   for (int b = 0; b < batch; ++b) total_work += plan_seq_work(sh, qo[b + 1] - qo[b], kv[b + 1] - kv[b], num_heads);
-  const int64_t chunk_target = plan_chunk_target(sh, total_work, slots);
+  // the tensor-core kernel's piece size is chosen by scoring candidate schedules
+  const int64_t chunk_target = kernel == VMLA_KERNEL_TC && splits == 0
+                                   ? plan_pick_chunk_host(sh, batch, num_heads, qo, kv, clusters, total_work)
+                                   : plan_chunk_target(sh, total_work, slots);
 
   int64_t unit = 0, part = 0, merge = 0;
   int max_s = 0;
@@ -90,7 +93,7 @@ int build_tc_schedule(const PlanParams& plan, int num_clusters, int unit_begin, 
   sched->total_units = U;
   sched->unit_base = unit_begin;
   sched->pad = 0;
-  // cost of a unit: its keys plus a fixed charge for filling and draining the pipeline
+  // cost of a unit: its keys plus a fixed charge for the unit's start and end
   struct Item { int64_t cost; int unit; };
   std::vector<Item> items;
   items.reserve(U);

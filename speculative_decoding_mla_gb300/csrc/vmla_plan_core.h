@@ -58,6 +58,19 @@ VMLA_HD int64_t plan_chunk_target(const PlanShape& sh, int64_t total_work, int64
   return per > sh.min_chunk ? per : (int64_t)sh.min_chunk;
 }
 
+// Piece length and count of a sequence of nk >= 1 keys for a chunk target (or
+// a forced count): the length is rounded up to the key alignment, then the
+// count is the one that leaves no piece empty.
+VMLA_HD void plan_pieces(const PlanShape& sh, int64_t nk, int splits, int64_t chunk_target, int64_t* chunk,
+                         int64_t* pieces) {
+  int64_t p = splits > 0 ? (int64_t)splits : plan_ceil_div(nk, chunk_target);
+  if (p > sh.max_splits) p = sh.max_splits;
+  if (p < 1) p = 1;
+  const int64_t c = plan_ceil_div(plan_ceil_div(nk, p), sh.key_align) * sh.key_align;
+  *chunk = c;
+  *pieces = plan_ceil_div(nk, c);
+}
+
 // Pieces of one sequence: fills n_rb, n_split and chunk of `s` (whose kv/q
 // lengths are set) and returns its units; *part_rows / *merge_rows receive the
 // fp32 partial rows and merge rows it needs.
@@ -73,12 +86,8 @@ VMLA_HD int64_t plan_split_seq(const PlanShape& sh, SeqPlan& s, int num_heads, i
   }
   const int64_t rows = (int64_t)s.n_q * num_heads;
   s.n_rb = (int32_t)plan_ceil_div(rows, sh.rows_per_unit);
-  int64_t pieces = splits > 0 ? (int64_t)splits : plan_ceil_div(s.n_kv, chunk_target);
-  if (pieces > sh.max_splits) pieces = sh.max_splits;
-  if (pieces < 1) pieces = 1;
-  // piece length rounded to the key alignment, then the count that leaves no piece empty
-  const int64_t chunk = plan_ceil_div(plan_ceil_div(s.n_kv, pieces), sh.key_align) * sh.key_align;
-  pieces = plan_ceil_div(s.n_kv, chunk);
+  int64_t chunk = 0, pieces = 0;
+  plan_pieces(sh, s.n_kv, splits, chunk_target, &chunk, &pieces);
   s.chunk = (int32_t)chunk;
   s.n_split = (int32_t)pieces;
   if (pieces > 1) {
@@ -88,13 +97,132 @@ VMLA_HD int64_t plan_split_seq(const PlanShape& sh, SeqPlan& s, int num_heads, i
   return (int64_t)s.n_rb * pieces;
 }
 
-// Cost of a tensor-core work unit for the cluster schedule: its keys plus a
-// fixed charge for filling and draining the pipeline.
+// ---------------------------------------------------------------- piece size of the tensor-core kernel
+// A unit's cost for the cluster schedule: its keys plus a fixed charge for
+// loading Q, filling and draining the pipeline and writing the result (about
+// five 128-key tiles' time, measured on the verify kernel).
+constexpr int64_t kUnitFixedKeys = 640;
+
 VMLA_HD int64_t plan_unit_cost(const SeqPlan& s, int unit) {
   const int64_t piece = (unit - s.unit_start) / s.n_rb;
   const int64_t lo = piece * s.chunk;
   const int64_t hi = lo + s.chunk < s.n_kv ? lo + s.chunk : (int64_t)s.n_kv;
-  return (hi - lo) + 256;
+  return (hi - lo) + kUnitFixedKeys;
+}
+
+// The planner picks the chunk target among kChunkCands candidates: candidate k
+// aims at m_k / 16 units per cluster on average (m from 12 to 192; candidate
+// kDefaultCand, m = 32, is two units per cluster).  Each candidate's units are
+// scored by the longest cluster load of a snake deal of the units sorted by
+// cost, plus the merge: its fp32 partial rows are written and read back at
+// about a twentieth of a key's time each, and a merge launch costs a tile.  A
+// candidate replaces the default only if it scores at least 3 % lower.
+// Batches of more than kSearchMaxBatch sequences keep the default.
+constexpr int kChunkCands = 32;
+constexpr int kDefaultCand = 10;
+constexpr int kSearchMaxBatch = 64;
+constexpr int kRunsPerSeq = 2;  // a sequence's units: its full pieces and its last piece
+constexpr int64_t kMergeRowsPerKey = 20;
+constexpr int64_t kMergeLaunchKeys = 128;
+
+VMLA_HD int64_t plan_merge_score(int64_t partial_rows) {
+  return partial_rows / kMergeRowsPerKey + (partial_rows > 0 ? kMergeLaunchKeys : 0);
+}
+
+VMLA_HD int plan_cand_m(int k) {
+  if (k < 10) return 12 + 2 * k;            // 12 .. 30
+  if (k < 20) return 32 + 4 * (k - 10);     // 32 .. 68
+  if (k < 28) return 72 + 8 * (k - 20);     // 72 .. 128
+  return 144 + 16 * (k - 28);               // 144 .. 192
+}
+
+VMLA_HD int64_t plan_cand_chunk(const PlanShape& sh, int64_t total_work, int clusters, int k) {
+  const int64_t ct = plan_ceil_div((total_work > 1 ? total_work : 1) * 16, (int64_t)clusters * plan_cand_m(k));
+  return ct > sh.min_chunk ? ct : (int64_t)sh.min_chunk;
+}
+
+// The two runs of equal-cost units of one sequence under a chunk target:
+// cost[0] x count[0] full pieces, cost[1] x count[1] last pieces (counts 0 for
+// a sequence without queries); returns the sequence's fp32 partial rows.
+VMLA_HD int64_t plan_seq_runs(const PlanShape& sh, int64_t nq, int64_t nk, int num_heads, int64_t chunk_target,
+                              int64_t (&cost)[kRunsPerSeq], int64_t (&count)[kRunsPerSeq]) {
+  cost[0] = cost[1] = 0;
+  count[0] = count[1] = 0;
+  if (nq == 0) return 0;
+  const int64_t rb = plan_ceil_div(nq * num_heads, sh.rows_per_unit);
+  int64_t chunk = 0, pieces = 0;
+  plan_pieces(sh, nk, 0, chunk_target, &chunk, &pieces);
+  cost[0] = chunk + kUnitFixedKeys;
+  count[0] = rb * (pieces - 1);
+  cost[1] = nk - (pieces - 1) * chunk + kUnitFixedKeys;
+  count[1] = rb;
+  return pieces > 1 ? nq * num_heads * pieces : 0;
+}
+
+// Units at positions p < x of a snake deal over C clusters (positions
+// 0..C-1 go to clusters 0..C-1, positions C..2C-1 to clusters C-1..0, and so
+// on) that land on cluster j.
+VMLA_HD int64_t plan_snake_share(int64_t x, int j, int C) {
+  const int64_t period = 2 * (int64_t)C;
+  const int64_t rem = x % period;
+  return 2 * (x / period) + (rem > j ? 1 : 0) + (rem > period - 1 - j ? 1 : 0);
+}
+
+// Sort position of run r among runs sorted by cost (descending), ties by run
+// index: the units of all runs that come before it.
+VMLA_HD bool plan_run_before(int64_t cost_a, int a, int64_t cost_b, int b) {
+  return cost_a > cost_b || (cost_a == cost_b && a < b);
+}
+
+// The chosen chunk target from the candidates' scores (-1: not a candidate).
+VMLA_HD int64_t plan_choose_cand(const PlanShape& sh, int64_t total_work, int clusters, const int64_t* score) {
+  int best = -1;
+  for (int k = 0; k < kChunkCands; ++k)
+    if (score[k] >= 0 && (best < 0 || score[k] < score[best])) best = k;
+  const int64_t d = score[kDefaultCand];
+  if (best < 0 || (d >= 0 && !(score[best] * 100 < d * 97))) best = kDefaultCand;
+  return plan_cand_chunk(sh, total_work, clusters, best);
+}
+
+// Host form of the choice (the device planner evaluates the same scores, one
+// warp per candidate, with the same integer arithmetic).
+inline int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_heads, const int32_t* qo,
+                                    const int32_t* kv, int clusters, int64_t total_work) {
+  const int64_t def = plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
+  if (batch > kSearchMaxBatch || batch < 1 || clusters < 1) return def;
+  const int R = kRunsPerSeq * batch;
+  int64_t cost[kRunsPerSeq * kSearchMaxBatch], count[kRunsPerSeq * kSearchMaxBatch],
+      rank[kRunsPerSeq * kSearchMaxBatch];
+  int64_t score[kChunkCands];
+  for (int k = 0; k < kChunkCands; ++k) {
+    const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
+    int64_t units = 0, part = 0;
+    for (int b = 0; b < batch; ++b) {
+      int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
+      part += plan_seq_runs(sh, (int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b], num_heads, ct, c2, n2);
+      for (int t = 0; t < kRunsPerSeq; ++t) {
+        cost[kRunsPerSeq * b + t] = c2[t];
+        count[kRunsPerSeq * b + t] = n2[t];
+        units += n2[t];
+      }
+    }
+    score[k] = -1;  // not a candidate: more units than one launch holds
+    if (units > kMaxTcUnits) continue;
+    for (int r = 0; r < R; ++r) {
+      rank[r] = 0;
+      for (int r2 = 0; r2 < R; ++r2)
+        if (plan_run_before(cost[r2], r2, cost[r], r)) rank[r] += count[r2];
+    }
+    int64_t worst = 0;
+    for (int j = 0; j < clusters; ++j) {
+      int64_t load = 0;
+      for (int r = 0; r < R; ++r)
+        load += cost[r] * (plan_snake_share(rank[r] + count[r], j, clusters) - plan_snake_share(rank[r], j, clusters));
+      worst = load > worst ? load : worst;
+    }
+    score[k] = worst + plan_merge_score(part);
+  }
+  return plan_choose_cand(sh, total_work, clusters, score);
 }
 
 }  // namespace vmla

@@ -268,9 +268,10 @@ def test_plan_rejects_bad_shapes(B):
 
 def test_plan_units_within_the_device_plan_bound(B):
     """The device-planned call sizes its partial area for caller bounds before any length is known:
-    with C clusters (two units each) the automatic plan makes at most 2C units plus one per row
-    block, each of 256 rows, and never more than 64 pieces of every query row.  The host planner
-    runs the same split arithmetic; check that bound on random length sets."""
+    with C clusters the automatic plan makes at most 12C units (its largest candidate aims at 12
+    units per cluster) plus one per row block, each of 256 rows, and never more than 64 pieces of
+    every query row.  The host planner runs the same split arithmetic; check that bound on random
+    length sets."""
     rng = np.random.default_rng(7)
     for trial in range(300):
         batch = int(rng.integers(1, 40))
@@ -281,8 +282,8 @@ def test_plan_units_within_the_device_plan_bound(B):
         info, per, qo, kv = _plan(B, 0, prefixes.tolist(), drafts.tolist(), H=H, sms=4 * clusters)
         rows = int(qo[-1]) * H
         row_blocks = -(-rows // 256) + batch
-        cap = min(256 * (2 * clusters + row_blocks), rows * 64)
-        assert info.num_units <= 2 * clusters + row_blocks
+        cap = min(256 * (12 * clusters + row_blocks), rows * 64)
+        assert info.num_units <= 12 * clusters + row_blocks
         assert info.partial_rows <= cap
     # forced piece counts: at most `splits` pieces of every row block
     for splits in (1, 3, 17, 64):
@@ -340,3 +341,89 @@ def test_prepared_call_marshals_once_and_reports_errors(B):
     with pytest.raises(B.VmlaError) as e:
         bad()
     assert e.value.status == B.VMLA_ERR_SHAPE
+
+
+def _piece_rule(qo, kv, H, clusters, search=True):
+    """The tensor-core planner's piece-size rule, stated on its own: candidate k aims at m_k / 16
+    units per cluster (chunk target ceil(16 W / (C m_k)), at least one 128-key tile); a sequence of
+    N keys gets ceil(N / target) pieces (at most 64), of a length rounded up to 128 keys; a unit
+    costs its keys plus 640; a candidate's score is the longest cluster load when its units, sorted
+    by cost (longest first), are dealt to the clusters in a snake order, plus a twentieth of a key
+    per fp32 partial row (query rows x pieces of every split sequence) and 128 keys when there is
+    any; the best-scoring candidate
+    replaces the default (m = 32) only when it scores at least 3 % lower; more than 64 sequences,
+    or more than 3072 units, leave the candidate set."""
+    ms = [12 + 2 * k for k in range(10)] + [32 + 4 * k for k in range(10)] + \
+         [72 + 8 * k for k in range(8)] + [144 + 16 * k for k in range(4)]
+    B = len(qo) - 1
+    nq = [int(qo[b + 1] - qo[b]) for b in range(B)]
+    nk = [int(kv[b + 1] - kv[b]) for b in range(B)]
+    rb = [-(-q * H // 256) for q in nq]
+    W = sum(r * n for r, n, q in zip(rb, nk, nq) if q)
+
+    def pieces(target):
+        out = []
+        for q, n in zip(nq, nk):
+            if q == 0:
+                out.append((1, max(n, 1)))
+                continue
+            p = min(max(-(-n // target), 1), 64)
+            ch = -(-(-(-n // p)) // 128) * 128
+            out.append((-(-n // ch), ch))
+        return out
+
+    def target(m):
+        return max(128, -(-max(W, 1) * 16 // (clusters * m)))
+
+    def score(m):
+        costs = []
+        part = 0
+        for (p, ch), q, r, n in zip(pieces(target(m)), nq, rb, nk):
+            if q == 0:
+                continue
+            for s in range(p):
+                costs += [min(ch, n - s * ch) + 640] * r
+            if p > 1:
+                part += q * H * p
+        if len(costs) > 3072:
+            return None
+        load = [0] * clusters
+        for i, c in enumerate(sorted(costs, reverse=True)):
+            rnd, j = divmod(i, clusters)
+            load[clusters - 1 - j if rnd % 2 else j] += c
+        return max(load) + part // 20 + (128 if part else 0)
+
+    m_def = 32
+    if search and B <= 64:
+        scores = [(score(m), k) for k, m in enumerate(ms)]
+        valid = [(s, k) for s, k in scores if s is not None]
+        d = scores[ms.index(m_def)][0]
+        if valid:
+            s_best, k_best = min(valid)
+            if d is None or s_best * 100 < d * 97:
+                return [p for p, _ in pieces(target(ms[k_best]))]
+    return [p for p, _ in pieces(target(m_def))]
+
+
+def test_tc_piece_size_rule(B):
+    """The host planner's per-sequence piece counts equal the rule stated independently above, on
+    the ragged workload shapes and random length sets (the device planner runs the same integer
+    arithmetic; its plans are compared bit for bit with the host's on the GPU)."""
+    rng = np.random.default_rng(13)
+    shapes = [([4096, 8192, 16384, 32768], [16] * 4, 64, 36), ([185000], [16], 64, 36),
+              ([32768] * 8, [64] * 8, 64, 36), ([1024], [16], 64, 36)]
+    for t in range(120):
+        b = int(rng.integers(1, 70))
+        prefixes = np.where(rng.random(b) < 0.3, rng.integers(0, 3000, b), rng.integers(0, 120000, b)).tolist()
+        drafts = rng.integers(0, 65, b).tolist()
+        shapes.append((prefixes, drafts, int(rng.choice([8, 16, 64, 128])), int(rng.integers(1, 40))))
+    for prefixes, drafts, H, clusters in shapes:
+        info, per, qo, kv = _plan(B, 0, prefixes, drafts, H=H, sms=4 * clusters)
+        want = _piece_rule(qo, kv, H, clusters)
+        got = [int(p) for p in per]
+        for b in range(len(drafts)):
+            if drafts[b] > 0:
+                assert got[b] == want[b], (prefixes, drafts, H, clusters, b)
+    # the ragged four-sequence batch leaves the default (two units per cluster)
+    info, per, qo, kv = _plan(B, 0, [4096, 8192, 16384, 32768], [16] * 4, H=64, sms=144)
+    assert [int(p) for p in per] != _piece_rule(qo, kv, 64, 36, search=False)
