@@ -133,6 +133,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
+  a.out_rows = (int64_t)total_q * num_heads;
+  a.part_rows = plan.partial_rows;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
   a.staged = runs ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_pool))
@@ -548,6 +550,8 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
+  a.out_rows = max_total_q * num_heads;
+  a.part_rows = L.part_cap;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
   a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);

@@ -108,6 +108,8 @@ struct RunArgs {
   float sm_scale;
   uint16_t* out;
   float* lse;
+  int64_t out_rows;         // rows of out and lse (query rows x heads, or their bound)
+  int64_t part_rows;        // rows of part_o and part_lse (or their bound)
   float* part_o;
   float* part_lse;  // log2 domain
   uint16_t* staged; // contiguous copy of the gathered KV rows, [total_kv, 576] (tensor-core kernel),

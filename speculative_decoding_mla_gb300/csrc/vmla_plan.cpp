@@ -14,6 +14,100 @@
 
 namespace vmla {
 
+// Host form of the piece-size choice.  The device planner scores each
+// candidate with the closed form per (run, cluster) pair; here the runs are
+// sorted once and the snake shares are summed by residue, which gives the
+// same integer scores in O(R log R + C) per candidate:
+//   load_j = sum_r cost_r (F_j(end_r) - F_j(start_r)),
+//   F_j(x) = 2 floor(x / 2C) + [x mod 2C > j] + [x mod 2C > 2C - 1 - j],
+// so load_j = K + S(j) + S(2C - 1 - j) with K the whole-period part and S(x)
+// the sum over residues v > x of (cost at end residue v) - (cost at start residue v).
+static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_heads, const int32_t* qo,
+                                    const int32_t* kv, int clusters, int64_t total_work) {
+  const int64_t def = plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
+  if (batch > kSearchMaxBatch || batch < 1 || clusters < 1) return def;
+  const int R = kRunsPerSeq * batch;
+  const int64_t period = 2 * (int64_t)clusters;
+  int64_t nq[kSearchMaxBatch], nk[kSearchMaxBatch];
+  for (int b = 0; b < batch; ++b) {
+    nq[b] = (int64_t)qo[b + 1] - qo[b];
+    nk[b] = (int64_t)kv[b + 1] - kv[b];
+  }
+  int64_t cost[kRunsPerSeq * kSearchMaxBatch], count[kRunsPerSeq * kSearchMaxBatch];
+  // sort keys: cost descending, then run index (costs are below 2^32, indexes below 2^8);
+  // each candidate starts from the previous candidate's order, which changes little
+  uint64_t key[kRunsPerSeq * kSearchMaxBatch];
+  for (int r = 0; r < R; ++r) key[r] = (uint64_t)r;
+  std::vector<int64_t> resid(period + 1);
+  int64_t score[kChunkCands];
+  int64_t prev_ct = -1;
+  for (int k = 0; k < kChunkCands; ++k) {
+    const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
+    if (ct == prev_ct) {  // the same pieces as the previous candidate
+      score[k] = score[k - 1];
+      continue;
+    }
+    prev_ct = ct;
+    int64_t units = 0, part = 0;
+    for (int b = 0; b < batch; ++b) {
+      int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
+      part += plan_seq_runs(sh, nq[b], nk[b], num_heads, ct, c2, n2);
+      for (int t = 0; t < kRunsPerSeq; ++t) {
+        cost[kRunsPerSeq * b + t] = c2[t];
+        count[kRunsPerSeq * b + t] = n2[t];
+        units += n2[t];
+      }
+    }
+    score[k] = -1;  // not a candidate: more units than one launch holds
+    if (units > kMaxTcUnits) continue;
+    for (int i = 0; i < R; ++i) {
+      const int r = (int)(key[i] & 0xFFu);
+      key[i] = ((uint64_t)(0xFFFFFFFFll - cost[r]) << 8) | (uint64_t)r;
+    }
+    for (int i = 1; i < R; ++i) {
+      const uint64_t x = key[i];
+      int j = i - 1;
+      while (j >= 0 && key[j] > x) {
+        key[j + 1] = key[j];
+        --j;
+      }
+      key[j + 1] = x;
+    }
+    std::fill(resid.begin(), resid.end(), 0);
+    // positions as quotient and residue modulo the period, advanced run by run
+    int64_t whole = 0, q_lo = 0, r_lo = 0;
+    for (int i = 0; i < R; ++i) {
+      const int r = (int)(key[i] & 0xFFu);
+      if (count[r] == 0) continue;
+      const int64_t n = count[r];
+      int64_t q_hi = q_lo + (n >= period ? n / period : 0), r_hi = r_lo + (n >= period ? n % period : n);
+      if (r_hi >= period) {
+        r_hi -= period;
+        ++q_hi;
+      }
+      whole += cost[r] * 2 * (q_hi - q_lo);
+      resid[r_hi] += cost[r];
+      resid[r_lo] -= cost[r];
+      q_lo = q_hi;
+      r_lo = r_hi;
+    }
+    // suffix sums: resid[x] becomes the sum over residues v > x
+    int64_t acc = 0;
+    for (int64_t x = period - 1; x >= 0; --x) {
+      const int64_t v = resid[x];
+      resid[x] = acc;
+      acc += v;
+    }
+    int64_t worst = 0;
+    for (int j = 0; j < clusters; ++j) {
+      const int64_t load = whole + resid[j] + resid[period - 1 - j];
+      worst = load > worst ? load : worst;
+    }
+    score[k] = worst + plan_merge_score(part);
+  }
+  return plan_choose_cand(sh, total_work, clusters, score);
+}
+
 WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   WorkspaceLayout w;

@@ -63,12 +63,16 @@ VMLA_HD int64_t plan_chunk_target(const PlanShape& sh, int64_t total_work, int64
 // count is the one that leaves no piece empty.
 VMLA_HD void plan_pieces(const PlanShape& sh, int64_t nk, int splits, int64_t chunk_target, int64_t* chunk,
                          int64_t* pieces) {
-  int64_t p = splits > 0 ? (int64_t)splits : plan_ceil_div(nk, chunk_target);
-  if (p > sh.max_splits) p = sh.max_splits;
-  if (p < 1) p = 1;
-  const int64_t c = plan_ceil_div(plan_ceil_div(nk, p), sh.key_align) * sh.key_align;
+  // nk < 2^31 (int32 offsets), so every sum and quotient below fits 32 bits
+  const uint32_t n = (uint32_t)nk, align = (uint32_t)sh.key_align;
+  uint32_t p = splits > 0 ? (uint32_t)splits
+               : chunk_target >= nk ? 1u
+                                    : (n + (uint32_t)chunk_target - 1u) / (uint32_t)chunk_target;
+  if (p > (uint32_t)sh.max_splits) p = (uint32_t)sh.max_splits;
+  if (p < 1u) p = 1u;
+  const uint32_t c = ((n + p - 1u) / p + align - 1u) / align * align;
   *chunk = c;
-  *pieces = plan_ceil_div(nk, c);
+  *pieces = (n + c - 1u) / c;
 }
 
 // Pieces of one sequence: fills n_rb, n_split and chunk of `s` (whose kv/q
@@ -149,7 +153,7 @@ VMLA_HD int64_t plan_seq_runs(const PlanShape& sh, int64_t nq, int64_t nk, int n
   cost[0] = cost[1] = 0;
   count[0] = count[1] = 0;
   if (nq == 0) return 0;
-  const int64_t rb = plan_ceil_div(nq * num_heads, sh.rows_per_unit);
+  const int64_t rb = (uint32_t)(nq * num_heads + sh.rows_per_unit - 1) / (uint32_t)sh.rows_per_unit;
   int64_t chunk = 0, pieces = 0;
   plan_pieces(sh, nk, 0, chunk_target, &chunk, &pieces);
   cost[0] = chunk + kUnitFixedKeys;
@@ -182,47 +186,6 @@ VMLA_HD int64_t plan_choose_cand(const PlanShape& sh, int64_t total_work, int cl
   const int64_t d = score[kDefaultCand];
   if (best < 0 || (d >= 0 && !(score[best] * 100 < d * 97))) best = kDefaultCand;
   return plan_cand_chunk(sh, total_work, clusters, best);
-}
-
-// Host form of the choice (the device planner evaluates the same scores, one
-// warp per candidate, with the same integer arithmetic).
-inline int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_heads, const int32_t* qo,
-                                    const int32_t* kv, int clusters, int64_t total_work) {
-  const int64_t def = plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
-  if (batch > kSearchMaxBatch || batch < 1 || clusters < 1) return def;
-  const int R = kRunsPerSeq * batch;
-  int64_t cost[kRunsPerSeq * kSearchMaxBatch], count[kRunsPerSeq * kSearchMaxBatch],
-      rank[kRunsPerSeq * kSearchMaxBatch];
-  int64_t score[kChunkCands];
-  for (int k = 0; k < kChunkCands; ++k) {
-    const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
-    int64_t units = 0, part = 0;
-    for (int b = 0; b < batch; ++b) {
-      int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
-      part += plan_seq_runs(sh, (int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b], num_heads, ct, c2, n2);
-      for (int t = 0; t < kRunsPerSeq; ++t) {
-        cost[kRunsPerSeq * b + t] = c2[t];
-        count[kRunsPerSeq * b + t] = n2[t];
-        units += n2[t];
-      }
-    }
-    score[k] = -1;  // not a candidate: more units than one launch holds
-    if (units > kMaxTcUnits) continue;
-    for (int r = 0; r < R; ++r) {
-      rank[r] = 0;
-      for (int r2 = 0; r2 < R; ++r2)
-        if (plan_run_before(cost[r2], r2, cost[r], r)) rank[r] += count[r2];
-    }
-    int64_t worst = 0;
-    for (int j = 0; j < clusters; ++j) {
-      int64_t load = 0;
-      for (int r = 0; r < R; ++r)
-        load += cost[r] * (plan_snake_share(rank[r] + count[r], j, clusters) - plan_snake_share(rank[r], j, clusters));
-      worst = load > worst ? load : worst;
-    }
-    score[k] = worst + plan_merge_score(part);
-  }
-  return plan_choose_cand(sh, total_work, clusters, score);
 }
 
 }  // namespace vmla

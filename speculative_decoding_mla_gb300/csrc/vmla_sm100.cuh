@@ -337,6 +337,16 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 // One box of a 2-D tensor map into this CTA's shared memory, completing the
 // transaction bytes on an mbarrier of this CTA or of its pair partner
 // (`bar_cluster` from mapa).
+// Tiled 2-D store of one box from this CTA's shared memory (bulk-group
+// completion: bulk_wait_group_read before the box is rewritten, bulk_wait_group
+// before the writes are relied on).  x * element size must be a multiple of 16
+// bytes; y must not be negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
                                                  uint32_t bar_cluster) {
   asm volatile(

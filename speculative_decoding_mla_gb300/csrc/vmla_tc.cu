@@ -419,6 +419,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     // rope part into shared memory; each part writes its share.  The previous
     // unit's MMAs are complete (its last S buffer was observed full).
     __syncwarp();
+    if (tid == 0 && rank == 0) VTRACE(20, uu);  // Q load of unit uu starts
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
 #pragma unroll 1
@@ -443,6 +444,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
+      if (tid == 0 && rank == 0) VTRACE(21, uu);  // Q of unit uu written
       // (the failure test withholds this signal: the score MMAs then never start and a
       // bounded wait expires)
       if (lane == 0 && a.test_fault != kFaultNoQReady) {
@@ -712,7 +714,9 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     // while the unit's last products finish
     mma_commit_pair(&sm.c.obar, kMixerMask);
     ++obn;
+    VTRACE(24, ui_idx - u_begin);  // epilogue command posted
     if (!command(kCmdEpilogue)) ok = false;
+    VTRACE(25, ui_idx - u_begin);  // epilogue done
   }
   if (!ok) {
     // after a failed wait: the last commit goes to this CTA only and is waited for
@@ -758,8 +762,9 @@ __device__ void mixer_release_role(TcSmem& sm, const RunArgs& a, int total_msgs,
 constexpr int kEpiThreads = 256;
 __device__ __forceinline__ int epi_gran(int row, int k) { return k ^ ((row >> 1) & 3); }  // conflict-free both ways
 
-__device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const TcSched& sched, const RunArgs& a,
-                                    uint32_t tbase, int u_begin, int u_end, uint32_t rank) {
+__device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const CUtensorMap* pmap,
+                                    const PlanParams& plan, const TcSched& sched, const RunArgs& a, uint32_t tbase,
+                                    int u_begin, int u_end, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp >= 7 ? 1 : 0;
   const int wq = warp & 3;
@@ -799,7 +804,10 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
     ++cmdn;
     named_bar_sync(2, kEpiThreads);
     const uint32_t cmd = sm.c.wg_cmd;
-    if ((cmd & 0xFF) == kCmdExit) return;
+    if ((cmd & 0xFF) == kCmdExit) {
+      if (lane == 0) bulk_wait_group<0>();  // this warp's output stores are written before the CTA leaves
+      return;
+    }
     __syncwarp();
     tc_fence_after();
     // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform
@@ -820,10 +828,13 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
         tmem_wait_st();
       }
     } else {
+      if (tid == 0 && rank == 2) VTRACE(22, uu);  // epilogue of unit uu starts
       // epilogue of unit ui_idx: O / l -> output row (or fp32 partial).  Each chunk
-      // of the warp's 32 rows goes through its shared-memory tile so that every
-      // store instruction writes eight rows' 64 contiguous bytes instead of one
-      // 16-byte piece of each of 32 rows.
+      // of the warp's 32 rows (64 bytes of each) goes through its shared-memory
+      // tile, laid out as a 64-byte-swizzled box, and leaves as one tiled TMA
+      // store; a group of 32 rows that runs past the unit's rows is stored by the
+      // lanes instead (eight rows' 64 contiguous bytes per instruction), so that
+      // nothing is written past them.
       const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
       const SeqPlan& sp = plan.seq[ui.b];
       const int f = uu & 1;
@@ -833,8 +844,33 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const float lse2 = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
       uint4(*tile)[4] = M.ep[ew];
+      const uint32_t tile_s = smem_u32(&M.ep[ew][0][0]);
       const int r_w = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + wq * 32;  // query row of lane 0
-      const int sub = lane >> 2, k4 = lane & 3;  // store phase: rows 8i + sub, granule k4
+      const bool whole = r_w + 32 <= ui.R;        // all 32 rows of the group belong to the unit
+      const int sub = lane >> 2, k4 = lane & 3;  // lane store phase: rows 8i + sub, granule k4
+      // the tile is rewritten only after the previous store has read it
+      auto tile_free = [&]() {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      };
+      auto tile_out = [&](const CUtensorMap* map, int x, int64_t y, auto* base) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (whole) {
+          if (lane == 0) {
+            tma_store_2d(map, tile_s, x, (int)y);
+            bulk_commit_group();
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = 8 * i + sub;
+            if (r_w + rr < ui.R)
+              reinterpret_cast<uint4*>(base + (y + rr) * kDv + x)[k4] = tile[rr][epi_gran(rr, k4)];
+          }
+          __syncwarp();
+        }
+      };
       if (sp.n_split == 1) {
         const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
         const int64_t orow_w = (int64_t)sp.q_off * H + r_w;
@@ -844,6 +880,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
           uint32_t v[32];
           tmem_ld32(tbase + lane_base + col, v);
           tmem_wait_ld();
+          tile_free();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tile[lane][epi_gran(lane, k)] = make_uint4(
@@ -851,14 +888,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
                 pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
                 pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
                 pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = 8 * i + sub;
-            if (r_w + rr < ui.R)
-              reinterpret_cast<uint4*>(a.out + (orow_w + rr) * kDv + col)[k4] = tile[rr][epi_gran(rr, k4)];
-          }
-          __syncwarp();
+          tile_out(omap, (int)col, orow_w, a.out);
         }
         if (valid && grp == 0) a.lse[orow] = lsum > 0.f ? lse2 * 0.6931471805599453f : -INFINITY;
       } else {
@@ -870,23 +900,18 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
           uint32_t v[16];
           tmem_ld16(tbase + lane_base + col, v);
           tmem_wait_ld();
+          tile_free();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tile[lane][epi_gran(lane, k)] = make_uint4(__float_as_uint(__uint_as_float(v[4 * k]) * inv),
                                                        __float_as_uint(__uint_as_float(v[4 * k + 1]) * inv),
                                                        __float_as_uint(__uint_as_float(v[4 * k + 2]) * inv),
                                                        __float_as_uint(__uint_as_float(v[4 * k + 3]) * inv));
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = 8 * i + sub;
-            if (r_w + rr < ui.R)
-              reinterpret_cast<uint4*>(a.part_o + (prow_w + rr) * kDv + col)[k4] = tile[rr][epi_gran(rr, k4)];
-          }
-          __syncwarp();
+          tile_out(pmap, (int)col, prow_w, a.part_o);
         }
         if (valid && grp == 0) a.part_lse[prow] = lse2;
       }
+      if (tid == 0 && rank == 2) VTRACE(23, uu);  // (thread 0's share of) the epilogue stored
       ++uu;
       ++ui_idx;
     }
@@ -907,7 +932,8 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const PlanParams& plan, const Tc
 
 // The kernel body; `plan` and `sched` are kernel parameters (host-planned
 // calls) or live in the workspace (device-planned calls).
-__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const PlanParams& plan, const TcSched& sched,
+__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CUtensorMap& omap,
+                                               const CUtensorMap& pmap, const PlanParams& plan, const TcSched& sched,
                                                const RunArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -947,6 +973,10 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
     sm.c.wait_cycles = a.wait_cycles;
     fence_mbar_init();
     prefetch_tensormap(&kmap);
+    if (rank >= 2) {
+      prefetch_tensormap(&omap);
+      prefetch_tensormap(&pmap);
+    }
   }
   __syncwarp();
   if (warp == 0) {
@@ -990,7 +1020,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
   } else if (warp == 6) {
     if (lane == 0) mixer_release_role(sm, a, total_msgs, rank);
   } else {
-    mixer_epilogue_role(sm, plan, sched, a, tbase, u_begin, u_end, rank);  // warps 2-5 and 7-10
+    mixer_epilogue_role(sm, &omap, &pmap, plan, sched, a, tbase, u_begin, u_end, rank);  // warps 2-5 and 7-10
   }
   __syncwarp();
   tc_fence_before();
@@ -1020,17 +1050,19 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const Pl
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ PlanParams plan,
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
+                 const __grid_constant__ CUtensorMap pmap, const __grid_constant__ PlanParams plan,
                  const __grid_constant__ TcSched sched, const RunArgs a) {
-  tc_verify_body(kmap, plan, sched, a);
+  tc_verify_body(kmap, omap, pmap, plan, sched, a);
 }
 
 // Same kernel with the plan and the cluster schedule read from the workspace,
 // where the device planner wrote them (stream-capture-safe calls).
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const PlanParams* __restrict__ plan,
+tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
+                       const __grid_constant__ CUtensorMap pmap, const PlanParams* __restrict__ plan,
                        const TcSched* __restrict__ sched, const RunArgs a) {
-  tc_verify_body(kmap, *plan, *sched, a);
+  tc_verify_body(kmap, omap, pmap, *plan, *sched, a);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1053,7 +1085,7 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 3 * sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 // attr: room for two attributes (the cluster shape, and an early start under
@@ -1081,6 +1113,28 @@ bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, 
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output maps of the epilogue: [rows x 512] of bf16 outputs or fp32 partials,
+// boxes of 32 rows x 64 bytes with 64-byte swizzle (the epilogue tiles' layout).
+bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, bool fp32) {
+  cuuint64_t gdim[2] = {(cuuint64_t)kDv, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t gstride[1] = {(cuuint64_t)kDv * (fp32 ? 4 : 2)};
+  cuuint32_t box[2] = {fp32 ? 16u : 32u, 32};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride,
+             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The three maps of a launch; without partial rows the partial map repeats
+// the output map (no unit of such a plan stores partials).
+bool encode_maps(EncodeTiledFn enc, const RunArgs& a, CUtensorMap* kmap, CUtensorMap* omap, CUtensorMap* pmap) {
+  if (!encode_rows(enc, kmap, a.staged, a.total_kv, kHalfKeys)) return false;
+  if (!encode_out(enc, omap, a.out, a.out_rows, false)) return false;
+  if (a.part_rows > 0 && a.part_o) return encode_out(enc, pmap, a.part_o, a.part_rows, true);
+  *pmap = *omap;
+  return true;
 }
 
 }  // namespace
@@ -1118,9 +1172,10 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   if (rc != VMLA_OK) return rc;
   clusters = clusters < kMaxClusters ? clusters : kMaxClusters;
   // 2-D map over the staged rows [total_kv x 576 bf16]: boxes of 64 rows x 64
-  // columns with 128-byte swizzle (scorer half tiles, mixer message chunks)
-  CUtensorMap kmap;
-  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys)) return VMLA_ERR_CUDA;
+  // columns with 128-byte swizzle (scorer half tiles, mixer message chunks),
+  // and the epilogue's output maps
+  CUtensorMap kmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   // units are independent: a plan with more than kMaxTcUnits runs as several launches
   static thread_local TcSched sched;
   for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
@@ -1130,7 +1185,8 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr, true);
     cfg.stream = (cudaStream_t)stream;
-    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, omap, pmap, plan, sched, a) != cudaSuccess)
+      return VMLA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
@@ -1142,13 +1198,15 @@ int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, 
   int rc = tc_max_clusters(&dev_clusters);
   if (rc != VMLA_OK) return rc;
   if (clusters < 1 || clusters > dev_clusters || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
-  // the map spans the staged area's capacity; the planned keys lie inside it
-  CUtensorMap kmap;
-  if (!encode_rows(enc, &kmap, a.staged, a.total_kv, kHalfKeys)) return VMLA_ERR_CUDA;
+  // the maps span the staged, output and partial areas' capacities; the planned
+  // keys and rows lie inside them
+  CUtensorMap kmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(clusters, attr, true);
   cfg.stream = (cudaStream_t)stream;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, plan, sched, a) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, omap, pmap, plan, sched, a) != cudaSuccess)
+    return VMLA_ERR_CUDA;
   return VMLA_OK;
 }
 
