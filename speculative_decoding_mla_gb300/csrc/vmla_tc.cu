@@ -73,6 +73,7 @@ constexpr int kClusterCtas = 4;
 constexpr uint32_t kSCol = 256;        // S buffers at TMEM columns 256 and 384
 constexpr float kTau = 8.0f;           // the running max is raised only when a tile exceeds it by 2^8
 constexpr uint16_t kScorerMask = 0x3, kMixerMask = 0xC;
+constexpr uint32_t kQBytes = 2 * kChunks * kKBox;  // a scorer CTA's 128 Q rows, all 576 columns
 
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
@@ -137,6 +138,7 @@ struct Ctl {
   uint64_t sread[2];            // rank 1: its softmax warps have read S buffer s
   uint64_t staged[kStages], stgfree[kStages];  // scorer: P staging buffer written / free again
   uint64_t qfull;               // Q of both scorer CTAs written (rank 0)
+  uint64_t qland, qfree;        // scorer: a unit's Q landed in the K stages / moved out of them
   uint64_t pfull[kPSlots], pfree[kPSlots], pdone[kPSlots];
   uint64_t finfull[2];          // mixer: unit finals received
   uint64_t finfree[2];          // scorer: the mixer's epilogue has read finals buffer f
@@ -274,14 +276,19 @@ __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched
 // a pair complete their bytes on the even CTA's barrier, which that CTA arms
 // for the pair.  Rows past the piece's end belong to other keys (masked by the
 // softmax) or lie outside the staged rows (zero fill).
-__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanParams& plan, const TcSched& sched,
-                              const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
+// Before each unit's first tile a scorer CTA also loads the unit's Q rows (its
+// 128) through both K stages: latent chunk c of row half h into stage h, chunk
+// c; the rope chunk into qrope.  The softmax warps move the latent part into
+// tensor memory and release the stages (qfree) before the first K tile loads.
+__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const CUtensorMap* qmap, const PlanParams& plan,
+                              const TcSched& sched, const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
   const bool scorer = rank < 2;
   const uint32_t q = rank & 1;
   const uint32_t leader = rank & 2u;
   const int nst = scorer ? 2 : kVStages;
   const uint32_t pair_bytes = scorer ? 2u * kChunks * kKBox : 2u * kVChunksCta * kKBox;
   int it = 0;  // loads issued (tiles for the scorer, messages for the mixer)
+  int uq = 0;  // Q loads issued (scorer)
   bool ok = true;
   // the kernel may start under the gather's tail: the staged rows are complete past this wait
   grid_dependency_wait();
@@ -292,6 +299,29 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
     // (a run outside the pool only reads the out-of-range fill; a check kernel reports it)
     const int row0 = a.run_base ? a.run_base[ui.b] : sp.kv_off;
     const int loads = scorer ? ui.n_tiles : ui.n_tiles * kMsgsPerTile;
+    if (scorer) {
+      // both stages free (the last two tiles' products are complete, and with them
+      // every product that read the previous Q), then Q in, then wait until it has
+      // been moved out; the tile loads below find these releases already complete
+      for (int k = 0; k < 2 && ok; ++k)
+        ok = wait_bar(sm, &sm.c.kfree[(it + k) % 2], (((it + k) / 2) & 1) ^ 1, a.status, 102);
+      if (!ok) break;
+      const int qy = sp.q_off * plan.num_heads + ui.rb * kRowsUnit + (int)q * kRowsCta;
+      const uint32_t qbar = smem_u32(&sm.c.qland);
+      mbar_arrive_expect_tx(&sm.c.qland, kQBytes);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h)
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          const uint32_t dst = c < kQChunks ? smem_u32(&sm.u.s.kv[h][c][0]) : smem_u32(sm.u.s.qrope) + h * kKBox;
+          tma_load_2d(dst, qmap, 64 * c, qy + 64 * h, qbar);
+        }
+      ++uq;
+      if (!wait_bar(sm, &sm.c.qfree, (uq - 1) & 1, a.status, 103)) {
+        ok = false;
+        break;
+      }
+    }
     for (int n = 0; n < loads; ++n) {
       const int s = it % nst;
       if (!wait_bar(sm, &sm.c.kfree[s], ((it / nst) & 1) ^ 1, a.status, 100)) {
@@ -325,6 +355,8 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const PlanPara
   // exit while one is still in flight
   for (int k = 1; k <= nst && it - k >= 0; ++k)
     drain_bar_live(sm, &sm.c.kfree[(it - k) % nst], ((it - k) / nst) & 1, a.status, 121);
+  // and the last Q load has landed (the softmax normally waited for it)
+  if (scorer && uq > 0) drain_bar_live(sm, &sm.c.qland, (uq - 1) & 1, a.status, 122);
 }
 
 // ------------------------------------------------------------------ rank 0: score MMA issuer (warp 1, lane 0)
@@ -415,41 +447,49 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
     const bool valid = r < ui.R;
-    // Q of this unit: latent part into TMEM columns 0..255 (two bf16 per column),
-    // rope part into shared memory; each part writes its share.  The previous
-    // unit's MMAs are complete (its last S buffer was observed full).
+    // Q of this unit, landed by the producer's TMA loads: latent chunk c of this
+    // row in stage (row / 64), chunk c (128-byte swizzled rows) goes to TMEM
+    // columns 32c .. 32c + 31 (two bf16 per column), each part its chunks; rows
+    // past the unit's rows get zeros (also in their rope columns, which the
+    // loads put into qrope).  The previous unit's products are complete (the
+    // producer waited for the last two tiles' releases before loading).
     __syncwarp();
-    if (tid == 0 && rank == 0) VTRACE(20, uu);  // Q load of unit uu starts
+    if (tid == 0 && rank == 0) VTRACE(20, uu);  // Q of unit uu awaited
+    wait_bar(sm, &sm.c.qland, uu & 1, a.status, 305);  // (a failed wait leaves garbage; the stop comes later)
     {
-      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((int64_t)sp.q_off * H + (valid ? r : 0)) * kDqk);
+      const int lr = row & 63;
+      const uint8_t* stage_rows = &S.kv[row >> 6][0][lr * 128];
 #pragma unroll 1
       for (int c = part; c < kQChunks; c += kParts) {
         uint32_t v[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint4 x = valid ? __ldg(qrow + c * 8 + k) : make_uint4(0, 0, 0, 0);
-          v[4 * k] = x.x;
-          v[4 * k + 1] = x.y;
-          v[4 * k + 2] = x.z;
-          v[4 * k + 3] = x.w;
+        for (int g = 0; g < 8; ++g) {
+          const uint4 x = valid ? *reinterpret_cast<const uint4*>(stage_rows + c * kKBox + ((g ^ (lr & 7)) << 4))
+                                : make_uint4(0, 0, 0, 0);
+          v[4 * g] = x.x;
+          v[4 * g + 1] = x.y;
+          v[4 * g + 2] = x.z;
+          v[4 * g + 3] = x.w;
         }
         tmem_st32(tbase + lane_base + (uint32_t)(c * 32), v);
       }
+      if (!valid)
 #pragma unroll
-      for (int g = (8 / kParts) * part; g < (8 / kParts) * (part + 1); ++g) {
-        const uint4 x = valid ? __ldg(qrow + kQChunks * 8 + g) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(S.qrope + row * 128 + ((g ^ (row & 7)) << 4)) = x;
-      }
+        for (int g = (8 / kParts) * part; g < (8 / kParts) * (part + 1); ++g)
+          *reinterpret_cast<uint4*>(S.qrope + row * 128 + ((g ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (tid == 0 && rank == 0) VTRACE(21, uu);  // Q of unit uu written
-      // (the failure test withholds this signal: the score MMAs then never start and a
-      // bounded wait expires)
-      if (lane == 0 && a.test_fault != kFaultNoQReady) {
-        if (rank == 0) mbar_arrive(&sm.c.qfull);
-        else mbar_arrive_remote(qfull_r);
+      if (lane == 0) {
+        mbar_arrive(&sm.c.qfree);  // the stages may take K tiles again
+        // (the failure test withholds this signal: the score MMAs then never start and a
+        // bounded wait expires)
+        if (a.test_fault != kFaultNoQReady) {
+          if (rank == 0) mbar_arrive(&sm.c.qfull);
+          else mbar_arrive_remote(qfull_r);
+        }
       }
     }
     const int i = valid ? r / H : 0;
@@ -932,9 +972,9 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const C
 
 // The kernel body; `plan` and `sched` are kernel parameters (host-planned
 // calls) or live in the workspace (device-planned calls).
-__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CUtensorMap& omap,
-                                               const CUtensorMap& pmap, const PlanParams& plan, const TcSched& sched,
-                                               const RunArgs& a) {
+__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CUtensorMap& qmap,
+                                               const CUtensorMap& omap, const CUtensorMap& pmap,
+                                               const PlanParams& plan, const TcSched& sched, const RunArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -966,6 +1006,8 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
       sm.c.peer_flags[s] = 0;
     }
     mbar_init(&sm.c.qfull, 2 * kSoftWarps);  // every softmax warp of both scorer CTAs
+    mbar_init(&sm.c.qland, 1);
+    mbar_init(&sm.c.qfree, kSoftWarps);
     mbar_init(&sm.c.cmd_full, 1);
     mbar_init(&sm.c.cmd_done, 2);
     mbar_init(&sm.c.obar, 1);
@@ -976,6 +1018,8 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
     if (rank >= 2) {
       prefetch_tensormap(&omap);
       prefetch_tensormap(&pmap);
+    } else {
+      prefetch_tensormap(&qmap);
     }
   }
   __syncwarp();
@@ -1003,7 +1047,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
   const uint32_t tbase = sm.c.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sm, &kmap, plan, sched, a, u_begin, u_end, rank);
+    if (lane == 0) producer_role(sm, &kmap, &qmap, plan, sched, a, u_begin, u_end, rank);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
@@ -1050,19 +1094,19 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
-                 const __grid_constant__ CUtensorMap pmap, const __grid_constant__ PlanParams plan,
-                 const __grid_constant__ TcSched sched, const RunArgs a) {
-  tc_verify_body(kmap, omap, pmap, plan, sched, a);
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
+                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
+  tc_verify_body(kmap, qmap, omap, pmap, plan, sched, a);
 }
 
 // Same kernel with the plan and the cluster schedule read from the workspace,
 // where the device planner wrote them (stream-capture-safe calls).
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
-                       const __grid_constant__ CUtensorMap pmap, const PlanParams* __restrict__ plan,
-                       const TcSched* __restrict__ sched, const RunArgs a) {
-  tc_verify_body(kmap, omap, pmap, *plan, *sched, a);
+tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
+                       const PlanParams* __restrict__ plan, const TcSched* __restrict__ sched, const RunArgs a) {
+  tc_verify_body(kmap, qmap, omap, pmap, *plan, *sched, a);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1085,7 +1129,7 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 3 * sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 4 * sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 // attr: room for two attributes (the cluster shape, and an early start under
@@ -1127,10 +1171,13 @@ bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The three maps of a launch; without partial rows the partial map repeats
-// the output map (no unit of such a plan stores partials).
-bool encode_maps(EncodeTiledFn enc, const RunArgs& a, CUtensorMap* kmap, CUtensorMap* omap, CUtensorMap* pmap) {
+// The four maps of a launch (staged KV rows, Q rows [query rows x heads x 576],
+// outputs, partials); without partial rows the partial map repeats the output
+// map (no unit of such a plan stores partials).
+bool encode_maps(EncodeTiledFn enc, const RunArgs& a, CUtensorMap* kmap, CUtensorMap* qmap, CUtensorMap* omap,
+                 CUtensorMap* pmap) {
   if (!encode_rows(enc, kmap, a.staged, a.total_kv, kHalfKeys)) return false;
+  if (!encode_rows(enc, qmap, const_cast<uint16_t*>(a.q), a.out_rows, 64)) return false;
   if (!encode_out(enc, omap, a.out, a.out_rows, false)) return false;
   if (a.part_rows > 0 && a.part_o) return encode_out(enc, pmap, a.part_o, a.part_rows, true);
   *pmap = *omap;
@@ -1174,8 +1221,8 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   // 2-D map over the staged rows [total_kv x 576 bf16]: boxes of 64 rows x 64
   // columns with 128-byte swizzle (scorer half tiles, mixer message chunks),
   // and the epilogue's output maps
-  CUtensorMap kmap, omap, pmap;
-  if (!encode_maps(enc, a, &kmap, &omap, &pmap)) return VMLA_ERR_CUDA;
+  CUtensorMap kmap, qmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   // units are independent: a plan with more than kMaxTcUnits runs as several launches
   static thread_local TcSched sched;
   for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
@@ -1185,7 +1232,7 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr, true);
     cfg.stream = (cudaStream_t)stream;
-    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, omap, pmap, plan, sched, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
       return VMLA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
@@ -1200,12 +1247,12 @@ int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, 
   if (clusters < 1 || clusters > dev_clusters || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
   // the maps span the staged, output and partial areas' capacities; the planned
   // keys and rows lie inside them
-  CUtensorMap kmap, omap, pmap;
-  if (!encode_maps(enc, a, &kmap, &omap, &pmap)) return VMLA_ERR_CUDA;
+  CUtensorMap kmap, qmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(clusters, attr, true);
   cfg.stream = (cudaStream_t)stream;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, omap, pmap, plan, sched, a) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
     return VMLA_ERR_CUDA;
   return VMLA_OK;
 }
