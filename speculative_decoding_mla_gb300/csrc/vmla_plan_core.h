@@ -104,8 +104,8 @@ VMLA_HD int64_t plan_split_seq(const PlanShape& sh, SeqPlan& s, int num_heads, i
 // ---------------------------------------------------------------- piece size of the tensor-core kernel
 // A unit's cost for the cluster schedule: its keys plus a fixed charge for
 // loading Q, filling and draining the pipeline and writing the result (about
-// five 128-key tiles' time, measured on the verify kernel).
-constexpr int64_t kUnitFixedKeys = 640;
+// three 128-key tiles' time, measured on the verify kernel).
+constexpr int64_t kUnitFixedKeys = 384;
 
 VMLA_HD int64_t plan_unit_cost(const SeqPlan& s, int unit) {
   const int64_t piece = (unit - s.unit_start) / s.n_rb;

@@ -347,7 +347,7 @@ def _piece_rule(qo, kv, H, clusters, search=True):
     """The tensor-core planner's piece-size rule, stated on its own: candidate k aims at m_k / 16
     units per cluster (chunk target ceil(16 W / (C m_k)), at least one 128-key tile); a sequence of
     N keys gets ceil(N / target) pieces (at most 64), of a length rounded up to 128 keys; a unit
-    costs its keys plus 640; a candidate's score is the longest cluster load when its units, sorted
+    costs its keys plus 384; a candidate's score is the longest cluster load when its units, sorted
     by cost (longest first), are dealt to the clusters in a snake order, plus a twentieth of a key
     per fp32 partial row (query rows x pieces of every split sequence) and 128 keys when there is
     any; the best-scoring candidate
@@ -382,7 +382,7 @@ def _piece_rule(qo, kv, H, clusters, search=True):
             if q == 0:
                 continue
             for s in range(p):
-                costs += [min(ch, n - s * ch) + 640] * r
+                costs += [min(ch, n - s * ch) + 384] * r
             if p > 1:
                 part += q * H * p
         if len(costs) > 3072:
