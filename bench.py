@@ -53,10 +53,11 @@ METRIC = "verify-attn KV tokens/sec, TFLOPS and HBM GB/s as % of GB300 roofline"
 
 # DRAM bytes (read + write) per verify launch from committed ncu captures of each workload's
 # first timed launch; valid only while the kernel and planner sources are the ones profiled.
-PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp")
-PROFILED_FINGERPRINT = "6e349c8de2df3f4c"
-PROFILED_TRAFFIC = {"contiguous_1k": 2.460e6, "paged_ragged": 82.29e6, "long_185k": 238.36e6, "tree_32k": 485.32e6,
-                    "sweep_q1": 756.03e6, "sweep_q4": 793.42e6, "sweep_q16": 825.56e6}
+PROFILED_SOURCES = ("speculative_decoding_mla_gb300/csrc/vmla_tc.cu", "speculative_decoding_mla_gb300/csrc/vmla_plan.cpp",
+                    "speculative_decoding_mla_gb300/csrc/vmla_plan_core.h")
+PROFILED_FINGERPRINT = "27690cd4204e00c4"
+PROFILED_TRAFFIC = {"contiguous_1k": 2.466e6, "paged_ragged": 78.49e6, "long_185k": 218.31e6, "tree_32k": 481.80e6,
+                    "sweep_q1": 757.89e6, "sweep_q4": 773.06e6, "sweep_q16": 825.48e6}
 
 
 def source_fingerprint(paths=None) -> str:
