@@ -280,8 +280,9 @@ __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched
 // 128) through both K stages: latent chunk c of row half h into stage h, chunk
 // c; the rope chunk into qrope.  The softmax warps move the latent part into
 // tensor memory and release the stages (qfree) before the first K tile loads.
-__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const CUtensorMap* qmap, const PlanParams& plan,
-                              const TcSched& sched, const RunArgs& a, int u_begin, int u_end, uint32_t rank) {
+__device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const CUtensorMap* vmap, const CUtensorMap* qmap,
+                              const PlanParams& plan, const TcSched& sched, const RunArgs& a, int u_begin, int u_end,
+                              uint32_t rank) {
   const bool scorer = rank < 2;
   const uint32_t q = rank & 1;
   const uint32_t leader = rank & 2u;
@@ -332,16 +333,14 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const CUtensor
       const uint32_t bar = mapa(smem_u32(&sm.c.kfull[s]), leader);
       if (q == 0) mbar_arrive_expect_tx(&sm.c.kfull[s], pair_bytes);
       if (scorer) {
+        // all nine column chunks of this CTA's 64 keys in one box (chunk-major in the stage)
         const int y = row0 + ui.k_lo + n * kTileKeys + kHalfKeys * (int)q;
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) tma_load_2d_pair(smem_u32(&sm.u.s.kv[s][c][0]), map, 64 * c, y, bar);
+        tma_load_3d_pair(smem_u32(&sm.u.s.kv[s][0][0]), map, 0, y, 0, bar);
       } else {
+        // value chunks {2q, 2q+1} and {2q+4, 2q+5} of the message's 64 keys, two chunks per box
         const int y = row0 + ui.k_lo + n * kMsgKeys;
-#pragma unroll 1
-        for (int j = 0; j < kVChunksCta; ++j) {
-          const int g = (j & 1) + 2 * (int)q + 4 * (j >> 1);
-          tma_load_2d_pair(smem_u32(&sm.u.m.v[s][j][0]), map, 64 * g, y, bar);
-        }
+        tma_load_3d_pair(smem_u32(&sm.u.m.v[s][0][0]), vmap, 0, y, 2 * (int)q, bar);
+        tma_load_3d_pair(smem_u32(&sm.u.m.v[s][2][0]), vmap, 0, y, 2 * (int)q + 4, bar);
       }
       ++it;
     }
@@ -972,9 +971,10 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const C
 
 // The kernel body; `plan` and `sched` are kernel parameters (host-planned
 // calls) or live in the workspace (device-planned calls).
-__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CUtensorMap& qmap,
-                                               const CUtensorMap& omap, const CUtensorMap& pmap,
-                                               const PlanParams& plan, const TcSched& sched, const RunArgs& a) {
+__device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                               const CUtensorMap& qmap, const CUtensorMap& omap,
+                                               const CUtensorMap& pmap, const PlanParams& plan,
+                                               const TcSched& sched, const RunArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1016,6 +1016,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     if (rank >= 2) {
+      prefetch_tensormap(&vmap);
       prefetch_tensormap(&omap);
       prefetch_tensormap(&pmap);
     } else {
@@ -1047,7 +1048,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
   const uint32_t tbase = sm.c.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sm, &kmap, &qmap, plan, sched, a, u_begin, u_end, rank);
+    if (lane == 0) producer_role(sm, &kmap, &vmap, &qmap, plan, sched, a, u_begin, u_end, rank);
   } else if (warp == 1) {
     if (lane == 0) {
       if (rank == 0) scorer_mma_role(sm, plan, sched, a, tbase, u_begin, u_end);
@@ -1094,19 +1095,21 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                 const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
-                 const __grid_constant__ PlanParams plan, const __grid_constant__ TcSched sched, const RunArgs a) {
-  tc_verify_body(kmap, qmap, omap, pmap, plan, sched, a);
+tc_verify_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                 const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                 const __grid_constant__ CUtensorMap pmap, const __grid_constant__ PlanParams plan,
+                 const __grid_constant__ TcSched sched, const RunArgs a) {
+  tc_verify_body(kmap, vmap, qmap, omap, pmap, plan, sched, a);
 }
 
 // Same kernel with the plan and the cluster schedule read from the workspace,
 // where the device planner wrote them (stream-capture-safe calls).
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                       const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
-                       const PlanParams* __restrict__ plan, const TcSched* __restrict__ sched, const RunArgs a) {
-  tc_verify_body(kmap, qmap, omap, pmap, *plan, *sched, a);
+tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                       const __grid_constant__ CUtensorMap pmap, const PlanParams* __restrict__ plan,
+                       const TcSched* __restrict__ sched, const RunArgs a) {
+  tc_verify_body(kmap, vmap, qmap, omap, pmap, *plan, *sched, a);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1129,7 +1132,7 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 4 * sizeof(CUtensorMap) < 32000,
+static_assert(sizeof(PlanParams) + sizeof(TcSched) + sizeof(RunArgs) + 5 * sizeof(CUtensorMap) < 32000,
               "kernel parameter budget");
 
 // attr: room for two attributes (the cluster shape, and an early start under
@@ -1159,6 +1162,21 @@ bool encode_rows(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over staged rows [rows x 576 bf16] seen as (64 columns, row, column
+// chunk) with strides 1152 B (row) and 128 B (chunk): a box of `box_rows` rows x
+// `box_chunks` chunks lands chunk-major in shared memory, each chunk a
+// 128-byte-swizzled [box_rows x 64] block, as the MMA descriptors expect.
+bool encode_rows_chunks(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, uint32_t box_rows,
+                        uint32_t box_chunks) {
+  cuuint64_t gdim[3] = {64, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)kChunks};
+  cuuint64_t gstride[2] = {(cuuint64_t)kRowBytes, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estride[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output maps of the epilogue: [rows x 512] of bf16 outputs or fp32 partials,
 // boxes of 32 rows x 64 bytes with 64-byte swizzle (the epilogue tiles' layout).
 bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, bool fp32) {
@@ -1171,12 +1189,14 @@ bool encode_out(EncodeTiledFn enc, CUtensorMap* map, void* base, int64_t rows, b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The four maps of a launch (staged KV rows, Q rows [query rows x heads x 576],
-// outputs, partials); without partial rows the partial map repeats the output
-// map (no unit of such a plan stores partials).
-bool encode_maps(EncodeTiledFn enc, const RunArgs& a, CUtensorMap* kmap, CUtensorMap* qmap, CUtensorMap* omap,
-                 CUtensorMap* pmap) {
-  if (!encode_rows(enc, kmap, a.staged, a.total_kv, kHalfKeys)) return false;
+// The five maps of a launch (staged KV rows for the scorer's K boxes and the
+// mixer's V boxes, Q rows [query rows x heads x 576], outputs, partials);
+// without partial rows the partial map repeats the output map (no unit of
+// such a plan stores partials).
+bool encode_maps(EncodeTiledFn enc, const RunArgs& a, CUtensorMap* kmap, CUtensorMap* vmap, CUtensorMap* qmap,
+                 CUtensorMap* omap, CUtensorMap* pmap) {
+  if (!encode_rows_chunks(enc, kmap, a.staged, a.total_kv, kHalfKeys, kChunks)) return false;
+  if (!encode_rows_chunks(enc, vmap, a.staged, a.total_kv, kMsgKeys, 2)) return false;
   if (!encode_rows(enc, qmap, const_cast<uint16_t*>(a.q), a.out_rows, 64)) return false;
   if (!encode_out(enc, omap, a.out, a.out_rows, false)) return false;
   if (a.part_rows > 0 && a.part_o) return encode_out(enc, pmap, a.part_o, a.part_rows, true);
@@ -1221,8 +1241,8 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   // 2-D map over the staged rows [total_kv x 576 bf16]: boxes of 64 rows x 64
   // columns with 128-byte swizzle (scorer half tiles, mixer message chunks),
   // and the epilogue's output maps
-  CUtensorMap kmap, qmap, omap, pmap;
-  if (!encode_maps(enc, a, &kmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
+  CUtensorMap kmap, vmap, qmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &vmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   // units are independent: a plan with more than kMaxTcUnits runs as several launches
   static thread_local TcSched sched;
   for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
@@ -1232,7 +1252,7 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr, true);
     cfg.stream = (cudaStream_t)stream;
-    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
       return VMLA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
@@ -1247,12 +1267,12 @@ int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, 
   if (clusters < 1 || clusters > dev_clusters || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
   // the maps span the staged, output and partial areas' capacities; the planned
   // keys and rows lie inside them
-  CUtensorMap kmap, qmap, omap, pmap;
-  if (!encode_maps(enc, a, &kmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
+  CUtensorMap kmap, vmap, qmap, omap, pmap;
+  if (!encode_maps(enc, a, &kmap, &vmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(clusters, attr, true);
   cfg.stream = (cudaStream_t)stream;
-  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tc_verify_kernel_dplan, kmap, vmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
     return VMLA_ERR_CUDA;
   return VMLA_OK;
 }
