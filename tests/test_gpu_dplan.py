@@ -153,3 +153,44 @@ def test_device_plan_long_185k_sampled_rows():
     rows = sample_rows(case)
     ref_o, ref_l = oracle_rows(case, rows, "long_185k/sampled")
     compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, "device plan / long_185k")
+
+
+def _random_batches():
+    """Ragged batches on which the piece-size search leaves the default: lengths, drafts and heads
+    drawn from a seeded generator (1 to 65 sequences; the last one above the search's 64)."""
+    rng = np.random.default_rng(430)
+    shapes = [(3, 64, [16, 4, 1], [30000, 500, 12000])]
+    for B, H, dmax, med in [(12, 16, 64, 3000), (33, 64, 4, 4000), (64, 8, 64, 800), (5, 128, 8, 8000),
+                            (65, 16, 16, 300)]:
+        drafts = rng.integers(1, dmax + 1, B).tolist()
+        prefixes = np.minimum(rng.lognormal(np.log(med), 1.0, B).astype(np.int64), 40000).tolist()
+        shapes.append((B, H, drafts, prefixes))
+    for i, (B, H, drafts, prefixes) in enumerate(shapes):
+        nd = int(sum(drafts))
+        yield synth.make_case(f"rand{i}", prefixes, drafts, num_heads=H,
+                              pool_slots=int(sum(prefixes)) + nd + 64, seed=431 + i)
+
+
+def test_device_plan_random_batches_bitwise():
+    """The device planner scores the same piece-size candidates as the host planner (one warp per
+    candidate) and must cut every sequence alike: bit-equal results on ragged random batches, and
+    sampled rows of two of them against the oracle."""
+    _, binding, _ = _mods()
+    from tests.test_capi_cpu import _piece_rule
+    from tests.test_gpu_parity import sample_rows
+    changed = 0
+    for k, case in enumerate(_random_batches()):
+        o1, l1, s1 = run_full(case, "tc")
+        o2, l2, s2 = run_dplan(case, slack_q=3, slack_kv=500)
+        assert s1 == 0 and s2 == 0, case.name
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2), case.name
+        info, per = binding.verify_attn_mla_plan(binding.VMLA_KERNEL_TC, case.qo_indptr, case.kv_indptr,
+                                                 case.num_heads, 0, 144)
+        default = _piece_rule(case.qo_indptr, case.kv_indptr, case.num_heads, 36, search=False)
+        changed += int([int(p) for p in per] != default)
+        if k in (0, 2):
+            rows = sample_rows(case, n=60, seed=k)
+            ref_o, ref_l = oracle.verify_rows(case, rows)
+            H = case.num_heads
+            compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, case.name)
+    assert changed >= 1  # the search chose another piece size on some of these batches
