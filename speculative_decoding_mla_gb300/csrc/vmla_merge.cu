@@ -6,8 +6,9 @@
 // the combination of partial softmaxes that the NSPLIT split-KV of "The Build
 // Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel",
 // implies.  One block per row, each of its four warps a quarter of the
-// columns with eight pieces' loads in flight per lane; pieces with
-// lse = -inf carry no weight (their partial rows are not read).
+// columns with twelve pieces' loads in flight per lane, the first twelve
+// issued together with the lse loads; pieces with lse = -inf carry no weight
+// (their partial rows, which may hold anything, are read but never used).
 //
 // Tree masks: the q x q visibility matrix of "The Build That Bridged Design
 // and Deployment", section "What This Build Achieves: The paged+bf16 Kernel",
@@ -21,7 +22,7 @@ namespace vmla {
 namespace {
 
 constexpr int kMergeWarps = 4;  // one per quarter of a 512-column row
-constexpr int kMergeBatch = 8;  // pieces loaded together
+constexpr int kMergeBatch = 12;  // pieces loaded together
 
 __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
                                            const float* __restrict__ part_lse, int lse_is_log2,
@@ -44,6 +45,12 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
   const int r = mrow - sp.merge_off;
   const int S = sp.n_split;
   const float to2 = lse_is_log2 ? 1.f : 1.4426950408889634f;
+  const float4* src0 = reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + r) * kDv) + c * 32 + lane;
+  const int64_t piece_stride = (int64_t)R * (kDv / 4);  // float4s between pieces of one row
+  // the first batch of partial rows is in flight while the weights are worked out
+  float4 v[kMergeBatch];
+#pragma unroll
+  for (int b = 0; b < kMergeBatch; ++b) v[b] = b < S ? __ldg(src0 + b * piece_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
   // lse of pieces lane and lane + 32 (S <= 64)
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < S) l0 = part_lse[(int64_t)sp.part_off + (int64_t)lane * R + r] * to2;
@@ -61,26 +68,23 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
   const float invW = 1.f / W;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
-    float4 v[kMergeBatch];
-    float ws[kMergeBatch];
+    if (s0 > 0) {
 #pragma unroll
-    for (int b = 0; b < kMergeBatch; ++b) {
-      const int s = s0 + b;
-      // every lane takes part in the shuffle; pieces past S or without weight are not read
-      // (an empty piece's partial row may hold anything)
-      ws[b] = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-      if (s >= S) ws[b] = 0.f;
-      const bool use = ws[b] != 0.f;  // warp-uniform
-      const float4* src =
-          reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + (int64_t)(use ? s : 0) * R + r) * kDv);
-      v[b] = use ? __ldg(src + c * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int b = 0; b < kMergeBatch; ++b)
+        v[b] = s0 + b < S ? __ldg(src0 + (s0 + b) * piece_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int b = 0; b < kMergeBatch; ++b) {
-      acc.x = fmaf(ws[b], v[b].x, acc.x);
-      acc.y = fmaf(ws[b], v[b].y, acc.y);
-      acc.z = fmaf(ws[b], v[b].z, acc.z);
-      acc.w = fmaf(ws[b], v[b].w, acc.w);
+      const int s = s0 + b;
+      // every lane takes part in the shuffle; a piece without weight is skipped by a
+      // select, so whatever its partial row holds never reaches the sum
+      const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+      if (s < S && w != 0.f) {
+        acc.x = fmaf(w, v[b].x, acc.x);
+        acc.y = fmaf(w, v[b].y, acc.y);
+        acc.z = fmaf(w, v[b].z, acc.z);
+        acc.w = fmaf(w, v[b].w, acc.w);
+      }
     }
   }
   *dst = make_uint2(pack_bf16x2(acc.x * invW, acc.y * invW), pack_bf16x2(acc.z * invW, acc.w * invW));
