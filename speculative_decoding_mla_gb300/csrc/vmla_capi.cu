@@ -74,7 +74,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
         const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
         const uint64_t* draft_mask, const int32_t* parent, const int32_t* kv_indptr_host,
         const int32_t* qo_indptr_host, int batch, int num_heads, float sm_scale, int splits, void* out, float* lse,
-        void* workspace, size_t workspace_bytes, void* stream, void* q_ready) {
+        void* workspace, size_t workspace_bytes, void* stream, void* q_ready, const PlanParams* plan_in,
+        const vmla_plan_info* info_in) {
   int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, pool_slots, splits);
   if (rc != VMLA_OK) return rc;
   // a positive finite scale (the kernels take row maxima over unscaled scores)
@@ -102,10 +103,16 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
     rc = tc_max_clusters(&clusters);
     if (rc != VMLA_OK) return rc;
   }
-  static thread_local PlanParams plan;  // large (20 KB); kept off the stack
+  static thread_local PlanParams own_plan;  // large (20 KB); kept off the stack
   vmla_plan_info info;
-  rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan, &info);
-  if (rc != VMLA_OK) return rc;
+  if (plan_in && info_in) {
+    info = *info_in;
+  } else {
+    rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &own_plan,
+                    &info);
+    if (rc != VMLA_OK) return rc;
+  }
+  const PlanParams& plan = plan_in && info_in ? *plan_in : own_plan;
   const WorkspaceLayout L =
       workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC && !runs ? total_kv : 0);
   if (workspace_bytes < L.total) return VMLA_ERR_WORKSPACE;
@@ -370,15 +377,11 @@ int host_side(HostSide** out) {
 }
 }  // namespace
 
-int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,
-                                     const int32_t* kv_indptr_host, int splits, int has_mask, int has_parent,
-                                     size_t* bytes) {
-  if (!bytes) return VMLA_ERR_NULL;
-  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, 0, splits);
-  if (rc != VMLA_OK) return rc;
-  size_t ws = 0;
-  rc = verify_attn_mla_workspace_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits, &ws);
-  if (rc != VMLA_OK) return rc;
+namespace {
+// The host-buffer call's device buffer: the workspace (ws bytes), then q, the
+// index arrays, the optional mask and parent arrays, out and lse.
+size_t host_buffer_bytes(size_t ws, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host, int batch,
+                         int num_heads, bool has_mask, bool has_parent) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   const size_t T = (size_t)qo_indptr_host[batch], N = (size_t)kv_indptr_host[batch], B = (size_t)batch;
   size_t total = up(ws);
@@ -389,7 +392,20 @@ int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo
   if (has_parent) total += up(T * 4);
   total += up(T * num_heads * VMLA_D_V * 2);   // out
   total += up(T * num_heads * 4);              // lse
-  *bytes = total;
+  return total;
+}
+}  // namespace
+
+int verify_attn_mla_host_buffer_size(int batch, int num_heads, const int32_t* qo_indptr_host,
+                                     const int32_t* kv_indptr_host, int splits, int has_mask, int has_parent,
+                                     size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int rc = check_common(kv_indptr_host, qo_indptr_host, batch, num_heads, 0, splits);
+  if (rc != VMLA_OK) return rc;
+  size_t ws = 0;
+  rc = verify_attn_mla_workspace_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits, &ws);
+  if (rc != VMLA_OK) return rc;
+  *bytes = host_buffer_bytes(ws, qo_indptr_host, kv_indptr_host, batch, num_heads, has_mask != 0, has_parent != 0);
   return VMLA_OK;
 }
 
@@ -404,14 +420,23 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   if (!aligned(device_buffer, VMLA_WORKSPACE_ALIGN)) return VMLA_ERR_ALIGN;
   const size_t T = (size_t)qo_indptr_host[batch], N = (size_t)kv_indptr_host[batch], B = (size_t)batch;
   if (T > 0 && (!q_host || !kv_indices_host || !out_host || !lse_host || !kv_pool)) return VMLA_ERR_NULL;
-  size_t need = 0;
-  rc = verify_attn_mla_host_buffer_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits,
-                                        draft_mask_host != nullptr, parent_host != nullptr, &need);
+  // the plan is built once here and handed to the call; its workspace (the tensor-core
+  // plan's, at most the size verify_attn_mla_host_buffer_size counted) leads the buffer
+  int sms = 0, clusters = 0;
+  rc = current_sm_count(&sms, true);
   if (rc != VMLA_OK) return rc;
+  rc = tc_max_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  static thread_local PlanParams plan;
+  vmla_plan_info info;
+  rc = build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan,
+                  &info);
+  if (rc != VMLA_OK) return rc;
+  const size_t ws = info.workspace_bytes;
+  const size_t need =
+      host_buffer_bytes(ws, qo_indptr_host, kv_indptr_host, batch, num_heads, draft_mask_host != nullptr,
+                        parent_host != nullptr);
   if (device_buffer_bytes < need) return VMLA_ERR_WORKSPACE;
-  size_t ws = 0;
-  rc = verify_attn_mla_workspace_size(batch, num_heads, qo_indptr_host, kv_indptr_host, splits, &ws);
-  if (rc != VMLA_OK) return rc;
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   char* p = static_cast<char*>(device_buffer);
   char* d_ws = p;            p += up(ws);
@@ -453,7 +478,7 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
                     nullptr, (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
                     qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream,
-                    hs ? (void*)hs->q_done : nullptr);
+                    hs ? (void*)hs->q_done : nullptr, &plan, &info);
   if (!ok || rc != VMLA_OK) {
     if (hs) cudaStreamSynchronize(hs->side);  // the buffer is the caller's again when this returns
     return ok ? rc : VMLA_ERR_CUDA;

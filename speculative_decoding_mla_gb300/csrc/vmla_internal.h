@@ -127,12 +127,15 @@ struct RunArgs {
 // slots run_base[b] .. run_base[b] + N_b - 1 (tensor-core kernel only).
 // kv_scale > 0: kv_pool holds e4m3 codes; the gather dequantizes them (tensor-core kernel only).
 // q_ready (a cudaEvent_t or NULL): the kernels that read q wait for it; the gather does not.
+// plan_in / info_in: a plan the caller already built for these lengths with this
+// device's SM and cluster counts (NULL: built here).
 int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slots, float kv_scale,
                const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
                const uint64_t* draft_mask, const int32_t* parent,
                const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, int batch, int num_heads,
                float sm_scale, int splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
-               void* stream, void* q_ready = nullptr);
+               void* stream, void* q_ready = nullptr, const PlanParams* plan_in = nullptr,
+               const vmla_plan_info* info_in = nullptr);
 
 // Device-planned calls (stream-capture safe): the plan and the cluster
 // schedule are computed on the device from the device indptr arrays.  The
