@@ -277,17 +277,17 @@ int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots,
  * that loads the library holds until the process exits.  The entry point
  * allocates and frees nothing.  A plan whose workspace
  * (verify_attn_mla_plan(VMLA_KERNEL_SIMT, ...).workspace_bytes) exceeds the
- * array returns VMLA_ERR_WORKSPACE before any launch.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Every call
+ * array returns VMLA_ERR_WORKSPACE before any launch.  Each call looks up the
+ * array's device address on the current device (cudaGetSymbolAddress, a host
+ * query; the first one on a device loads the library's module there, so make
+ * that first call before any stream capture).  Every call
  * on a device shares the one array and leaves its contents behind: calls that
  * may overlap on the GPU (different streams without ordering) race on it, so
  * order them on one stream.  Faults a kernel detects (a slot outside the pool,
  * malformed parents) are recorded in the array's status word, which
- * verify_attn_mla_simt_static_check() reads.  The device address of the array
- * is looked up once per device and kept; after cudaDeviceReset the library's
- * module is loaded again and that address is stale, so a process that resets a
- * device must not call this entry point on it afterwards. */
+ * verify_attn_mla_simt_static_check() reads.  No address is kept between calls,
+ * so the entry point stays usable after cudaDeviceReset (the module is loaded
+ * again, possibly elsewhere, and the next call looks it up there). */
 int verify_attn_mla_simt_static(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
                                 const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
                                 const int32_t* parent, const int32_t* kv_indptr_host,

@@ -9,8 +9,6 @@
 // entry point only removes the workspace argument.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "vmla_internal.h"
 
 namespace vmla {
@@ -19,23 +17,13 @@ namespace {
 // Scratch for the status word, ancestor masks and split partials of one call.
 __device__ __align__(256) unsigned char g_vmla_static_scratch[VMLA_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per
-// device (the host-side symbol is only a stand-in for it).
+// Device address of the scratch array on the current device.  It is looked up on
+// every call (a host-side lookup in the loaded module): after a device reset the
+// module is loaded again and the array may sit elsewhere, so no address is kept.
 int static_scratch(void** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return VMLA_ERR_DEVICE;
-  if (dev < 0 || dev >= kMaxDevices) return VMLA_ERR_DEVICE;
-  std::lock_guard<std::mutex> g(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_vmla_static_scratch) != cudaSuccess || !p) return VMLA_ERR_CUDA;
-    g_static_ptr[dev] = p;
-  }
-  *ptr = g_static_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_vmla_static_scratch) != cudaSuccess || !p) return VMLA_ERR_CUDA;
+  *ptr = p;
   return VMLA_OK;
 }
 
