@@ -10,7 +10,8 @@
 // One CTA per SM, W loader warps and one consumer thread that frees a stage
 // after a fixed hold (0 or 1500 ns, standing in for the MMAs).  The slots of a
 // load are read before the previous load's copies are issued.  Prints µs per
-// 73,728-byte load per SM.
+// 73,728-byte load per SM.  A last sweep repeats the tiled loads with the
+// shared-memory request padded (unused bytes), which leaves the SM less L1.
 //
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -std=c++17 \
 //        -Ispeculative_decoding_mla_gb300/csrc -Iinclude -o /tmp/load_paths \
@@ -169,8 +170,8 @@ typedef CUresult (*EncFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, 
 
 template <int MODE>
 float run(const CUtensorMap& tm, const CUtensorMap& gm, const uint8_t* pool, const int* idx, int n_idx, int rows,
-          int tiles, int W, int delay, int grid) {
-  size_t smem = sizeof(Smem) + 1024;
+          int tiles, int W, int delay, int grid, size_t pad = 0) {
+  size_t smem = sizeof(Smem) + 1024 + pad;
   CK(cudaFuncSetAttribute(probe<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cudaEvent_t a, b;
   cudaEventCreate(&a);
@@ -242,5 +243,13 @@ int main() {
       }
     }
   }
+  // tiled loads with the shared-memory request padded to about 148, 196 and 225 KB
+  for (int delay : {0, 1500})
+    for (size_t pad : {(size_t)0, (size_t)49152, (size_t)77824}) {
+      const float ms = run<0>(tm, gm, pool, idx, rows, rows, tiles, 1, delay, sms, pad);
+      const double us_tile = ms * 1e3 / tiles;
+      printf("smem %6zu B delay %4d tma_tile  %.3f us/tile  %.1f GB/s/SM\n", sizeof(Smem) + 1024 + pad, delay, us_tile,
+             kStageBytes / (us_tile * 1e3));
+    }
   return 0;
 }
