@@ -40,14 +40,11 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
   for (int r = 0; r < R; ++r) key[r] = (uint64_t)r;
   std::vector<int64_t> resid(period + 1);
   int64_t score[kChunkCands];
-  int64_t prev_ct = -1;
-  for (int k = 0; k < kChunkCands; ++k) {
+  int64_t best = -1;  // lowest exact score so far
+  // the default first, so that its exact score bounds the others from the start
+  for (int i = 0; i < kChunkCands; ++i) {
+    const int k = i == 0 ? kDefaultCand : (i <= kDefaultCand ? i - 1 : i);
     const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
-    if (ct == prev_ct) {  // the same pieces as the previous candidate
-      score[k] = score[k - 1];
-      continue;
-    }
-    prev_ct = ct;
     int64_t units = 0, part = 0;
     for (int b = 0; b < batch; ++b) {
       int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
@@ -60,13 +57,27 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
     }
     score[k] = -1;  // not a candidate: more units than one launch holds
     if (units > kMaxTcUnits) continue;
-    for (int i = 0; i < R; ++i) {
-      const int r = (int)(key[i] & 0xFFu);
-      key[i] = ((uint64_t)(0xFFFFFFFFll - cost[r]) << 8) | (uint64_t)r;
+    // a lower bound of the score: some cluster carries at least the mean load and
+    // one carries the largest unit; a candidate whose bound exceeds the best exact
+    // score cannot be chosen (nor tie), so its bound stands in for its score
+    int64_t total = 0, largest = 0;
+    for (int r = 0; r < R; ++r) {
+      total += cost[r] * count[r];
+      if (count[r] > 0 && cost[r] > largest) largest = cost[r];
     }
-    for (int i = 1; i < R; ++i) {
-      const uint64_t x = key[i];
-      int j = i - 1;
+    const int64_t mean = (total + clusters - 1) / clusters;
+    const int64_t bound = (mean > largest ? mean : largest) + plan_merge_score(part);
+    if (k != kDefaultCand && best >= 0 && bound > best) {
+      score[k] = bound;
+      continue;
+    }
+    for (int j2 = 0; j2 < R; ++j2) {
+      const int r = (int)(key[j2] & 0xFFu);
+      key[j2] = ((uint64_t)(0xFFFFFFFFll - cost[r]) << 8) | (uint64_t)r;
+    }
+    for (int j2 = 1; j2 < R; ++j2) {
+      const uint64_t x = key[j2];
+      int j = j2 - 1;
       while (j >= 0 && key[j] > x) {
         key[j + 1] = key[j];
         --j;
@@ -76,8 +87,8 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
     std::fill(resid.begin(), resid.end(), 0);
     // positions as quotient and residue modulo the period, advanced run by run
     int64_t whole = 0, q_lo = 0, r_lo = 0;
-    for (int i = 0; i < R; ++i) {
-      const int r = (int)(key[i] & 0xFFu);
+    for (int j2 = 0; j2 < R; ++j2) {
+      const int r = (int)(key[j2] & 0xFFu);
       if (count[r] == 0) continue;
       const int64_t n = count[r];
       int64_t q_hi = q_lo + (n >= period ? n / period : 0), r_hi = r_lo + (n >= period ? n % period : n);
@@ -104,6 +115,7 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
       worst = load > worst ? load : worst;
     }
     score[k] = worst + plan_merge_score(part);
+    if (best < 0 || score[k] < best) best = score[k];
   }
   return plan_choose_cand(sh, total_work, clusters, score);
 }
