@@ -10,8 +10,9 @@
 // One CTA per SM, W loader warps and one consumer thread that frees a stage
 // after a fixed hold (0 or 1500 ns, standing in for the MMAs).  The slots of a
 // load are read before the previous load's copies are issued.  Prints µs per
-// 73,728-byte load per SM.  A last sweep repeats the tiled loads with the
-// shared-memory request padded (unused bytes), which leaves the SM less L1.
+// 73,728-byte load per SM.  Two last sweeps repeat the tiled loads with the
+// shared-memory request padded (unused bytes), which leaves the SM less L1, and
+// with each CTA starting at its own phase of the hold (loads not in step).
 //
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -std=c++17 \
 //        -Ispeculative_decoding_mla_gb300/csrc -Iinclude -o /tmp/load_paths \
@@ -61,7 +62,7 @@ template <int MODE>
 __global__ void __launch_bounds__(416, 1) probe(const __grid_constant__ CUtensorMap tmap,
                                                 const __grid_constant__ CUtensorMap gmap, const uint8_t* pool,
                                                 const int* idx, int n_idx, int pool_rows, int tiles, int W,
-                                                int delay_ns) {
+                                                int delay_ns, int phase_ns) {
   extern __shared__ uint8_t raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,6 +75,11 @@ __global__ void __launch_bounds__(416, 1) probe(const __grid_constant__ CUtensor
   }
   __syncthreads();
   if (warp < W) {
+    if (phase_ns > 0) {  // this CTA's loads start at its own phase of the hold (bounded wait on the timer)
+      const unsigned long long t0 = gtimer(), wait = (unsigned long long)((blockIdx.x * 97) % phase_ns);
+      for (int k = 0; k < (1 << 22) && gtimer() - t0 < wait; ++k) {
+      }
+    }
     // slots of this tile's 64 rows: lane l holds rows l and l + 32 (prefetched one tile ahead)
     int s_lo;
     int s_hi = idx[(((long long)blockIdx.x * tiles) * 64 + lane + 32) % n_idx];
@@ -170,17 +176,17 @@ typedef CUresult (*EncFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, 
 
 template <int MODE>
 float run(const CUtensorMap& tm, const CUtensorMap& gm, const uint8_t* pool, const int* idx, int n_idx, int rows,
-          int tiles, int W, int delay, int grid, size_t pad = 0) {
+          int tiles, int W, int delay, int grid, size_t pad = 0, int phase = 0) {
   size_t smem = sizeof(Smem) + 1024 + pad;
   CK(cudaFuncSetAttribute(probe<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cudaEvent_t a, b;
   cudaEventCreate(&a);
   cudaEventCreate(&b);
-  probe<MODE><<<grid, (W + 1) * 32, smem>>>(tm, gm, pool, idx, n_idx, rows, tiles, W, delay);
+  probe<MODE><<<grid, (W + 1) * 32, smem>>>(tm, gm, pool, idx, n_idx, rows, tiles, W, delay, phase);
   CK(cudaGetLastError());
   CK(cudaDeviceSynchronize());
   cudaEventRecord(a);
-  probe<MODE><<<grid, (W + 1) * 32, smem>>>(tm, gm, pool, idx, n_idx, rows, tiles, W, delay);
+  probe<MODE><<<grid, (W + 1) * 32, smem>>>(tm, gm, pool, idx, n_idx, rows, tiles, W, delay, phase);
   cudaEventRecord(b);
   CK(cudaDeviceSynchronize());
   float ms;
@@ -251,5 +257,12 @@ int main() {
       printf("smem %6zu B delay %4d tma_tile  %.3f us/tile  %.1f GB/s/SM\n", sizeof(Smem) + 1024 + pad, delay, us_tile,
              kStageBytes / (us_tile * 1e3));
     }
+  // tiled loads under a 1.5 us hold with each CTA starting at its own phase (0 .. 1.5 us)
+  for (int phase : {0, 1500}) {
+    const float ms = run<0>(tm, gm, pool, idx, rows, rows, tiles, 1, 1500, sms, 0, phase);
+    const double us_tile = ms * 1e3 / tiles;
+    printf("phase spread %4d ns delay 1500 tma_tile  %.3f us/tile  %.1f GB/s/SM\n", phase, us_tile,
+           kStageBytes / (us_tile * 1e3));
+  }
   return 0;
 }
