@@ -378,8 +378,9 @@ int host_side(HostSide** out) {
 }  // namespace
 
 namespace {
-// The host-buffer call's device buffer: the workspace (ws bytes), then q, the
-// index arrays, the optional mask and parent arrays, out and lse.
+// The host-buffer call's device buffer: q, the index arrays, the optional mask
+// and parent arrays, out and lse, then the workspace (ws bytes), so that the
+// inputs' places do not depend on the plan.
 size_t host_buffer_bytes(size_t ws, const int32_t* qo_indptr_host, const int32_t* kv_indptr_host, int batch,
                          int num_heads, bool has_mask, bool has_parent) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
@@ -420,26 +421,8 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   if (!aligned(device_buffer, VMLA_WORKSPACE_ALIGN)) return VMLA_ERR_ALIGN;
   const size_t T = (size_t)qo_indptr_host[batch], N = (size_t)kv_indptr_host[batch], B = (size_t)batch;
   if (T > 0 && (!q_host || !kv_indices_host || !out_host || !lse_host || !kv_pool)) return VMLA_ERR_NULL;
-  // the plan is built once here and handed to the call; its workspace (the tensor-core
-  // plan's, at most the size verify_attn_mla_host_buffer_size counted) leads the buffer
-  int sms = 0, clusters = 0;
-  rc = current_sm_count(&sms, true);
-  if (rc != VMLA_OK) return rc;
-  rc = tc_max_clusters(&clusters);
-  if (rc != VMLA_OK) return rc;
-  static thread_local PlanParams plan;
-  vmla_plan_info info;
-  rc = build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &plan,
-                  &info);
-  if (rc != VMLA_OK) return rc;
-  const size_t ws = info.workspace_bytes;
-  const size_t need =
-      host_buffer_bytes(ws, qo_indptr_host, kv_indptr_host, batch, num_heads, draft_mask_host != nullptr,
-                        parent_host != nullptr);
-  if (device_buffer_bytes < need) return VMLA_ERR_WORKSPACE;
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   char* p = static_cast<char*>(device_buffer);
-  char* d_ws = p;            p += up(ws);
   char* d_q = p;             p += up(T * num_heads * VMLA_D_QK * 2);
   char* d_kvp = p;           p += up((B + 1) * 4);
   char* d_qop = p;           p += up((B + 1) * 4);
@@ -450,6 +433,8 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   if (parent_host) { d_par = p; p += up(T * 4); }
   char* d_out = p;           p += up(T * num_heads * VMLA_D_V * 2);
   char* d_lse = p;           p += up(T * num_heads * 4);
+  char* d_ws = p;  // the plan's workspace follows the inputs
+  if (device_buffer_bytes < (size_t)(d_ws - static_cast<char*>(device_buffer))) return VMLA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
   // q crosses on a side stream while the gather runs; only the kernels after the
@@ -459,6 +444,7 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     rc = host_side(&hs);
     if (rc != VMLA_OK) return rc;
   }
+  // the copies go out first; the plan is built on the host while they cross
   bool ok = true;
   ok = ok && cudaMemcpyAsync(d_kvp, kv_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(d_qop, qo_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
@@ -474,13 +460,30 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, hs->side) == cudaSuccess;
     ok = ok && cudaEventRecord(hs->q_done, hs->side) == cudaSuccess;
   }
-  if (ok)
+  // the plan, built once here and handed to the call (its workspace is the tensor-core
+  // plan's, at most the size verify_attn_mla_host_buffer_size counted)
+  int sms = 0, clusters = 0;
+  static thread_local PlanParams plan;
+  vmla_plan_info info;
+  if (ok) {
+    rc = current_sm_count(&sms, true);
+    if (rc == VMLA_OK) rc = tc_max_clusters(&clusters);
+    if (rc == VMLA_OK)
+      rc = build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters,
+                      &plan, &info);
+  }
+  const size_t ws = rc == VMLA_OK ? info.workspace_bytes : 0;
+  if (ok && rc == VMLA_OK && device_buffer_bytes < (size_t)(d_ws - static_cast<char*>(device_buffer)) + ws)
+    rc = VMLA_ERR_WORKSPACE;
+  if (ok && rc == VMLA_OK)
     rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
                     nullptr, (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
                     qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream,
                     hs ? (void*)hs->q_done : nullptr, &plan, &info);
   if (!ok || rc != VMLA_OK) {
-    if (hs) cudaStreamSynchronize(hs->side);  // the buffer is the caller's again when this returns
+    // the buffer is the caller's again when this returns: the copies already issued are waited for
+    if (hs) cudaStreamSynchronize(hs->side);
+    cudaStreamSynchronize(st);
     return ok ? rc : VMLA_ERR_CUDA;
   }
   if (!hs) return verify_attn_mla_check(d_ws, stream);  // nothing to compute
