@@ -29,8 +29,8 @@ VMLA_HD PlanShape plan_shape(int kernel) {
     s.max_splits = 64;
   } else {
     // tensor-core kernel: one unit = 256 query rows on a cluster of four SMs
-    // (a scorer pair and a mixer pair); about two units per cluster leave the
-    // greedy schedule room to balance
+    // (a scorer pair and a mixer pair); the piece size is chosen per call among
+    // candidates (plan_cand_chunk), two units per cluster being the default
     s.rows_per_unit = 256;
     s.units_per_sm = 2;  // per cluster of four SMs; the caller divides the SM count
     s.key_align = 128;   // the kernel's tile

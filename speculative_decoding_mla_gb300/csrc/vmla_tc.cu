@@ -270,9 +270,10 @@ __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched
 
 // ------------------------------------------------------------------ producer (warp 0, lane 0, every CTA)
 // Scorer CTA q loads keys [64q, 64q + 64) of each 128-key tile, all nine
-// column chunks (64-row x 64-column boxes), into two tile stages; mixer CTA q
-// loads value chunks {2q, 2q+1, 2q+4, 2q+5} of each 64-key message (the N
-// halves the pair's P V MMAs expect) into kVStages message stages.  Both CTAs of
+// column chunks (one 3-D box: 64 rows x 9 chunks of 64 columns, chunk-major),
+// into two tile stages; mixer CTA q loads value chunks {2q, 2q+1, 2q+4, 2q+5}
+// of each 64-key message (two boxes of two chunks; the N halves the pair's P V
+// MMAs expect) into kVStages message stages.  Both CTAs of
 // a pair complete their bytes on the even CTA's barrier, which that CTA arms
 // for the pair.  Rows past the piece's end belong to other keys (masked by the
 // softmax) or lie outside the staged rows (zero fill).
