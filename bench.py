@@ -535,7 +535,37 @@ def defragmented_runs(args, case, dc, flush_buf, tokens):
     if status != 0:
         raise RuntimeError(f"verify on runs: {binding.status_string(status)}")
     ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    # a decode loop keeps the runs: each step appends only its new rows (here the drafts, the
+    # last Q_b rows of every sequence) and then verifies on the runs; timed as one event pair
+    nq = np.diff(case.qo_indptr).astype(np.int64)
+    first = torch.from_numpy((n - nq).astype(np.int32)).to(dc.q.device)
+
+    def decode_step():
+        binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, dst,
+                                              base_d, first, st)
+        call()
+
+    for _ in range(max(3, args.warmup)):
+        decode_step()
+    torch.cuda.synchronize()
+    steps = []
+    for _ in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        decode_step()
+        b.record()
+        steps.append((a, b))
+    torch.cuda.synchronize()
+    if int(st[0]) != 0 or binding.verify_attn_mla_check(ws) != 0:
+        raise RuntimeError("decode step on runs reported a fault")
+    dms = float(np.mean([a.elapsed_time(b) for a, b in steps]))
     return {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "KV tokens/s", "defrag_ms_once": defrag_ms,
+            "decode_step": {"ms_per_step": dms, "value": tokens / (dms / 1e3), "unit": "KV tokens/s",
+                            "appended_rows_per_step": int(nq.sum()),
+                            "note": "verify_attn_mla_defrag_append of the step's new rows (the drafts) into the "
+                                    "runs, then verify_attn_mla_runs; one event pair per step"},
             "note": "rows compacted once into 128-aligned pool runs (verify_attn_mla_defrag), then "
                     "verify_attn_mla_runs each step: no per-call gather; events around each call"}
 

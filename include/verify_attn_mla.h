@@ -181,6 +181,22 @@ int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_
                            const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
                            int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream);
 
+/* The same copy for a decode loop that keeps its runs across steps: rows
+ * j < first_row[b] of sequence b are already in place in its run (an earlier
+ * defragmentation of the same run wrote them) and are left alone; rows
+ * j >= first_row[b] are copied, and the run's tail is zeroed, as above.  A step
+ * that accepted a_b tokens and drafts Q_b new ones passes the previous step's
+ * accepted prefix length, so only the new rows cross.  The pages have no
+ * counterpart; it is the persistent layout kept up to date per step.
+ *   first_row [batch] int32 device: 0 <= first_row[b] <= N_b; a value outside
+ *             records VMLA_ERR_INDEX (with the sequence index) in status_word
+ *             and that sequence is skipped.
+ * Argument errors return before the launch.  No host synchronisation. */
+int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch,
+                                  void* dst_pool, int64_t dst_slots, const int32_t* run_base,
+                                  const int32_t* first_row, uint32_t* status_word, void* stream);
+
 /* verify_attn_mla on rows that lie in runs of the pool: the rows of sequence b
  * are kv_pool slots run_base[b] .. run_base[b] + N_b - 1 (its last Q_b rows
  * being the drafts), and the slots after each run up to a multiple of 128 hold

@@ -158,7 +158,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   if (runs) {
     // the runs must lie in the pool (the kernel reads whatever the tile loads
     // return; this check reports a run outside it)
-    rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, batch, total_kv, nullptr, pool_slots, run_base, true, status,
+    rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, kv_indptr_host, batch, total_kv, nullptr, pool_slots, run_base,
+                       true, status,
                        stream);
     if (rc != VMLA_OK) return rc;
   } else if (kernel == VMLA_KERNEL_TC) {
@@ -274,9 +275,10 @@ int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t*
   return VMLA_OK;
 }
 
-int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
-                           const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
-                           int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream) {
+namespace {
+int defrag_impl(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
+                const int32_t* kv_indptr_host, int batch, void* dst_pool, int64_t dst_slots, const int32_t* run_base,
+                const int32_t* first_row, uint32_t* status_word, void* stream) {
   if (!kv_indptr_host) return VMLA_ERR_NULL;
   if (batch < 0 || batch > VMLA_MAX_BATCH || src_slots < 0 || src_slots > INT32_MAX || dst_slots < 0 ||
       dst_slots > INT32_MAX || kv_indptr_host[0] != 0)
@@ -286,13 +288,32 @@ int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_
   const int64_t total_kv = batch > 0 ? kv_indptr_host[batch] : 0;
   if (total_kv == 0) return VMLA_OK;
   if (!src_pool || !dst_pool || !kv_indptr || !kv_indices || !run_base) return VMLA_ERR_NULL;
-  if (!aligned(src_pool, 16) || !aligned(dst_pool, 16) || !aligned(status_word, 4) || !aligned(run_base, 4))
+  if (!aligned(src_pool, 16) || !aligned(dst_pool, 16) || !aligned(status_word, 4) || !aligned(run_base, 4) ||
+      !aligned(first_row, 4))
     return VMLA_ERR_ALIGN;
   int sms = 0;
   int rc = current_sm_count(&sms, true);
   if (rc != VMLA_OK) return rc;
-  return launch_defrag(static_cast<const uint16_t*>(src_pool), src_slots, kv_indptr, kv_indices, batch, total_kv,
-                       static_cast<uint16_t*>(dst_pool), dst_slots, run_base, false, status_word, stream);
+  return launch_defrag(static_cast<const uint16_t*>(src_pool), src_slots, kv_indptr, kv_indices, kv_indptr_host,
+                       batch, total_kv, static_cast<uint16_t*>(dst_pool), dst_slots, run_base, false, status_word,
+                       stream, first_row);
+}
+}  // namespace
+
+int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
+                           const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
+                           int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream) {
+  return defrag_impl(src_pool, src_slots, kv_indptr, kv_indices, kv_indptr_host, batch, dst_pool, dst_slots,
+                     run_base, nullptr, status_word, stream);
+}
+
+int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch,
+                                  void* dst_pool, int64_t dst_slots, const int32_t* run_base,
+                                  const int32_t* first_row, uint32_t* status_word, void* stream) {
+  if (batch > 0 && kv_indptr_host && kv_indptr_host[batch] > 0 && !first_row) return VMLA_ERR_NULL;
+  return defrag_impl(src_pool, src_slots, kv_indptr, kv_indices, kv_indptr_host, batch, dst_pool, dst_slots,
+                     run_base, first_row, status_word, stream);
 }
 
 int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,

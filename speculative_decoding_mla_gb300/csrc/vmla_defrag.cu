@@ -11,10 +11,14 @@
 // run reads them (with no weight) and stale contents could hold non-finite
 // bf16 values.  verify_attn_mla_runs then reads the runs with no gather.
 //
-// One warp per row, as in the gather: lane l moves 16-byte granules l, l+32
-// and l+64 (< 72).  A source slot outside the pool records VMLA_ERR_INDEX and
+// One block per 128 rows of a run (grid rows are sequences), one warp per row
+// at a time as in the gather: lane l moves 16-byte granules l, l+32 and l+64
+// (< 72).  A source slot outside the pool records VMLA_ERR_INDEX and
 // writes a zero row; a run outside the destination records VMLA_ERR_INDEX
-// (with the sequence index) and is skipped.
+// (with the sequence index) and is skipped.  With first_row (the append form,
+// for a decode loop), rows j < first_row[b] are already in the run and are
+// left alone; a first_row[b] outside [0, N_b] records VMLA_ERR_INDEX (with the
+// sequence index) and that sequence is skipped.
 #include <cuda_runtime.h>
 
 #include "vmla_device.cuh"
@@ -34,45 +38,41 @@ __device__ __forceinline__ bool run_ok(const int32_t* kv_indptr, const int32_t* 
   return n >= 0 && base >= 0 && base + n <= slots;
 }
 
+__device__ __forceinline__ bool first_ok(const int32_t* kv_indptr, const int32_t* first_row, int b) {
+  if (!first_row) return true;
+  const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+  return first_row[b] >= 0 && first_row[b] <= n;
+}
+
+// Grid: x = blocks of kRunAlign rows of a run (its rows, then its zeroed tail),
+// y = sequence.  A block below first_row[b] or past the run returns at once, so
+// an append touches only the blocks that hold new rows.
 __global__ void __launch_bounds__(kDefragWarps * 32)
 defrag_kernel(const uint4* __restrict__ src, int64_t src_slots, const int32_t* __restrict__ kv_indptr,
-              const int32_t* __restrict__ kv_indices, int batch, int64_t total_kv, uint4* __restrict__ dst,
-              int64_t dst_slots, const int32_t* __restrict__ run_base, uint32_t* status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = (int64_t)blockIdx.x * kDefragWarps + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)gridDim.x * kDefragWarps;
-  const int64_t items = total_kv + (int64_t)batch * kRunAlign;  // rows, then each run's tail candidates
-  for (int64_t it = warp0; it < items; it += nwarps) {
-    int b;
-    int64_t r;
-    bool zero;
-    if (it < total_kv) {
-      int lo = 0, hi = batch;  // sequence owning row it: last b with kv_indptr[b] <= it
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (kv_indptr[mid] <= it) lo = mid; else hi = mid;
-      }
-      b = lo;
-      r = it - kv_indptr[b];
-      zero = false;
-    } else {
-      b = (int)((it - total_kv) / kRunAlign);
-      const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
-      r = n + (it - total_kv) % kRunAlign;
-      if (r >= round_run(n)) continue;  // warp-uniform
-      zero = true;
-    }
-    if (!run_ok(kv_indptr, run_base, b, dst_slots)) {
-      if (lane == 0 && r == 0 && !zero) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
-      continue;
-    }
+              const int32_t* __restrict__ kv_indices, uint4* __restrict__ dst, int64_t dst_slots,
+              const int32_t* __restrict__ run_base, const int32_t* __restrict__ first_row, uint32_t* status) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.y;
+  const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
+  const int64_t lo = (int64_t)blockIdx.x * kRunAlign;
+  if (lo >= round_run(n)) return;  // past this run and its tail
+  if (!run_ok(kv_indptr, run_base, b, dst_slots) || !first_ok(kv_indptr, first_row, b)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
+    return;
+  }
+  const int64_t first = first_row ? first_row[b] : 0;
+  if (lo + kRunAlign <= first && lo + kRunAlign <= n) return;  // rows already in the run, no tail here
+  for (int64_t r = lo + warp; r < lo + kRunAlign; r += kDefragWarps) {
+    const bool zero = r >= n;
+    if (!zero && r < first) continue;  // already in the run (warp-uniform)
     const int64_t row = (int64_t)run_base[b] + r;
     if (row >= dst_slots) continue;  // a tail past the pool: the tile loads read zeros there
     uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0;
     if (!zero) {
-      const int32_t slot = kv_indices[it];
+      const int64_t j = (int64_t)kv_indptr[b] + r;
+      const int32_t slot = kv_indices[j];
       const bool ok = slot >= 0 && (int64_t)slot < src_slots;
-      if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)it);
+      if (!ok && lane == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)j);
       if (ok) {
         const uint4* s = src + (int64_t)slot * kRowU4;
         v0 = s[lane];
@@ -97,25 +97,28 @@ __global__ void run_check_kernel(const int32_t* __restrict__ kv_indptr, const in
 }  // namespace
 
 int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
-                  int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots, const int32_t* run_base,
-                  bool check_only, uint32_t* status, void* stream) {
+                  const int32_t* kv_indptr_host, int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots,
+                  const int32_t* run_base, bool check_only, uint32_t* status, void* stream,
+                  const int32_t* first_row) {
   if (batch == 0) return VMLA_OK;
   if (check_only) {
     run_check_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(kv_indptr, run_base, batch, dst_slots,
                                                                            status);
     return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
   }
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                cudaSuccess)
-    return VMLA_ERR_CUDA;
-  const int64_t items = total_kv + (int64_t)batch * kRunAlign;
-  const int64_t need = (items + kDefragWarps - 1) / kDefragWarps;
-  const int64_t cap = (int64_t)sms * 8;
-  const int blocks = (int)(need < cap ? need : cap);
-  defrag_kernel<<<blocks, kDefragWarps * 32, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const uint4*>(src_pool), src_slots, kv_indptr, kv_indices, batch, total_kv,
-      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, status);
+  // blocks of kRunAlign rows over the longest run with its tail, one grid row per sequence
+  (void)total_kv;
+  int64_t longest = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t len = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
+    longest = len > longest ? len : longest;
+  }
+  const int64_t xblocks = (longest + kRunAlign - 1) / kRunAlign;
+  if (xblocks == 0) return VMLA_OK;
+  if (xblocks > INT32_MAX || batch > 65535) return VMLA_ERR_SHAPE;
+  defrag_kernel<<<dim3((unsigned)xblocks, (unsigned)batch), kDefragWarps * 32, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const uint4*>(src_pool), src_slots, kv_indptr, kv_indices,
+      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, first_row, status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

@@ -118,3 +118,62 @@ def test_runs_long_185k_sampled_rows():
     rows = sample_rows(case)
     ref_o, ref_l = oracle_rows(case, rows, "long_185k/sampled")
     compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, "runs / long_185k")
+
+
+def test_defrag_append_equals_full_defrag():
+    """A decode step's append: the runs hold an earlier state (each sequence g_b rows shorter); the append
+    copies only rows j >= first_row[b] = N_b - g_b of the new state.  The run regions then equal a full
+    defragmentation of the new state bit for bit, and the runs call on them equals the gather path; a
+    first_row past N_b is reported."""
+    torch, binding, device = _mods()
+    case = small("ragged", seed=515)
+    dc = device.to_device(case)
+    n = np.diff(case.kv_indptr).astype(np.int64)
+    rng = np.random.default_rng(516)
+    grow = np.array([int(rng.integers(1, k + 1)) if k > 0 else 0 for k in n], np.int64)
+    old_n = n - grow
+    old_indptr = np.zeros(case.batch + 1, np.int32)
+    old_indptr[1:] = np.cumsum(old_n)
+    ind = dc.kv_indices.cpu().numpy()
+    old_ind = np.concatenate([ind[case.kv_indptr[b]:case.kv_indptr[b] + old_n[b]] for b in range(case.batch)])
+    base, slots = _bases(case)
+    base_d = torch.from_numpy(base).cuda()
+
+    def nan_pool():
+        return torch.full((slots, 576), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    a = nan_pool()
+    binding.verify_attn_mla_defrag(dc.kv_pool, torch.from_numpy(old_indptr).cuda(),
+                                   torch.from_numpy(old_ind.astype(np.int32)).cuda(), old_indptr, a, base_d, st)
+    first = torch.from_numpy((n - grow).astype(np.int32)).cuda()
+    binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, a, base_d,
+                                          first, st)
+    b_pool = nan_pool()
+    binding.verify_attn_mla_defrag(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, b_pool, base_d, st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    av = a.view(torch.int16).cpu().numpy()
+    bv = b_pool.view(torch.int16).cpu().numpy()
+    for b in range(case.batch):
+        lo, hi = int(base[b]), int(base[b]) + int((n[b] + 127) // 128 * 128)
+        assert np.array_equal(av[lo:hi], bv[lo:hi]), b
+    # the runs call on the appended runs equals the gather path
+    out, lse = device.alloc_outputs(dc)
+    ws = torch.empty(max(256, binding.verify_attn_mla_runs_workspace_size(dc.qo_indptr_host, dc.kv_indptr_host,
+                                                                           dc.num_heads, 0)),
+                     dtype=torch.uint8, device="cuda")
+    binding.verify_attn_mla_runs(dc.q, a, dc.kv_indptr, base_d, dc.qo_indptr, dc.kv_indptr_host, dc.qo_indptr_host,
+                                 out, lse, ws, dc.sm_scale)
+    assert binding.verify_attn_mla_check(ws) == 0
+    o1, l1, s1 = run_full(case, "tc")
+    assert s1 == 0
+    assert np.array_equal(device.bf16_to_f64(out), o1) and np.array_equal(lse.cpu().numpy().astype(np.float64), l1)
+    # a first row past a sequence's length is reported, and that sequence is left alone
+    bad = first.clone()
+    bad[1] = int(n[1]) + 1
+    st.zero_()
+    binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, a, base_d,
+                                          bad, st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == binding.VMLA_ERR_INDEX and int(st[1]) == 1
