@@ -542,7 +542,7 @@ def defragmented_runs(args, case, dc, flush_buf, tokens):
 
     def decode_step():
         binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, dst,
-                                              base_d, first, st)
+                                              base_d, first, st, max_new_rows=int(nq.max()))
         call()
 
     for _ in range(max(3, args.warmup)):

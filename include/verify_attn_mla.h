@@ -191,11 +191,16 @@ int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_
  *   first_row [batch] int32 device: 0 <= first_row[b] <= N_b; a value outside
  *             records VMLA_ERR_INDEX (with the sequence index) in status_word
  *             and that sequence is skipped.
+ *   max_new_rows  a bound on N_b - first_row[b] known to the caller (the launch
+ *             then covers only that many rows past each first_row), or 0 for
+ *             none; a sequence with more new rows records VMLA_ERR_INDEX and
+ *             is skipped.  Negative: VMLA_ERR_SHAPE.
  * Argument errors return before the launch.  No host synchronisation. */
 int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
                                   const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch,
                                   void* dst_pool, int64_t dst_slots, const int32_t* run_base,
-                                  const int32_t* first_row, uint32_t* status_word, void* stream);
+                                  const int32_t* first_row, int64_t max_new_rows, uint32_t* status_word,
+                                  void* stream);
 
 /* verify_attn_mla on rows that lie in runs of the pool: the rows of sequence b
  * are kv_pool slots run_base[b] .. run_base[b] + N_b - 1 (its last Q_b rows

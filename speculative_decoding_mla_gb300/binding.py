@@ -82,7 +82,7 @@ def _load(path: str = LIB_PATH):
                                         sz, vp],
         "verify_attn_mla_tree_accept": [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp],
         "verify_attn_mla_defrag": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, vp],
-        "verify_attn_mla_defrag_append": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, vp, vp],
+        "verify_attn_mla_defrag_append": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, i64, vp, vp],
         "verify_attn_mla_runs": run,
         "verify_attn_mla_runs_workspace_size": [i32, i32, vp, vp, i32, ctypes.POINTER(sz)],
         "verify_attn_mla_test_fault": [i32, i64],
@@ -274,15 +274,16 @@ def verify_attn_mla_defrag(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_
 
 
 def verify_attn_mla_defrag_append(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, first_row,
-                                  status_word=None, stream=None):
-    """The defragmentation for a decode loop: rows below first_row[b] are already in sequence b's run."""
+                                  status_word=None, stream=None, max_new_rows=0):
+    """The defragmentation for a decode loop: rows below first_row[b] are already in sequence b's run
+    (max_new_rows: a bound on the new rows per sequence, or 0)."""
     kvh = _host_i32(kv_indptr_host)
     rc = _lib.verify_attn_mla_defrag_append(_d(src_pool, 2, "src_pool"), int(src_pool.shape[0]),
                                             _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
                                             kvh.ctypes.data, len(kvh) - 1, _d(dst_pool, 2, "dst_pool"),
                                             int(dst_pool.shape[0]), _d(run_base, 4, "run_base"),
-                                            _d(first_row, 4, "first_row"), _d(status_word, 4, "status_word"),
-                                            _stream(stream))
+                                            _d(first_row, 4, "first_row"), int(max_new_rows),
+                                            _d(status_word, 4, "status_word"), _stream(stream))
     _check(rc, "verify_attn_mla_defrag_append")
 
 

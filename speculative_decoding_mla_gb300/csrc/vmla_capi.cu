@@ -278,7 +278,7 @@ int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t*
 namespace {
 int defrag_impl(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
                 const int32_t* kv_indptr_host, int batch, void* dst_pool, int64_t dst_slots, const int32_t* run_base,
-                const int32_t* first_row, uint32_t* status_word, void* stream) {
+                const int32_t* first_row, int64_t max_new, uint32_t* status_word, void* stream) {
   if (!kv_indptr_host) return VMLA_ERR_NULL;
   if (batch < 0 || batch > VMLA_MAX_BATCH || src_slots < 0 || src_slots > INT32_MAX || dst_slots < 0 ||
       dst_slots > INT32_MAX || kv_indptr_host[0] != 0)
@@ -296,7 +296,7 @@ int defrag_impl(const void* src_pool, int64_t src_slots, const int32_t* kv_indpt
   if (rc != VMLA_OK) return rc;
   return launch_defrag(static_cast<const uint16_t*>(src_pool), src_slots, kv_indptr, kv_indices, kv_indptr_host,
                        batch, total_kv, static_cast<uint16_t*>(dst_pool), dst_slots, run_base, false, status_word,
-                       stream, first_row);
+                       stream, first_row, max_new);
 }
 }  // namespace
 
@@ -304,16 +304,18 @@ int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_
                            const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch, void* dst_pool,
                            int64_t dst_slots, const int32_t* run_base, uint32_t* status_word, void* stream) {
   return defrag_impl(src_pool, src_slots, kv_indptr, kv_indices, kv_indptr_host, batch, dst_pool, dst_slots,
-                     run_base, nullptr, status_word, stream);
+                     run_base, nullptr, 0, status_word, stream);
 }
 
 int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
                                   const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch,
                                   void* dst_pool, int64_t dst_slots, const int32_t* run_base,
-                                  const int32_t* first_row, uint32_t* status_word, void* stream) {
+                                  const int32_t* first_row, int64_t max_new_rows, uint32_t* status_word,
+                                  void* stream) {
   if (batch > 0 && kv_indptr_host && kv_indptr_host[batch] > 0 && !first_row) return VMLA_ERR_NULL;
+  if (max_new_rows < 0) return VMLA_ERR_SHAPE;
   return defrag_impl(src_pool, src_slots, kv_indptr, kv_indices, kv_indptr_host, batch, dst_pool, dst_slots,
-                     run_base, first_row, status_word, stream);
+                     run_base, first_row, max_new_rows, status_word, stream);
 }
 
 int verify_attn_mla_simt(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,

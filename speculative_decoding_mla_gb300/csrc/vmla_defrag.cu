@@ -46,21 +46,26 @@ __device__ __forceinline__ bool first_ok(const int32_t* kv_indptr, const int32_t
 
 // Grid: x = blocks of kRunAlign rows of a run (its rows, then its zeroed tail),
 // y = sequence.  A block below first_row[b] or past the run returns at once, so
-// an append touches only the blocks that hold new rows.
+// an append touches only the blocks that hold new rows.  With max_new > 0 the
+// x blocks start at the kRunAlign boundary below first_row[b] (the grid then
+// covers max_new new rows and the tail), and a sequence with more new rows
+// records VMLA_ERR_INDEX and is skipped.
 __global__ void __launch_bounds__(kDefragWarps * 32)
 defrag_kernel(const uint4* __restrict__ src, int64_t src_slots, const int32_t* __restrict__ kv_indptr,
               const int32_t* __restrict__ kv_indices, uint4* __restrict__ dst, int64_t dst_slots,
-              const int32_t* __restrict__ run_base, const int32_t* __restrict__ first_row, uint32_t* status) {
+              const int32_t* __restrict__ run_base, const int32_t* __restrict__ first_row, int64_t max_new,
+              uint32_t* status) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int64_t n = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
-  const int64_t lo = (int64_t)blockIdx.x * kRunAlign;
-  if (lo >= round_run(n)) return;  // past this run and its tail
-  if (!run_ok(kv_indptr, run_base, b, dst_slots) || !first_ok(kv_indptr, first_row, b)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
+  const bool valid = run_ok(kv_indptr, run_base, b, dst_slots) && first_ok(kv_indptr, first_row, b);
+  const int64_t first = first_row && valid ? first_row[b] : 0;
+  const int64_t lo = (max_new > 0 ? first / kRunAlign * kRunAlign : 0) + (int64_t)blockIdx.x * kRunAlign;
+  if (!valid || (max_new > 0 && n - first > max_new)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && n > 0) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
     return;
   }
-  const int64_t first = first_row ? first_row[b] : 0;
+  if (lo >= round_run(n)) return;  // past this run and its tail
   if (lo + kRunAlign <= first && lo + kRunAlign <= n) return;  // rows already in the run, no tail here
   for (int64_t r = lo + warp; r < lo + kRunAlign; r += kDefragWarps) {
     const bool zero = r >= n;
@@ -99,7 +104,7 @@ __global__ void run_check_kernel(const int32_t* __restrict__ kv_indptr, const in
 int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
                   const int32_t* kv_indptr_host, int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots,
                   const int32_t* run_base, bool check_only, uint32_t* status, void* stream,
-                  const int32_t* first_row) {
+                  const int32_t* first_row, int64_t max_new) {
   if (batch == 0) return VMLA_OK;
   if (check_only) {
     run_check_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(kv_indptr, run_base, batch, dst_slots,
@@ -113,12 +118,16 @@ int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv
     const int64_t len = (int64_t)kv_indptr_host[b + 1] - kv_indptr_host[b];
     longest = len > longest ? len : longest;
   }
-  const int64_t xblocks = (longest + kRunAlign - 1) / kRunAlign;
+  // all of the longest run, or (append with a bound) the new rows from the boundary below
+  // first_row plus the tail: max_new + 2 (kRunAlign - 1) rows at most
+  const int64_t span = max_new > 0 && max_new < longest ? max_new + 2 * (kRunAlign - 1) : longest;
+  const int64_t xblocks = (span + kRunAlign - 1) / kRunAlign;
   if (xblocks == 0) return VMLA_OK;
   if (xblocks > INT32_MAX || batch > 65535) return VMLA_ERR_SHAPE;
   defrag_kernel<<<dim3((unsigned)xblocks, (unsigned)batch), kDefragWarps * 32, 0, (cudaStream_t)stream>>>(
       reinterpret_cast<const uint4*>(src_pool), src_slots, kv_indptr, kv_indices,
-      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, first_row, status);
+      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, first_row, max_new > 0 && max_new < longest ? max_new : 0,
+      status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

@@ -152,12 +152,13 @@ def test_defrag_and_runs_argument_errors_before_any_launch(B):
     assert runs(base=fake + 2) == B.VMLA_ERR_ALIGN
     def append(**kw):
         a = dict(src=fake, ss=16, kvp=fake, kvi=fake, kvh=kvh.ctypes.data, batch=1, dst=fake, ds=64, base=fake,
-                 first=fake, st=None, stream=None)
+                 first=fake, mx=0, st=None, stream=None)
         a.update(kw)
         return L.verify_attn_mla_defrag_append(*a.values())
     assert append(first=None) == B.VMLA_ERR_NULL
     assert append(first=fake + 2) == B.VMLA_ERR_ALIGN
     assert append(batch=-1) == B.VMLA_ERR_SHAPE
+    assert append(mx=-1) == B.VMLA_ERR_SHAPE
     assert append(kvh=np.array([0, 0], np.int32).ctypes.data, first=None) == B.VMLA_OK  # nothing to copy
     import torch
     if not torch.cuda.is_available():

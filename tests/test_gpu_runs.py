@@ -149,15 +149,23 @@ def test_defrag_append_equals_full_defrag():
     first = torch.from_numpy((n - grow).astype(np.int32)).cuda()
     binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, a, base_d,
                                           first, st)
+    # the same append with the launch bounded by the largest number of new rows
+    a2 = nan_pool()
+    binding.verify_attn_mla_defrag(dc.kv_pool, torch.from_numpy(old_indptr).cuda(),
+                                   torch.from_numpy(old_ind.astype(np.int32)).cuda(), old_indptr, a2, base_d, st)
+    binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, a2, base_d,
+                                          first, st, max_new_rows=int(grow.max()))
     b_pool = nan_pool()
     binding.verify_attn_mla_defrag(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, b_pool, base_d, st)
     torch.cuda.synchronize()
     assert int(st[0]) == 0
     av = a.view(torch.int16).cpu().numpy()
+    a2v = a2.view(torch.int16).cpu().numpy()
     bv = b_pool.view(torch.int16).cpu().numpy()
     for b in range(case.batch):
         lo, hi = int(base[b]), int(base[b]) + int((n[b] + 127) // 128 * 128)
         assert np.array_equal(av[lo:hi], bv[lo:hi]), b
+        assert np.array_equal(a2v[lo:hi], bv[lo:hi]), b
     # the runs call on the appended runs equals the gather path
     out, lse = device.alloc_outputs(dc)
     ws = torch.empty(max(256, binding.verify_attn_mla_runs_workspace_size(dc.qo_indptr_host, dc.kv_indptr_host,
@@ -177,3 +185,13 @@ def test_defrag_append_equals_full_defrag():
                                           bad, st)
     torch.cuda.synchronize()
     assert int(st[0]) == binding.VMLA_ERR_INDEX and int(st[1]) == 1
+    # a sequence with more new rows than the stated bound is reported and left alone
+    big = int(np.argmax(grow))
+    if grow[big] > 1:
+        st.zero_()
+        before = a.view(torch.int16).clone()
+        binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, a,
+                                              base_d, first, st, max_new_rows=int(grow[big]) - 1)
+        torch.cuda.synchronize()
+        assert int(st[0]) == binding.VMLA_ERR_INDEX
+        assert torch.equal(a.view(torch.int16), before)  # the rows were already there: nothing changed
