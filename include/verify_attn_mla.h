@@ -75,19 +75,34 @@ typedef struct vmla_plan_info {
   int64_t partial_rows;     /* fp32 partial (row, split) results kept in the workspace */
   int64_t merge_rows;       /* query rows whose splits the merge kernel combines */
   size_t workspace_bytes;   /* bytes verify_attn_mla needs in `workspace` */
+  int32_t lane_width;       /* tensor-core kernel: 0 = equal pieces dealt to the clusters; G > 0 = the
+                               lane plan (lanes of G clusters, each sequence's work cut where the
+                               lanes' shares end) */
+  int32_t lane_count;       /* lanes with work in a lane plan, else 0 */
 } vmla_plan_info;
 
 /* Kernel families a plan can be made for. */
 #define VMLA_KERNEL_TC 0   /* tcgen05 / TMEM tensor-core kernel (what verify_attn_mla runs) */
 #define VMLA_KERNEL_SIMT 1 /* plain CUDA-core kernel (verify_attn_mla_simt) */
 
+/* `splits` value that makes the tensor-core planner take its lane plan
+ * whenever the lanes fit (at most 64 of them), instead of only when it scores
+ * lower; the CUDA-core kernel treats it as 0. */
+#define VMLA_SPLITS_LANES (-1)
+
 /* Split planner.  Splits each sequence's key range into contiguous pieces so
  * that the work units fill `num_sms` SMs (the NSPLIT occupancy fix of "The
  * Build That Unlocked 3-6x Decode Speedup", section "Broader Significance").
+ * For the tensor-core kernel with splits = 0 the plan is made for num_sms / 4
+ * clusters: either equal pieces per sequence, or (when it balances the
+ * clusters better) the lane plan, whose pieces end where the lanes' shares of
+ * all sequences' work end (info->lane_width > 0).
  *   qo_indptr_host, kv_indptr_host: host arrays [batch+1], starting at 0.
  *   splits: 0 = choose per sequence; k > 0 = k pieces for every sequence
- *           (capped so that no piece is empty).
- *   splits_out: optional host array [batch] receiving each sequence's count.
+ *           (capped so that no piece is empty); VMLA_SPLITS_LANES = the lane
+ *           plan where it fits.
+ *   splits_out: optional host array [batch] receiving each sequence's count
+ *           (lane plan: the most pieces any of its row blocks has).
  * Returns VMLA_OK or VMLA_ERR_NULL / VMLA_ERR_SHAPE.  Pure host code. */
 int verify_attn_mla_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_host,
                          const int32_t* kv_indptr_host, int splits, int num_sms, vmla_plan_info* info,
@@ -117,7 +132,8 @@ int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_i
  *   kv_indptr_host, qo_indptr_host: host copies of the two indptr arrays; read
  *               during the call to build the plan, not retained.
  *   sm_scale    score scale, finite and > 0 (1/sqrt(192) for the target model)
- *   splits      0 = planner's choice; k > 0 forces k pieces per sequence
+ *   splits      0 = planner's choice; k > 0 forces k pieces per sequence;
+ *               VMLA_SPLITS_LANES takes the lane plan where it fits
  *   out         [T_q, H, 512] bf16 (16 B aligned);  lse [T_q, H] fp32
  *   workspace   >= verify_attn_mla_workspace_size() bytes, 256 B aligned.
  *               Holds the status word, ancestor masks, split partials and a

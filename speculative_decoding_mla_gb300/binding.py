@@ -29,6 +29,7 @@ VMLA_ERR_DEVICE = -8
 VMLA_ERR_PARENT = -9
 VMLA_KERNEL_TC = 0
 VMLA_KERNEL_SIMT = 1
+VMLA_SPLITS_LANES = -1  # splits value: the tensor-core planner takes its lane plan where it fits
 D_QK = 576
 D_V = 512
 
@@ -52,7 +53,8 @@ class VmlaError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("num_units", ctypes.c_int32), ("max_splits", ctypes.c_int32), ("partial_rows", ctypes.c_int64),
-                ("merge_rows", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
+                ("merge_rows", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t), ("lane_width", ctypes.c_int32),
+                ("lane_count", ctypes.c_int32)]
 
 
 def _load(path: str = LIB_PATH):

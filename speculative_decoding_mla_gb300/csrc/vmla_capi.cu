@@ -22,7 +22,7 @@ int check_common(const int32_t* kv_indptr_host, const int32_t* qo_indptr_host, i
                  int64_t pool_slots, int splits) {
   if (!kv_indptr_host || !qo_indptr_host) return VMLA_ERR_NULL;
   if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
-  if (splits < 0 || splits > 64 || pool_slots < 0 || pool_slots > INT32_MAX) return VMLA_ERR_SHAPE;
+  if (splits < VMLA_SPLITS_LANES || splits > 64 || pool_slots < 0 || pool_slots > INT32_MAX) return VMLA_ERR_SHAPE;
   if (kv_indptr_host[0] != 0 || qo_indptr_host[0] != 0) return VMLA_ERR_SHAPE;
   for (int b = 0; b < batch; ++b) {
     int64_t nq = (int64_t)qo_indptr_host[b + 1] - qo_indptr_host[b];
@@ -523,7 +523,7 @@ namespace {
 // Bounds of a device-planned call (host values only).
 int check_dplan_bounds(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits) {
   if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
-  if (splits < 0 || splits > 64) return VMLA_ERR_SHAPE;
+  if (splits < VMLA_SPLITS_LANES || splits > 64) return VMLA_ERR_SHAPE;
   if (max_total_q < 0 || max_total_q > (int64_t)batch * VMLA_MAX_DRAFT) return VMLA_ERR_SHAPE;
   if (max_total_kv < 0 || max_total_kv > INT32_MAX) return VMLA_ERR_SHAPE;
   return VMLA_OK;

@@ -10,7 +10,9 @@
 // a cluster schedule for the tensor-core kernel (units sorted by cost, dealt
 // to the clusters in a snake order, then in unit order within each cluster).
 // The piece size is the host planner's choice among the same candidates,
-// scored with the same integer arithmetic, one warp per candidate.
+// scored with the same integer arithmetic, one warp per candidate, and the
+// lane plan replaces it under the host planner's rule (one thread per
+// sequence, block-wide prefix sums for the streams' positions).
 // The areas of the workspace are sized for caller-given upper bounds on the
 // query and key totals.
 #include <cuda_runtime.h>
@@ -27,6 +29,7 @@ static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
 static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
 static_assert(kPlanThreads / 32 == kChunkCands, "one warp per piece-size candidate");
 static_assert(kChunkCands * kRunsPerSeq * kSearchMaxBatch <= kSortKeys, "candidate runs fit the sort keys");
+static_assert(5 * VMLA_MAX_BATCH <= kSortKeys, "the lane plan's prefix sums fit the sort keys");
 
 __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -136,7 +139,8 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   __shared__ int64_t s_units[VMLA_MAX_BATCH], s_part[VMLA_MAX_BATCH], s_merge[VMLA_MAX_BATCH];
   __shared__ uint64_t keys[kSortKeys];
   __shared__ unsigned long long s_work;
-  __shared__ int s_bad, s_maxs;
+  __shared__ int s_bad, s_maxs, s_cand, s_lanes;
+  __shared__ unsigned int s_misfit;
   __shared__ int64_t s_score[kChunkCands];
   __shared__ int64_t s_chunk;
   const int tid = threadIdx.x;
@@ -145,6 +149,7 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     s_work = 0;
     s_bad = 0;
     s_maxs = 0;
+    s_misfit = 0;
   }
   __syncthreads();
   // lengths: each thread checks one sequence and adds its work
@@ -162,6 +167,8 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   __syncthreads();
   const bool lengths_ok = s_bad == 0;
   const int64_t total_work = (int64_t)s_work;
+  const bool force_lanes = splits == VMLA_SPLITS_LANES;
+  if (force_lanes) splits = 0;  // the uniform plan it falls back on is the planner's own
   const bool search = lengths_ok && splits == 0 && batch >= 1 && batch <= kSearchMaxBatch;
   if (search) {
     const int w = tid >> 5;
@@ -170,11 +177,103 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     if ((tid & 31) == 0) s_score[w] = sc;
   }
   __syncthreads();
-  if (tid == 0)
-    s_chunk = search ? plan_choose_cand(sh, total_work, clusters, s_score)
-                     : plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
+  if (tid == 0) {
+    s_cand = search ? plan_choose_cand(s_score) : kDefaultCand;
+    s_chunk = plan_cand_chunk(sh, total_work, clusters, s_cand);
+  }
   __syncthreads();
   const int64_t chunk_target = s_chunk;
+
+  // ---- the lane plan, weighed against the chosen uniform plan (plan_lanes_host's rule)
+  const int64_t R = nq * num_heads;
+  const int64_t n_rb = tid < batch && nq > 0 ? plan_ceil_div(R, sh.rows_per_unit) : 0;
+  if (n_rb > 0) atomicOr(&s_misfit, plan_lane_misfit(n_rb));
+  // prefix sums over the sequences in the sort keys' space (free until the schedule)
+  int64_t* l_cost = reinterpret_cast<int64_t*>(keys);
+  int64_t* l_stream = l_cost + VMLA_MAX_BATCH;
+  int64_t* l_part = l_stream + VMLA_MAX_BATCH;
+  int64_t* l_merge = l_part + VMLA_MAX_BATCH;
+  int64_t* l_units = l_merge + VMLA_MAX_BATCH;
+  __syncthreads();
+  const int G = plan_lane_width(s_misfit);
+  const int lanes = clusters / G;
+  const int64_t ng = n_rb / G;
+  const int64_t span = plan_stream_span(nk);
+  if (tid < batch) {
+    l_cost[tid] = ng * span;
+    l_stream[tid] = ng;
+  }
+  __syncthreads();
+  block_scan(l_cost, batch);
+  block_scan(l_stream, batch);
+  const int64_t W = batch > 0 ? l_cost[batch - 1] : 0;
+  const int64_t Lt = plan_lane_tiles(W, lanes);
+  const bool lane_fit =
+      (search || (force_lanes && lengths_ok)) && lanes >= 1 && lanes <= sh.max_splits && W >= 1 && W <= INT32_MAX;
+  int64_t lpr = 0, lmr = 0, lps = 0, lsplit = 1;
+  if (lane_fit && n_rb > 0)
+    lsplit = plan_lane_seq_split(l_cost[tid] - ng * span, ng, nk, Lt, R, (int64_t)G * sh.rows_per_unit, &lpr, &lmr,
+                                 &lps);
+  if (tid < batch) {
+    l_part[tid] = lpr;
+    l_merge[tid] = lmr;
+    l_units[tid] = lps * G;
+  }
+  __syncthreads();
+  block_scan(l_part, batch);
+  block_scan(l_merge, batch);
+  block_scan(l_units, batch);
+  if (tid == 0) {
+    const int64_t lpart = batch > 0 ? l_part[batch - 1] : 0;
+    s_lanes = lane_fit && lpart <= INT32_MAX / kDv &&
+              (force_lanes || plan_prefer_lanes(plan_lane_score(Lt, lpart), s_score[s_cand]));
+  }
+  __syncthreads();
+  if (s_lanes) {
+    if (tid < batch) {
+      SeqPlan lp = {};
+      lp.kv_off = kv[tid];
+      lp.n_kv = (int32_t)nk;
+      lp.q_off = qo[tid];
+      lp.n_q = (int32_t)nq;
+      lp.unit_start = (int32_t)(l_stream[tid] - ng);
+      lp.lane_cost = (int32_t)(l_cost[tid] - ng * span);
+      lp.part_off = (int32_t)(l_part[tid] - lpr);
+      lp.merge_off = (int32_t)(l_merge[tid] - lmr);
+      lp.chunk = nk > 1 ? (int32_t)nk : 1;
+      lp.n_split = (int32_t)lsplit;
+      lp.n_rb = (int32_t)n_rb;
+      pp->seq[tid] = lp;
+      if (n_rb > 0) atomicMax(&s_maxs, (int)lsplit);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int64_t part = batch > 0 ? l_part[batch - 1] : 0;
+      const bool ok = part <= part_cap;
+      const int lane_count = (int)plan_ceil_div(W, Lt);
+      pp->batch = batch;
+      pp->num_heads = num_heads;
+      pp->rows_per_unit = sh.rows_per_unit;
+      pp->total_units = ok ? (int32_t)l_units[batch - 1] : 0;
+      pp->merge_rows = ok ? (int32_t)l_merge[batch - 1] : 0;
+      pp->max_splits = ok ? s_maxs : 0;
+      pp->partial_rows = ok ? (int32_t)part : 0;
+      pp->lane_width = G;
+      pp->lane_tiles = (int32_t)Lt;
+      pp->lane_total = (int32_t)W;
+      pp->lane_count = ok ? lane_count : 0;
+      pp->pad = 0;
+      status[2] = ok ? (uint32_t)kv[batch] : 0u;
+      status[3] = ok ? (uint32_t)qo[batch] : 0u;
+      if (!ok) record_status(status, VMLA_ERR_SHAPE, 2u);
+      sched->num_clusters = ok ? lane_count * G : 0;
+      sched->total_units = ok ? (int32_t)l_units[batch - 1] : 0;
+      sched->unit_base = 0;
+      sched->pad = 0;
+    }
+    return;
+  }
+  __syncthreads();
   SeqPlan sp = {};
   int64_t u = 0, pr = 0, mr = 0;
   if (tid < batch) {
@@ -210,6 +309,10 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     pp->merge_rows = ok ? (int32_t)merge : 0;
     pp->max_splits = ok ? s_maxs : 0;
     pp->partial_rows = ok ? (int32_t)part : 0;
+    pp->lane_width = 0;
+    pp->lane_tiles = 0;
+    pp->lane_total = 0;
+    pp->lane_count = 0;
     pp->pad = 0;
     status[2] = ok ? (uint32_t)kv[batch] : 0u;  // rows the gather stages
     status[3] = ok ? (uint32_t)qo[batch] : 0u;  // draft rows the mask kernel expands
@@ -265,10 +368,14 @@ DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t 
   // units are at most clusters x m / 16 + (row blocks) with the planner's own
   // piece count (the largest candidate m; each sequence's pieces exceed its
   // share by less than one), or splits x (row blocks) when the count is
-  // forced; 256 partial rows each
+  // forced; 256 partial rows each.  A lane plan's partial rows are at most
+  // 256 (clusters + 2 row blocks): a stream of T tiles has at most
+  // (T - 1) / L + 2 pieces, and the streams' tiles times their row blocks sum
+  // to at most G W <= clusters L.
   const int64_t row_blocks = plan_ceil_div(max_total_q * num_heads, sh.rows_per_unit) + batch;
   const int64_t units = splits > 0 ? (int64_t)splits * row_blocks
-                                   : plan_ceil_div((int64_t)clusters * plan_cand_m(kChunkCands - 1), 16) + row_blocks;
+                                   : plan_ceil_div((int64_t)clusters * plan_cand_m(kChunkCands - 1), 16) +
+                                         2 * row_blocks;
   int64_t cap = units * sh.rows_per_unit;
   const int64_t all = max_total_q * num_heads * sh.max_splits;
   if (cap > all) cap = all;

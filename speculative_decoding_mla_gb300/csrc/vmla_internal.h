@@ -13,17 +13,28 @@ constexpr int kDv = VMLA_D_V;
 constexpr int kRowBytes = kDqk * 2;  // 1152 bytes per latent KV row / per query head
 
 // Per-sequence entry of a split plan (passed to the kernels by value).
+//
+// Two forms.  Uniform plan (lane_width 0): sequence b's keys are cut into
+// n_split pieces of `chunk` keys, and each (piece, row block) is a work unit
+// that the cluster schedule deals out.  Lane plan (tensor-core kernel,
+// lane_width G > 0): the clusters form lanes of G; each sequence's row blocks
+// form n_rb / G streams of G row blocks over all its key tiles, laid end to
+// end in a cost space (a stream spans its tiles plus kUnitFixedTiles); lane l
+// takes the cost interval [l L, (l + 1) L) of every stream it meets, and
+// cluster j of the lane takes row block g G + j of stream g.  A stream's pieces
+// are the lanes it meets (vmla_plan_core.h).
 struct SeqPlan {
   int32_t kv_off;      // kv_indptr[b]
   int32_t n_kv;        // N_b keys (prefix + drafts)
   int32_t q_off;       // qo_indptr[b]
   int32_t n_q;         // Q_b drafts
-  int32_t unit_start;  // first work unit of this sequence
+  int32_t unit_start;  // first work unit (uniform plan) or first stream (lane plan) of this sequence
   int32_t n_rb;        // row blocks (rows r = i*H + h, in blocks of rows_per_unit)
-  int32_t n_split;     // key-range pieces
-  int32_t chunk;       // keys per piece (piece s covers [s*chunk, min(N_b, (s+1)*chunk)))
+  int32_t n_split;     // key-range pieces (lane plan: the most of any of its streams)
+  int32_t chunk;       // keys per piece (piece s covers [s*chunk, min(N_b, (s+1)*chunk))); uniform plan
   int32_t part_off;    // first partial row of this sequence (partial row = part_off + s*R_b + r)
   int32_t merge_off;   // first merge row (monotone over b; only split sequences own merge rows)
+  int32_t lane_cost;   // lane plan: cost-space position of its first stream (monotone over b)
 };
 
 struct PlanParams {
@@ -34,6 +45,10 @@ struct PlanParams {
   int32_t rows_per_unit;
   int32_t max_splits;
   int32_t partial_rows;
+  int32_t lane_width;  // G of a lane plan, 0 for a uniform plan
+  int32_t lane_tiles;  // L: cost-space length each lane takes
+  int32_t lane_total;  // W: cost-space length of all streams
+  int32_t lane_count;  // lanes with work (the launch has lane_count x G clusters)
   int32_t pad;
   SeqPlan seq[VMLA_MAX_BATCH];
 };

@@ -1,7 +1,9 @@
 // Split merge and draft-tree mask expansion.
 //
 // Merge: each split piece s of a query row left a normalised partial output
-// o_s and its log-sum-exp; the row's result is
+// o_s and its log-sum-exp (in a lane plan only the rows of streams cut into
+// several pieces are merge rows: the others have their results already); the
+// row's result is
 //   lse = log sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s,
 // the combination of partial softmaxes that the NSPLIT split-KV of "The Build
 // Script Edit", section "Context: The Long Road to a Custom sm_120 Kernel",
@@ -17,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "vmla_device.cuh"
+#include "vmla_plan_core.h"
 
 namespace vmla {
 namespace {
@@ -42,8 +45,28 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
   const SeqPlan& sp = plan.seq[lo];
   const int H = plan.num_heads;
   const int R = sp.n_q * H;
-  const int r = mrow - sp.merge_off;
-  const int S = sp.n_split;
+  int r = mrow - sp.merge_off;
+  int S = sp.n_split;
+  if (plan.lane_width > 0) {
+    // lane plan: the sequence's merge rows are the rows of its streams cut into more than
+    // one piece, stream by stream (a stream in one lane was written by the verify kernel)
+    const int64_t T = plan_seq_tiles(sp.n_kv), per = (int64_t)plan.lane_width * plan.rows_per_unit;
+    const int ng = sp.n_rb / plan.lane_width;
+    int m = r;
+    S = 0;
+    for (int g = 0; g < ng; ++g) {
+      const int p = (int)plan_stream_pieces(sp.lane_cost + g * (T + kUnitFixedTiles), T, plan.lane_tiles);
+      if (p < 2) continue;
+      const int rows = (int)plan_stream_rows(g, per, R);
+      if (m < rows) {
+        r = (int)(g * per) + m;
+        S = p;
+        break;
+      }
+      m -= rows;
+    }
+    if (S == 0) return;  // past the split streams' rows (not reached for a consistent plan)
+  }
   const float to2 = lse_is_log2 ? 1.f : 1.4426950408889634f;
   const float4* src0 = reinterpret_cast<const float4*>(part_o + ((int64_t)sp.part_off + r) * kDv) + c * 32 + lane;
   const int64_t piece_stride = (int64_t)R * (kDv / 4);  // float4s between pieces of one row

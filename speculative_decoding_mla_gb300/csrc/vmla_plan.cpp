@@ -22,9 +22,11 @@ namespace vmla {
 //   F_j(x) = 2 floor(x / 2C) + [x mod 2C > j] + [x mod 2C > 2C - 1 - j],
 // so load_j = K + S(j) + S(2C - 1 - j) with K the whole-period part and S(x)
 // the sum over residues v > x of (cost at end residue v) - (cost at start residue v).
+// *chosen_score: the chosen candidate's score, or -1 when the search does not run.
 static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_heads, const int32_t* qo,
-                                    const int32_t* kv, int clusters, int64_t total_work) {
+                                    const int32_t* kv, int clusters, int64_t total_work, int64_t* chosen_score) {
   const int64_t def = plan_cand_chunk(sh, total_work, clusters, kDefaultCand);
+  *chosen_score = -1;
   if (batch > kSearchMaxBatch || batch < 1 || clusters < 1) return def;
   const int R = kRunsPerSeq * batch;
   const int64_t period = 2 * (int64_t)clusters;
@@ -117,7 +119,81 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
     score[k] = worst + plan_merge_score(part);
     if (best < 0 || score[k] < best) best = score[k];
   }
-  return plan_choose_cand(sh, total_work, clusters, score);
+  const int k = plan_choose_cand(score);
+  *chosen_score = score[k];
+  return plan_cand_chunk(sh, total_work, clusters, k);
+}
+
+// The lane plan (vmla_plan_core.h) of a tensor-core call, written into pp if it
+// scores lower than the uniform plan's `uniform_score` (or, forced, whenever the
+// lanes fit); returns whether it did.
+static bool plan_lanes_host(const PlanShape& sh, int batch, int num_heads, const int32_t* qo, const int32_t* kv,
+                            int clusters, int64_t uniform_score, bool forced, PlanParams* pp) {
+  if (uniform_score < 0 && !forced) return false;
+  uint32_t misfit = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t nq = (int64_t)qo[b + 1] - qo[b];
+    if (nq > 0) misfit |= plan_lane_misfit(plan_ceil_div(nq * num_heads, sh.rows_per_unit));
+  }
+  const int G = plan_lane_width(misfit);
+  const int lanes = clusters / G;
+  if (lanes < 1 || lanes > sh.max_splits) return false;
+  int64_t W = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t nq = (int64_t)qo[b + 1] - qo[b];
+    if (nq > 0) W += plan_ceil_div(nq * num_heads, sh.rows_per_unit) / G * plan_stream_span((int64_t)kv[b + 1] - kv[b]);
+  }
+  if (W < 1 || W > INT32_MAX) return false;
+  const int64_t L = plan_lane_tiles(W, lanes);
+  int64_t c0 = 0, part = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t nq = (int64_t)qo[b + 1] - qo[b], nk = (int64_t)kv[b + 1] - kv[b];
+    if (nq == 0) continue;
+    const int64_t ng = plan_ceil_div(nq * num_heads, sh.rows_per_unit) / G;
+    int64_t pr = 0, mr = 0, ps = 0;
+    plan_lane_seq_split(c0, ng, nk, L, nq * num_heads, (int64_t)G * sh.rows_per_unit, &pr, &mr, &ps);
+    part += pr;
+    c0 += ng * plan_stream_span(nk);
+  }
+  if ((!forced && !plan_prefer_lanes(plan_lane_score(L, part), uniform_score)) || part > INT32_MAX / kDv)
+    return false;
+  // the plan: streams in sequence order, each sequence's partial rows and merge rows after the previous ones
+  int64_t stream = 0, units = 0, merge = 0;
+  int max_s = 0;
+  c0 = 0;
+  part = 0;
+  for (int b = 0; b < batch; ++b) {
+    SeqPlan& s = pp->seq[b];
+    const int64_t nq = (int64_t)qo[b + 1] - qo[b], nk = (int64_t)kv[b + 1] - kv[b];
+    s.unit_start = (int32_t)stream;
+    s.lane_cost = (int32_t)c0;
+    s.part_off = (int32_t)part;
+    s.merge_off = (int32_t)merge;
+    s.chunk = nk > 1 ? (int32_t)nk : 1;
+    s.n_split = 1;
+    s.n_rb = 0;
+    if (nq == 0) continue;
+    s.n_rb = (int32_t)plan_ceil_div(nq * num_heads, sh.rows_per_unit);
+    const int64_t ng = s.n_rb / G;
+    int64_t pr = 0, mr = 0, ps = 0;
+    s.n_split =
+        (int32_t)plan_lane_seq_split(c0, ng, nk, L, nq * num_heads, (int64_t)G * sh.rows_per_unit, &pr, &mr, &ps);
+    part += pr;
+    merge += mr;
+    units += ps * G;
+    stream += ng;
+    c0 += ng * plan_stream_span(nk);
+    max_s = std::max<int>(max_s, s.n_split);
+  }
+  pp->total_units = (int32_t)units;
+  pp->merge_rows = (int32_t)merge;
+  pp->max_splits = max_s;
+  pp->partial_rows = (int32_t)part;
+  pp->lane_width = G;
+  pp->lane_tiles = (int32_t)L;
+  pp->lane_total = (int32_t)W;
+  pp->lane_count = (int32_t)plan_ceil_div(W, L);
+  return true;
 }
 
 WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows) {
@@ -137,7 +213,9 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   if (!qo || !kv || !pp) return VMLA_ERR_NULL;
   if (kernel != VMLA_KERNEL_TC && kernel != VMLA_KERNEL_SIMT) return VMLA_ERR_SHAPE;
   if (batch < 0 || batch > VMLA_MAX_BATCH || num_heads < 1 || num_heads > VMLA_MAX_HEADS) return VMLA_ERR_SHAPE;
-  if (splits < 0 || num_sms < 1) return VMLA_ERR_SHAPE;
+  if (splits < VMLA_SPLITS_LANES || num_sms < 1) return VMLA_ERR_SHAPE;
+  const bool force_lanes = splits == VMLA_SPLITS_LANES;
+  if (force_lanes) splits = 0;  // the uniform plan it falls back on is the planner's own
   if (qo[0] != 0 || kv[0] != 0) return VMLA_ERR_SHAPE;
   for (int b = 0; b < batch; ++b)
     if (plan_check_seq((int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b]) != VMLA_OK) return VMLA_ERR_SHAPE;
@@ -153,9 +231,11 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   int64_t total_work = 0;  // (row block) x (keys)
   for (int b = 0; b < batch; ++b) total_work += plan_seq_work(sh, qo[b + 1] - qo[b], kv[b + 1] - kv[b], num_heads);
   // the tensor-core kernel's piece size is chosen by scoring candidate schedules
-  const int64_t chunk_target = kernel == VMLA_KERNEL_TC && splits == 0
-                                   ? plan_pick_chunk_host(sh, batch, num_heads, qo, kv, clusters, total_work)
-                                   : plan_chunk_target(sh, total_work, slots);
+  int64_t uniform_score = -1;
+  const int64_t chunk_target =
+      kernel == VMLA_KERNEL_TC && splits == 0
+          ? plan_pick_chunk_host(sh, batch, num_heads, qo, kv, clusters, total_work, &uniform_score)
+          : plan_chunk_target(sh, total_work, slots);
 
   int64_t unit = 0, part = 0, merge = 0;
   int max_s = 0;
@@ -179,12 +259,18 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo, const in
   pp->merge_rows = (int32_t)merge;
   pp->max_splits = max_s;
   pp->partial_rows = (int32_t)part;
+  // the tensor-core kernel may take the lane plan instead (it rewrites the pieces)
+  if (kernel == VMLA_KERNEL_TC && splits == 0)
+    plan_lanes_host(sh, batch, num_heads, qo, kv, clusters, uniform_score, force_lanes, pp);
   if (info) {
-    info->num_units = (int32_t)unit;
-    info->max_splits = max_s;
-    info->partial_rows = part;
-    info->merge_rows = merge;
-    info->workspace_bytes = workspace_layout(qo[batch], part, kernel == VMLA_KERNEL_TC ? kv[batch] : 0).total;
+    info->num_units = pp->total_units;
+    info->max_splits = pp->max_splits;
+    info->partial_rows = pp->partial_rows;
+    info->merge_rows = pp->merge_rows;
+    info->workspace_bytes =
+        workspace_layout(qo[batch], pp->partial_rows, kernel == VMLA_KERNEL_TC ? kv[batch] : 0).total;
+    info->lane_width = pp->lane_width;
+    info->lane_count = pp->lane_count;
   }
   return VMLA_OK;
 }

@@ -178,14 +178,98 @@ VMLA_HD bool plan_run_before(int64_t cost_a, int a, int64_t cost_b, int b) {
   return cost_a > cost_b || (cost_a == cost_b && a < b);
 }
 
-// The chosen chunk target from the candidates' scores (-1: not a candidate).
-VMLA_HD int64_t plan_choose_cand(const PlanShape& sh, int64_t total_work, int clusters, const int64_t* score) {
+// The chosen candidate from the candidates' scores (-1: not a candidate).
+VMLA_HD int plan_choose_cand(const int64_t* score) {
   int best = -1;
   for (int k = 0; k < kChunkCands; ++k)
     if (score[k] >= 0 && (best < 0 || score[k] < score[best])) best = k;
   const int64_t d = score[kDefaultCand];
   if (best < 0 || (d >= 0 && !(score[best] * 100 < d * 97))) best = kDefaultCand;
-  return plan_cand_chunk(sh, total_work, clusters, best);
+  return best;
+}
+
+// ---------------------------------------------------------------- lane plan of the tensor-core kernel
+// The uniform plan deals equal pieces to the clusters; when the sequences'
+// lengths do not divide into the clusters evenly its longest cluster load can
+// sit well above the mean.  The lane plan instead cuts the work where the
+// clusters' shares end (the wrap-around rule for splittable jobs on identical
+// machines: lay the jobs end to end and cut every L): each stream (G row blocks
+// of one sequence over all its key tiles) occupies its tiles plus a fixed
+// charge in a cost space, and lane l takes [l L, (l + 1) L).  The G clusters of
+// a lane take the G row blocks of the same stream pieces, so that they read the
+// same key tiles at about the same time and share them through L2.  A stream
+// cut into several pieces leaves fp32 partials that the merge combines; a
+// stream within one lane writes its rows directly.
+constexpr int kLaneMaxWidth = 4;
+constexpr int64_t kUnitFixedTiles = kUnitFixedKeys / 128;
+
+// Widths 2..kLaneMaxWidth that do not divide a sequence's row-block count (bit g).
+VMLA_HD uint32_t plan_lane_misfit(int64_t n_rb) {
+  uint32_t m = 0;
+  if (n_rb > 0)
+    for (int g = 2; g <= kLaneMaxWidth; ++g)
+      if (n_rb % g != 0) m |= 1u << g;
+  return m;
+}
+
+// Lane width: the largest g <= kLaneMaxWidth that divides every sequence's row
+// blocks (the OR of their misfit masks), so that every stream has G row blocks.
+VMLA_HD int plan_lane_width(uint32_t misfit) {
+  for (int g = kLaneMaxWidth; g >= 2; --g)
+    if (!(misfit & (1u << g))) return g;
+  return 1;
+}
+
+VMLA_HD int64_t plan_seq_tiles(int64_t nk) { return (nk + 127) / 128; }
+
+// Cost-space length of one stream of a sequence with nk keys: its tiles, then the fixed charge.
+VMLA_HD int64_t plan_stream_span(int64_t nk) { return plan_seq_tiles(nk) + kUnitFixedTiles; }
+
+// Pieces of a stream whose T tiles start at cost position a: the lanes of length L it meets.
+VMLA_HD int64_t plan_stream_pieces(int64_t a, int64_t T, int64_t L) { return (a + T - 1) / L - a / L + 1; }
+
+// Lane length for total cost W over `lanes` lanes (at least one tile).
+VMLA_HD int64_t plan_lane_tiles(int64_t W, int lanes) {
+  const int64_t L = plan_ceil_div(W, lanes > 0 ? lanes : 1);
+  return L > 0 ? L : 1;
+}
+
+// Query rows of stream g of a sequence with R rows (its last row block may be short).
+VMLA_HD int64_t plan_stream_rows(int64_t g, int64_t rows_per_stream, int64_t R) {
+  const int64_t hi = (g + 1) * rows_per_stream < R ? (g + 1) * rows_per_stream : R;
+  return hi - g * rows_per_stream;
+}
+
+// Pieces (the most of any of its streams), partial rows and merge rows (the
+// rows of its streams cut into more than one piece) of sequence b in a lane
+// plan whose streams of b start at cost position c0: n_groups streams of span
+// each, R = Q_b H query rows, rows_per_stream = G x 256.
+VMLA_HD int64_t plan_lane_seq_split(int64_t c0, int64_t n_groups, int64_t nk, int64_t L, int64_t R,
+                                    int64_t rows_per_stream, int64_t* part_rows, int64_t* merge_rows,
+                                    int64_t* pieces_sum) {
+  const int64_t T = plan_seq_tiles(nk), span = plan_stream_span(nk);
+  int64_t most = 1, sum = 0, merge = 0;
+  for (int64_t g = 0; g < n_groups; ++g) {
+    const int64_t p = plan_stream_pieces(c0 + g * span, T, L);
+    most = p > most ? p : most;
+    sum += p;
+    if (p > 1) merge += plan_stream_rows(g, rows_per_stream, R);
+  }
+  *part_rows = most > 1 ? R * most : 0;
+  *merge_rows = merge;
+  *pieces_sum = sum;
+  return most;
+}
+
+// Score of a lane plan in the uniform plan's units (keys): a lane carries at
+// most L plus the fixed charge of the stream it continues, and the merge.
+VMLA_HD int64_t plan_lane_score(int64_t L, int64_t partial_rows) {
+  return (L + kUnitFixedTiles) * 128 + plan_merge_score(partial_rows);
+}
+
+// The lane plan replaces the chosen uniform plan when it scores at least 3 % lower.
+VMLA_HD bool plan_prefer_lanes(int64_t lane_score, int64_t uniform_score) {
+  return uniform_score >= 0 && lane_score * 100 < uniform_score * 97;
 }
 
 }  // namespace vmla

@@ -44,9 +44,11 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "vmla_device.cuh"
+#include "vmla_plan_core.h"
 #include "vmla_sm100.cuh"
 
 namespace vmla {
@@ -78,7 +80,8 @@ constexpr uint32_t kQBytes = 2 * kChunks * kKBox;  // a scorer CTA's 128 Q rows,
 enum Cmd : uint32_t { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
 // Optional pipeline trace (compile with -DVMLA_TRACE): global-timer stamps of
-// each hand-off for the first kTraceTiles tiles of cluster 0.
+// each hand-off for the first kTraceTiles tiles of cluster 0, and (events 26-31)
+// one stamp or count per cluster at the cluster's own index.
 #ifdef VMLA_TRACE
 constexpr int kTraceTiles = 256;
 constexpr int kTraceEvents = 32;
@@ -90,9 +93,20 @@ __device__ __forceinline__ void vtrace(int ev, int tile) {
     g_vmla_trace[ev * kTraceTiles + tile] = t;
   }
 }
+__device__ __forceinline__ void vtrace_cluster(int ev, uint64_t value, bool stamp) {
+  const uint32_t c = cluster_id_x();
+  if (ev >= 0 && ev < kTraceEvents && c < (uint32_t)kTraceTiles) {
+    if (stamp) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(value));
+    g_vmla_trace[ev * kTraceTiles + c] = value;
+  }
+}
 #define VTRACE(ev, tile) vtrace(ev, tile)
+#define VTRACE_CLUSTER(ev) vtrace_cluster(ev, 0, true)
+#define VTRACE_CLUSTER_VALUE(ev, v) vtrace_cluster(ev, v, false)
 #else
 #define VTRACE(ev, tile) ((void)0)
+#define VTRACE_CLUSTER(ev) ((void)0)
+#define VTRACE_CLUSTER_VALUE(ev, v) ((void)0)
 #endif
 
 // One P message covers half a tile (64 keys): two staging buffers of this
@@ -165,10 +179,14 @@ struct TcSmem {
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
 
+// One work unit: row block rb of sequence b over keys [k_lo, k_hi), piece
+// `piece` of the n_pieces that cover those rows' keys (one: the unit writes
+// the rows' results, else fp32 partials for the merge).
 struct UnitInfo {
-  int b, rb, piece, R, prefix, k_lo, k_hi, n_tiles;
+  int b, rb, piece, n_pieces, R, prefix, k_lo, k_hi, n_tiles;
 };
 
+// Unit u of a uniform plan.
 __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
   UnitInfo ui;
   ui.b = seq_of_unit(p, u);
@@ -176,12 +194,76 @@ __device__ __forceinline__ UnitInfo decode_unit(const PlanParams& p, int u) {
   const int local = u - s.unit_start;
   ui.rb = local % s.n_rb;
   ui.piece = local / s.n_rb;
+  ui.n_pieces = s.n_split;
   ui.R = s.n_q * p.num_heads;
   ui.prefix = s.n_kv - s.n_q;
   ui.k_lo = ui.piece * s.chunk;
   ui.k_hi = min(s.n_kv, ui.k_lo + s.chunk);
   ui.n_tiles = (ui.k_hi - ui.k_lo + kTileKeys - 1) / kTileKeys;
   return ui;
+}
+
+// Last sequence whose first stream starts at or before cost position x (a
+// sequence without streams shares its position with the next one, so the
+// search lands on one with streams for any x below the total).
+__device__ __forceinline__ int lane_seq_at(const PlanParams& p, int64_t x) {
+  int lo = 0, hi = p.batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.seq[mid].lane_cost <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Streams [*s_begin, *s_end) of a lane plan whose tiles meet lane l's interval
+// [l L, (l + 1) L) of the cost space.
+__device__ __forceinline__ void lane_streams(const PlanParams& p, int l, int* s_begin, int* s_end) {
+  const int64_t L = p.lane_tiles, W = p.lane_total, P = (int64_t)l * L;
+  *s_begin = *s_end = 0;
+  if (P >= W) return;
+  const int64_t Q = P + L < W ? P + L : W;
+  const SeqPlan& s = p.seq[lane_seq_at(p, P)];
+  const int64_t T = plan_seq_tiles(s.n_kv), g0 = (P - s.lane_cost) / (T + kUnitFixedTiles);
+  int first = s.unit_start + (int)g0;
+  if (P - s.lane_cost - g0 * (T + kUnitFixedTiles) >= T) ++first;  // P lies in that stream's fixed charge
+  const SeqPlan& s2 = p.seq[lane_seq_at(p, Q - 1)];
+  int64_t g2 = (Q - 1 - s2.lane_cost) / plan_stream_span(s2.n_kv);
+  const int64_t ng2 = s2.n_rb / p.lane_width;
+  if (g2 > ng2 - 1) g2 = ng2 - 1;
+  const int last = s2.unit_start + (int)g2;
+  *s_begin = first;
+  *s_end = last + 1 > first ? last + 1 : first;
+}
+
+// Stream s of a lane plan as seen by cluster j of lane l: row block g G + j of
+// the stream's sequence over the tiles of the stream that fall in the lane.
+__device__ __forceinline__ UnitInfo decode_lane_unit(const PlanParams& p, int s, int l, int j) {
+  UnitInfo ui;
+  ui.b = seq_of_unit(p, s);
+  const SeqPlan& sp = p.seq[ui.b];
+  const int64_t g = s - sp.unit_start;
+  const int64_t T = plan_seq_tiles(sp.n_kv), L = p.lane_tiles;
+  const int64_t A = sp.lane_cost + g * (T + kUnitFixedTiles);  // cost position of the stream's first tile
+  const int64_t P = (int64_t)l * L;
+  const int64_t lo = (P > A ? P : A) - A;
+  const int64_t hi = (P + L < A + T ? P + L : A + T) - A;
+  ui.rb = (int)(g * p.lane_width + j);
+  ui.piece = (int)(l - A / L);
+  ui.n_pieces = (int)plan_stream_pieces(A, T, L);
+  ui.R = sp.n_q * p.num_heads;
+  ui.prefix = sp.n_kv - sp.n_q;
+  ui.k_lo = (int)(lo * kTileKeys);
+  ui.k_hi = min(sp.n_kv, (int)(hi * kTileKeys));
+  ui.n_tiles = (int)(hi - lo);
+  return ui;
+}
+
+// The k-th entry of this cluster's work list: an index of the schedule's order
+// (uniform plan) or a stream index (lane plan).
+__device__ __forceinline__ UnitInfo unit_at(const PlanParams& p, const TcSched& sched, int k) {
+  if (p.lane_width == 0) return decode_unit(p, sched.unit_base + sched.order[k]);
+  const int cid = (int)cluster_id_x();
+  return decode_lane_unit(p, k, cid / p.lane_width, cid % p.lane_width);
 }
 
 // Sets the abort flag of every CTA of the cluster.
@@ -264,7 +346,7 @@ __device__ __noinline__ void settle_after_abort() {
 
 __device__ __forceinline__ int total_tiles(const PlanParams& plan, const TcSched& sched, int u_begin, int u_end) {
   int total = 0;
-  for (int k = u_begin; k < u_end; ++k) total += decode_unit(plan, sched.unit_base + sched.order[k]).n_tiles;
+  for (int k = u_begin; k < u_end; ++k) total += unit_at(plan, sched, k).n_tiles;
   return total;
 }
 
@@ -294,8 +376,9 @@ __device__ void producer_role(TcSmem& sm, const CUtensorMap* map, const CUtensor
   bool ok = true;
   // the kernel may start under the gather's tail: the staged rows are complete past this wait
   grid_dependency_wait();
+  if (rank == 0) VTRACE_CLUSTER(28);  // the launch before this one is complete
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+    const UnitInfo ui = unit_at(plan, sched, ui_idx);
     const SeqPlan& sp = plan.seq[ui.b];
     // first row of the sequence in the tensor map: its staged offset, or its pool run
     // (a run outside the pool only reads the out-of-range fill; a check kernel reports it)
@@ -368,7 +451,7 @@ __device__ void scorer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSche
   ScorerSmem& S = sm.u.s;
   int it = 0, uu = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+    const UnitInfo ui = unit_at(plan, sched, ui_idx);
     if (!wait_bar(sm, &sm.c.qfull, uu & 1, a.status, 200)) break;
     tc_fence_after();
     bool ok = true;
@@ -443,7 +526,7 @@ __device__ void scorer_softmax_role(TcSmem& sm, const PlanParams& plan, const Tc
   // stream is complete (the kernel may start under the gather's tail)
   grid_dependency_wait();
   for (int ui_idx = u_begin; ui_idx < u_end && !stop; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+    const UnitInfo ui = unit_at(plan, sched, ui_idx);
     const SeqPlan& sp = plan.seq[ui.b];
     const int r = ui.rb * kRowsUnit + (int)(rank & 1) * kRowsCta + row;
     const bool valid = r < ui.R;
@@ -624,7 +707,7 @@ __device__ void scorer_sender_role(TcSmem& sm, const PlanParams& plan, const TcS
   const uint32_t mixer = rank + 2;
   int it = 0, uu = 0, msg = 0;
   for (int ui_idx = u_begin; ui_idx < u_end; ++ui_idx, ++uu) {
-    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+    const UnitInfo ui = unit_at(plan, sched, ui_idx);
     for (int t = 0; t < ui.n_tiles; ++t, ++it) {
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
         const int sg = msg % kStages;
@@ -711,7 +794,7 @@ __device__ void mixer_mma_role(TcSmem& sm, const PlanParams& plan, const TcSched
     return r;
   };
   for (int ui_idx = u_begin; ui_idx < u_end && ok; ++ui_idx) {
-    const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+    const UnitInfo ui = unit_at(plan, sched, ui_idx);
     for (int t = 0; t < ui.n_tiles && ok; ++t, ++it) {
       for (int j = 0; j < kMsgsPerTile; ++j, ++msg) {
         const int s = msg % kVStages;  // V stage of this message
@@ -846,6 +929,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const C
     const uint32_t cmd = sm.c.wg_cmd;
     if ((cmd & 0xFF) == kCmdExit) {
       if (lane == 0) bulk_wait_group<0>();  // this warp's output stores are written before the CTA leaves
+      if (tid == 0 && rank == 2) VTRACE_CLUSTER(29);  // the last unit's outputs written
       return;
     }
     __syncwarp();
@@ -875,7 +959,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const C
       // store; a group of 32 rows that runs past the unit's rows is stored by the
       // lanes instead (eight rows' 64 contiguous bytes per instruction), so that
       // nothing is written past them.
-      const UnitInfo ui = decode_unit(plan, sched.unit_base + sched.order[ui_idx]);
+      const UnitInfo ui = unit_at(plan, sched, ui_idx);
       const SeqPlan& sp = plan.seq[ui.b];
       const int f = uu & 1;
       const float m = M.fin[f].m[row], lsum = M.fin[f].l[row];
@@ -911,7 +995,7 @@ __device__ void mixer_epilogue_role(TcSmem& sm, const CUtensorMap* omap, const C
           __syncwarp();
         }
       };
-      if (sp.n_split == 1) {
+      if (ui.n_pieces == 1) {
         const int64_t orow = (int64_t)sp.q_off * H + (valid ? r : 0);
         const int64_t orow_w = (int64_t)sp.q_off * H + r_w;
 #pragma unroll 1
@@ -981,8 +1065,18 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int cid = (int)cluster_id_x();
-  const int u_begin = cid < sched.num_clusters ? sched.start[cid] : 0;
-  const int u_end = cid < sched.num_clusters ? sched.start[cid + 1] : 0;
+  // this cluster's work list: positions [u_begin, u_end) of the schedule's order,
+  // or the streams its lane meets
+  int u_begin = 0, u_end = 0;
+  if (cid < sched.num_clusters) {
+    if (plan.lane_width == 0) {
+      u_begin = sched.start[cid];
+      u_end = sched.start[cid + 1];
+    } else {
+      lane_streams(plan, cid / plan.lane_width, &u_begin, &u_end);
+    }
+  }
+  if (threadIdx.x == 0 && rank == 0) VTRACE_CLUSTER(26);  // cluster entered
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kVStages; ++s) {
@@ -1047,6 +1141,10 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
   cluster_arrive();
   cluster_wait();
   const uint32_t tbase = sm.c.tmem_base;
+  if (threadIdx.x == 0 && rank == 0) {
+    VTRACE_CLUSTER(27);  // set up (barriers, TMEM, receive slots armed)
+    VTRACE_CLUSTER_VALUE(31, ((uint64_t)(u_end - u_begin) << 32) | (uint32_t)n_tiles_all);
+  }
 
   if (warp == 0) {
     if (lane == 0) producer_role(sm, &kmap, &vmap, &qmap, plan, sched, a, u_begin, u_end, rank);
@@ -1084,6 +1182,7 @@ __device__ __forceinline__ void tc_verify_body(const CUtensorMap& kmap, const CU
   // raises it in every CTA of the cluster before the barrier.
   cluster_arrive();
   cluster_wait();
+  if (threadIdx.x == 0 && rank == 0) VTRACE_CLUSTER(30);  // every role of the cluster finished
   if (sm.c.abort_flag) {
     if (threadIdx.x == 0) settle_after_abort();
     __syncthreads();
@@ -1244,8 +1343,20 @@ int launch_tc(const PlanParams& plan, const RunArgs& a, void* stream) {
   // and the epilogue's output maps
   CUtensorMap kmap, vmap, qmap, omap, pmap;
   if (!encode_maps(enc, a, &kmap, &vmap, &qmap, &omap, &pmap)) return VMLA_ERR_CUDA;
-  // units are independent: a plan with more than kMaxTcUnits runs as several launches
   static thread_local TcSched sched;
+  if (plan.lane_width > 0) {
+    // a lane plan: one launch of lane_count lanes, each cluster working out its own streams
+    std::memset(&sched, 0, sizeof(sched));
+    sched.num_clusters = plan.lane_count * plan.lane_width;
+    sched.total_units = plan.total_units;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config(sched.num_clusters, attr, true);
+    cfg.stream = (cudaStream_t)stream;
+    if (cudaLaunchKernelEx(&cfg, tc_verify_kernel, kmap, vmap, qmap, omap, pmap, plan, sched, a) != cudaSuccess)
+      return VMLA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  }
+  // units are independent: a plan with more than kMaxTcUnits runs as several launches
   for (int u0 = 0; u0 < plan.total_units; u0 += kMaxTcUnits) {
     const int u1 = plan.total_units - u0 < kMaxTcUnits ? plan.total_units : u0 + kMaxTcUnits;
     rc = build_tc_schedule(plan, clusters < u1 - u0 ? clusters : u1 - u0, u0, u1, &sched);

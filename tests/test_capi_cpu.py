@@ -67,6 +67,7 @@ def test_argument_errors_before_any_launch(B):
     assert _run_raw(B, **{**good, "qoh": np.array([0, 9], np.int32)}) == B.VMLA_ERR_SHAPE  # drafts > keys
     assert _run_raw(B, **{**good, "kvh": np.array([1, 8], np.int32)}) == B.VMLA_ERR_SHAPE
     assert _run_raw(B, **{**good, "splits": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_raw(B, **{**good, "splits": -2}) == B.VMLA_ERR_SHAPE  # -1 is VMLA_SPLITS_LANES
     assert _run_raw(B, **{**good, "scale": 0.0}) == B.VMLA_ERR_SHAPE
     assert _run_raw(B, **{**good, "scale": -0.1}) == B.VMLA_ERR_SHAPE
     assert _run_raw(B, **{**good, "scale": float("inf")}) == B.VMLA_ERR_SHAPE
@@ -281,8 +282,9 @@ def test_plan_units_within_the_device_plan_bound(B):
     """The device-planned call sizes its partial area for caller bounds before any length is known:
     with C clusters the automatic plan makes at most 12C units (its largest candidate aims at 12
     units per cluster) plus one per row block, each of 256 rows, and never more than 64 pieces of
-    every query row.  The host planner runs the same split arithmetic; check that bound on random
-    length sets."""
+    every query row; a lane plan makes at most C + 2 per row block (a stream of T tiles meets at most
+    (T - 1) / L + 2 lanes).  The host planner runs the same split arithmetic; check that bound on
+    random length sets."""
     rng = np.random.default_rng(7)
     for trial in range(300):
         batch = int(rng.integers(1, 40))
@@ -293,9 +295,11 @@ def test_plan_units_within_the_device_plan_bound(B):
         info, per, qo, kv = _plan(B, 0, prefixes.tolist(), drafts.tolist(), H=H, sms=4 * clusters)
         rows = int(qo[-1]) * H
         row_blocks = -(-rows // 256) + batch
-        cap = min(256 * (12 * clusters + row_blocks), rows * 64)
-        assert info.num_units <= 12 * clusters + row_blocks
+        cap = min(256 * (12 * clusters + 2 * row_blocks), rows * 64)
+        assert info.num_units <= 12 * clusters + 2 * row_blocks
         assert info.partial_rows <= cap
+        if info.lane_width:
+            assert info.num_units <= clusters + 2 * row_blocks
     # forced piece counts: at most `splits` pieces of every row block
     for splits in (1, 3, 17, 64):
         info, per, qo, kv = _plan(B, 0, [5000, 100, 70000], [16, 3, 64], H=64, splits=splits, sms=144)
@@ -363,7 +367,16 @@ def _piece_rule(qo, kv, H, clusters, search=True):
     per fp32 partial row (query rows x pieces of every split sequence) and 128 keys when there is
     any; the best-scoring candidate
     replaces the default (m = 32) only when it scores at least 3 % lower; more than 64 sequences,
-    or more than 3072 units, leave the candidate set."""
+    or more than 3072 units, leave the candidate set.
+
+    Then the lane plan (only when the search ran): G = the largest of 4, 3, 2 dividing every
+    sequence's row-block count (else 1), C // G lanes (1 to 64 of them); each sequence has
+    rb / G streams, each taking ceil(N / 128) tiles and then 3 more in a line of cost W; lanes
+    of L = ceil(W / lanes) cut that line, and a stream's pieces are the lanes its tiles meet; a
+    sequence's count is the most of any of its streams; the lane plan scores (L + 3) * 128 plus
+    the same merge charge and replaces the uniform choice when it scores at least 3 % lower.
+    A lane plan's merge rows are the rows of its streams cut into more than one piece.
+    Returns the counts and the lane plan's merge rows (None: the uniform plan)."""
     ms = [12 + 2 * k for k in range(10)] + [32 + 4 * k for k in range(10)] + \
          [72 + 8 * k for k in range(8)] + [144 + 16 * k for k in range(4)]
     B = len(qo) - 1
@@ -404,16 +417,52 @@ def _piece_rule(qo, kv, H, clusters, search=True):
             load[clusters - 1 - j if rnd % 2 else j] += c
         return max(load) + part // 20 + (128 if part else 0)
 
+    def lanes_plan(uniform_score):
+        rbs = [r for r, q in zip(rb, nq) if q]
+        G = next((g for g in (4, 3, 2) if all(r % g == 0 for r in rbs)), 1)
+        lanes = clusters // G
+        if not 1 <= lanes <= 64:
+            return None
+        W = sum(r // G * (-(-n // 128) + 3) for r, n, q in zip(rb, nk, nq) if q)
+        if W < 1:
+            return None
+        L = max(1, -(-W // lanes))
+        pos, counts, part, merge = 0, [], 0, 0
+        for r, n, q in zip(rb, nk, nq):
+            if q == 0:
+                counts.append(1)
+                continue
+            T = -(-n // 128)
+            most = 1
+            for g in range(r // G):
+                p = (pos + T - 1) // L - pos // L + 1
+                most = max(most, p)
+                if p > 1:  # the merge combines the rows of this stream's G row blocks
+                    merge += min(q * H, (g + 1) * G * 256) - g * G * 256
+                pos += T + 3
+            counts.append(most)
+            if most > 1:
+                part += q * H * most
+        lane_score = (L + 3) * 128 + part // 20 + (128 if part else 0)
+        ok = uniform_score is None or lane_score * 100 < uniform_score * 97
+        return (counts, merge) if ok else None
+
     m_def = 32
     if search and B <= 64:
         scores = [(score(m), k) for k, m in enumerate(ms)]
         valid = [(s, k) for s, k in scores if s is not None]
         d = scores[ms.index(m_def)][0]
+        chosen, chosen_score = m_def, d
         if valid:
             s_best, k_best = min(valid)
             if d is None or s_best * 100 < d * 97:
-                return [p for p, _ in pieces(target(ms[k_best]))]
-    return [p for p, _ in pieces(target(m_def))]
+                chosen, chosen_score = ms[k_best], s_best
+        if chosen_score is not None:
+            lane = lanes_plan(chosen_score)
+            if lane is not None:
+                return lane[0], lane[1]
+        return [p for p, _ in pieces(target(chosen))], None
+    return [p for p, _ in pieces(target(m_def))], None
 
 
 def test_tc_piece_size_rule(B):
@@ -428,13 +477,36 @@ def test_tc_piece_size_rule(B):
         prefixes = np.where(rng.random(b) < 0.3, rng.integers(0, 3000, b), rng.integers(0, 120000, b)).tolist()
         drafts = rng.integers(0, 65, b).tolist()
         shapes.append((prefixes, drafts, int(rng.choice([8, 16, 64, 128])), int(rng.integers(1, 40))))
+    lane_plans = 0
     for prefixes, drafts, H, clusters in shapes:
         info, per, qo, kv = _plan(B, 0, prefixes, drafts, H=H, sms=4 * clusters)
-        want = _piece_rule(qo, kv, H, clusters)
+        want, lane_merge = _piece_rule(qo, kv, H, clusters)
         got = [int(p) for p in per]
+        assert (info.lane_width > 0) == (lane_merge is not None), (prefixes, drafts, H, clusters)
+        if lane_merge is not None:
+            assert info.merge_rows == lane_merge
+            lane_plans += 1
         for b in range(len(drafts)):
             if drafts[b] > 0:
                 assert got[b] == want[b], (prefixes, drafts, H, clusters, b)
-    # the ragged four-sequence batch leaves the default (two units per cluster)
+    assert 10 < lane_plans < len(shapes) - 10  # both forms occur
+    # the ragged four-sequence batch takes the lane plan: lanes of four clusters (four row blocks per
+    # sequence), streams of 33, 65, 129 and 257 tiles cut every 56 cost units into 1, 2, 4 and 5 pieces
     info, per, qo, kv = _plan(B, 0, [4096, 8192, 16384, 32768], [16] * 4, H=64, sms=144)
-    assert [int(p) for p in per] != _piece_rule(qo, kv, 64, 36, search=False)
+    assert info.lane_width == 4 and info.lane_count == 9
+    assert [int(p) for p in per] == [1, 2, 4, 5]
+    assert [int(p) for p in per] != _piece_rule(qo, kv, 64, 36, search=False)[0]
+    # one long sequence keeps its equal pieces (one per cluster already balances it)
+    info, per, qo, kv = _plan(B, 0, [185000], [16], H=64, sms=144)
+    assert info.lane_width == 0 and int(per[0]) == 9
+    # VMLA_SPLITS_LANES takes the lane plan wherever it fits (the rule above without the score
+    # comparison), also past 64 sequences
+    for prefixes, drafts, H, clusters in shapes[:40] + [([700] * 80, [3] * 80, 64, 36)]:
+        info, per, qo, kv = _plan(B, 0, prefixes, drafts, H=H, splits=B.VMLA_SPLITS_LANES, sms=4 * clusters)
+        rbs = [-(-d * H // 256) for d in drafts if d > 0]
+        G = next((g for g in (4, 3, 2) if all(r % g == 0 for r in rbs)), 1)
+        assert info.lane_width == (G if 1 <= clusters // G <= 64 and rbs else 0), (prefixes, drafts, H, clusters)
+    # the CUDA-core kernel takes it as 0
+    i0, p0, _, _ = _plan(B, 1, [5000, 300], [4, 16], H=64)
+    i1, p1, _, _ = _plan(B, 1, [5000, 300], [4, 16], H=64, splits=B.VMLA_SPLITS_LANES)
+    assert list(p0) == list(p1) and i1.lane_width == 0
