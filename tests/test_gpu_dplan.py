@@ -173,12 +173,12 @@ def _random_batches():
 
 def test_device_plan_random_batches_bitwise():
     """The device planner scores the same piece-size candidates as the host planner (one warp per
-    candidate) and must cut every sequence alike: bit-equal results on ragged random batches, and
-    sampled rows of two of them against the oracle."""
+    candidate), weighs the lane plan the same way, and must cut every sequence alike: bit-equal
+    results on ragged random batches, and sampled rows of two of them against the oracle."""
     _, binding, _ = _mods()
     from tests.test_capi_cpu import _piece_rule
     from tests.test_gpu_parity import sample_rows
-    changed = 0
+    changed = lanes = 0
     for k, case in enumerate(_random_batches()):
         o1, l1, s1 = run_full(case, "tc")
         o2, l2, s2 = run_dplan(case, slack_q=3, slack_kv=500)
@@ -186,11 +186,13 @@ def test_device_plan_random_batches_bitwise():
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2), case.name
         info, per = binding.verify_attn_mla_plan(binding.VMLA_KERNEL_TC, case.qo_indptr, case.kv_indptr,
                                                  case.num_heads, 0, 144)
-        default = _piece_rule(case.qo_indptr, case.kv_indptr, case.num_heads, 36, search=False)
+        default, _ = _piece_rule(case.qo_indptr, case.kv_indptr, case.num_heads, 36, search=False)
         changed += int([int(p) for p in per] != default)
+        lanes += int(info.lane_width > 0)
         if k in (0, 2):
             rows = sample_rows(case, n=60, seed=k)
             ref_o, ref_l = oracle.verify_rows(case, rows)
             H = case.num_heads
             compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, case.name)
-    assert changed >= 1  # the search chose another piece size on some of these batches
+    assert changed >= 1  # the search chose another piece size (or the lane plan) on some of these batches
+    assert lanes >= 1  # and the lane plan on some
