@@ -100,3 +100,25 @@ def test_full_size_lane_plan_every_row(name):
     o, l, st = run_full(case, "tc")
     assert st == 0
     compare(o.reshape(-1, o.shape[-1]), l.reshape(-1), ref_o, ref_l, f"tc/{name} every row")
+
+
+def test_lane_plan_many_sequences_every_row():
+    """VMLA_SPLITS_LANES on 80 short sequences (past the candidate search's 64, so the device
+    planner takes its forced path): lanes of one cluster meeting up to five streams, several lanes
+    starting inside a stream's fixed charge; every row against the oracle, and the device plan
+    bit for bit."""
+    binding = _lanes()
+    rng = np.random.default_rng(900)
+    prefixes = rng.integers(50, 3000, 80).tolist()
+    drafts = rng.integers(1, 5, 80).tolist()
+    case = synth.make_case("lanes_b80", prefixes, drafts, num_heads=64,
+                           pool_slots=sum(prefixes) + sum(drafts) + 99, seed=703)
+    info, per = _plan_info(case, binding.VMLA_SPLITS_LANES)
+    assert info.lane_width == 1 and int(np.max(per)) > 1
+    ref_o, ref_l = oracle.verify(case)
+    o, l, st = run_full(case, "tc", splits=binding.VMLA_SPLITS_LANES)
+    assert st == 0
+    compare(o, l, ref_o, ref_l, "lanes/b80")
+    o2, l2, s2 = run_dplan(case, splits=binding.VMLA_SPLITS_LANES, slack_q=7, slack_kv=300)
+    assert s2 == 0
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
