@@ -275,18 +275,29 @@ def verify_attn_mla_defrag(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_
     _check(rc, "verify_attn_mla_defrag")
 
 
+def _append_args(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, first_row, status_word=None,
+                 stream=None, max_new_rows=0):
+    kvh = _host_i32(kv_indptr_host)
+    args = (_d(src_pool, 2, "src_pool"), int(src_pool.shape[0]), _d(kv_indptr, 4, "kv_indptr"),
+            _d(kv_indices, 4, "kv_indices"), kvh.ctypes.data, len(kvh) - 1, _d(dst_pool, 2, "dst_pool"),
+            int(dst_pool.shape[0]), _d(run_base, 4, "run_base"), _d(first_row, 4, "first_row"), int(max_new_rows),
+            _d(status_word, 4, "status_word"), _stream(stream))
+    return args, (src_pool, kv_indptr, kv_indices, kvh, dst_pool, run_base, first_row, status_word)
+
+
 def verify_attn_mla_defrag_append(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, first_row,
                                   status_word=None, stream=None, max_new_rows=0):
     """The defragmentation for a decode loop: rows below first_row[b] are already in sequence b's run
     (max_new_rows: a bound on the new rows per sequence, or 0)."""
-    kvh = _host_i32(kv_indptr_host)
-    rc = _lib.verify_attn_mla_defrag_append(_d(src_pool, 2, "src_pool"), int(src_pool.shape[0]),
-                                            _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
-                                            kvh.ctypes.data, len(kvh) - 1, _d(dst_pool, 2, "dst_pool"),
-                                            int(dst_pool.shape[0]), _d(run_base, 4, "run_base"),
-                                            _d(first_row, 4, "first_row"), int(max_new_rows),
-                                            _d(status_word, 4, "status_word"), _stream(stream))
-    _check(rc, "verify_attn_mla_defrag_append")
+    args, _ = _append_args(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, first_row,
+                           status_word, stream, max_new_rows)
+    _check(_lib.verify_attn_mla_defrag_append(*args), "verify_attn_mla_defrag_append")
+
+
+def prepare_verify_attn_mla_defrag_append(*a, **k) -> Prepared:
+    """verify_attn_mla_defrag_append with its arguments checked and marshalled once."""
+    args, keep = _append_args(*a, **k)
+    return Prepared(_lib.verify_attn_mla_defrag_append, "verify_attn_mla_defrag_append", args, keep)
 
 
 def verify_attn_mla_runs_workspace_size(qo_indptr_host, kv_indptr_host, num_heads: int, splits: int = 0) -> int:
@@ -305,19 +316,39 @@ def verify_attn_mla_runs(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_h
          kv_indptr_host, qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
 
 
+def prepare_verify_attn_mla_runs(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_host, qo_indptr_host, out,
+                                 lse, workspace, sm_scale, draft_mask=None, parent=None, splits=0,
+                                 stream=None) -> Prepared:
+    """verify_attn_mla_runs with its arguments checked and marshalled once."""
+    args, keep = _run_args(q, kv_pool, kv_indptr, run_base, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+                           workspace, sm_scale, draft_mask, parent, splits, stream)
+    return Prepared(_lib.verify_attn_mla_runs, "verify_attn_mla_runs", args, keep)
+
+
+def _fp8_args(q, kv_pool_e4m3, kv_scale, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host, out, lse,
+              workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
+    kvh = _host_i32(kv_indptr_host)
+    qoh = _host_i32(qo_indptr_host)
+    args = (_d(q, 2, "q"), _d(kv_pool_e4m3, 1, "kv_pool_e4m3"), int(kv_pool_e4m3.shape[0]), float(kv_scale),
+            _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"), _d(qo_indptr, 4, "qo_indptr"),
+            _d(draft_mask, 8, "draft_mask"), _d(parent, 4, "parent"), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1,
+            int(q.shape[1]), float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
+            _d(workspace, 0, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    return args, (q, kv_pool_e4m3, kv_indptr, kv_indices, qo_indptr, kvh, qoh, out, lse, workspace, draft_mask, parent)
+
+
 def verify_attn_mla_fp8(q, kv_pool_e4m3, kv_scale, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host,
                         out, lse, workspace, sm_scale, draft_mask=None, parent=None, splits=0, stream=None):
     """verify_attn_mla on an e4m3 latent pool ([S, 576] uint8 codes) with one scale."""
-    kvh = _host_i32(kv_indptr_host)
-    qoh = _host_i32(qo_indptr_host)
-    rc = _lib.verify_attn_mla_fp8(_d(q, 2, "q"), _d(kv_pool_e4m3, 1, "kv_pool_e4m3"), int(kv_pool_e4m3.shape[0]),
-                                  float(kv_scale), _d(kv_indptr, 4, "kv_indptr"), _d(kv_indices, 4, "kv_indices"),
-                                  _d(qo_indptr, 4, "qo_indptr"), _d(draft_mask, 8, "draft_mask"),
-                                  _d(parent, 4, "parent"), kvh.ctypes.data, qoh.ctypes.data, len(kvh) - 1,
-                                  int(q.shape[1]), float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
-                                  _d(workspace, 0, "workspace"), workspace.numel() * workspace.element_size(),
-                                  _stream(stream))
-    _check(rc, "verify_attn_mla_fp8")
+    args, _ = _fp8_args(q, kv_pool_e4m3, kv_scale, kv_indptr, kv_indices, qo_indptr, kv_indptr_host, qo_indptr_host,
+                        out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
+    _check(_lib.verify_attn_mla_fp8(*args), "verify_attn_mla_fp8")
+
+
+def prepare_verify_attn_mla_fp8(*a, **k) -> Prepared:
+    """verify_attn_mla_fp8 with its arguments checked and marshalled once."""
+    args, keep = _fp8_args(*a, **k)
+    return Prepared(_lib.verify_attn_mla_fp8, "verify_attn_mla_fp8", args, keep)
 
 
 def verify_attn_mla_test_fault(fault: int, wait_cycles: int = 0):

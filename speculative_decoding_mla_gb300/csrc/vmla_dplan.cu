@@ -56,7 +56,9 @@ __device__ int64_t candidate_score(const PlanShape& sh, const int32_t* qo, const
   int64_t units = 0, part = 0;
   for (int b = ln; b < batch; b += 32) {
     int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
-    part += plan_seq_runs(sh, (int64_t)qo[b + 1] - qo[b], (int64_t)kv[b + 1] - kv[b], num_heads, ct, c2, n2);
+    const int64_t nq = (int64_t)qo[b + 1] - qo[b];
+    part += plan_seq_runs(sh, nq, (int64_t)kv[b + 1] - kv[b], num_heads, plan_row_blocks(sh, nq, num_heads), ct, c2,
+                          n2);
     for (int t = 0; t < kRunsPerSeq; ++t) {
       runs[kRunsPerSeq * b + t] = ((uint64_t)c2[t] << 32) | (uint64_t)n2[t];
       units += n2[t];

@@ -14,10 +14,11 @@
 
 namespace vmla {
 
-// Host form of the piece-size choice.  The device planner scores each
-// candidate with the closed form per (run, cluster) pair; here the runs are
-// sorted once and the snake shares are summed by residue, which gives the
-// same integer scores in O(R log R + C) per candidate:
+// Host form of the piece-size choice.  The device planner scores every
+// candidate with the closed form per (run, cluster) pair; here the candidates
+// are scored best bound first and the rest pruned (which cannot change the
+// choice), and the runs of a scored candidate are sorted and the snake shares
+// summed by residue, which gives the same integer scores in O(R log R + C):
 //   load_j = sum_r cost_r (F_j(end_r) - F_j(start_r)),
 //   F_j(x) = 2 floor(x / 2C) + [x mod 2C > j] + [x mod 2C > 2C - 1 - j],
 // so load_j = K + S(j) + S(2C - 1 - j) with K the whole-period part and S(x)
@@ -30,77 +31,77 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
   if (batch > kSearchMaxBatch || batch < 1 || clusters < 1) return def;
   const int R = kRunsPerSeq * batch;
   const int64_t period = 2 * (int64_t)clusters;
-  int64_t nq[kSearchMaxBatch], nk[kSearchMaxBatch];
+  int64_t nq[kSearchMaxBatch], nk[kSearchMaxBatch], rbs[kSearchMaxBatch];
   for (int b = 0; b < batch; ++b) {
     nq[b] = (int64_t)qo[b + 1] - qo[b];
     nk[b] = (int64_t)kv[b + 1] - kv[b];
+    rbs[b] = plan_row_blocks(sh, nq[b], num_heads);
   }
-  int64_t cost[kRunsPerSeq * kSearchMaxBatch], count[kRunsPerSeq * kSearchMaxBatch];
-  // sort keys: cost descending, then run index (costs are below 2^32, indexes below 2^8);
-  // each candidate starts from the previous candidate's order, which changes little
-  uint64_t key[kRunsPerSeq * kSearchMaxBatch];
-  for (int r = 0; r < R; ++r) key[r] = (uint64_t)r;
-  std::vector<int64_t> resid(period + 1);
-  int64_t score[kChunkCands];
-  int64_t best = -1;  // lowest exact score so far
-  // the default first, so that its exact score bounds the others from the start
-  for (int i = 0; i < kChunkCands; ++i) {
-    const int k = i == 0 ? kDefaultCand : (i <= kDefaultCand ? i - 1 : i);
+  // pass 1: every candidate's runs, partial rows and lower bound (some cluster carries at
+  // least the mean load and one carries the largest unit)
+  static thread_local int64_t cost[kChunkCands][kRunsPerSeq * kSearchMaxBatch];
+  static thread_local int64_t count[kChunkCands][kRunsPerSeq * kSearchMaxBatch];
+  int64_t score[kChunkCands], bound[kChunkCands], part[kChunkCands];
+  for (int k = 0; k < kChunkCands; ++k) {
     const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
-    int64_t units = 0, part = 0;
+    int64_t units = 0, prt = 0, total = 0, largest = 0;
     for (int b = 0; b < batch; ++b) {
       int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
-      part += plan_seq_runs(sh, nq[b], nk[b], num_heads, ct, c2, n2);
+      prt += plan_seq_runs(sh, nq[b], nk[b], num_heads, rbs[b], ct, c2, n2);
       for (int t = 0; t < kRunsPerSeq; ++t) {
-        cost[kRunsPerSeq * b + t] = c2[t];
-        count[kRunsPerSeq * b + t] = n2[t];
+        cost[k][kRunsPerSeq * b + t] = c2[t];
+        count[k][kRunsPerSeq * b + t] = n2[t];
         units += n2[t];
+        total += c2[t] * n2[t];
+        if (n2[t] > 0 && c2[t] > largest) largest = c2[t];
       }
-    }
-    score[k] = -1;  // not a candidate: more units than one launch holds
-    if (units > kMaxTcUnits) continue;
-    // a lower bound of the score: some cluster carries at least the mean load and
-    // one carries the largest unit; a candidate whose bound exceeds the best exact
-    // score cannot be chosen (nor tie), so its bound stands in for its score
-    int64_t total = 0, largest = 0;
-    for (int r = 0; r < R; ++r) {
-      total += cost[r] * count[r];
-      if (count[r] > 0 && cost[r] > largest) largest = cost[r];
     }
     const int64_t mean = (total + clusters - 1) / clusters;
-    const int64_t bound = (mean > largest ? mean : largest) + plan_merge_score(part);
-    if (k != kDefaultCand && best >= 0 && bound > best) {
-      score[k] = bound;
-      continue;
+    part[k] = prt;
+    bound[k] = (mean > largest ? mean : largest) + plan_merge_score(prt);
+    score[k] = units > kMaxTcUnits ? -1 : -2;  // -1: not a candidate (more units than one launch holds)
+  }
+  // pass 2: exact scores, the default first, then the others by increasing bound (ties by
+  // candidate); a candidate whose bound exceeds the best exact score so far cannot be chosen
+  // (nor tie), so its bound stands in for its score, and so do those of all after it.  The
+  // candidate with the lowest exact score, and every one that ties it, is always scored
+  // exactly, so the choice is the one a full evaluation makes.
+  int order[kChunkCands];
+  int n_order = 0;
+  if (score[kDefaultCand] == -2) order[n_order++] = kDefaultCand;
+  for (int k = 0; k < kChunkCands; ++k)
+    if (k != kDefaultCand && score[k] == -2) order[n_order++] = k;
+  std::sort(order + (n_order > 0 && order[0] == kDefaultCand ? 1 : 0), order + n_order,
+            [&](int x, int y) { return bound[x] < bound[y] || (bound[x] == bound[y] && x < y); });
+  uint64_t key[kRunsPerSeq * kSearchMaxBatch];
+  std::vector<int64_t> resid(period + 1);
+  int64_t best = -1;  // lowest exact score so far
+  for (int i = 0; i < n_order; ++i) {
+    const int k = order[i];
+    if (k != kDefaultCand && best >= 0 && bound[k] > best) {
+      for (int i2 = i; i2 < n_order; ++i2) score[order[i2]] = bound[order[i2]];
+      break;
     }
-    for (int j2 = 0; j2 < R; ++j2) {
-      const int r = (int)(key[j2] & 0xFFu);
-      key[j2] = ((uint64_t)(0xFFFFFFFFll - cost[r]) << 8) | (uint64_t)r;
-    }
-    for (int j2 = 1; j2 < R; ++j2) {
-      const uint64_t x = key[j2];
-      int j = j2 - 1;
-      while (j >= 0 && key[j] > x) {
-        key[j + 1] = key[j];
-        --j;
-      }
-      key[j + 1] = x;
-    }
+    const int64_t* cst = cost[k];
+    const int64_t* cnt = count[k];
+    // runs by cost, descending (costs are below 2^32, indexes below 2^8)
+    for (int r = 0; r < R; ++r) key[r] = ((uint64_t)(0xFFFFFFFFll - cst[r]) << 8) | (uint64_t)r;
+    std::sort(key, key + R);
     std::fill(resid.begin(), resid.end(), 0);
     // positions as quotient and residue modulo the period, advanced run by run
     int64_t whole = 0, q_lo = 0, r_lo = 0;
     for (int j2 = 0; j2 < R; ++j2) {
       const int r = (int)(key[j2] & 0xFFu);
-      if (count[r] == 0) continue;
-      const int64_t n = count[r];
+      if (cnt[r] == 0) continue;
+      const int64_t n = cnt[r];
       int64_t q_hi = q_lo + (n >= period ? n / period : 0), r_hi = r_lo + (n >= period ? n % period : n);
       if (r_hi >= period) {
         r_hi -= period;
         ++q_hi;
       }
-      whole += cost[r] * 2 * (q_hi - q_lo);
-      resid[r_hi] += cost[r];
-      resid[r_lo] -= cost[r];
+      whole += cst[r] * 2 * (q_hi - q_lo);
+      resid[r_hi] += cst[r];
+      resid[r_lo] -= cst[r];
       q_lo = q_hi;
       r_lo = r_hi;
     }
@@ -116,7 +117,7 @@ static int64_t plan_pick_chunk_host(const PlanShape& sh, int batch, int num_head
       const int64_t load = whole + resid[j] + resid[period - 1 - j];
       worst = load > worst ? load : worst;
     }
-    score[k] = worst + plan_merge_score(part);
+    score[k] = worst + plan_merge_score(part[k]);
     if (best < 0 || score[k] < best) best = score[k];
   }
   const int k = plan_choose_cand(score);

@@ -52,6 +52,11 @@ VMLA_HD int64_t plan_seq_work(const PlanShape& sh, int64_t nq, int64_t nk, int n
   return nq == 0 ? 0 : plan_ceil_div(nq * num_heads, sh.rows_per_unit) * nk;
 }
 
+// Row blocks of a sequence with nq drafts (rows_per_unit is a power of two).
+VMLA_HD int64_t plan_row_blocks(const PlanShape& sh, int64_t nq, int num_heads) {
+  return (nq * num_heads + sh.rows_per_unit - 1) / sh.rows_per_unit;
+}
+
 // Keys per piece the planner aims at so that `slots` units run at once.
 VMLA_HD int64_t plan_chunk_target(const PlanShape& sh, int64_t total_work, int64_t slots) {
   const int64_t per = plan_ceil_div(total_work > 1 ? total_work : 1, slots);
@@ -59,8 +64,9 @@ VMLA_HD int64_t plan_chunk_target(const PlanShape& sh, int64_t total_work, int64
 }
 
 // Piece length and count of a sequence of nk >= 1 keys for a chunk target (or
-// a forced count): the length is rounded up to the key alignment, then the
-// count is the one that leaves no piece empty.
+// a forced count): the length is rounded up to the key alignment (a power of
+// two in both kernel families), then the count is the one that leaves no
+// piece empty.
 VMLA_HD void plan_pieces(const PlanShape& sh, int64_t nk, int splits, int64_t chunk_target, int64_t* chunk,
                          int64_t* pieces) {
   // nk < 2^31 (int32 offsets), so every sum and quotient below fits 32 bits
@@ -70,7 +76,7 @@ VMLA_HD void plan_pieces(const PlanShape& sh, int64_t nk, int splits, int64_t ch
                                     : (n + (uint32_t)chunk_target - 1u) / (uint32_t)chunk_target;
   if (p > (uint32_t)sh.max_splits) p = (uint32_t)sh.max_splits;
   if (p < 1u) p = 1u;
-  const uint32_t c = ((n + p - 1u) / p + align - 1u) / align * align;
+  const uint32_t c = ((n + p - 1u) / p + align - 1u) & ~(align - 1u);
   *chunk = c;
   *pieces = (n + c - 1u) / c;
 }
@@ -148,12 +154,13 @@ VMLA_HD int64_t plan_cand_chunk(const PlanShape& sh, int64_t total_work, int clu
 // The two runs of equal-cost units of one sequence under a chunk target:
 // cost[0] x count[0] full pieces, cost[1] x count[1] last pieces (counts 0 for
 // a sequence without queries); returns the sequence's fp32 partial rows.
-VMLA_HD int64_t plan_seq_runs(const PlanShape& sh, int64_t nq, int64_t nk, int num_heads, int64_t chunk_target,
-                              int64_t (&cost)[kRunsPerSeq], int64_t (&count)[kRunsPerSeq]) {
+// rb: the sequence's row blocks, ceil(nq H / rows_per_unit) (the caller computes it
+// once for all candidates).
+VMLA_HD int64_t plan_seq_runs(const PlanShape& sh, int64_t nq, int64_t nk, int num_heads, int64_t rb,
+                              int64_t chunk_target, int64_t (&cost)[kRunsPerSeq], int64_t (&count)[kRunsPerSeq]) {
   cost[0] = cost[1] = 0;
   count[0] = count[1] = 0;
   if (nq == 0) return 0;
-  const int64_t rb = (uint32_t)(nq * num_heads + sh.rows_per_unit - 1) / (uint32_t)sh.rows_per_unit;
   int64_t chunk = 0, pieces = 0;
   plan_pieces(sh, nk, 0, chunk_target, &chunk, &pieces);
   cost[0] = chunk + kUnitFixedKeys;
