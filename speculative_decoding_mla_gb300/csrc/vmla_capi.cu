@@ -578,7 +578,8 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   PlanParams* plan = reinterpret_cast<PlanParams*>(ws + L.plan_off);
   TcSched* sched = reinterpret_cast<TcSched*>(ws + L.sched_off);
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(status, 0, 16, st) != cudaSuccess) return VMLA_ERR_CUDA;
+  // status words 0-3 and the planner's block counter (word 4)
+  if (cudaMemsetAsync(status, 0, 32, st) != cudaSuccess) return VMLA_ERR_CUDA;
   if (batch == 0 || max_total_q == 0) return VMLA_OK;
   rc = launch_device_plan(qo_indptr, kv_indptr, batch, num_heads, splits, clusters, max_total_q, max_total_kv,
                           L.part_cap, plan, sched, status, stream);

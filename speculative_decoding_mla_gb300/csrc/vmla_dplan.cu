@@ -10,9 +10,10 @@
 // a cluster schedule for the tensor-core kernel (units sorted by cost, dealt
 // to the clusters in a snake order, then in unit order within each cluster).
 // The piece size is the host planner's choice among the same candidates,
-// scored with the same integer arithmetic, one warp per candidate, and the
-// lane plan replaces it under the host planner's rule (one thread per
-// sequence, block-wide prefix sums for the streams' positions).
+// scored with the same integer arithmetic, one block per candidate (the last
+// block to finish makes the plan), and the lane plan replaces it under the
+// host planner's rule (one thread per sequence, block-wide prefix sums for the
+// streams' positions).
 // The areas of the workspace are sized for caller-given upper bounds on the
 // query and key totals.
 #include <cuda_runtime.h>
@@ -27,80 +28,70 @@ constexpr int kPlanThreads = 1024;
 constexpr int kSortKeys = 4096;  // power of two, at least kMaxTcUnits
 static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
 static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
-static_assert(kPlanThreads / 32 == kChunkCands, "one warp per piece-size candidate");
-static_assert(kChunkCands * kRunsPerSeq * kSearchMaxBatch <= kSortKeys, "candidate runs fit the sort keys");
+static_assert(4 * kRunsPerSeq * kSearchMaxBatch <= kSortKeys, "a candidate's scratch fits the sort keys");
+static_assert(kMaxClusters <= kRunsPerSeq * kSearchMaxBatch, "cluster loads fit the scratch");
+static_assert(kRunsPerSeq * kSearchMaxBatch <= kPlanThreads, "one thread per run");
 static_assert(5 * VMLA_MAX_BATCH <= kSortKeys, "the lane plan's prefix sums fit the sort keys");
 
-__device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
-  for (int o = 16; o > 0; o >>= 1) {
-    const int64_t x = __shfl_xor_sync(0xffffffffu, v, o);
-    v = x > v ? x : v;
-  }
-  return v;
-}
-
-// Score of candidate k (plan_pick_chunk_host's, for one warp): the longest
-// cluster load of the snake deal of its units plus the merge's charge, or -1
-// when they exceed one launch.  runs: this warp's kRunsPerSeq * kSearchMaxBatch words, each run
-// packed as cost << 32 | sort position << 16 | count (costs are below 2^32,
-// counts below 2^12 and positions below kMaxTcUnits).
-__device__ int64_t candidate_score(const PlanShape& sh, const int32_t* qo, const int32_t* kv, int batch,
-                                   int num_heads, int clusters, int64_t total_work, int k, uint64_t* runs) {
-  const int ln = threadIdx.x & 31;
-  const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
+// Score of candidate k (plan_pick_chunk_host's) by a whole block: the longest
+// cluster load of the snake deal of its units plus the merge's charge, or -1 when
+// they exceed one launch.  Runs are ranked by cost (descending, ties by run), a
+// run's sort position being the units of the runs before it; each (cluster, run)
+// pair adds its cost times the run's units that land on the cluster.  Scratch:
+// 4 x kRunsPerSeq x kSearchMaxBatch words of shared memory.
+__device__ int64_t block_candidate_score(const PlanShape& sh, const int32_t* qo, const int32_t* kv, int batch,
+                                         int num_heads, int clusters, int64_t total_work, int k, int64_t* scratch) {
+  __shared__ unsigned long long s_units, s_part, s_worst;
+  constexpr int kRuns = kRunsPerSeq * kSearchMaxBatch;
+  int64_t* cost = scratch;
+  int64_t* cnt = scratch + kRuns;
+  int64_t* pos = scratch + 2 * kRuns;
+  int64_t* load = scratch + 3 * kRuns;  // kMaxClusters <= kRuns entries
+  const int tid = threadIdx.x;
   const int R = kRunsPerSeq * batch;
-  int64_t units = 0, part = 0;
-  for (int b = ln; b < batch; b += 32) {
+  const int64_t ct = plan_cand_chunk(sh, total_work, clusters, k);
+  if (tid == 0) {
+    s_units = 0;
+    s_part = 0;
+    s_worst = 0;
+  }
+  for (int j = tid; j < clusters; j += blockDim.x) load[j] = 0;
+  __syncthreads();
+  if (tid < batch) {
     int64_t c2[kRunsPerSeq], n2[kRunsPerSeq];
-    const int64_t nq = (int64_t)qo[b + 1] - qo[b];
-    part += plan_seq_runs(sh, nq, (int64_t)kv[b + 1] - kv[b], num_heads, plan_row_blocks(sh, nq, num_heads), ct, c2,
-                          n2);
+    const int64_t nq = (int64_t)qo[tid + 1] - qo[tid];
+    const int64_t prt = plan_seq_runs(sh, nq, (int64_t)kv[tid + 1] - kv[tid], num_heads,
+                                      plan_row_blocks(sh, nq, num_heads), ct, c2, n2);
+    int64_t units = 0;
     for (int t = 0; t < kRunsPerSeq; ++t) {
-      runs[kRunsPerSeq * b + t] = ((uint64_t)c2[t] << 32) | (uint64_t)n2[t];
+      cost[kRunsPerSeq * tid + t] = c2[t];
+      cnt[kRunsPerSeq * tid + t] = n2[t];
       units += n2[t];
     }
+    atomicAdd(&s_units, (unsigned long long)units);
+    atomicAdd(&s_part, (unsigned long long)prt);
   }
-  units = warp_sum_i64(units);
-  part = warp_sum_i64(part);
-  __syncwarp();
-  if (units > kMaxTcUnits) return -1;
-  // sort positions (each lane holds those of its runs until every lane has read the costs)
-  constexpr int kPerLane = kRunsPerSeq * kSearchMaxBatch / 32;
-  int64_t rank[kPerLane];
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    const int r = ln + 32 * i;
-    rank[i] = 0;
-    if (r < R) {
-      const int64_t cr = (int64_t)(runs[r] >> 32);
-      for (int r2 = 0; r2 < R; ++r2) {
-        const uint64_t x = runs[r2];
-        if (plan_run_before((int64_t)(x >> 32), r2, cr, r)) rank[i] += (int64_t)(x & 0xFFFFu);
-      }
-    }
+  __syncthreads();
+  if (s_units > (unsigned long long)kMaxTcUnits) return -1;  // the same value in every thread
+  if (tid < R) {
+    const int64_t cr = cost[tid];
+    int64_t p = 0;
+    for (int r2 = 0; r2 < R; ++r2)
+      if (plan_run_before(cost[r2], r2, cr, tid)) p += cnt[r2];
+    pos[tid] = p;
   }
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    const int r = ln + 32 * i;
-    if (r < R) runs[r] |= (uint64_t)rank[i] << 16;
+  __syncthreads();
+  for (int q = tid; q < clusters * R; q += blockDim.x) {
+    const int j = q / R, r = q - j * R;
+    const int64_t n = cnt[r];
+    if (n == 0) continue;
+    const int64_t add = cost[r] * (plan_snake_share(pos[r] + n, j, clusters) - plan_snake_share(pos[r], j, clusters));
+    if (add != 0) atomicAdd(reinterpret_cast<unsigned long long*>(&load[j]), (unsigned long long)add);
   }
-  __syncwarp();
-  int64_t worst = 0;
-  for (int j = ln; j < clusters; j += 32) {
-    int64_t load = 0;
-    for (int r = 0; r < R; ++r) {
-      const uint64_t x = runs[r];
-      const int64_t cost = (int64_t)(x >> 32), pos = (int64_t)((x >> 16) & 0xFFFFu), n = (int64_t)(x & 0xFFFFu);
-      load += cost * (plan_snake_share(pos + n, j, clusters) - plan_snake_share(pos, j, clusters));
-    }
-    worst = load > worst ? load : worst;
-  }
-  return warp_max_i64(worst) + plan_merge_score(part);
+  __syncthreads();
+  if (tid < clusters) atomicMax(&s_worst, (unsigned long long)load[tid]);
+  __syncthreads();
+  return (int64_t)s_worst + plan_merge_score((int64_t)s_part);
 }
 
 // Ascending bitonic sort of the first n keys in shared memory (n a power of
@@ -138,10 +129,14 @@ __global__ void __launch_bounds__(kPlanThreads)
 device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ kv, int batch, int num_heads,
                    int splits, int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
                    PlanParams* __restrict__ pp, TcSched* __restrict__ sched, uint32_t* status) {
+  // status[4]: blocks done with their candidate (zeroed before the launch, and again by
+  // the last block); status[8..]: the candidates' scores (int64)
+  unsigned int* done = status + 4;
+  int64_t* scores = reinterpret_cast<int64_t*>(status + 8);
   __shared__ int64_t s_units[VMLA_MAX_BATCH], s_part[VMLA_MAX_BATCH], s_merge[VMLA_MAX_BATCH];
   __shared__ uint64_t keys[kSortKeys];
   __shared__ unsigned long long s_work;
-  __shared__ int s_bad, s_maxs, s_cand, s_lanes;
+  __shared__ int s_bad, s_maxs, s_cand, s_lanes, s_last;
   __shared__ unsigned int s_misfit;
   __shared__ int64_t s_score[kChunkCands];
   __shared__ int64_t s_chunk;
@@ -172,12 +167,20 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   const bool force_lanes = splits == VMLA_SPLITS_LANES;
   if (force_lanes) splits = 0;  // the uniform plan it falls back on is the planner's own
   const bool search = lengths_ok && splits == 0 && batch >= 1 && batch <= kSearchMaxBatch;
-  if (search) {
-    const int w = tid >> 5;
-    const int64_t sc = candidate_score(sh, qo, kv, batch, num_heads, clusters, total_work, w,
-                                       keys + w * (kRunsPerSeq * kSearchMaxBatch));
-    if ((tid & 31) == 0) s_score[w] = sc;
+  // every block scores one candidate (the launch has kChunkCands blocks when a search
+  // can run); the last block to finish reads all the scores and makes the plan
+  if (search && blockIdx.x < kChunkCands) {
+    const int64_t sc = block_candidate_score(sh, qo, kv, batch, num_heads, clusters, total_work, (int)blockIdx.x,
+                                             reinterpret_cast<int64_t*>(keys));
+    if (tid == 0) scores[blockIdx.x] = sc;
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1 ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  if (tid == 0) *done = 0;  // ready for the next call (or graph replay)
+  if (tid < kChunkCands) s_score[tid] = search && tid < (int)gridDim.x ? __ldcg(&scores[tid]) : -1;
   __syncthreads();
   if (tid == 0) {
     s_cand = search ? plan_choose_cand(s_score) : kDefaultCand;
@@ -383,7 +386,7 @@ DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t 
   if (cap > all) cap = all;
   DplanLayout L;
   L.status_off = 0;
-  L.plan_off = up(16);
+  L.plan_off = up(32 + sizeof(int64_t) * kChunkCands);  // status words, the block counter, candidate scores
   L.sched_off = L.plan_off + up(sizeof(PlanParams));
   L.masks_off = L.sched_off + up(sizeof(TcSched));
   L.part_o_off = L.masks_off + up((size_t)max_total_q * 8);
@@ -398,9 +401,12 @@ int launch_device_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int b
                        int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
                        PlanParams* plan, TcSched* sched, uint32_t* status, void* stream) {
   if (batch < 0 || batch > VMLA_MAX_BATCH || clusters < 1 || clusters > kMaxClusters) return VMLA_ERR_SHAPE;
-  device_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(qo_indptr, kv_indptr, batch, num_heads, splits,
-                                                                   clusters, max_total_q, max_total_kv, part_cap,
-                                                                   plan, sched, status);
+  // one block per piece-size candidate when the candidate search can run (its lengths
+  // are checked on the device), else one block
+  const bool search = (splits == 0 || splits == VMLA_SPLITS_LANES) && batch >= 1 && batch <= kSearchMaxBatch;
+  device_plan_kernel<<<search ? kChunkCands : 1, kPlanThreads, 0, (cudaStream_t)stream>>>(
+      qo_indptr, kv_indptr, batch, num_heads, splits, clusters, max_total_q, max_total_kv, part_cap, plan, sched,
+      status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

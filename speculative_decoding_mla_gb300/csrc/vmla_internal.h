@@ -157,7 +157,8 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
 // workspace holds, after the status words, the plan, the schedule, and areas
 // sized for upper bounds on the lengths fixed by the caller.
 struct DplanLayout {
-  size_t status_off;  // uint32 status, info, rows to gather, draft rows to mask
+  size_t status_off;  // uint32 status, info, rows to gather, draft rows to mask; planner block counter
+                      // (word 4) and candidate scores (int64 from word 8)
   size_t plan_off;    // PlanParams
   size_t sched_off;   // TcSched
   size_t masks_off;   // uint64 [max_total_q]

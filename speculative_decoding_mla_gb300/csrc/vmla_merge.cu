@@ -27,15 +27,11 @@ namespace {
 constexpr int kMergeWarps = 4;  // one per quarter of a 512-column row
 constexpr int kMergeBatch = 12;  // pieces loaded together
 
-__device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
-                                           const float* __restrict__ part_lse, int lse_is_log2,
-                                           uint16_t* __restrict__ out, float* __restrict__ lse) {
-  // block = one merge row; warp c = its columns 4 * (32 c + lane) .. + 3
+// Merge row mrow (< plan.merge_rows) by one block; warp c = its columns 4 * (32 c + lane) .. + 3.
+__device__ __forceinline__ void merge_row(const PlanParams& plan, int mrow, const float* __restrict__ part_o,
+                                          const float* __restrict__ part_lse, int lse_is_log2,
+                                          uint16_t* __restrict__ out, float* __restrict__ lse) {
   const int c = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // launched to start under the verify kernel's tail: its partials first
-  grid_dependency_wait();
-  const int mrow = blockIdx.x;
-  if (mrow >= plan.merge_rows) return;
   // sequence owning merge row mrow: last b with merge_off <= mrow
   int lo = 0, hi = plan.batch;
   while (hi - lo > 1) {
@@ -112,6 +108,17 @@ __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* 
   }
   *dst = make_uint2(pack_bf16x2(acc.x * invW, acc.y * invW), pack_bf16x2(acc.z * invW, acc.w * invW));
   if (c == 0 && lane == 0) lse[orow] = (M + log2f(W)) * 0.6931471805599453f;
+}
+
+// Each block merges rows blockIdx.x, blockIdx.x + gridDim.x, ... of the plan's merge rows
+// (one row per block when the grid has a block per merge row).
+__device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
+                                           const float* __restrict__ part_lse, int lse_is_log2,
+                                           uint16_t* __restrict__ out, float* __restrict__ lse) {
+  // launched to start under the verify kernel's tail: its partials first
+  grid_dependency_wait();
+  const int rows = plan.merge_rows;
+  for (int mrow = blockIdx.x; mrow < rows; mrow += gridDim.x) merge_row(plan, mrow, part_o, part_lse, lse_is_log2, out, lse);
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -191,9 +198,17 @@ int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* pa
                        uint16_t* out, float* lse, void* stream) {
   if (max_rows <= 0) return VMLA_OK;
   if (max_rows > INT32_MAX) return VMLA_ERR_SHAPE;
+  // the merge rows are known only on the device: a grid that fills the GPU once (16
+  // blocks of four warps per SM), each block taking every grid-th row, instead of a
+  // block per row of the bound (most of which would find nothing to do)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return VMLA_ERR_CUDA;
+  const int64_t fill = (int64_t)sms * 16;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {early_start_attribute()};
-  cfg.gridDim = dim3((unsigned)max_rows, 1, 1);
+  cfg.gridDim = dim3((unsigned)(max_rows < fill ? max_rows : fill), 1, 1);
   cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
   cfg.stream = (cudaStream_t)stream;
   cfg.attrs = attr;

@@ -54,7 +54,8 @@ VMLA_HD int64_t plan_seq_work(const PlanShape& sh, int64_t nq, int64_t nk, int n
 
 // Row blocks of a sequence with nq drafts (rows_per_unit is a power of two).
 VMLA_HD int64_t plan_row_blocks(const PlanShape& sh, int64_t nq, int num_heads) {
-  return (nq * num_heads + sh.rows_per_unit - 1) / sh.rows_per_unit;
+  // nq H <= 64 x 128: 32-bit arithmetic
+  return ((uint32_t)(nq * num_heads) + (uint32_t)sh.rows_per_unit - 1u) / (uint32_t)sh.rows_per_unit;
 }
 
 // Keys per piece the planner aims at so that `slots` units run at once.
@@ -174,9 +175,11 @@ VMLA_HD int64_t plan_seq_runs(const PlanShape& sh, int64_t nq, int64_t nk, int n
 // 0..C-1 go to clusters 0..C-1, positions C..2C-1 to clusters C-1..0, and so
 // on) that land on cluster j.
 VMLA_HD int64_t plan_snake_share(int64_t x, int j, int C) {
-  const int64_t period = 2 * (int64_t)C;
-  const int64_t rem = x % period;
-  return 2 * (x / period) + (rem > j ? 1 : 0) + (rem > period - 1 - j ? 1 : 0);
+  // x <= kMaxTcUnits and 2C <= 2 kMaxClusters: 32-bit division (a 64-bit one is a
+  // slow emulated sequence on the GPU, where this runs for every run and cluster)
+  const uint32_t period = 2u * (uint32_t)C, xx = (uint32_t)x;
+  const uint32_t q = xx / period, rem = xx - q * period;
+  return 2 * (int64_t)q + (rem > (uint32_t)j ? 1 : 0) + (rem > period - 1u - (uint32_t)j ? 1 : 0);
 }
 
 // Sort position of run r among runs sorted by cost (descending), ties by run
@@ -233,7 +236,11 @@ VMLA_HD int64_t plan_seq_tiles(int64_t nk) { return (nk + 127) / 128; }
 VMLA_HD int64_t plan_stream_span(int64_t nk) { return plan_seq_tiles(nk) + kUnitFixedTiles; }
 
 // Pieces of a stream whose T tiles start at cost position a: the lanes of length L it meets.
-VMLA_HD int64_t plan_stream_pieces(int64_t a, int64_t T, int64_t L) { return (a + T - 1) / L - a / L + 1; }
+// (a + T <= W <= INT32_MAX in a lane plan: 32-bit arithmetic.)
+VMLA_HD int64_t plan_stream_pieces(int64_t a, int64_t T, int64_t L) {
+  const uint32_t aa = (uint32_t)a, ll = (uint32_t)L;
+  return (int64_t)((aa + (uint32_t)T - 1u) / ll - aa / ll) + 1;
+}
 
 // Lane length for total cost W over `lanes` lanes (at least one tile).
 VMLA_HD int64_t plan_lane_tiles(int64_t W, int lanes) {
