@@ -563,11 +563,33 @@ def defragmented_runs(args, case, dc, flush_buf, tokens):
     dms = timed_from_idle(decode_step, args.steps, flush_buf)
     if int(st[0]) != 0 or binding.verify_attn_mla_check(ws) != 0:
         raise RuntimeError("decode step on runs reported a fault")
+    # the same decode step captured once in a CUDA graph: the append with a bound and the call on
+    # the runs with the plan made on the device, so that replays stay valid as the lengths change
+    T, H, N = dc.total_q, dc.num_heads, int(case.kv_indptr[-1])
+    gws = torch.empty(binding.verify_attn_mla_runs_device_plan_workspace_size(case.batch, H, T, N, args.splits),
+                      dtype=torch.uint8, device=dc.q.device)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        binding.verify_attn_mla_defrag_append(dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.kv_indptr_host, dst,
+                                              base_d, first, st, max_new_rows=int(nq.max()))
+        binding.verify_attn_mla_runs_device_plan(dc.q, dst, dc.kv_indptr, base_d, dc.qo_indptr, case.batch, T, N,
+                                                 out, lse, gws, dc.sm_scale, parent=dc.parent, splits=args.splits)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    gms = timed_from_idle(graph.replay, args.steps, flush_buf)
+    if int(st[0]) != 0 or binding.verify_attn_mla_check(gws) != 0:
+        raise RuntimeError("captured decode step on runs reported a fault")
     return {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "KV tokens/s", "defrag_ms_once": defrag_ms,
             "decode_step": {"ms_per_step": dms, "value": tokens / (dms / 1e3), "unit": "KV tokens/s",
                             "appended_rows_per_step": int(nq.sum()),
                             "note": "verify_attn_mla_defrag_append of the step's new rows (the drafts) into the "
                                     "runs, then verify_attn_mla_runs; one event pair per step from an idle GPU"},
+            "decode_step_graph": {"ms_per_step": gms, "value": tokens / (gms / 1e3), "unit": "KV tokens/s",
+                                  "note": "the decode step captured once in a CUDA graph (append with a bound, then "
+                                          "verify_attn_mla_runs_device_plan); one replay per step from an idle GPU"},
             "note": "rows compacted once into 128-aligned pool runs (verify_attn_mla_defrag), then "
                     "verify_attn_mla_runs each step: no per-call gather; one event pair per call from an idle "
                     "GPU, as the main step"}

@@ -210,7 +210,11 @@ int verify_attn_mla_defrag(const void* src_pool, int64_t src_slots, const int32_
  *   max_new_rows  a bound on N_b - first_row[b] known to the caller (the launch
  *             then covers only that many rows past each first_row), or 0 for
  *             none; a sequence with more new rows records VMLA_ERR_INDEX and
- *             is skipped.  Negative: VMLA_ERR_SHAPE.
+ *             is skipped.  Negative: VMLA_ERR_SHAPE.  With a bound the launch
+ *             depends on no host length (it is made even when the host copy
+ *             says the runs are empty), so the call can be captured in a CUDA
+ *             graph once and replayed as the runs grow (kv_indptr, kv_indices
+ *             and first_row are read on the device at each replay).
  * Argument errors return before the launch.  No host synchronisation. */
 int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const int32_t* kv_indptr,
                                   const int32_t* kv_indices, const int32_t* kv_indptr_host, int batch,
@@ -234,6 +238,26 @@ int verify_attn_mla_runs(const void* q, const void* kv_pool, int64_t pool_slots,
                          void* workspace, size_t workspace_bytes, void* stream);
 int verify_attn_mla_runs_workspace_size(int batch, int num_heads, const int32_t* qo_indptr_host,
                                         const int32_t* kv_indptr_host, int splits, size_t* bytes);
+
+/* verify_attn_mla_runs for CUDA-graph capture: the plan is made on the device
+ * from the device indptr arrays, as verify_attn_mla_device_plan makes it, and
+ * the rows are read from their runs (no gather).  Arguments as for
+ * verify_attn_mla_device_plan, with run_base [batch] int32 (device) in place
+ * of kv_indices; max_total_kv bounds kv_indptr[batch] at every replay.  The
+ * workspace holds no staged rows:
+ * verify_attn_mla_runs_device_plan_workspace_size() bytes.  A decode loop can
+ * capture this call after verify_attn_mla_defrag_append (with a bound on the
+ * new rows) and replay both as its sequences grow.  Results equal
+ * verify_attn_mla_runs' bit for bit.  Argument errors return before any
+ * launch; lengths past the bounds make the call compute nothing and record
+ * VMLA_ERR_SHAPE; a run outside the pool records VMLA_ERR_INDEX. */
+int verify_attn_mla_runs_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q,
+                                                    int64_t max_total_kv, int splits, size_t* bytes);
+int verify_attn_mla_runs_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                     const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                     const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                                     int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Failure test only.  For the calling thread's later calls of the tensor-core
  * entry points: fault 1 makes the kernel's softmax warps withhold the signal

@@ -42,6 +42,7 @@ EXPORTS = (
     "verify_attn_mla_tree_accept", "verify_attn_mla_defrag", "verify_attn_mla_runs",
     "verify_attn_mla_runs_workspace_size", "verify_attn_mla_test_fault", "verify_attn_mla_fp8",
     "verify_attn_mla_simt_static_check", "verify_attn_mla_defrag_append",
+    "verify_attn_mla_runs_device_plan_workspace_size", "verify_attn_mla_runs_device_plan",
 )
 
 
@@ -82,6 +83,9 @@ def _load(path: str = LIB_PATH):
         "verify_attn_mla_device_plan_workspace_size": [i32, i32, i64, i64, i32, ctypes.POINTER(sz)],
         "verify_attn_mla_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp, vp,
                                         sz, vp],
+        "verify_attn_mla_runs_device_plan_workspace_size": [i32, i32, i64, i64, i32, ctypes.POINTER(sz)],
+        "verify_attn_mla_runs_device_plan": [vp, vp, i64, vp, vp, vp, vp, vp, i32, i32, i64, i64, f32, i32, vp, vp,
+                                             vp, sz, vp],
         "verify_attn_mla_tree_accept": [vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp],
         "verify_attn_mla_defrag": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, vp],
         "verify_attn_mla_defrag_append": [vp, i64, vp, vp, vp, i32, vp, i64, vp, vp, i64, vp, vp],
@@ -239,28 +243,52 @@ def verify_attn_mla(q, kv_pool, kv_indptr, kv_indices, qo_indptr, kv_indptr_host
          qo_indptr_host, out, lse, workspace, sm_scale, draft_mask, parent, splits, stream)
 
 
+def _dplan_ws(fn, name, batch, num_heads, max_total_q, max_total_kv, splits):
+    n = ctypes.c_size_t(0)
+    _check(fn(int(batch), int(num_heads), int(max_total_q), int(max_total_kv), int(splits), ctypes.byref(n)), name)
+    return int(n.value)
+
+
 def verify_attn_mla_device_plan_workspace_size(batch: int, num_heads: int, max_total_q: int, max_total_kv: int,
                                                splits: int = 0) -> int:
-    n = ctypes.c_size_t(0)
-    _check(_lib.verify_attn_mla_device_plan_workspace_size(int(batch), int(num_heads), int(max_total_q),
-                                                           int(max_total_kv), int(splits), ctypes.byref(n)),
-           "verify_attn_mla_device_plan_workspace_size")
-    return int(n.value)
+    return _dplan_ws(_lib.verify_attn_mla_device_plan_workspace_size, "verify_attn_mla_device_plan_workspace_size",
+                     batch, num_heads, max_total_q, max_total_kv, splits)
+
+
+def verify_attn_mla_runs_device_plan_workspace_size(batch: int, num_heads: int, max_total_q: int, max_total_kv: int,
+                                                    splits: int = 0) -> int:
+    return _dplan_ws(_lib.verify_attn_mla_runs_device_plan_workspace_size,
+                     "verify_attn_mla_runs_device_plan_workspace_size", batch, num_heads, max_total_q, max_total_kv,
+                     splits)
+
+
+def _dplan_call(fn, name, q, kv_pool, kv_indptr, rows, rows_name, qo_indptr, batch, max_total_q, max_total_kv, out,
+                lse, workspace, sm_scale, draft_mask, parent, splits, stream, num_heads, pool_slots):
+    H = int(num_heads if num_heads is not None else q.shape[1])
+    S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
+    rc = fn(_d(q, 2, "q"), _d(kv_pool, 2, "kv_pool"), S, _d(kv_indptr, 4, "kv_indptr"), _d(rows, 4, rows_name),
+            _d(qo_indptr, 4, "qo_indptr"), _d(draft_mask, 8, "draft_mask"), _d(parent, 4, "parent"), int(batch), H,
+            int(max_total_q), int(max_total_kv), float(sm_scale), int(splits), _d(out, 2, "out"), _d(lse, 4, "lse"),
+            _d(workspace, 0, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, name)
 
 
 def verify_attn_mla_device_plan(q, kv_pool, kv_indptr, kv_indices, qo_indptr, batch: int, max_total_q: int,
                                 max_total_kv: int, out, lse, workspace, sm_scale, draft_mask=None, parent=None,
                                 splits=0, stream=None, num_heads=None, pool_slots=None):
     """Stream-capture-safe verify attention: the plan is built on the device from the device indptr arrays."""
-    H = int(num_heads if num_heads is not None else q.shape[1])
-    S = int(pool_slots if pool_slots is not None else kv_pool.shape[0])
-    rc = _lib.verify_attn_mla_device_plan(_d(q, 2, "q"), _d(kv_pool, 2, "kv_pool"), S, _d(kv_indptr, 4, "kv_indptr"),
-                                          _d(kv_indices, 4, "kv_indices"), _d(qo_indptr, 4, "qo_indptr"),
-                                          _d(draft_mask, 8, "draft_mask"), _d(parent, 4, "parent"), int(batch), H,
-                                          int(max_total_q), int(max_total_kv), float(sm_scale), int(splits),
-                                          _d(out, 2, "out"), _d(lse, 4, "lse"), _d(workspace, 0, "workspace"),
-                                          workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "verify_attn_mla_device_plan")
+    _dplan_call(_lib.verify_attn_mla_device_plan, "verify_attn_mla_device_plan", q, kv_pool, kv_indptr, kv_indices,
+                "kv_indices", qo_indptr, batch, max_total_q, max_total_kv, out, lse, workspace, sm_scale, draft_mask,
+                parent, splits, stream, num_heads, pool_slots)
+
+
+def verify_attn_mla_runs_device_plan(q, kv_pool, kv_indptr, run_base, qo_indptr, batch: int, max_total_q: int,
+                                     max_total_kv: int, out, lse, workspace, sm_scale, draft_mask=None, parent=None,
+                                     splits=0, stream=None, num_heads=None, pool_slots=None):
+    """verify_attn_mla_runs with the plan built on the device (capture-safe; rows read from their pool runs)."""
+    _dplan_call(_lib.verify_attn_mla_runs_device_plan, "verify_attn_mla_runs_device_plan", q, kv_pool, kv_indptr,
+                run_base, "run_base", qo_indptr, batch, max_total_q, max_total_kv, out, lse, workspace, sm_scale,
+                draft_mask, parent, splits, stream, num_heads, pool_slots)
 
 
 def verify_attn_mla_defrag(src_pool, kv_indptr, kv_indices, kv_indptr_host, dst_pool, run_base, status_word=None,

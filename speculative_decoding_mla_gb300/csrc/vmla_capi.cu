@@ -286,7 +286,9 @@ int defrag_impl(const void* src_pool, int64_t src_slots, const int32_t* kv_indpt
   for (int b = 0; b < batch; ++b)
     if (kv_indptr_host[b + 1] < kv_indptr_host[b]) return VMLA_ERR_SHAPE;
   const int64_t total_kv = batch > 0 ? kv_indptr_host[batch] : 0;
-  if (total_kv == 0) return VMLA_OK;
+  // nothing to copy; an append with a bound launches anyway (batch > 0), so that a captured
+  // launch serves later replays whose runs are not empty
+  if (total_kv == 0 && !(max_new > 0 && batch > 0)) return VMLA_OK;
   if (!src_pool || !dst_pool || !kv_indptr || !kv_indices || !run_base) return VMLA_ERR_NULL;
   if (!aligned(src_pool, 16) || !aligned(dst_pool, 16) || !aligned(status_word, 4) || !aligned(run_base, 4) ||
       !aligned(first_row, 4))
@@ -312,7 +314,8 @@ int verify_attn_mla_defrag_append(const void* src_pool, int64_t src_slots, const
                                   void* dst_pool, int64_t dst_slots, const int32_t* run_base,
                                   const int32_t* first_row, int64_t max_new_rows, uint32_t* status_word,
                                   void* stream) {
-  if (batch > 0 && kv_indptr_host && kv_indptr_host[batch] > 0 && !first_row) return VMLA_ERR_NULL;
+  if (batch > 0 && kv_indptr_host && (kv_indptr_host[batch] > 0 || max_new_rows > 0) && !first_row)
+    return VMLA_ERR_NULL;
   if (max_new_rows < 0) return VMLA_ERR_SHAPE;
   return defrag_impl(src_pool, src_slots, kv_indptr, kv_indices, kv_indptr_host, batch, dst_pool, dst_slots,
                      run_base, first_row, max_new_rows, status_word, stream);
@@ -536,42 +539,33 @@ int dplan_clusters(int* clusters) {
 }
 }  // namespace
 
-int verify_attn_mla_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv,
-                                               int splits, size_t* bytes) {
-  if (!bytes) return VMLA_ERR_NULL;
-  int rc = check_dplan_bounds(batch, num_heads, max_total_q, max_total_kv, splits);
-  if (rc != VMLA_OK) return rc;
-  int sms = 0, clusters = 0;
-  rc = current_sm_count(&sms, true);
-  if (rc != VMLA_OK) return rc;
-  rc = dplan_clusters(&clusters);
-  if (rc != VMLA_OK) return rc;
-  *bytes = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters).total;
-  return VMLA_OK;
-}
-
-int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
-                                const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
-                                const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
-                                int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
-                                void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// Device-planned call on staged rows (kv_indices given, run_base NULL: the gather runs)
+// or on pool runs (run_base given: no gather, a run check instead).
+int device_plan_impl(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, const int32_t* run_base, const int32_t* qo_indptr,
+                     const uint64_t* draft_mask, const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                     int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  const bool runs = run_base != nullptr;
   int rc = check_dplan_bounds(batch, num_heads, max_total_q, max_total_kv, splits);
   if (rc != VMLA_OK) return rc;
   if (pool_slots < 0 || pool_slots > INT32_MAX) return VMLA_ERR_SHAPE;
   if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return VMLA_ERR_SHAPE;
   if (!workspace) return VMLA_ERR_NULL;
   if (batch > 0 && (!kv_indptr || !qo_indptr)) return VMLA_ERR_NULL;
-  if (max_total_q > 0 && (!q || !kv_pool || !kv_indices || !out || !lse)) return VMLA_ERR_NULL;
+  if (max_total_q > 0 && (!q || !kv_pool || (!runs && !kv_indices) || !out || !lse)) return VMLA_ERR_NULL;
   if (max_total_kv > 0 && pool_slots == 0) return VMLA_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
-      !aligned(workspace, VMLA_WORKSPACE_ALIGN) || !aligned(draft_mask, 8) || !aligned(parent, 4))
+      !aligned(workspace, VMLA_WORKSPACE_ALIGN) || !aligned(draft_mask, 8) || !aligned(parent, 4) ||
+      !aligned(run_base, 4))
     return VMLA_ERR_ALIGN;
   int sms = 0, clusters = 0;
   rc = current_sm_count(&sms, true);
   if (rc != VMLA_OK) return rc;
   rc = dplan_clusters(&clusters);
   if (rc != VMLA_OK) return rc;
-  const DplanLayout L = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters);
+  const DplanLayout L = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters, !runs);
   if (workspace_bytes < L.total) return VMLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
@@ -606,16 +600,71 @@ int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool
   a.part_rows = L.part_cap;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
-  a.staged = reinterpret_cast<uint16_t*>(ws + L.staged_off);
-  a.total_kv = max_total_kv;  // the staged capacity; the planner's count is in status word 2
-  a.run_base = nullptr;
+  // rows: the staged copy (its capacity; the planner's count is in status word 2) or the pool's runs
+  a.staged = runs ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_pool))
+                  : reinterpret_cast<uint16_t*>(ws + L.staged_off);
+  a.total_kv = runs ? pool_slots : max_total_kv;
+  a.run_base = run_base;
   a.kv_scale = 0.f;
   a.status = status;
-  rc = launch_gather_dplan(a, status + 2, stream);
+  if (runs) {
+    // the runs must lie in the pool (a run outside it is reported; its keys read the tile loads' zero fill)
+    rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, nullptr, batch, 0, nullptr, pool_slots, run_base, true, status,
+                       stream);
+  } else {
+    rc = launch_gather_dplan(a, status + 2, stream);
+  }
   if (rc != VMLA_OK) return rc;
   rc = launch_tc_dplan(plan, sched, clusters, a, stream);
   if (rc != VMLA_OK) return rc;
   return launch_merge_dplan(plan, max_total_q * num_heads, a.part_o, a.part_lse, a.out, a.lse, stream);
+}
+
+int device_plan_workspace(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits, bool staged,
+                          size_t* bytes) {
+  if (!bytes) return VMLA_ERR_NULL;
+  int rc = check_dplan_bounds(batch, num_heads, max_total_q, max_total_kv, splits);
+  if (rc != VMLA_OK) return rc;
+  int sms = 0, clusters = 0;
+  rc = current_sm_count(&sms, true);
+  if (rc != VMLA_OK) return rc;
+  rc = dplan_clusters(&clusters);
+  if (rc != VMLA_OK) return rc;
+  *bytes = dplan_layout(batch, num_heads, max_total_q, max_total_kv, splits, clusters, staged).total;
+  return VMLA_OK;
+}
+}  // namespace
+
+int verify_attn_mla_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv,
+                                               int splits, size_t* bytes) {
+  return device_plan_workspace(batch, num_heads, max_total_q, max_total_kv, splits, true, bytes);
+}
+
+int verify_attn_mla_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                                int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return device_plan_impl(q, kv_pool, pool_slots, kv_indptr, kv_indices, nullptr, qo_indptr, draft_mask, parent, batch,
+                          num_heads, max_total_q, max_total_kv, sm_scale, splits, out, lse, workspace,
+                          workspace_bytes, stream);
+}
+
+int verify_attn_mla_runs_device_plan_workspace_size(int batch, int num_heads, int64_t max_total_q,
+                                                    int64_t max_total_kv, int splits, size_t* bytes) {
+  return device_plan_workspace(batch, num_heads, max_total_q, max_total_kv, splits, false, bytes);
+}
+
+int verify_attn_mla_runs_device_plan(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
+                                     const int32_t* run_base, const int32_t* qo_indptr, const uint64_t* draft_mask,
+                                     const int32_t* parent, int batch, int num_heads, int64_t max_total_q,
+                                     int64_t max_total_kv, float sm_scale, int splits, void* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch > 0 && !run_base) return VMLA_ERR_NULL;
+  static const int32_t kNone = 0;  // any non-null pointer selects the runs mode when batch is 0
+  return device_plan_impl(q, kv_pool, pool_slots, kv_indptr, nullptr, run_base ? run_base : &kNone, qo_indptr,
+                          draft_mask, parent, batch, num_heads, max_total_q, max_total_kv, sm_scale, splits, out, lse,
+                          workspace, workspace_bytes, stream);
 }
 
 int verify_attn_mla_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft_token,

@@ -119,15 +119,16 @@ int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv
     longest = len > longest ? len : longest;
   }
   // all of the longest run, or (append with a bound) the new rows from the boundary below
-  // first_row plus the tail: max_new + 2 (kRunAlign - 1) rows at most
-  const int64_t span = max_new > 0 && max_new < longest ? max_new + 2 * (kRunAlign - 1) : longest;
+  // first_row plus the tail: max_new + 2 (kRunAlign - 1) rows at most.  With a bound the
+  // grid depends on nothing else, so a captured launch stays valid as the runs grow.
+  const bool bounded = max_new > 0;
+  const int64_t span = bounded ? max_new + 2 * (kRunAlign - 1) : longest;
   const int64_t xblocks = (span + kRunAlign - 1) / kRunAlign;
   if (xblocks == 0) return VMLA_OK;
   if (xblocks > INT32_MAX || batch > 65535) return VMLA_ERR_SHAPE;
   defrag_kernel<<<dim3((unsigned)xblocks, (unsigned)batch), kDefragWarps * 32, 0, (cudaStream_t)stream>>>(
       reinterpret_cast<const uint4*>(src_pool), src_slots, kv_indptr, kv_indices,
-      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, first_row, max_new > 0 && max_new < longest ? max_new : 0,
-      status);
+      reinterpret_cast<uint4*>(dst_pool), dst_slots, run_base, first_row, bounded ? max_new : 0, status);
   return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
 }
 

@@ -367,7 +367,7 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
 }  // namespace
 
 DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits,
-                         int clusters) {
+                         int clusters, bool staged) {
   auto up = [](size_t x) { return (x + VMLA_WORKSPACE_ALIGN - 1) / VMLA_WORKSPACE_ALIGN * VMLA_WORKSPACE_ALIGN; };
   const PlanShape sh = plan_shape(VMLA_KERNEL_TC);
   // units are at most clusters x m / 16 + (row blocks) with the planner's own
@@ -392,7 +392,7 @@ DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t 
   L.part_o_off = L.masks_off + up((size_t)max_total_q * 8);
   L.part_lse_off = L.part_o_off + up((size_t)cap * kDv * 4);
   L.staged_off = L.part_lse_off + up((size_t)cap * 4);
-  L.total = L.staged_off + up((size_t)max_total_kv * kRowBytes);
+  L.total = L.staged_off + (staged ? up((size_t)max_total_kv * kRowBytes) : 0);
   L.part_cap = cap;
   return L;
 }

@@ -168,8 +168,9 @@ struct DplanLayout {
   size_t total;
   int64_t part_cap;   // partial rows the area holds
 };
+// staged = false: rows read from pool runs, no staging area.
 DplanLayout dplan_layout(int batch, int num_heads, int64_t max_total_q, int64_t max_total_kv, int splits,
-                         int clusters);
+                         int clusters, bool staged = true);
 
 // Planner kernel: reads qo_indptr / kv_indptr [batch+1] on the device, writes
 // the plan and the schedule into the workspace, the gather and mask row counts

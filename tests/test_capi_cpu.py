@@ -80,11 +80,11 @@ def test_argument_errors_before_any_launch(B):
         assert _run_raw(B, **good) == B.VMLA_ERR_DEVICE
 
 
-def _run_dplan(B, **kw):
+def _run_dplan(B, fn="verify_attn_mla_device_plan", **kw):
     args = dict(q=None, kv=None, S=16, kvp=None, kvi=None, qop=None, dm=None, par=None, batch=1, H=4, maxq=2,
                 maxkv=8, scale=0.1, splits=0, out=None, lse=None, ws=None, wsb=0, stream=None)
     args.update(kw)
-    return B.lib().verify_attn_mla_device_plan(args["q"], args["kv"], args["S"], args["kvp"], args["kvi"],
+    return getattr(B.lib(), fn)(args["q"], args["kv"], args["S"], args["kvp"], args["kvi"],
                                                args["qop"], args["dm"], args["par"], args["batch"], args["H"],
                                                args["maxq"], args["maxkv"], args["scale"], args["splits"],
                                                args["out"], args["lse"], args["ws"], args["wsb"], args["stream"])
@@ -108,6 +108,13 @@ def test_device_plan_argument_errors_before_any_launch(B):
     assert _run_dplan(B, **{**good, "scale": float("nan")}) == B.VMLA_ERR_SHAPE
     assert _run_dplan(B, **{**good, "S": 0}) == B.VMLA_ERR_SHAPE
     assert _run_dplan(B, **{**good, "q": fake + 2}) == B.VMLA_ERR_ALIGN
+    # the same call on pool runs (run_base in kv_indices' place)
+    runs = "verify_attn_mla_runs_device_plan"
+    assert _run_dplan(B, fn=runs, **{**good, "kvi": None}) == B.VMLA_ERR_NULL  # run_base
+    assert _run_dplan(B, fn=runs, **{**good, "kvi": fake + 2}) == B.VMLA_ERR_ALIGN
+    assert _run_dplan(B, fn=runs, **{**good, "splits": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, fn=runs, **{**good, "maxq": 65}) == B.VMLA_ERR_SHAPE
+    assert _run_dplan(B, fn=runs, **{**good, "ws": None}) == B.VMLA_ERR_NULL
     assert _run_dplan(B, **{**good, "ws": fake + 16}) == B.VMLA_ERR_ALIGN
     import ctypes
     n = ctypes.c_size_t(0)
