@@ -26,11 +26,13 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kSortKeys = 4096;  // power of two, at least kMaxTcUnits
+constexpr int kCountedSchedule = 256;  // schedules of at most this many units are placed by counting
 static_assert(kSortKeys >= kMaxTcUnits, "schedule sort size");
 static_assert(VMLA_MAX_BATCH <= kPlanThreads, "one thread per sequence");
 static_assert(4 * kRunsPerSeq * kSearchMaxBatch <= kSortKeys, "a candidate's scratch fits the sort keys");
 static_assert(kMaxClusters <= kRunsPerSeq * kSearchMaxBatch, "cluster loads fit the scratch");
 static_assert(kRunsPerSeq * kSearchMaxBatch <= kPlanThreads, "one thread per run");
+static_assert(kCountedSchedule <= kPlanThreads, "one thread per counted unit");
 static_assert(5 * VMLA_MAX_BATCH <= kSortKeys, "the lane plan's prefix sums fit the sort keys");
 
 // Score of candidate k (plan_pick_chunk_host's) by a whole block: the longest
@@ -327,6 +329,46 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   // schedule: units by decreasing cost (ties by unit), dealt to the clusters
   // in a snake order, then in unit order within each cluster
   const int U = ok ? (int)units : 0;
+  const int C = clusters;
+  if (U <= kCountedSchedule) {
+    // few units: each thread finds its unit's place by counting the keys before it (the
+    // keys are distinct), which gives the sorts' order without their barriers
+    uint64_t key = ~0ull;
+    if (tid < U) {
+      const int64_t cost = plan_unit_cost(pp->seq[seq_of_unit(*pp, tid)], tid);
+      key = ((uint64_t)(0x7FFFFFFFll - cost) << 32) | (uint32_t)tid;
+      keys[tid] = key;
+    }
+    __syncthreads();
+    uint64_t key2 = ~0ull;
+    if (tid < U) {
+      int p = 0;
+      for (int j = 0; j < U; ++j) p += keys[j] < key ? 1 : 0;
+      const int round = p / C, j = p - round * C;
+      const int c = (round & 1) ? C - 1 - j : j;
+      key2 = ((uint64_t)c << 32) | (uint32_t)tid;
+    }
+    __syncthreads();
+    if (tid < U) keys[tid] = key2;
+    __syncthreads();
+    if (tid < U) {
+      int p = 0;
+      for (int j = 0; j < U; ++j) p += keys[j] < key2 ? 1 : 0;
+      sched->order[p] = (uint16_t)tid;
+    }
+    for (int c = tid; c <= C; c += blockDim.x) {
+      int n = 0;  // units dealt to clusters before c
+      for (int j = 0; j < U; ++j) n += (int)(keys[j] >> 32) < c ? 1 : 0;
+      sched->start[c] = (uint16_t)n;
+    }
+    if (tid == 0) {
+      sched->num_clusters = ok ? C : 0;
+      sched->total_units = U;
+      sched->unit_base = 0;
+      sched->pad = 0;
+    }
+    return;
+  }
   int n_sort = 2;  // sort only as many keys as there are units (rounded up to a power of two)
   while (n_sort < U) n_sort <<= 1;
   for (int k = tid; k < n_sort; k += blockDim.x) {
@@ -339,7 +381,6 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
   }
   __syncthreads();
   block_sort(keys, n_sort);
-  const int C = clusters;
   for (int p = tid; p < U; p += blockDim.x) {
     const int round = p / C, j = p - round * C;
     const int c = (round & 1) ? C - 1 - j : j;
