@@ -19,7 +19,7 @@ constexpr int kRowBytes = kDqk * 2;  // 1152 bytes per latent KV row / per query
 // that the cluster schedule deals out.  Lane plan (tensor-core kernel,
 // lane_width G > 0): the clusters form lanes of G; each sequence's row blocks
 // form n_rb / G streams of G row blocks over all its key tiles, laid end to
-// end in a cost space (a stream spans its tiles plus kUnitFixedTiles); lane l
+// end in a cost space (a stream spans its tiles plus kLaneStreamTiles); lane l
 // takes the cost interval [l L, (l + 1) L) of every stream it meets, and
 // cluster j of the lane takes row block g G + j of stream g.  A stream's pieces
 // are the lanes it meets (vmla_plan_core.h).

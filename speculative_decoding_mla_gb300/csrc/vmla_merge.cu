@@ -51,7 +51,7 @@ __device__ __forceinline__ void merge_row(const PlanParams& plan, int mrow, cons
     int m = r;
     S = 0;
     for (int g = 0; g < ng; ++g) {
-      const int p = (int)plan_stream_pieces(sp.lane_cost + g * (T + kUnitFixedTiles), T, plan.lane_tiles);
+      const int p = (int)plan_stream_pieces(sp.lane_cost + g * (T + kLaneStreamTiles), T, plan.lane_tiles);
       if (p < 2) continue;
       const int rows = (int)plan_stream_rows(g, per, R);
       if (m < rows) {

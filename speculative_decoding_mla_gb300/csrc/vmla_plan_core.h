@@ -212,6 +212,8 @@ VMLA_HD int plan_choose_cand(const int64_t* score) {
 // stream within one lane writes its rows directly.
 constexpr int kLaneMaxWidth = 4;
 constexpr int64_t kUnitFixedTiles = kUnitFixedKeys / 128;
+// A stream's fixed charge in the lane plan's cost space, in tiles.
+constexpr int64_t kLaneStreamTiles = 5;
 
 // Widths 2..kLaneMaxWidth that do not divide a sequence's row-block count (bit g).
 VMLA_HD uint32_t plan_lane_misfit(int64_t n_rb) {
@@ -233,7 +235,7 @@ VMLA_HD int plan_lane_width(uint32_t misfit) {
 VMLA_HD int64_t plan_seq_tiles(int64_t nk) { return (nk + 127) / 128; }
 
 // Cost-space length of one stream of a sequence with nk keys: its tiles, then the fixed charge.
-VMLA_HD int64_t plan_stream_span(int64_t nk) { return plan_seq_tiles(nk) + kUnitFixedTiles; }
+VMLA_HD int64_t plan_stream_span(int64_t nk) { return plan_seq_tiles(nk) + kLaneStreamTiles; }
 
 // Pieces of a stream whose T tiles start at cost position a: the lanes of length L it meets.
 // (a + T <= W <= INT32_MAX in a lane plan: 32-bit arithmetic.)

@@ -223,9 +223,9 @@ __device__ __forceinline__ void lane_streams(const PlanParams& p, int l, int* s_
   if (P >= W) return;
   const int64_t Q = P + L < W ? P + L : W;
   const SeqPlan& s = p.seq[lane_seq_at(p, P)];
-  const int64_t T = plan_seq_tiles(s.n_kv), g0 = (P - s.lane_cost) / (T + kUnitFixedTiles);
+  const int64_t T = plan_seq_tiles(s.n_kv), g0 = (P - s.lane_cost) / (T + kLaneStreamTiles);
   int first = s.unit_start + (int)g0;
-  if (P - s.lane_cost - g0 * (T + kUnitFixedTiles) >= T) ++first;  // P lies in that stream's fixed charge
+  if (P - s.lane_cost - g0 * (T + kLaneStreamTiles) >= T) ++first;  // P lies in that stream's fixed charge
   const SeqPlan& s2 = p.seq[lane_seq_at(p, Q - 1)];
   int64_t g2 = (Q - 1 - s2.lane_cost) / plan_stream_span(s2.n_kv);
   const int64_t ng2 = s2.n_rb / p.lane_width;
@@ -243,7 +243,7 @@ __device__ __forceinline__ UnitInfo decode_lane_unit(const PlanParams& p, int s,
   const SeqPlan& sp = p.seq[ui.b];
   const int64_t g = s - sp.unit_start;
   const int64_t T = plan_seq_tiles(sp.n_kv), L = p.lane_tiles;
-  const int64_t A = sp.lane_cost + g * (T + kUnitFixedTiles);  // cost position of the stream's first tile
+  const int64_t A = sp.lane_cost + g * (T + kLaneStreamTiles);  // cost position of the stream's first tile
   const int64_t P = (int64_t)l * L;
   const int64_t lo = (P > A ? P : A) - A;
   const int64_t hi = (P + L < A + T ? P + L : A + T) - A;

@@ -378,7 +378,7 @@ def _piece_rule(qo, kv, H, clusters, search=True):
 
     Then the lane plan (only when the search ran): G = the largest of 4, 3, 2 dividing every
     sequence's row-block count (else 1), C // G lanes (1 to 64 of them); each sequence has
-    rb / G streams, each taking ceil(N / 128) tiles and then 3 more in a line of cost W; lanes
+    rb / G streams, each taking ceil(N / 128) tiles and then 5 more in a line of cost W; lanes
     of L = ceil(W / lanes) cut that line, and a stream's pieces are the lanes its tiles meet; a
     sequence's count is the most of any of its streams; the lane plan scores (L + 3) * 128 plus
     the same merge charge and replaces the uniform choice when it scores at least 3 % lower.
@@ -430,7 +430,7 @@ def _piece_rule(qo, kv, H, clusters, search=True):
         lanes = clusters // G
         if not 1 <= lanes <= 64:
             return None
-        W = sum(r // G * (-(-n // 128) + 3) for r, n, q in zip(rb, nk, nq) if q)
+        W = sum(r // G * (-(-n // 128) + 5) for r, n, q in zip(rb, nk, nq) if q)
         if W < 1:
             return None
         L = max(1, -(-W // lanes))
@@ -446,7 +446,7 @@ def _piece_rule(qo, kv, H, clusters, search=True):
                 most = max(most, p)
                 if p > 1:  # the merge combines the rows of this stream's G row blocks
                     merge += min(q * H, (g + 1) * G * 256) - g * G * 256
-                pos += T + 3
+                pos += T + 5
             counts.append(most)
             if most > 1:
                 part += q * H * most
