@@ -136,9 +136,13 @@ int verify_attn_mla_workspace_size(int batch, int num_heads, const int32_t* qo_i
  *               VMLA_SPLITS_LANES takes the lane plan where it fits
  *   out         [T_q, H, 512] bf16 (16 B aligned);  lse [T_q, H] fp32
  *   workspace   >= verify_attn_mla_workspace_size() bytes, 256 B aligned.
- *               Holds the status word, ancestor masks, split partials and a
- *               contiguous copy of the gathered KV rows (1152 B per key).
+ *               Holds the status word, ancestor masks, a contiguous copy of
+ *               the gathered KV rows (1152 B per key) and split partials.
  *               Calls that share a workspace must be ordered on one stream.
+ * The mask and gather kernels are queued before the plan is built (the host
+ * plans while they run).  So a workspace large enough for the masks and rows
+ * but not for the plan's partials returns VMLA_ERR_WORKSPACE with those kernels
+ * queued: they write only inside the workspace, out and lse are untouched.
  * No host synchronisation and no allocation happen inside the call. */
 int verify_attn_mla(const void* q, const void* kv_pool, int64_t pool_slots, const int32_t* kv_indptr,
                     const int32_t* kv_indices, const int32_t* qo_indptr, const uint64_t* draft_mask,

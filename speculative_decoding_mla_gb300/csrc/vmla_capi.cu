@@ -41,6 +41,7 @@ struct Timing {
   std::vector<char> merged;
 };
 Timing g_timing;
+constexpr char kTimingFailed = 4;  // `merged` value of a call that failed after taking its slot
 
 cudaEvent_t timing_event(int call, int k) { return g_timing.ev[(size_t)call * 6 + k]; }
 
@@ -105,16 +106,13 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   }
   static thread_local PlanParams own_plan;  // large (20 KB); kept off the stack
   vmla_plan_info info;
-  if (plan_in && info_in) {
-    info = *info_in;
-  } else {
-    rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &own_plan,
-                    &info);
-    if (rc != VMLA_OK) return rc;
-  }
-  const PlanParams& plan = plan_in && info_in ? *plan_in : own_plan;
-  const WorkspaceLayout L =
-      workspace_layout(total_q, info.partial_rows, kernel == VMLA_KERNEL_TC && !runs ? total_kv : 0);
+  const bool have_plan = plan_in && info_in;
+  if (have_plan) info = *info_in;
+  // The areas no plan sizes (status, masks, staged rows) lead the workspace, so the
+  // kernels that fill them are queued first and the host builds the plan while they
+  // run; without a plan in hand only that part of the size is checked before them.
+  const int64_t staged_rows = kernel == VMLA_KERNEL_TC && !runs ? total_kv : 0;
+  WorkspaceLayout L = workspace_layout(total_q, have_plan ? info.partial_rows : 0, staged_rows);
   if (workspace_bytes < L.total) return VMLA_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status_off);
@@ -141,9 +139,6 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.out_rows = (int64_t)total_q * num_heads;
-  a.part_rows = plan.partial_rows;
-  a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
-  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
   a.staged = runs ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_pool))
                   : reinterpret_cast<uint16_t*>(ws + L.staged_off);
   a.total_kv = runs ? pool_slots : total_kv;
@@ -155,31 +150,50 @@ int run_verify(int kernel, const void* q, const void* kv_pool, int64_t pool_slot
     std::lock_guard<std::mutex> g(g_timing.mu);
     if (g_timing.n < g_timing.cap) slot = g_timing.n++;
   }
+  // a call that fails past this point leaves its timing slot marked, and the readout skips it
+  auto failed = [&](int code) {
+    if (slot >= 0) g_timing.merged[slot] = kTimingFailed;
+    return code;
+  };
   if (runs) {
     // the runs must lie in the pool (the kernel reads whatever the tile loads
     // return; this check reports a run outside it)
     rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, kv_indptr_host, batch, total_kv, nullptr, pool_slots, run_base,
                        true, status,
                        stream);
-    if (rc != VMLA_OK) return rc;
+    if (rc != VMLA_OK) return failed(rc);
   } else if (kernel == VMLA_KERNEL_TC) {
     // KV rows of every sequence gathered once into a contiguous staging area, so
     // that the verify kernel streams them with tiled TMA loads
     if (slot >= 0) cudaEventRecord(timing_event(slot, 4), st);
     rc = launch_gather(a, stream);
-    if (rc != VMLA_OK) return rc;
+    if (rc != VMLA_OK) return failed(rc);
     if (slot >= 0) cudaEventRecord(timing_event(slot, 5), st);
   }
-  if (q_ready && cudaStreamWaitEvent(st, (cudaEvent_t)q_ready, 0) != cudaSuccess) return VMLA_ERR_CUDA;
+  if (!have_plan) {
+    // (the shapes passed check_common, so the plan itself does not fail; a workspace
+    // too small for its partial rows is reported with the staged rows already queued)
+    rc = build_plan(kernel, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters, &own_plan,
+                    &info);
+    if (rc != VMLA_OK) return failed(rc);
+    L = workspace_layout(total_q, info.partial_rows, staged_rows);
+    if (workspace_bytes < L.total) return failed(VMLA_ERR_WORKSPACE);
+  }
+  const PlanParams& plan = have_plan ? *plan_in : own_plan;
+  a.part_rows = plan.partial_rows;
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
+  a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
+  if (q_ready && cudaStreamWaitEvent(st, (cudaEvent_t)q_ready, 0) != cudaSuccess) return failed(VMLA_ERR_CUDA);
   if (slot >= 0) cudaEventRecord(timing_event(slot, 0), st);
   rc = kernel == VMLA_KERNEL_SIMT ? launch_simt(plan, a, stream) : launch_tc(plan, a, stream);
-  if (rc != VMLA_OK) return rc;
+  if (rc != VMLA_OK) return failed(rc);
   if (slot >= 0) {
     cudaEventRecord(timing_event(slot, 1), st);
     g_timing.merged[slot] = (char)((plan.merge_rows > 0 ? 1 : 0) | (kernel == VMLA_KERNEL_TC ? 2 : 0));
     if (plan.merge_rows > 0) cudaEventRecord(timing_event(slot, 2), st);
   }
   rc = launch_merge(plan, a.part_o, a.part_lse, 1, a.out, a.lse, stream);
+  if (rc != VMLA_OK) return failed(rc);
   if (slot >= 0 && plan.merge_rows > 0) cudaEventRecord(timing_event(slot, 3), st);
   return rc;
 }
@@ -722,9 +736,11 @@ int verify_attn_mla_timing_read(float* gather_ms, float* verify_ms, float* merge
     return cudaEventElapsedTime(out, timing_event(call, k0), timing_event(call, k1)) == cudaSuccess;
   };
   for (int i = 0; i < n; ++i) {
-    if (!elapsed(&verify_ms[i], i, 0, 1)) return VMLA_ERR_CUDA;
     merge_ms[i] = 0.f;
     gather_ms[i] = 0.f;
+    verify_ms[i] = 0.f;
+    if (g_timing.merged[i] == kTimingFailed) continue;  // a failed call: zeros
+    if (!elapsed(&verify_ms[i], i, 0, 1)) return VMLA_ERR_CUDA;
     if ((g_timing.merged[i] & 1) && !elapsed(&merge_ms[i], i, 2, 3)) return VMLA_ERR_CUDA;
     if ((g_timing.merged[i] & 2) && !elapsed(&gather_ms[i], i, 4, 5)) return VMLA_ERR_CUDA;
   }

@@ -94,12 +94,14 @@ int build_plan(int kernel, int batch, int num_heads, const int32_t* qo_indptr_ho
 int tc_max_clusters(int* out);
 
 // Workspace layout (offsets in bytes from the workspace base, each 256 B aligned).
+// The areas that do not depend on the plan come first, so that the kernels that
+// fill them can be queued before the plan is built.
 struct WorkspaceLayout {
   size_t status_off;  // uint32 status, uint32 info, 2 spare words
   size_t masks_off;   // uint64 [T_q] ancestor masks
+  size_t staged_off;  // bf16 [staged_rows, 576]: every sequence's KV rows, contiguous (tensor-core kernel)
   size_t part_o_off;  // float [partial_rows, 512]
   size_t part_lse_off;// float [partial_rows]   (log2 domain)
-  size_t staged_off;  // bf16 [staged_rows, 576]: every sequence's KV rows, contiguous (tensor-core kernel)
   size_t total;
 };
 WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t staged_rows);

@@ -202,10 +202,10 @@ WorkspaceLayout workspace_layout(int64_t total_q, int64_t partial_rows, int64_t 
   WorkspaceLayout w;
   w.status_off = 0;
   w.masks_off = up(16);
-  w.part_o_off = w.masks_off + up((size_t)total_q * 8);
+  w.staged_off = w.masks_off + up((size_t)total_q * 8);
+  w.part_o_off = w.staged_off + up((size_t)staged_rows * kRowBytes);
   w.part_lse_off = w.part_o_off + up((size_t)partial_rows * kDv * 4);
-  w.staged_off = w.part_lse_off + up((size_t)partial_rows * 4);
-  w.total = w.staged_off + up((size_t)staged_rows * kRowBytes);
+  w.total = w.part_lse_off + up((size_t)partial_rows * 4);
   return w;
 }
 

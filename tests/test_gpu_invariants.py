@@ -180,6 +180,35 @@ def test_small_workspace_is_rejected():
     assert e.value.status == binding.VMLA_ERR_WORKSPACE
 
 
+def test_workspace_short_of_the_partials_only_is_rejected_after_the_gather():
+    """A workspace that holds the status word, masks and staged rows but not the plan's
+    partials: the call queues the gather (planned afterwards, on the host) and then reports
+    VMLA_ERR_WORKSPACE; out and lse are untouched, and a call with enough room is correct."""
+    torch, binding, device = _mods()
+    case = small("ragged", seed=309)
+    dc = device.to_device(case)
+    T, N = int(case.qo_indptr[-1]), int(case.kv_indptr[-1])
+    up = lambda x: (x + 255) // 256 * 256
+    n_rows = 256 + up(T * 8) + up(N * 1152)  # status, masks, staged rows
+    n_full = binding.verify_attn_mla_workspace_size(dc.qo_indptr_host, dc.kv_indptr_host, dc.num_heads, 7)
+    assert n_full > n_rows
+    out = torch.full((T, dc.num_heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, dc.num_heads), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(n_rows, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.VmlaError) as e:
+        binding.verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
+                                dc.qo_indptr_host, out, lse, ws, dc.sm_scale, splits=7)
+    assert e.value.status == binding.VMLA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all() and torch.isnan(lse).all()
+    ws2 = torch.empty(n_full, dtype=torch.uint8, device="cuda")
+    binding.verify_attn_mla(dc.q, dc.kv_pool, dc.kv_indptr, dc.kv_indices, dc.qo_indptr, dc.kv_indptr_host,
+                            dc.qo_indptr_host, out, lse, ws2, dc.sm_scale, splits=7)
+    assert binding.verify_attn_mla_check(ws2) == 0
+    ref_o, ref_l = oracle.verify(case)
+    compare(device.bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_o, ref_l, "after a short workspace")
+
+
 def test_bounded_wait_expiry_reports_timeout_and_context_stays_usable():
     """A signal that never comes (the test flag withholds Q-ready): the kernel's bounded wait
     expires, the status word says VMLA_ERR_TIMEOUT, and the next call works normally."""
