@@ -32,7 +32,9 @@
  *   - The caller owns every buffer.  The library keeps no pointer after a call
  *     returns and allocates no device memory in these entry points.
  *   - Errors are returned as a vmla_status (int); nothing throws.  Argument
- *     errors are detected on the host before any launch.  Faults seen by a
+ *     errors are detected on the host before any launch (one exception, a
+ *     workspace short of the plan's partial rows, is described at
+ *     verify_attn_mla).  Faults seen by a
  *     kernel (a slot index outside the pool, malformed parents, a bounded wait
  *     that ran out) are recorded in the workspace's status word and reported by
  *     verify_attn_mla_check().
