@@ -30,6 +30,25 @@ namespace {
 constexpr int kMergeWarps = 4;      // warps per block
 constexpr int kMergeInFlight = 12;  // 16-byte loads a lane keeps in flight
 
+// Warps per merge row: the count (4, 2 or 1) with the fewest rounds of the row's loads
+// times waves of resident warps (64 per SM); ties go to more warps per row.
+__host__ __device__ inline int merge_warps_per_row(int64_t rows, int max_pieces, int sms) {
+  const int64_t resident = (int64_t)(sms > 0 ? sms : 1) * 64;
+  int best = 4;
+  int64_t best_cost = -1;
+  for (int wpr = 4; wpr >= 1; wpr >>= 1) {
+    const int64_t batch = kMergeInFlight / (4 / wpr);
+    const int64_t rounds = (max_pieces + batch - 1) / batch;
+    const int64_t waves = (rows * wpr + resident - 1) / resident;
+    const int64_t cost = (rounds > 0 ? rounds : 1) * waves;
+    if (best_cost < 0 || cost < best_cost) {
+      best = wpr;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 // Sequence, row and piece count of merge row mrow (< plan.merge_rows); returns the
 // sequence, with *S = 0 when the row is not a merge row of this plan.
 __device__ __forceinline__ int merge_locate(const PlanParams& plan, int mrow, int* r_out, int* S_out) {
@@ -148,8 +167,6 @@ template <int WPR>
 __device__ __forceinline__ void merge_body(const PlanParams& plan, const float* __restrict__ part_o,
                                            const float* __restrict__ part_lse, int lse_is_log2,
                                            uint16_t* __restrict__ out, float* __restrict__ lse) {
-  // launched to start under the verify kernel's tail: its partials first
-  grid_dependency_wait();
   constexpr int kRowsPerBlock = kMergeWarps / WPR;
   const int w = threadIdx.x >> 5;
   const int rows = plan.merge_rows;
@@ -162,14 +179,22 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 merge_kernel(const __grid_constant__ PlanParams plan, const float* __restrict__ part_o,
              const float* __restrict__ part_lse, int lse_is_log2, uint16_t* __restrict__ out,
              float* __restrict__ lse) {
+  // launched to start under the verify kernel's tail: its partials first
+  grid_dependency_wait();
   merge_body<WPR>(plan, part_o, part_lse, lse_is_log2, out, lse);
 }
 
-// The plan in the workspace (device-planned calls); rows past its merge rows exit.
+// The plan in the workspace (device-planned calls), read past the wait; the grid is one
+// wave of resident warps (`sms` SMs' worth), and the row split follows the same rule as
+// the host-planned launch.
 __global__ void __launch_bounds__(kMergeWarps * 32)
-merge_kernel_dplan(const PlanParams* __restrict__ plan, const float* __restrict__ part_o,
+merge_kernel_dplan(const PlanParams* __restrict__ plan, int sms, const float* __restrict__ part_o,
                    const float* __restrict__ part_lse, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  merge_body<4>(*plan, part_o, part_lse, 1, out, lse);
+  grid_dependency_wait();
+  const int wpr = merge_warps_per_row(plan->merge_rows, plan->max_splits, sms);
+  if (wpr == 4) merge_body<4>(*plan, part_o, part_lse, 1, out, lse);
+  else if (wpr == 2) merge_body<2>(*plan, part_o, part_lse, 1, out, lse);
+  else merge_body<1>(*plan, part_o, part_lse, 1, out, lse);
 }
 
 __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ qo_indptr,
@@ -207,25 +232,6 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32
 }
 
 }  // namespace
-
-// Warps per merge row: the count (4, 2 or 1) with the fewest rounds of the row's loads
-// times waves of resident warps (64 per SM); ties go to more warps per row.
-int merge_warps_per_row(int64_t rows, int max_pieces, int sms) {
-  const int64_t resident = (int64_t)(sms > 0 ? sms : 1) * 64;
-  int best = 4;
-  int64_t best_cost = -1;
-  for (int wpr = 4; wpr >= 1; wpr >>= 1) {
-    const int64_t batch = kMergeInFlight / (4 / wpr);
-    const int64_t rounds = (max_pieces + batch - 1) / batch;
-    const int64_t waves = (rows * wpr + resident - 1) / resident;
-    const int64_t cost = (rounds > 0 ? rounds : 1) * waves;
-    if (best_cost < 0 || cost < best_cost) {
-      best = wpr;
-      best_cost = cost;
-    }
-  }
-  return best;
-}
 
 int launch_merge(const PlanParams& plan, const float* part_o, const float* part_lse, int lse_is_log2,
                  uint16_t* out, float* lse, void* stream) {
@@ -277,7 +283,7 @@ int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* pa
   cfg.stream = (cudaStream_t)stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, merge_kernel_dplan, plan, part_o, part_lse, out, lse) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, merge_kernel_dplan, plan, sms, part_o, part_lse, out, lse) != cudaSuccess)
     return VMLA_ERR_CUDA;
   return VMLA_OK;
 }
