@@ -427,8 +427,9 @@ def run_ours(args, rank, local, world):
         e2e_total += time.perf_counter() - t0
     e2e_s = e2e_total / args.steps
     e2e_max, e2e_tokens = reduce_max_sum(e2e_s, float(tokens), world, dev if world > 1 else None)
-    h2d = q_h.numel() * 2 + kvi_h.numel() * 4 + 2 * (case.batch + 1) * 4 + (par_h.numel() * 4 if par_h is not None
-                                                                               else 0)
+    # bytes that cross to the device: q, the indices (read in place by the gather, being page-locked)
+    # and, for a tree, its parents and qo_indptr; kv_indptr is read on the host for the plan only
+    h2d = q_h.numel() * 2 + kvi_h.numel() * 4 + ((par_h.numel() + case.batch + 1) * 4 if par_h is not None else 0)
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     # the stream-capture-safe entry point (plan computed on the device) captured

@@ -484,17 +484,32 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     rc = host_side(&hs);
     if (rc != VMLA_OK) return rc;
   }
-  // the copies go out first; the plan is built on the host while they cross
+  // The copies go out first; the plan is built on the host while they cross.  On staged
+  // rows the kernels read no kv_indptr on the device (the plan carries the lengths) and
+  // only the tree-mask kernel reads qo_indptr, so neither crosses unless needed.  Page-locked
+  // indices are read by the gather itself through their mapped device address (4 bytes per
+  // 2304 it moves); other host memory is copied first.
+  const int32_t* kvi_dev = reinterpret_cast<const int32_t*>(d_kvi);
+  bool kvi_mapped = false;
+  if (T > 0 && N > 0) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, kv_indices_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer) {
+      kvi_dev = static_cast<const int32_t*>(pa.devicePointer);
+      kvi_mapped = true;
+    } else {
+      cudaGetLastError();  // an unregistered pointer leaves an error to clear
+    }
+  }
   bool ok = true;
-  ok = ok && cudaMemcpyAsync(d_kvp, kv_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
-  ok = ok && cudaMemcpyAsync(d_qop, qo_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
+  if (d_par) ok = ok && cudaMemcpyAsync(d_qop, qo_indptr_host, (B + 1) * 4, h2d, st) == cudaSuccess;
   if (T > 0) {
-    ok = ok && cudaMemcpyAsync(d_kvi, kv_indices_host, N * 4, h2d, st) == cudaSuccess;
+    if (!kvi_mapped) ok = ok && cudaMemcpyAsync(d_kvi, kv_indices_host, N * 4, h2d, st) == cudaSuccess;
     if (d_mask) ok = ok && cudaMemcpyAsync(d_mask, draft_mask_host, T * 8, h2d, st) == cudaSuccess;
     if (d_par) ok = ok && cudaMemcpyAsync(d_par, parent_host, T * 4, h2d, st) == cudaSuccess;
   }
   if (hs) {
-    // starts once the indices have crossed, so that it shares the link with no other copy
+    // starts once the copies above have crossed, so that it shares the link with no other copy
     ok = ok && cudaEventRecord(hs->start, st) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(hs->side, hs->start, 0) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, hs->side) == cudaSuccess;
@@ -516,7 +531,8 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
   if (ok && rc == VMLA_OK && device_buffer_bytes < (size_t)(d_ws - static_cast<char*>(device_buffer)) + ws)
     rc = VMLA_ERR_WORKSPACE;
   if (ok && rc == VMLA_OK)
-    rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, (const int32_t*)d_kvi,
+    // (d_kvp is the kv_indptr slot of the buffer, left unfilled: nothing on this path reads it)
+    rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, kvi_dev,
                     nullptr, (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
                     qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream,
                     hs ? (void*)hs->q_done : nullptr, &plan, &info);

@@ -123,6 +123,42 @@ def test_host_entry_point_matches_device_path():
     assert np.array_equal(o1, o2) and np.array_equal(l1, lse_h.numpy().astype(np.float64))
 
 
+def test_host_entry_point_indices_pageable_pinned_and_offset():
+    """The host-buffer call reads page-locked indices in place (through their mapped device address)
+    and copies other host memory first: pageable indices, pinned indices, and pinned indices that
+    start inside their allocation all give the device call's bits, with an explicit draft mask."""
+    torch, binding, device = _mods()
+    case = small("ragged", seed=312)
+    T, H = case.q.shape[0], case.num_heads
+    rng = np.random.default_rng(5)
+    mask = np.zeros(T, dtype=np.uint64)
+    for b in range(case.batch):
+        q0, q1 = int(case.qo_indptr[b]), int(case.qo_indptr[b + 1])
+        for i in range(q1 - q0):
+            bits = int(rng.integers(0, 1 << max(i, 1))) & ((1 << i) - 1)
+            mask[q0 + i] = np.uint64(bits | (1 << i))
+    o1, l1, st = run_full(case, "tc", draft_mask=mask)
+    assert st == 0
+    kv = device.to_device(case).kv_pool
+    q_h = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    m_h = torch.from_numpy(mask.view(np.int64)).pin_memory()
+    n = binding.verify_attn_mla_host_buffer_size(case.qo_indptr, case.kv_indptr, H, has_mask=True)
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    N = len(case.kv_indices)
+    pinned_big = torch.zeros(N + 37, dtype=torch.int32).pin_memory()
+    pinned_big[37:] = torch.from_numpy(case.kv_indices)
+    for what, kvi_h in [("pageable", torch.from_numpy(case.kv_indices.copy())),
+                        ("pinned", torch.from_numpy(case.kv_indices).pin_memory()),
+                        ("pinned, offset", pinned_big[37:])]:
+        assert kvi_h.is_pinned() == (what != "pageable")
+        out_h = torch.full((T, H, 512), -1, dtype=torch.int16).pin_memory()
+        lse_h = torch.full((T, H), float("nan"), dtype=torch.float32).pin_memory()
+        binding.verify_attn_mla_host(q_h, kv, case.kv_indptr, kvi_h, case.qo_indptr, out_h, lse_h, buf,
+                                     case.sm_scale, draft_mask_host=m_h)
+        o2 = synth.bf16_bits_to_f64(out_h.numpy().view(np.uint16))
+        assert np.array_equal(o1, o2) and np.array_equal(l1, lse_h.numpy().astype(np.float64)), what
+
+
 def test_host_entry_point_reports_a_bad_slot():
     """The host-buffer call returns the device status word (read back with its results): a slot
     outside the pool gives VMLA_ERR_INDEX, and the next good call on the same buffers returns 0."""
