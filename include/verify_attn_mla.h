@@ -391,14 +391,18 @@ int verify_attn_mla_tree_mask(const int32_t* parent, const int32_t* qo_indptr, i
 int verify_attn_mla_check(const void* workspace, void* stream);
 
 /* Host-buffer form for callers whose per-step inputs live in host memory.
- * Copies q, the indptr/indices arrays and the optional mask/parent array from
- * host memory into `device_buffer`, runs verify_attn_mla against the
- * device-resident kv_pool, copies out and lse back into host memory, and
- * synchronises `stream` before returning (so the returned status includes the
- * device status word).  Host buffers should be pinned for asynchronous copies.
- * q crosses on a side stream after the indices, while the gather runs (the
- * kernels after the gather wait for it); out, lse and the status words return
- * by asynchronous copies on `stream` before its one synchronisation.  The
+ * Brings q, kv_indices and the optional mask/parent array (with qo_indptr for
+ * a parent array) from host memory into `device_buffer`, runs verify_attn_mla
+ * against the device-resident kv_pool, copies out and lse back into host
+ * memory, and synchronises `stream` before returning (so the returned status
+ * includes the device status word).  The indptr arrays are read on the host
+ * for the plan.  Host buffers should be pinned for asynchronous copies; pinned
+ * (page-locked) kv_indices are not copied but read in place by the gather
+ * kernel through their mapped device address, so the call must not overlap a
+ * change of them (it returns only when the stream is done).  q crosses on a
+ * side stream after the other inputs, while the gather runs (the kernels after
+ * the gather wait for it); out, lse and the status words return by
+ * asynchronous copies on `stream` before its one synchronisation.  The
  * library keeps one such side stream, two events and an 8-byte pinned status
  * slot per calling thread and device, created at the first call.
  * device_buffer must hold verify_attn_mla_host_buffer_size() bytes (256 B
