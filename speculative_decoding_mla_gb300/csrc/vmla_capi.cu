@@ -515,27 +515,15 @@ int verify_attn_mla_host(const void* q_host, const void* kv_pool, int64_t pool_s
     ok = ok && cudaMemcpyAsync(d_q, q_host, T * num_heads * VMLA_D_QK * 2, h2d, hs->side) == cudaSuccess;
     ok = ok && cudaEventRecord(hs->q_done, hs->side) == cudaSuccess;
   }
-  // the plan, built once here and handed to the call (its workspace is the tensor-core
-  // plan's, at most the size verify_attn_mla_host_buffer_size counted)
-  int sms = 0, clusters = 0;
-  static thread_local PlanParams plan;
-  vmla_plan_info info;
-  if (ok) {
-    rc = current_sm_count(&sms, true);
-    if (rc == VMLA_OK) rc = tc_max_clusters(&clusters);
-    if (rc == VMLA_OK)
-      rc = build_plan(VMLA_KERNEL_TC, batch, num_heads, qo_indptr_host, kv_indptr_host, splits, sms, clusters,
-                      &plan, &info);
-  }
-  const size_t ws = rc == VMLA_OK ? info.workspace_bytes : 0;
-  if (ok && rc == VMLA_OK && device_buffer_bytes < (size_t)(d_ws - static_cast<char*>(device_buffer)) + ws)
-    rc = VMLA_ERR_WORKSPACE;
-  if (ok && rc == VMLA_OK)
+  // the call queues its gather, then builds the plan on the host while the rows move
+  // (the buffer's workspace part is checked against the plan there)
+  if (ok)
     // (d_kvp is the kv_indptr slot of the buffer, left unfilled: nothing on this path reads it)
-    rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, kvi_dev,
-                    nullptr, (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
-                    qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws, ws, stream,
-                    hs ? (void*)hs->q_done : nullptr, &plan, &info);
+    rc = run_verify(VMLA_KERNEL_TC, d_q, kv_pool, pool_slots, 0.f, (const int32_t*)d_kvp, kvi_dev, nullptr,
+                    (const int32_t*)d_qop, (const uint64_t*)d_mask, (const int32_t*)d_par, kv_indptr_host,
+                    qo_indptr_host, batch, num_heads, sm_scale, splits, d_out, (float*)d_lse, d_ws,
+                    device_buffer_bytes - (size_t)(d_ws - static_cast<char*>(device_buffer)), stream,
+                    hs ? (void*)hs->q_done : nullptr);
   if (!ok || rc != VMLA_OK) {
     // the buffer is the caller's again when this returns: the copies already issued are waited for
     if (hs) cudaStreamSynchronize(hs->side);
