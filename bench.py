@@ -478,8 +478,9 @@ def run_ours(args, rank, local, world):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_tokens / e2e_max, "unit": "KV tokens/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h),
-                    "note": "q, indptr/indices (and parents) copied in, out and lse copied back every step; "
-                            "the KV cache stays resident in HBM"},
+                    "note": "every step q crosses in from pinned host memory, the pinned indices are read in place "
+                            "by the gather (and a tree's parents and qo_indptr are copied), out and lse are copied "
+                            "back; the KV cache stays resident in HBM"},
             "gpu_launches": int(launches_per_step * args.steps),
             "device_plan_graph": graph,
             "tree_accept": accept,
