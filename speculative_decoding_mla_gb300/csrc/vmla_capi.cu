@@ -597,12 +597,8 @@ int device_plan_impl(const void* q, const void* kv_pool, int64_t pool_slots, con
                           L.part_cap, plan, sched, status, stream);
   if (rc != VMLA_OK) return rc;
   const uint64_t* masks = draft_mask;
-  if (!masks && parent) {
-    uint64_t* m = reinterpret_cast<uint64_t*>(ws + L.masks_off);
-    rc = launch_tree_mask_dplan(parent, qo_indptr, batch, max_total_q, status + 3, m, status, stream);
-    if (rc != VMLA_OK) return rc;
-    masks = m;
-  }
+  uint64_t* tree_masks = !masks && parent ? reinterpret_cast<uint64_t*>(ws + L.masks_off) : nullptr;
+  if (tree_masks) masks = tree_masks;
   RunArgs a;
   test_fault_settings(&a.test_fault, &a.wait_cycles);
   a.q = static_cast<const uint16_t*>(q);
@@ -618,21 +614,29 @@ int device_plan_impl(const void* q, const void* kv_pool, int64_t pool_slots, con
   a.part_rows = L.part_cap;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o_off);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse_off);
-  // rows: the staged copy (its capacity; the planner's count is in status word 2) or the pool's runs
+  // rows: the staged copy (its capacity; the gather stages kv_indptr[batch] of them) or the pool's runs
   a.staged = runs ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kv_pool))
                   : reinterpret_cast<uint16_t*>(ws + L.staged_off);
   a.total_kv = runs ? pool_slots : max_total_kv;
   a.run_base = run_base;
   a.kv_scale = 0.f;
   a.status = status;
+  // In stream order: the planner; the gather, started beside it (it reads no plan; it
+  // waits for the planner before it completes); the tree masks (they
+  // need the planner's count); the verify kernel, which reads the plan only once all of
+  // that is complete; the merge.  On pool runs the check of the runs takes the gather's place.
   if (runs) {
     // the runs must lie in the pool (a run outside it is reported; its keys read the tile loads' zero fill)
     rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, nullptr, batch, 0, nullptr, pool_slots, run_base, true, status,
                        stream);
   } else {
-    rc = launch_gather_dplan(a, status + 2, stream);
+    rc = launch_gather_dplan(a, kv_indptr + batch, stream);
   }
   if (rc != VMLA_OK) return rc;
+  if (tree_masks) {
+    rc = launch_tree_mask_dplan(parent, qo_indptr, batch, max_total_q, status + 3, tree_masks, status, stream);
+    if (rc != VMLA_OK) return rc;
+  }
   rc = launch_tc_dplan(plan, sched, clusters, a, stream);
   if (rc != VMLA_OK) return rc;
   return launch_merge_dplan(plan, max_total_q * num_heads, a.part_o, a.part_lse, a.out, a.lse, stream);

@@ -127,10 +127,20 @@ __device__ void block_scan(int64_t* v, int n) {
   }
 }
 
+// Lengths the plan cannot take: VMLA_ERR_SHAPE replaces whatever the gather, which runs
+// beside the planner on the lengths it was given, recorded about their slots.
+__device__ __forceinline__ void record_shape_error(uint32_t* status, uint32_t info) {
+  atomicExch(status, (uint32_t)VMLA_ERR_SHAPE);
+  status[1] = info;
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ kv, int batch, int num_heads,
                    int splits, int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
                    PlanParams* __restrict__ pp, TcSched* __restrict__ sched, uint32_t* status) {
+  // the gather may start at once beside this grid (it reads no plan, and it waits for
+  // this grid before it completes)
+  grid_dependents_launch();
   // status[4]: blocks done with their candidate (zeroed before the launch, and again by
   // the last block); status[8..]: the candidates' scores (int64)
   unsigned int* done = status + 4;
@@ -272,7 +282,7 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
       pp->pad = 0;
       status[2] = ok ? (uint32_t)kv[batch] : 0u;
       status[3] = ok ? (uint32_t)qo[batch] : 0u;
-      if (!ok) record_status(status, VMLA_ERR_SHAPE, 2u);
+      if (!ok) record_shape_error(status, 2u);
       sched->num_clusters = ok ? lane_count * G : 0;
       sched->total_units = ok ? (int32_t)l_units[batch - 1] : 0;
       sched->unit_base = 0;
@@ -321,9 +331,9 @@ device_plan_kernel(const int32_t* __restrict__ qo, const int32_t* __restrict__ k
     pp->lane_total = 0;
     pp->lane_count = 0;
     pp->pad = 0;
-    status[2] = ok ? (uint32_t)kv[batch] : 0u;  // rows the gather stages
+    status[2] = ok ? (uint32_t)kv[batch] : 0u;  // key rows of the plan (diagnostic)
     status[3] = ok ? (uint32_t)qo[batch] : 0u;  // draft rows the mask kernel expands
-    if (!ok) record_status(status, VMLA_ERR_SHAPE, lengths_ok ? 2u : (uint32_t)s_bad);
+    if (!ok) record_shape_error(status, lengths_ok ? 2u : (uint32_t)s_bad);
   }
   __syncthreads();
   // schedule: units by decreasing cost (ties by unit), dealt to the clusters

@@ -37,18 +37,20 @@ constexpr int kRowsPerWarp = 4;  // rows a gather warp has in flight
 
 __global__ void __launch_bounds__(kGatherWarps * 32)
 gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int32_t* __restrict__ kv_indices,
-                   int64_t total_kv, const uint32_t* __restrict__ rows_dev, uint4* __restrict__ staged,
+                   int64_t total_kv, const int32_t* __restrict__ total_dev, uint4* __restrict__ staged,
                    uint32_t* status) {
   // the verify kernel may be scheduled as this grid's blocks retire (it waits for
   // the staged rows before it reads them)
   grid_dependents_launch();
   const int lane = threadIdx.x & 31;
   int64_t end = total_kv;
-  if (rows_dev) {
-    // device-planned call: total_kv is the staged capacity and the planner
-    // counted the rows; the tile after the last row is zeroed too, as the tile
-    // loads' out-of-range fill would be, since it holds an earlier call's rows
-    const int64_t cap = total_kv, r = *rows_dev;
+  if (total_dev) {
+    // device-planned call: total_kv is the staged capacity and the rows are
+    // kv_indptr[batch] of them (kv_indices holds the capacity's worth, so a count
+    // the planner will reject still reads inside it); the tile after the last row
+    // is zeroed too, as the tile loads' out-of-range fill would be, since it holds
+    // an earlier call's rows
+    const int64_t cap = total_kv, r = *total_dev > 0 ? *total_dev : 0;
     total_kv = r < cap ? r : cap;
     end = total_kv + kTileRows < cap ? total_kv + kTileRows : cap;
   }
@@ -89,6 +91,10 @@ gather_rows_kernel(const uint4* __restrict__ pool, int64_t pool_slots, const int
       if (lane < kRowU4 - 64) dst[lane + 64] = v[k][2];
     }
   }
+  // Started beside the device planner, this grid completes only after it (the kernels
+  // after the gather read the plan); for a gather launched after its predecessor has
+  // completed the wait returns at once.
+  grid_dependency_wait();
 }
 
 // Two e4m3 codes (low byte first) -> two bf16 (low half first): exact to
@@ -141,34 +147,44 @@ gather_rows_fp8_kernel(const uint4* __restrict__ pool, int64_t pool_slots, float
 }  // namespace
 
 namespace {
-int launch_gather_impl(const RunArgs& a, const uint32_t* rows_dev, void* stream) {
+int launch_gather_impl(const RunArgs& a, const int32_t* total_dev, void* stream) {
   if (a.total_kv == 0) return VMLA_OK;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess)
     return VMLA_ERR_CUDA;
   const int64_t need = (a.total_kv + kGatherWarps * kRowsPerWarp - 1) / (kGatherWarps * kRowsPerWarp);
-  const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 8 warps per SM keep enough rows in flight
+  // 8 blocks of 8 warps per SM keep enough rows in flight.  Beside the device planner the
+  // blocks that find no room start as its blocks retire; a grid that left the planner's SMs
+  // out would run the whole gather on fewer SMs, which costs more than the late start
+  const int64_t cap = (int64_t)sms * 8;
   const int blocks = (int)(need < cap ? need : cap);
   if (a.kv_scale > 0.f) {
-    if (rows_dev) return VMLA_ERR_SHAPE;  // e4m3 pools are read by host-planned calls only
+    if (total_dev) return VMLA_ERR_SHAPE;  // e4m3 pools are read by host-planned calls only
     gather_rows_fp8_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
         reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_scale, a.kv_indices, a.total_kv,
         reinterpret_cast<uint4*>(a.staged), a.status);
     return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
   }
-  gather_rows_kernel<<<blocks, kGatherWarps * 32, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const uint4*>(a.kv), a.pool_slots, a.kv_indices, a.total_kv, rows_dev,
-      reinterpret_cast<uint4*>(a.staged), a.status);
-  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {early_start_attribute()};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kGatherWarps * 32, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = total_dev ? 1 : 0;  // early start only beside the device planner
+  if (cudaLaunchKernelEx(&cfg, gather_rows_kernel, reinterpret_cast<const uint4*>(a.kv), a.pool_slots,
+                         a.kv_indices, a.total_kv, total_dev, reinterpret_cast<uint4*>(a.staged), a.status) !=
+      cudaSuccess)
+    return VMLA_ERR_CUDA;
+  return VMLA_OK;
 }
 }  // namespace
 
 int launch_gather(const RunArgs& a, void* stream) { return launch_gather_impl(a, nullptr, stream); }
 
-// a.total_kv is the staged capacity; the kernel gathers *rows_dev rows of it
-int launch_gather_dplan(const RunArgs& a, const uint32_t* rows_dev, void* stream) {
-  return launch_gather_impl(a, rows_dev, stream);
+int launch_gather_dplan(const RunArgs& a, const int32_t* total_dev, void* stream) {
+  return launch_gather_impl(a, total_dev, stream);
 }
 
 }  // namespace vmla

@@ -182,8 +182,10 @@ int launch_device_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int b
                        int clusters, int64_t max_total_q, int64_t max_total_kv, int64_t part_cap,
                        PlanParams* plan, TcSched* sched, uint32_t* status, void* stream);
 int launch_tc_dplan(const PlanParams* plan, const TcSched* sched, int clusters, const RunArgs& args, void* stream);
-// Gather of the rows counted in *rows_dev (at most args.total_kv, the staged capacity).
-int launch_gather_dplan(const RunArgs& args, const uint32_t* rows_dev, void* stream);
+// Gather of the rows counted in *total_dev (kv_indptr[batch], clamped to [0, args.total_kv],
+// the staged capacity), launched to start beside the planner kernel just queued; it waits
+// for the planner before it completes.
+int launch_gather_dplan(const RunArgs& args, const int32_t* total_dev, void* stream);
 int launch_merge_dplan(const PlanParams* plan, int64_t max_rows, const float* part_o, const float* part_lse,
                        uint16_t* out, float* lse, void* stream);
 int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int batch, int64_t max_total_q,

@@ -200,6 +200,10 @@ merge_kernel_dplan(const PlanParams* __restrict__ plan, int sms, const float* __
 __global__ void tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ qo_indptr,
                                  int batch, int total_q, const uint32_t* __restrict__ rows_dev,
                                  uint64_t* __restrict__ mask_out, uint32_t* status) {
+  // device-planned calls start it early behind the gather: the planner's count first
+  // (a launch after its predecessor has completed passes the wait at once)
+  grid_dependents_launch();
+  grid_dependency_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (rows_dev) {  // device-planned call: the planner's count of draft rows (0 when the lengths are bad)
     const int r = (int)*rows_dev;
@@ -293,9 +297,17 @@ int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int 
   if (max_total_q <= 0) return VMLA_OK;
   if (max_total_q > INT32_MAX) return VMLA_ERR_SHAPE;
   const int total_q = (int)max_total_q;
-  tree_mask_kernel<<<(total_q + 127) / 128, 128, 0, (cudaStream_t)stream>>>(parent, qo_indptr, batch, total_q,
-                                                                             rows_dev, mask_out, status);
-  return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {early_start_attribute()};
+  cfg.gridDim = dim3((unsigned)((total_q + 127) / 128), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tree_mask_kernel, parent, qo_indptr, batch, total_q, rows_dev, mask_out, status) !=
+      cudaSuccess)
+    return VMLA_ERR_CUDA;
+  return VMLA_OK;
 }
 
 }  // namespace vmla

@@ -1209,6 +1209,9 @@ tc_verify_kernel_dplan(const __grid_constant__ CUtensorMap kmap, const __grid_co
                        const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                        const __grid_constant__ CUtensorMap pmap, const PlanParams* __restrict__ plan,
                        const TcSched* __restrict__ sched, const RunArgs a) {
+  // started early behind a kernel that itself may still wait for the planner: the plan
+  // and the schedule are read only once everything before this launch is complete
+  grid_dependency_wait();
   tc_verify_body(kmap, vmap, qmap, omap, pmap, *plan, *sched, a);
 }
 
