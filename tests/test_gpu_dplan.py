@@ -196,3 +196,31 @@ def test_device_plan_random_batches_bitwise():
             compare(o2.reshape(-1, o2.shape[-1])[rows], l2.reshape(-1)[rows], ref_o, ref_l, case.name)
     assert changed >= 1  # the search chose another piece size (or the lane plan) on some of these batches
     assert lanes >= 1  # and the lane plan on some
+
+
+def test_length_error_wins_over_slot_error():
+    """The gather starts beside the planner on the lengths it is given, so it may meet a slot outside
+    the pool in entries the planner goes on to reject: the status word then says VMLA_ERR_SHAPE (the
+    length error), and out and lse keep their contents.  With valid lengths the same bad slot is
+    reported as VMLA_ERR_INDEX."""
+    torch, binding, device = _mods()
+    case = small("ragged", seed=840)
+    dc = device.to_device(case)
+    T, H, B = dc.total_q, dc.num_heads, case.batch
+    maxq, maxkv = T, int(case.kv_indptr[-1])
+    q = dc.q.clone()
+    kvi = torch.full((maxkv,), case.pool_slots + 9, dtype=torch.int32, device="cuda")  # every slot outside
+    out = torch.full((maxq, H, 512), 0.25, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((maxq, H), 0.25, dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.verify_attn_mla_device_plan_workspace_size(B, H, maxq, maxkv, 0), dtype=torch.uint8,
+                     device="cuda")
+    bad = np.array(case.kv_indptr, np.int32)
+    bad[-1] = maxkv + 3  # past the bound: the planner refuses the lengths
+    kvp_bad = torch.from_numpy(bad).cuda()
+    binding.verify_attn_mla_device_plan(q, dc.kv_pool, kvp_bad, kvi, dc.qo_indptr, B, maxq, maxkv, out, lse, ws,
+                                        dc.sm_scale)
+    assert binding.verify_attn_mla_check(ws) == binding.VMLA_ERR_SHAPE
+    assert bool(torch.all(out == 0.25)) and bool(torch.all(lse == 0.25))
+    binding.verify_attn_mla_device_plan(q, dc.kv_pool, dc.kv_indptr, kvi, dc.qo_indptr, B, maxq, maxkv, out, lse, ws,
+                                        dc.sm_scale)
+    assert binding.verify_attn_mla_check(ws) == binding.VMLA_ERR_INDEX
