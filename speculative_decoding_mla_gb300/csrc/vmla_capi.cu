@@ -624,11 +624,12 @@ int device_plan_impl(const void* q, const void* kv_pool, int64_t pool_slots, con
   // In stream order: the planner; the gather, started beside it (it reads no plan; it
   // waits for the planner before it completes); the tree masks (they
   // need the planner's count); the verify kernel, which reads the plan only once all of
-  // that is complete; the merge.  On pool runs the check of the runs takes the gather's place.
+  // that is complete; the merge.  On pool runs the check of the runs takes the gather's place
+  // (also started beside the planner, and waiting for it before it completes).
   if (runs) {
     // the runs must lie in the pool (a run outside it is reported; its keys read the tile loads' zero fill)
     rc = launch_defrag(nullptr, 0, kv_indptr, nullptr, nullptr, batch, 0, nullptr, pool_slots, run_base, true, status,
-                       stream);
+                       stream, nullptr, 0, true);
   } else {
     rc = launch_gather_dplan(a, kv_indptr + batch, stream);
   }

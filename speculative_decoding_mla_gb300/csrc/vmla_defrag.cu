@@ -97,6 +97,9 @@ __global__ void run_check_kernel(const int32_t* __restrict__ kv_indptr, const in
                                  int batch, int64_t slots, uint32_t* status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < batch && !run_ok(kv_indptr, run_base, b, slots)) record_status(status, VMLA_ERR_INDEX, (uint32_t)b);
+  // started beside the device planner, this grid completes only after it (the verify kernel
+  // after it reads the plan); launched after its predecessor has completed, the wait returns
+  grid_dependency_wait();
 }
 
 }  // namespace
@@ -104,12 +107,19 @@ __global__ void run_check_kernel(const int32_t* __restrict__ kv_indptr, const in
 int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
                   const int32_t* kv_indptr_host, int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots,
                   const int32_t* run_base, bool check_only, uint32_t* status, void* stream,
-                  const int32_t* first_row, int64_t max_new) {
+                  const int32_t* first_row, int64_t max_new, bool beside_planner) {
   if (batch == 0) return VMLA_OK;
   if (check_only) {
-    run_check_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(kv_indptr, run_base, batch, dst_slots,
-                                                                           status);
-    return cudaGetLastError() == cudaSuccess ? VMLA_OK : VMLA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {early_start_attribute()};
+    cfg.gridDim = dim3((unsigned)((batch + 127) / 128), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = beside_planner ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, run_check_kernel, kv_indptr, run_base, batch, dst_slots, status) == cudaSuccess
+               ? VMLA_OK
+               : VMLA_ERR_CUDA;
   }
   // blocks of kRunAlign rows over the longest run with its tail, one grid row per sequence
   (void)total_kv;

@@ -193,12 +193,13 @@ int launch_tree_mask_dplan(const int32_t* parent, const int32_t* qo_indptr, int 
 
 // Copies the rows of every sequence into its run of dst_pool and zeroes each
 // run's tail up to a multiple of 128 rows; with check_only, records
-// VMLA_ERR_INDEX for runs outside [0, dst_slots) without copying.  first_row
-// (device [batch], or NULL): rows below it are already in place and skipped.
+// VMLA_ERR_INDEX for runs outside [0, dst_slots) without copying (beside_planner: the
+// check starts beside the device planner kernel just queued and completes after it).
+// first_row (device [batch], or NULL): rows below it are already in place and skipped.
 int launch_defrag(const uint16_t* src_pool, int64_t src_slots, const int32_t* kv_indptr, const int32_t* kv_indices,
                   const int32_t* kv_indptr_host, int batch, int64_t total_kv, uint16_t* dst_pool, int64_t dst_slots,
                   const int32_t* run_base, bool check_only, uint32_t* status, void* stream,
-                  const int32_t* first_row = nullptr, int64_t max_new = 0);
+                  const int32_t* first_row = nullptr, int64_t max_new = 0, bool beside_planner = false);
 
 int launch_tree_accept(const int32_t* qo_indptr, const int32_t* parent, const int32_t* draft, const int32_t* target,
                        const int32_t* root, int batch, int total_q, int32_t* accept_len, int32_t* path,
